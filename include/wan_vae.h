@@ -1,0 +1,182 @@
+/*
+ * wan_vae.h — C ABI of the GB300 (sm_103a) Wan2.2-TI2V-5B VAE decode.
+ *
+ * What it computes is defined on the page "wan22_vae_decode/reference.py"
+ * (FastVideo; a standalone description of diffusers'
+ * AutoencoderKLWan._decode): decode(z, weights, dtype) maps latents
+ * z [B, 48, T, H/16, W/16] to a video [B, 3, 4T-3, H, W] in [-1, 1]:
+ *   1. post_quant_conv, a 1x1x1 conv 48 -> 48 over all T frames
+ *      (module docstring, "What is computed", item 1);
+ *   2. the decoder run causally, chunk by chunk, each causal conv carrying the
+ *      last two frames of its input to the next chunk (item 2; section
+ *      "Causal caches"; section "The first latent frame yields one frame");
+ *   3. unpatchify, video[b, k, f, 2y+i, 2x+j] = out[b, 4k+2j+i, f, y, x]
+ *      (item 3);
+ *   4. clamp to [-1, 1] (item 4).
+ *
+ * Conventions (all entry points):
+ *  - Pointers named as device pointers are CUDA device memory owned by the
+ *    caller; they must stay valid until the work enqueued on `stream`
+ *    completes.  The library never frees caller memory.
+ *  - All work is enqueued on the caller's stream; no entry point blocks the
+ *    host unless its comment says so.
+ *  - Every call returns a wan_status; nothing is thrown across the ABI.  The
+ *    calling thread's last error message is available from
+ *    wan_vae_last_error().
+ *  - Arithmetic runs in the library's CUDA kernels; there is no CPU path.  If
+ *    no CUDA device is present, calls that would launch work return
+ *    WAN_ERR_CUDA.
+ */
+#ifndef WAN_VAE_H
+#define WAN_VAE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* wan_cuda_stream;
+
+typedef enum {
+  WAN_OK = 0,
+  WAN_ERR_INVALID_ARG = 1,      /* null pointer, non-positive size, bad option */
+  WAN_ERR_DTYPE = 2,            /* dtype not WAN_F32 / WAN_BF16 (the page's ValueError) */
+  WAN_ERR_MISSING_WEIGHT = 3,   /* a required parameter name is absent */
+  WAN_ERR_SHAPE = 4,            /* a tensor shape disagrees with the architecture */
+  WAN_ERR_UNSUPPORTED = 5,      /* valid input this build does not handle */
+  WAN_ERR_OOM = 6,              /* device allocation failed */
+  WAN_ERR_CUDA = 7,             /* a CUDA runtime/driver call failed */
+  WAN_ERR_STATE = 8,            /* handle used out of order */
+  WAN_ERR_INTERNAL = 9,         /* a kernel reported an error (e.g. a bounded wait expired) */
+  WAN_ERR_NOT_IMPLEMENTED = 10
+} wan_status;
+
+/* Element types.  WAN_F32: IEEE fp32.  WAN_BF16: bfloat16 (top half of an fp32). */
+typedef enum { WAN_F32 = 0, WAN_BF16 = 1 } wan_dtype;
+
+/* One parameter of the weight table, under diffusers' names ("decoder.*",
+ * "post_quant_conv.*"; other names are ignored, as the page's decode keeps
+ * only those two prefixes).  `data` is device memory, contiguous, in PyTorch
+ * layout: conv3d weights [Cout, Cin, kt, kh, kw], conv2d weights
+ * [Cout, Cin, kh, kw], biases [Cout], RMS-norm gammas any shape of C values. */
+typedef struct {
+  const char* name;
+  const void* data;
+  int32_t dtype;    /* wan_dtype */
+  int32_t ndim;     /* 1..5 */
+  int64_t shape[5];
+} wan_tensor;
+
+typedef struct wan_vae_model wan_vae_model;
+typedef struct wan_vae_stream wan_vae_stream;
+
+/* Output frames of a T-frame latent: 4T - 3 for T >= 1 (page section "The
+ * first latent frame yields one frame"), 0 for T < 1.  Host only. */
+int64_t wan_vae_out_frames(int64_t T);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* wan_vae_last_error(void);
+
+/* Name of a status code. */
+const char* wan_vae_status_string(int32_t status);
+
+/* Packs the 110 decoder + post_quant_conv tensors into a library-owned model
+ * (weights rounded to bf16 for the tensor cores, K-major, per-tap channel
+ * blocks padded to 64; biases and sqrt(C)*gamma kept in fp32).  The
+ * architecture (decoder base dim b, channels 4b/4b/2b/b) is inferred from
+ * decoder.conv_in.weight [4b, 48, 3, 3, 3]; every other shape is checked
+ * against it.  `dtype` is the decode precision: WAN_BF16 computes with bf16
+ * operands and fp32 accumulation (the page's section "Precision", bf16
+ * mode).  WAN_F32 returns WAN_ERR_NOT_IMPLEMENTED in this build.
+ * The caller's tensors may be freed once the work enqueued on `stream` is
+ * done.  Errors: WAN_ERR_INVALID_ARG, WAN_ERR_DTYPE, WAN_ERR_MISSING_WEIGHT,
+ * WAN_ERR_SHAPE, WAN_ERR_OOM, WAN_ERR_CUDA. */
+wan_status wan_vae_model_create(const wan_tensor* weights, int32_t n_weights, int32_t dtype,
+                                wan_cuda_stream stream, wan_vae_model** model);
+/* Frees the model (synchronises with the device; no work may be pending). */
+void wan_vae_model_destroy(wan_vae_model* model);
+/* Decoder base dim b of a model (256 for TI2V-5B), or -1 for NULL. */
+int32_t wan_vae_model_base_dim(const wan_vae_model* model);
+
+/* A decode stream: the causal caches (two frames per 3-frame conv, page
+ * section "Causal caches") and the activation workspace for latents of
+ * B x h x w, decoding at most `max_chunk` latent frames per call.  The
+ * workspace is allocated here (one device allocation) and zero-filled; the
+ * stream starts at the first chunk.  Errors: WAN_ERR_INVALID_ARG, WAN_ERR_OOM,
+ * WAN_ERR_CUDA, WAN_ERR_UNSUPPORTED (h or w not representable). */
+wan_status wan_vae_stream_create(const wan_vae_model* model, int32_t B, int32_t h, int32_t w, int32_t max_chunk,
+                                 wan_vae_stream** stream_state);
+/* Forgets all history (clears the caches on `stream`); the next chunk is a
+ * first chunk again. */
+wan_status wan_vae_stream_reset(wan_vae_stream* st, wan_cuda_stream stream);
+/* Frees the stream state (synchronises with the device). */
+void wan_vae_stream_destroy(wan_vae_stream* st);
+/* Bytes of device workspace the stream holds. */
+int64_t wan_vae_stream_workspace_bytes(const wan_vae_stream* st);
+/* Blocks until the stream's enqueued work is done and reports any error a
+ * kernel recorded (WAN_ERR_INTERNAL with a message) or a CUDA error. */
+wan_status wan_vae_stream_sync_status(wan_vae_stream* st, wan_cuda_stream stream);
+
+/* Decodes latent frames t0 .. t0+n-1 of z [B, 48, z_frames, h, w] (device,
+ * NCDHW, z_dtype) as the next chunk of the stream (page functions decode /
+ * decode_chunk; 1 <= n <= max_chunk).  Writes 4n - 3 video frames on the
+ * stream's first chunk, 4n on later ones, into out [B, 3, out_frames, 16h, 16w]
+ * (device, out_dtype) at frames out_f0 ... .  If `preclamp` is not NULL it
+ * receives the same frames before the clamp, fp32, same layout as out.
+ * Errors: WAN_ERR_INVALID_ARG (sizes, frame ranges), WAN_ERR_DTYPE, WAN_ERR_CUDA,
+ * WAN_ERR_INTERNAL (an earlier chunk's kernel reported an error). */
+wan_status wan_vae_decode_chunk(wan_vae_stream* st, const void* z, int32_t z_dtype, int64_t z_frames, int64_t t0,
+                                int32_t n, void* out, int32_t out_dtype, int64_t out_frames, int64_t out_f0,
+                                float* preclamp, wan_cuda_stream stream);
+
+/* Resets the stream and decodes all T latent frames of z [B, 48, T, h, w]
+ * into out [B, 3, 4T-3, 16h, 16w], in chunks of max_chunk frames. */
+wan_status wan_vae_decode_clip(wan_vae_stream* st, const void* z, int32_t z_dtype, int32_t T, void* out,
+                               int32_t out_dtype, float* preclamp, wan_cuda_stream stream);
+
+/* As wan_vae_decode_clip, with z and out in HOST memory (page-locked memory
+ * is recommended): copies each chunk's latents in, decodes, and copies each
+ * chunk's frames out while the next chunk decodes.  Blocks the host until the
+ * video is in `out_host`. */
+wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int32_t z_dtype, int32_t T,
+                                    void* out_host, int32_t out_dtype, wan_cuda_stream stream);
+
+/* One-shot decode (the page's decode(z, weights, dtype)): packs the weights,
+ * decodes z [B, 48, T, h, w] (device, z_dtype) into out [B, 3, 4T-3, 16h, 16w]
+ * (device, `dtype`) and releases its temporaries, all stream-ordered
+ * (stream-ordered allocator; no host synchronisation). */
+wan_status wan_vae_decode(const void* z, int32_t z_dtype, int32_t B, int32_t T, int32_t h, int32_t w,
+                          const wan_tensor* weights, int32_t n_weights, void* out, int32_t dtype,
+                          wan_cuda_stream stream);
+
+/* ---- layer entry points (the building blocks, exposed for testing) ---- */
+
+/* The mid-block attention (page section "What is computed", "The parts",
+ * fourth bullet, WanAttentionBlock), per frame: n = RMS norm of x; q, k, v =
+ * channels [0,C), [C,2C), [2C,3C) of a 1x1 conv C -> 3C of n; single-head
+ * softmax(q k^T / sqrt(C)) v over the H*W positions; a 1x1 conv C -> C;
+ * plus x.  x, out: [N][H*W][C] bf16 channels-last (device); weights: the
+ * five tensors named *norm.gamma, *to_qkv.weight, *to_qkv.bias, *proj.weight,
+ * *proj.bias.  C must be a multiple of 64 and at most 1024.  Temporaries come
+ * from the stream-ordered allocator. */
+wan_status wan_attention_block(const void* x, int32_t N, int32_t H, int32_t W, int32_t C, const wan_tensor* weights,
+                               int32_t n_weights, void* out, wan_cuda_stream stream);
+
+/* One causal conv (page "The parts", first bullet, WanCausalConv3d): x
+ * [B][n_hist + F][H][W][Cin] bf16 channels-last (device), its first n_hist
+ * (0..2) frames being the conv's history; zero padding kh//2, kw//2 in space
+ * and 2*(kt//2) frames in time (history first, zeros for the missing ones).
+ * weight [Cout, Cin, kt, kh, kw] (w_dtype), bias [Cout] (w_dtype), kt, kh,
+ * kw in {1, 3}.  out [B][F][H][W][Cout] bf16 (device).  Cout must be a
+ * multiple of 16.  Temporaries come from the stream-ordered allocator. */
+wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F, int32_t H, int32_t W, int32_t Cin,
+                             const void* weight, const void* bias, int32_t w_dtype, int32_t Cout, int32_t kt,
+                             int32_t kh, int32_t kw, void* out, wan_cuda_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WAN_VAE_H */

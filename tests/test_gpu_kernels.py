@@ -1,0 +1,91 @@
+"""Layer parity on the GPU: the tensor-core causal conv and the attention
+block, through the C ABI, against the CPU oracle on the same bf16 inputs."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import lib_ready, to_dev
+
+pytestmark = pytest.mark.gpu
+RNG = np.random.default_rng(77)
+
+
+@pytest.fixture(scope="module")
+def wv():
+    return lib_ready()
+
+
+def _bf(a):
+    return oracle.round_bf16(np.asarray(a, np.float32))
+
+
+# (B, n_hist, F, H, W, Cin, Cout, kernel): tiles of 16x8 positions, ragged
+# edges, channel counts off the 64-block, 1/2 history frames, all kernel shapes
+CONV_CASES = [
+    (1, 0, 1, 8, 16, 64, 64, (3, 3, 3)),
+    (1, 2, 2, 12, 20, 48, 256, (3, 3, 3)),
+    (2, 1, 2, 30, 52, 128, 128, (3, 3, 3)),
+    (1, 2, 3, 9, 17, 256, 512, (3, 1, 1)),
+    (1, 0, 2, 5, 7, 64, 16, (1, 1, 1)),
+    (1, 2, 2, 17, 33, 256, 16, (3, 3, 3)),
+    (1, 0, 1, 11, 24, 1024, 256, (3, 3, 3)),
+    (1, 1, 1, 4, 4, 16, 32, (3, 3, 3)),
+    (1, 0, 2, 19, 21, 512, 512, (1, 3, 3)),
+]
+
+
+@pytest.mark.parametrize("case", CONV_CASES, ids=lambda c: "B{}h{}F{}_{}x{}_{}to{}_k{}{}{}".format(*c[:7], *c[7]))
+def test_causal_conv_vs_oracle(wv, case):
+    B, nh, F, H, W, Cin, Cout, k = case
+    x = _bf(RNG.standard_normal((B, nh + F, H, W, Cin)))
+    w = _bf(RNG.uniform(-1, 1, (Cout, Cin, *k)) / math.sqrt(Cin * np.prod(k)))
+    b = _bf(RNG.uniform(-0.1, 0.1, Cout))
+    got = wv.causal_conv3d(to_dev(x, torch.bfloat16), nh, to_dev(w), to_dev(b)).float().cpu().numpy()
+    torch.cuda.synchronize()
+    xn = x.transpose(0, 4, 1, 2, 3)                      # NCDHW
+    ref = oracle.causal_conv(xn[:, :, nh:], w, b, xn[:, :, :nh] if nh else None).transpose(0, 2, 3, 4, 1)
+    # fp32 accumulation of exact bf16 products; the output is rounded to bf16
+    err = np.abs(got - ref)
+    assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max()), float(err.max())
+
+
+def _attn_weights(C, seed):
+    r = np.random.default_rng(seed)
+    return {
+        "a.norm.gamma": _bf(1 + 0.1 * r.standard_normal(C)),
+        "a.to_qkv.weight": _bf(r.uniform(-1, 1, (3 * C, C, 1, 1)) / math.sqrt(C)),
+        "a.to_qkv.bias": _bf(r.uniform(-1, 1, 3 * C) / math.sqrt(C)),
+        "a.proj.weight": _bf(r.uniform(-1, 1, (C, C, 1, 1)) / math.sqrt(C)),
+        "a.proj.bias": _bf(r.uniform(-1, 1, C) / math.sqrt(C)),
+    }
+
+
+def _attention_check(wv, N, C, H, W, frames, seed):
+    w = _attn_weights(C, seed)
+    x = _bf(np.random.default_rng(seed + 1).standard_normal((N, H * W, C)))
+    got = wv.attention_block(to_dev(x, torch.bfloat16), {k: to_dev(v) for k, v in w.items()}, H, W)
+    got = got.float().cpu().numpy()
+    for f in frames:
+        xf = x[f].reshape(H, W, C).transpose(2, 0, 1)[None, :, None]    # [1, C, 1, H, W]
+        ref = oracle.attention(xf, w, "a")[0, :, 0].transpose(1, 2, 0).reshape(H * W, C)
+        err = np.abs(got[f] - ref)
+        rel = np.linalg.norm(got[f] - ref) / np.linalg.norm(ref)
+        assert err.max() <= 4e-2 and rel <= 1e-2, (f, float(err.max()), float(rel))
+
+
+def test_attention_small(wv):
+    _attention_check(wv, N=3, C=64, H=4, W=9, frames=range(3), seed=5)
+
+
+def test_attention_ragged_positions(wv):
+    _attention_check(wv, N=2, C=128, H=7, W=23, frames=range(2), seed=6)
+
+
+def test_attention_full_width_720p_frames(wv):
+    """The isolated attention block at its full size: 8 frames of 44x80
+    positions, C = 1024; frames 0 and 7 checked against the oracle."""
+    _attention_check(wv, N=8, C=1024, H=44, W=80, frames=(0, 7), seed=2)

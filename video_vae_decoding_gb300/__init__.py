@@ -1,0 +1,185 @@
+"""GB300 (sm_103a) Wan2.2-TI2V-5B VAE decode.
+
+A thin Python binding over the C ABI of ``include/wan_vae.h``: it only
+marshals torch CUDA tensors (device memory, streams) into the library's
+calls.  Every step of the decode runs in the library's CUDA kernels; if the
+library is not built, calls raise instead of falling back to anything else.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import WAN_BF16, WAN_F32, WanError, WanTensor, check, load  # noqa: F401
+
+__all__ = ["Model", "DecodeStream", "decode", "attention_block", "causal_conv3d", "out_frames", "WanError"]
+
+
+def _code(dtype: torch.dtype) -> int:
+    if dtype == torch.float32:
+        return WAN_F32
+    if dtype == torch.bfloat16:
+        return WAN_BF16
+    raise ValueError(f"dtype must be torch.float32 or torch.bfloat16, not {dtype}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def out_frames(T: int) -> int:
+    return int(load().wan_vae_out_frames(T))
+
+
+def weight_table(weights: "dict[str, torch.Tensor]"):
+    """wan_tensor array describing `weights` (kept alive by the returned list)."""
+    items = list(weights.items())
+    arr = (WanTensor * len(items))()
+    keep = []
+    for i, (name, t) in enumerate(items):
+        if t.dim() > 5:
+            raise ValueError(f"{name}: more than 5 dimensions")
+        bname = name.encode()
+        keep.append(bname)
+        keep.append(t)
+        arr[i].name = bname
+        arr[i].data = _dev(t, name)
+        arr[i].dtype = {torch.float32: WAN_F32, torch.bfloat16: WAN_BF16}.get(t.dtype, 99)
+        arr[i].ndim = t.dim()
+        for d in range(t.dim()):
+            arr[i].shape[d] = t.shape[d]
+    return arr, keep
+
+
+class Model:
+    """Packed decoder weights (wan_vae_model_create)."""
+
+    def __init__(self, weights: "dict[str, torch.Tensor]", dtype: torch.dtype = torch.bfloat16, stream=None):
+        lib = load()
+        arr, keep = weight_table(weights)
+        h = ctypes.c_void_p()
+        check(lib.wan_vae_model_create(arr, len(keep) // 2, _code(dtype), _stream(stream), ctypes.byref(h)))
+        self._h = h
+        self.dtype = dtype
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def base_dim(self) -> int:
+        return int(load().wan_vae_model_base_dim(self._h))
+
+    def close(self):
+        if self._h:
+            load().wan_vae_model_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class DecodeStream:
+    """Causal caches + workspace for B x h x w latents (wan_vae_stream_create)."""
+
+    def __init__(self, model: Model, B: int, h: int, w: int, max_chunk: int = 4):
+        lib = load()
+        s = ctypes.c_void_p()
+        check(lib.wan_vae_stream_create(model.handle, B, h, w, max_chunk, ctypes.byref(s)))
+        self._s = s
+        self.model = model
+        self.B, self.h, self.w, self.max_chunk = B, h, w, max_chunk
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(load().wan_vae_stream_workspace_bytes(self._s))
+
+    def reset(self, stream=None):
+        check(load().wan_vae_stream_reset(self._s, _stream(stream)))
+
+    def sync_status(self, stream=None):
+        check(load().wan_vae_stream_sync_status(self._s, _stream(stream)))
+
+    def decode_chunk(self, z, t0, n, out, out_f0, preclamp=None, stream=None):
+        p = 0 if preclamp is None else _dev(preclamp, "preclamp")
+        check(load().wan_vae_decode_chunk(self._s, _dev(z, "z"), _code(z.dtype), z.shape[2], t0, n, _dev(out, "out"),
+                                          _code(out.dtype), out.shape[2], out_f0, p or None, _stream(stream)))
+
+    def decode_clip(self, z, out=None, out_dtype=None, preclamp=None, stream=None):
+        B, _, T, h, w = z.shape
+        if out is None:
+            out = torch.empty((B, 3, 4 * T - 3, 16 * h, 16 * w), device=z.device,
+                              dtype=out_dtype or self.model.dtype)
+        p = 0 if preclamp is None else _dev(preclamp, "preclamp")
+        check(load().wan_vae_decode_clip(self._s, _dev(z, "z"), _code(z.dtype), T, _dev(out, "out"), _code(out.dtype),
+                                         p or None, _stream(stream)))
+        return out
+
+    def decode_clip_host(self, z_host: torch.Tensor, out_host: torch.Tensor, stream=None):
+        """z_host, out_host: CPU tensors (pinned recommended); blocks until done."""
+        for t, n in ((z_host, "z_host"), (out_host, "out_host")):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{n} must be a contiguous host tensor")
+        check(load().wan_vae_decode_clip_host(self._s, z_host.data_ptr(), _code(z_host.dtype), z_host.shape[2],
+                                              out_host.data_ptr(), _code(out_host.dtype), _stream(stream)))
+        return out_host
+
+    def close(self):
+        if self._s:
+            load().wan_vae_stream_destroy(self._s)
+            self._s = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def decode(z: torch.Tensor, weights: "dict[str, torch.Tensor]", dtype: torch.dtype = torch.float32, stream=None):
+    """One-shot decode(z, weights, dtype) -> video [B, 3, 4T-3, 16h, 16w] of `dtype`."""
+    code = _code(dtype)
+    B, _, T, h, w = z.shape
+    out = torch.empty((B, 3, 4 * T - 3, 16 * h, 16 * w), device=z.device, dtype=dtype)
+    arr, keep = weight_table(weights)
+    check(load().wan_vae_decode(_dev(z, "z"), _code(z.dtype), B, T, h, w, arr, len(keep) // 2, _dev(out, "out"), code,
+                                _stream(stream)))
+    return out
+
+
+def attention_block(x: torch.Tensor, weights: "dict[str, torch.Tensor]", H: int, W: int, stream=None):
+    """x [N, H*W, C] bf16 channels-last -> attention(x) + x, same layout."""
+    N, HW, C = x.shape
+    out = torch.empty_like(x)
+    arr, keep = weight_table(weights)
+    check(load().wan_attention_block(_dev(x, "x"), N, H, W, C, arr, len(keep) // 2, _dev(out, "out"),
+                                     _stream(stream)))
+    return out
+
+
+def causal_conv3d(x: torch.Tensor, n_hist: int, weight: torch.Tensor, bias: torch.Tensor, stream=None):
+    """x [B, n_hist + F, H, W, Cin] bf16 channels-last -> [B, F, H, W, Cout] bf16."""
+    B, Ft, H, W, Cin = x.shape
+    Cout, _, kt, kh, kw = weight.shape
+    F = Ft - n_hist
+    out = torch.empty((B, F, H, W, Cout), device=x.device, dtype=torch.bfloat16)
+    if weight.dtype != bias.dtype:
+        raise ValueError("weight and bias must share a dtype")
+    check(load().wan_causal_conv3d(_dev(x, "x"), B, n_hist, F, H, W, Cin, _dev(weight, "weight"), _dev(bias, "bias"),
+                                   _code(weight.dtype), Cout, kt, kh, kw, _dev(out, "out"), _stream(stream)))
+    return out

@@ -1,0 +1,84 @@
+"""ctypes declarations of the C ABI in include/wan_vae.h (marshalling only)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libwanvae.so")
+
+WAN_F32, WAN_BF16 = 0, 1
+
+STATUS = {
+    0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_DTYPE", 3: "WAN_ERR_MISSING_WEIGHT", 4: "WAN_ERR_SHAPE",
+    5: "WAN_ERR_UNSUPPORTED", 6: "WAN_ERR_OOM", 7: "WAN_ERR_CUDA", 8: "WAN_ERR_STATE", 9: "WAN_ERR_INTERNAL",
+    10: "WAN_ERR_NOT_IMPLEMENTED",
+}
+
+
+class WanTensor(ctypes.Structure):
+    _fields_ = [
+        ("name", ctypes.c_char_p),
+        ("data", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("ndim", ctypes.c_int32),
+        ("shape", ctypes.c_int64 * 5),
+    ]
+
+
+_vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "wan_vae_out_frames": (_i64, [_i64]),
+    "wan_vae_last_error": (ctypes.c_char_p, []),
+    "wan_vae_status_string": (ctypes.c_char_p, [_i32]),
+    "wan_vae_model_create": (_i32, [ctypes.POINTER(WanTensor), _i32, _i32, _vp, ctypes.POINTER(_vp)]),
+    "wan_vae_model_destroy": (None, [_vp]),
+    "wan_vae_model_base_dim": (_i32, [_vp]),
+    "wan_vae_stream_create": (_i32, [_vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_vp)]),
+    "wan_vae_stream_reset": (_i32, [_vp, _vp]),
+    "wan_vae_stream_destroy": (None, [_vp]),
+    "wan_vae_stream_workspace_bytes": (_i64, [_vp]),
+    "wan_vae_stream_sync_status": (_i32, [_vp, _vp]),
+    "wan_vae_decode_chunk": (_i32, [_vp, _vp, _i32, _i64, _i64, _i32, _vp, _i32, _i64, _i64, _vp, _vp]),
+    "wan_vae_decode_clip": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]),
+    "wan_vae_decode_clip_host": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp]),
+    "wan_vae_decode": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(WanTensor), _i32, _vp, _i32, _vp]),
+    "wan_attention_block": (_i32, [_vp, _i32, _i32, _i32, _i32, ctypes.POINTER(WanTensor), _i32, _vp, _vp]),
+    "wan_causal_conv3d": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                 _vp, _vp]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libwanvae.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m video_vae_decoding_gb300.build` "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class WanError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def check(status: int) -> None:
+    if status != 0:
+        msg = load().wan_vae_last_error()
+        raise WanError(status, msg.decode() if msg else "")

@@ -1,0 +1,304 @@
+// Implicit-GEMM convolution / batched GEMM on the sm_103a tensor cores.
+//
+// One CTA computes a 128 x BN output tile: 128 positions of one output frame
+// (a box_w x box_h rectangle) by BN output channels, accumulated in fp32 in
+// tensor memory.  Warp roles (256 threads):
+//   warp 0, lane 0   TMA producer: per K block, one 5-D tile load of the A
+//                    activation box (64 channels x box_w x box_h, zero-filled
+//                    outside the frame) and one 3-D load of the B weight block
+//   warp 1, lane 0   MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per block
+//   warp 2           TMEM allocation / release
+//   warps 4-7        epilogue: tcgen05.ld of the accumulator, bias, residual /
+//                    DupUp3D / unpatchify, stores
+// A STAGES-deep shared-memory ring, with one "full" and one "empty" mbarrier
+// per stage, overlaps the loads with the MMAs.  All waits are bounded.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace wan {
+
+template <int BN>
+struct ConvCfg {
+  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
+  static constexpr int kBBytes = BN * kBlockK * 2;
+  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 1) + 16;
+};
+
+__device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16]) {
+  if (f32) {
+    float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    d[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+    d[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                      pack_bf16x2(v[14], v[15]));
+  }
+}
+
+__device__ __forceinline__ void add16(const void* src, int f32, float (&v)[16]) {
+  if (f32) {
+    const float4* s = reinterpret_cast<const float4*>(src);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 a = s[i];
+      v[4 * i] += a.x;
+      v[4 * i + 1] += a.y;
+      v[4 * i + 2] += a.z;
+      v[4 * i + 3] += a.w;
+    }
+  } else {
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 a = s[h];
+      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * h + 2 * i] += bf16_lo(w[i]);
+        v[8 * h + 2 * i + 1] += bf16_hi(w[i]);
+      }
+    }
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(256, 1)
+    conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
+                     const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
+  using Cfg = ConvCfg<BN>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * Cfg::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * Cfg::kBBytes);
+  uint64_t* empty = full + S;
+  uint64_t* accum = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int t = blockIdx.x;
+  const int tn = t % args.tiles_n;
+  t /= args.tiles_n;
+  const int tx = t % args.tiles_x;
+  t /= args.tiles_x;
+  const int ty = t % args.tiles_y;
+  t /= args.tiles_y;
+  const int f = t % args.frames;
+  const int b = t / args.frames;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(accum), 1);
+    fence_mbar_init();
+    tma_prefetch_map(&mapA0);
+    tma_prefetch_map(&mapA1);
+    tma_prefetch_map(&mapB);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    int it = 0;
+    bool ok = true;
+    const int gB = args.b_per_frame ? (b * args.b_gstride + f) : 0;
+    for (int ti = 0; ti < args.n_taps && ok; ++ti) {
+      const ConvTap tp = args.taps[ti];
+      const CUtensorMap* am = tp.src ? &mapA1 : &mapA0;
+      const int fr = args.src_f0[tp.src] + f + tp.dt;
+      const int x0 = tx * args.box_w + tp.dx;
+      const int y0 = ty * args.box_h + tp.dy;
+      for (int kb = 0; kb < tp.nkb; ++kb, ++it) {
+        const int s = it % S;
+        const int r = it / S;
+        if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
+        tma_load_5d(smem_u32(sA + s * Cfg::kABytes), am, fb, tp.a_c0 + kb * kBlockK, x0, y0, fr, b);
+        tma_load_3d(smem_u32(sB + s * Cfg::kBBytes), &mapB, fb, tp.b_k0 + kb * kBlockK, tn * BN, gB);
+      }
+    }
+    // Do not leave while copies into this CTA's shared memory are in flight.
+    for (int j = (it > S ? it - S : 0); j < it; ++j)
+      mbar_wait_bounded(smem_u32(&full[j % S]), (j / S) & 1, args.err, kDevTimeoutFull);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
+    for (int it = 0; it < args.total_kb; ++it) {
+      const int s = it % S;
+      if (!mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull)) break;
+      tc_fence_after();
+      const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
+      const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+#pragma unroll
+      for (int k = 0; k < kBlockK / 16; ++k)
+        umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
+      umma_commit(smem_u32(&empty[s]));
+    }
+    umma_commit(smem_u32(accum));  // also on an aborted loop: tracks the MMAs in flight
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const bool got = mbar_wait_bounded(smem_u32(accum), 0, args.err, kDevTimeoutAccum);
+    tc_fence_after();
+    const int q = warp - 4;
+    const int m = q * 32 + lane;
+    const int yy = ty * args.box_h + m / args.box_w;
+    const int xx = tx * args.box_w + m % args.box_w;
+    const bool valid = got && yy < args.H && xx < args.W;
+    const long long pos = (long long)yy * args.W + xx;
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+    for (int c = 0; c < BN / 16; ++c) {
+      const int n0 = tn * BN + c * 16;
+      if (n0 >= args.N) break;  // warp-uniform
+      __syncwarp();               // tcgen05.ld is .sync.aligned: all 32 lanes together
+      uint32_t r[16];
+      tmem_ld16(tbase + c * 16, r);
+      tmem_ld_wait();
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+      if (args.bias) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (n0 + i < args.N) v[i] += __ldg(args.bias + n0 + i);
+      }
+      if (!valid) continue;       // lanes re-converge at the __syncwarp above
+      if constexpr (EPI == kEpiVideo) {
+        const long long base = (long long)b * args.vid_bs + (long long)(args.out_f0 + f) * (4LL * args.H * args.W);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float a0 = v[4 * k + i], a1 = v[4 * k + 2 + i];  // column offsets j = 0, 1
+            const long long off =
+                base + k * args.vid_cs + (long long)(2 * yy + i) * (2LL * args.W) + 2LL * xx;
+            if (args.preclamp) *reinterpret_cast<float2*>(args.preclamp + off) = make_float2(a0, a1);
+            const float c0 = fminf(fmaxf(a0, -1.f), 1.f), c1 = fminf(fmaxf(a1, -1.f), 1.f);
+            if (args.out_f32)
+              *reinterpret_cast<float2*>(static_cast<float*>(args.out) + off) = make_float2(c0, c1);
+            else
+              *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(args.out) + off) = pack_bf16x2(c0, c1);
+          }
+        }
+      } else {
+        if constexpr (EPI == kEpiStore) {
+          if (args.res) {
+            const long long ro =
+                (long long)b * args.res_bs + (long long)(args.res_f0 + f) * args.res_fs + pos * args.res_ldc + n0;
+            const void* rp = args.res_f32 ? (const void*)(static_cast<const float*>(args.res) + ro)
+                                          : (const void*)(static_cast<const __nv_bfloat16*>(args.res) + ro);
+            add16(rp, args.res_f32, v);
+          }
+        } else {  // kEpiDup
+          const int sf = (f + (args.dup_first ? args.dup_ft - 1 : 0)) / args.dup_ft;
+          const long long sp = (long long)(yy >> 1) * args.dup_W + (xx >> 1);
+          const __nv_bfloat16* src =
+              static_cast<const __nv_bfloat16*>(args.dup) + (long long)b * args.dup_bs + (long long)sf * args.dup_fs +
+              sp * args.dup_ldc;
+          if (args.dup_pairs) {
+            // channel c reads source channel 2c + (row & 1)
+            const uint4* s4 = reinterpret_cast<const uint4*>(src + 2 * n0);
+            const int odd = yy & 1;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const uint4 a = s4[h];
+              const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[4 * h + i] += odd ? bf16_hi(w[i]) : bf16_lo(w[i]);
+            }
+          } else {
+            add16(src + n0, 0, v);
+          }
+        }
+        int fo = args.out_f0 + f * args.out_fmul;
+        int no = n0;
+        if (args.interleave_c > 0 && n0 >= args.interleave_c) {
+          fo += 1;
+          no -= args.interleave_c;
+        }
+        const long long oo = (long long)b * args.out_bs + (long long)fo * args.out_fs + pos * args.out_ldc + no;
+        void* op = args.out_f32 ? (void*)(static_cast<float*>(args.out) + oo)
+                                : (void*)(static_cast<__nv_bfloat16*>(args.out) + oo);
+        store16(op, args.out_f32, v);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
+  using Cfg = ConvCfg<BN>;
+  auto kern = conv_gemm_kernel<BN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  const ConvArgs& a = L.args;
+  const long long grid = (long long)a.tiles_n * a.tiles_x * a.tiles_y * a.frames * a.batches;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)grid, 256, Cfg::kSmem, stream>>>(L.a0, L.a1, L.b, a);
+  return cudaGetLastError();
+}
+
+size_t conv_smem_bytes(int bn) {
+  switch (bn) {
+    case 16: return ConvCfg<16>::kSmem;
+    case 32: return ConvCfg<32>::kSmem;
+    case 64: return ConvCfg<64>::kSmem;
+    case 128: return ConvCfg<128>::kSmem;
+    case 256: return ConvCfg<256>::kSmem;
+  }
+  return 0;
+}
+
+cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
+  if (L.epi == kEpiVideo) {
+    if (L.bn != 16) return cudaErrorInvalidValue;
+    return launch_t<16, kEpiVideo>(L, stream);
+  }
+  if (L.epi == kEpiDup) {
+    switch (L.bn) {
+      case 16: return launch_t<16, kEpiDup>(L, stream);
+      case 32: return launch_t<32, kEpiDup>(L, stream);
+      case 64: return launch_t<64, kEpiDup>(L, stream);
+      case 128: return launch_t<128, kEpiDup>(L, stream);
+      case 256: return launch_t<256, kEpiDup>(L, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
+  switch (L.bn) {
+    case 16: return launch_t<16, kEpiStore>(L, stream);
+    case 32: return launch_t<32, kEpiStore>(L, stream);
+    case 64: return launch_t<64, kEpiStore>(L, stream);
+    case 128: return launch_t<128, kEpiStore>(L, stream);
+    case 256: return launch_t<256, kEpiStore>(L, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace wan

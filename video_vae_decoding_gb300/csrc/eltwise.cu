@@ -1,0 +1,335 @@
+// Memory-bound kernels of the decode: RMS norm (+SiLU), nearest x2 upsample,
+// frame copies, post_quant_conv, attention softmax and V transpose, the causal
+// cache ring shift, and weight packing.  All activations are channels-last
+// bf16; every access is a 16-byte vector of 8 channels where the layout allows.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace wan {
+
+namespace {
+
+__device__ __forceinline__ const __nv_bfloat16* at(const FrameView& v, int b, int f, long long p) {
+  return static_cast<const __nv_bfloat16*>(v.base) + b * v.bs + (long long)(v.f0 + f) * v.fs + p * v.ldc;
+}
+__device__ __forceinline__ __nv_bfloat16* at_mut(const FrameView& v, int b, int f, long long p) {
+  return static_cast<__nv_bfloat16*>(v.base) + b * v.bs + (long long)(v.f0 + f) * v.fs + p * v.ldc;
+}
+
+inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + per_block - 1) / per_block); }
+
+// One warp per position; up to kMaxChunks 8-channel chunks per lane.
+constexpr int kNormMaxC = 1024;
+template <bool SILU>
+__global__ void rms_norm_kernel(FrameView in, FrameView out, const float* __restrict__ gs, int C, int F, int P,
+                                long long rows) {
+  const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const long long p = row % P;
+  const int f = (int)((row / P) % F);
+  const int b = (int)(row / ((long long)P * F));
+  const __nv_bfloat16* src = at(in, b, f, p);
+  __nv_bfloat16* dst = at_mut(out, b, f, p);
+  constexpr int kMaxChunks = kNormMaxC / 256;
+  uint4 x[kMaxChunks];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxChunks; ++j) {
+    const int c = lane * 8 + j * 256;
+    if (c < C) {
+      x[j] = *reinterpret_cast<const uint4*>(src + c);
+      const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = bf16_lo(w[i]), bb = bf16_hi(w[i]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(bb, bb, ss);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float rinv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+#pragma unroll
+  for (int j = 0; j < kMaxChunks; ++j) {
+    const int c = lane * 8 + j * 256;
+    if (c < C) {
+      const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+      const float4 g0 = *reinterpret_cast<const float4*>(gs + c);
+      const float4 g1 = *reinterpret_cast<const float4*>(gs + c + 4);
+      const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a = bf16_lo(w[i]) * rinv * g[2 * i];
+        float bb = bf16_hi(w[i]) * rinv * g[2 * i + 1];
+        if (SILU) {
+          a = a / (1.0f + expf(-a));
+          bb = bb / (1.0f + expf(-bb));
+        }
+        o[i] = pack_bf16x2(a, bb);
+      }
+      *reinterpret_cast<uint4*>(dst + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+__global__ void upsample2x_kernel(FrameView in, FrameView out, int C8, int F, int H, int W, long long n) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int c = (int)(i % C8) * 8;
+  long long r = i / C8;
+  const int X = (int)(r % (2 * W));
+  r /= 2 * W;
+  const int Y = (int)(r % (2 * H));
+  r /= 2 * H;
+  const int f = (int)(r % F);
+  const int b = (int)(r / F);
+  const uint4 v = *reinterpret_cast<const uint4*>(at(in, b, f, (long long)(Y >> 1) * W + (X >> 1)) + c);
+  *reinterpret_cast<uint4*>(at_mut(out, b, f, (long long)Y * (2 * W) + X) + c) = v;
+}
+
+__global__ void copy_frames_kernel(FrameView in, FrameView out, int C8, int F, int P, long long n) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int c = (int)(i % C8) * 8;
+  long long r = i / C8;
+  const long long p = r % P;
+  r /= P;
+  const int f = (int)(r % F);
+  const int b = (int)(r / F);
+  *reinterpret_cast<uint4*>(at_mut(out, b, f, p) + c) = *reinterpret_cast<const uint4*>(at(in, b, f, p) + c);
+}
+
+// post_quant_conv (1x1x1, 48 -> 48) on NCDHW latents; one thread per position.
+constexpr int kZ = 48;
+__global__ void post_quant_kernel(const void* __restrict__ z, int z_f32, int Tz, int t0, int F, int P,
+                                  const float* __restrict__ w, const float* __restrict__ bias, FrameView out,
+                                  long long n, int round_z) {
+  __shared__ float sw[kZ * kZ];
+  __shared__ float sb[kZ];
+  for (int i = threadIdx.x; i < kZ * kZ; i += blockDim.x) sw[i] = w[i];
+  for (int i = threadIdx.x; i < kZ; i += blockDim.x) sb[i] = bias[i];
+  __syncthreads();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const long long p = i % P;
+  const int f = (int)((i / P) % F);
+  const int b = (int)(i / ((long long)P * F));
+  float zin[kZ];
+  const long long base = ((long long)b * kZ * Tz + (t0 + f)) * P + p;  // z[b][c][t][p]
+#pragma unroll
+  for (int c = 0; c < kZ; ++c) {
+    const long long o = base + (long long)c * Tz * P;
+    zin[c] = z_f32 ? static_cast<const float*>(z)[o]
+                   : __bfloat162float(static_cast<const __nv_bfloat16*>(z)[o]);
+    if (round_z) zin[c] = __bfloat162float(__float2bfloat16_rn(zin[c]));
+  }
+  __nv_bfloat16* dst = at_mut(out, b, f, p);
+  for (int co = 0; co < kZ; co += 8) {
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float s = sb[co + k];
+#pragma unroll
+      for (int c = 0; c < kZ; ++c) s = fmaf(sw[(co + k) * kZ + c], zin[c], s);
+      acc[k] = s;
+    }
+    *reinterpret_cast<uint4*>(dst + co) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
+  for (int c = kZ; c < out.ldc; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+}
+
+// One 256-thread block per row.
+__global__ void softmax_rows_kernel(const float* __restrict__ S, long long ld_s, __nv_bfloat16* __restrict__ Pm,
+                                    long long ld_p, int n, float scale) {
+  const float* s = S + (long long)blockIdx.x * ld_s;
+  __nv_bfloat16* p = Pm + (long long)blockIdx.x * ld_p;
+  __shared__ float red[32];
+  float mx = -INFINITY;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) mx = fmaxf(mx, s[j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  mx = red[0];
+  __syncthreads();
+  float sum = 0.f;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) sum += expf((s[j] - mx) * scale);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = 1.0f / red[0];
+  for (int j = threadIdx.x; j < n; j += blockDim.x) p[j] = __float2bfloat16_rn(expf((s[j] - mx) * scale) * inv);
+}
+
+// 32 x 32 tiles through shared memory.
+__global__ void transpose_kernel(const __nv_bfloat16* __restrict__ src, long long src_gs, int ld_src,
+                                 __nv_bfloat16* __restrict__ dst, long long dst_gs, int ld_dst, int P, int C) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  const int g = blockIdx.z;
+  const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const __nv_bfloat16* s = src + g * src_gs;
+  __nv_bfloat16* d = dst + g * dst_gs;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int p = p0 + r, c = c0 + threadIdx.x;
+    if (p < P && c < C) tile[r][threadIdx.x] = s[(long long)p * ld_src + c];
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int c = c0 + r, p = p0 + threadIdx.x;
+    if (p < P && c < C) d[(long long)c * ld_dst + p] = tile[threadIdx.x][r];
+  }
+}
+
+struct RingTable {
+  RingShift r[kMaxRings];
+};
+
+// slots (0, 1) <- slots (F, F + 1).  One thread owns one 8-channel vector at
+// the same offset in all four slots, so the overlapping F == 1 case (slot 1
+// is read and written) is race-free.
+__global__ void ring_shift_kernel(const __grid_constant__ RingTable t) {
+  const RingShift& R = t.r[blockIdx.y];
+  const long long n8 = R.frame_elems / 8;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8 * R.batches;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long b = i / n8, e = (i % n8) * 8;
+    __nv_bfloat16* base = R.base + b * R.batch_stride + e;
+    const uint4 a = *reinterpret_cast<const uint4*>(base + (long long)R.F * R.frame_elems);
+    const uint4 c = *reinterpret_cast<const uint4*>(base + (long long)(R.F + 1) * R.frame_elems);
+    *reinterpret_cast<uint4*>(base) = a;
+    *reinterpret_cast<uint4*>(base + R.frame_elems) = c;
+  }
+}
+
+__global__ void pack_weight_kernel(const void* __restrict__ src, int src_f32, int Co, int Ci, int taps,
+                                   __nv_bfloat16* __restrict__ dst, int ld, int k0, int ci_pad, long long n) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int tap = (int)(i % taps);
+  const int ci = (int)((i / taps) % Ci);
+  const int co = (int)(i / ((long long)taps * Ci));
+  const float v = src_f32 ? static_cast<const float*>(src)[i] : __bfloat162float(static_cast<const __nv_bfloat16*>(src)[i]);
+  dst[(long long)co * ld + k0 + (long long)tap * ci_pad + ci] = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float load_any(const void* p, int f32, int i, int rnd) {
+  const float v = f32 ? static_cast<const float*>(p)[i] : __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  return rnd ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
+
+__global__ void to_f32_kernel(const void* __restrict__ src, int src_f32, const void* __restrict__ src2, int src2_f32,
+                              float* __restrict__ dst, int n, float scale, int rnd) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float v = load_any(src, src_f32, i, rnd) * scale;
+  if (src2) v += load_any(src2, src2_f32, i, rnd);
+  dst[i] = v;
+}
+
+}  // namespace
+
+cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, bool silu,
+                            cudaStream_t s) {
+  if (C > kNormMaxC || C % 8) return cudaErrorInvalidValue;
+  const long long rows = (long long)B * F * P;
+  if (rows == 0) return cudaSuccess;
+  const unsigned grid = blocks_for(rows, 8);
+  if (silu)
+    rms_norm_kernel<true><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows);
+  else
+    rms_norm_kernel<false><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_upsample2x(FrameView in, FrameView out, int C, int B, int F, int H, int W, cudaStream_t s) {
+  if (C % 8) return cudaErrorInvalidValue;
+  const long long n = (long long)B * F * 4 * H * W * (C / 8);
+  if (n == 0) return cudaSuccess;
+  upsample2x_kernel<<<blocks_for(n, 256), 256, 0, s>>>(in, out, C / 8, F, H, W, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F, int P, cudaStream_t s) {
+  if (C % 8) return cudaErrorInvalidValue;
+  const long long n = (long long)B * F * P * (C / 8);
+  if (n == 0) return cudaSuccess;
+  copy_frames_kernel<<<blocks_for(n, 256), 256, 0, s>>>(in, out, C / 8, F, P, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_post_quant(const void* z, int z_f32, int B, int Tz, int t0, int F, int P, const float* w,
+                              const float* bias, FrameView out, int round_z_bf16, cudaStream_t s) {
+  if (out.ldc % 8 || out.ldc < kZ) return cudaErrorInvalidValue;
+  const long long n = (long long)B * F * P;
+  if (n == 0) return cudaSuccess;
+  post_quant_kernel<<<blocks_for(n, 128), 128, 0, s>>>(z, z_f32, Tz, t0, F, P, w, bias, out, n, round_z_bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_rows(const float* S, long long ld_s, __nv_bfloat16* P, long long ld_p, int n, long long R,
+                                float scale, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  if (R > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  softmax_rows_kernel<<<(unsigned)R, 256, 0, s>>>(S, ld_s, P, ld_p, n, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const __nv_bfloat16* src, long long src_gs, int ld_src, __nv_bfloat16* dst,
+                             long long dst_gs, int ld_dst, int G, int P, int C, cudaStream_t s) {
+  if (G == 0 || P == 0 || C == 0) return cudaSuccess;
+  dim3 grid((P + 31) / 32, (C + 31) / 32, G), block(32, 8);
+  transpose_kernel<<<grid, block, 0, s>>>(src, src_gs, ld_src, dst, dst_gs, ld_dst, P, C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_shift(const RingShift* rings, int n, cudaStream_t s) {
+  for (int i0 = 0; i0 < n; i0 += kMaxRings) {
+    RingTable t{};
+    const int m = (n - i0) < kMaxRings ? (n - i0) : kMaxRings;
+    for (int i = 0; i < m; ++i) {
+      t.r[i] = rings[i0 + i];
+      if (t.r[i].frame_elems % 8) return cudaErrorInvalidValue;
+    }
+    dim3 grid(296, m);
+    ring_shift_kernel<<<grid, 256, 0, s>>>(t);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_pack_weight(const void* src, int src_f32, int Co, int Ci, int taps, __nv_bfloat16* dst, int ld,
+                               int k0, int ci_pad, cudaStream_t s) {
+  const long long n = (long long)Co * Ci * taps;
+  if (n == 0) return cudaSuccess;
+  pack_weight_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, src_f32, Co, Ci, taps, dst, ld, k0, ci_pad, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_f32(const void* src, int src_f32, const void* src2, int src2_f32, float* dst, int n,
+                          float scale, int round_bf16, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  to_f32_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, src_f32, src2, src2_f32, dst, n, scale, round_bf16);
+  return cudaGetLastError();
+}
+
+}  // namespace wan

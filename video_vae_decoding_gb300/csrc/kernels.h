@@ -1,0 +1,137 @@
+// Launch descriptors shared by the host planner and the CUDA kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace wan {
+
+// ---------------------------------------------------------------------------
+// Implicit-GEMM convolution on the 5th-generation tensor cores.
+//
+// Output tile: 128 positions (a box_w x box_h spatial rectangle of one output
+// frame) x BN output channels.  The K loop walks a list of taps; each tap is
+// one kernel offset (dt, dy, dx) of one A source, contributing nkb blocks of
+// 64 input channels.  A tiles are TMA-loaded from a channels-last activation
+// tensor [B][F][H][W][C] whose out-of-range coordinates read zero, which is
+// the convolution's zero padding in space.  Frame coordinates index the
+// tensor's frame slots directly: a causal conv's input tensor keeps its two
+// history frames in slots 0-1 in front of the current frames.
+// ---------------------------------------------------------------------------
+constexpr int kMaxTaps = 96;
+constexpr int kTileM = 128;
+constexpr int kBlockK = 64;
+
+struct ConvTap {
+  int8_t src;     // A source: 0 or 1
+  int8_t dt;      // frame offset added to the source frame base
+  int8_t dy, dx;  // spatial offsets of the source position (kernel offset minus padding)
+  int16_t a_c0;   // first channel of the tap in the A source
+  int16_t nkb;    // 64-channel blocks
+  int32_t b_k0;   // first K column of the tap in the B operand
+};
+
+enum EpiMode : int { kEpiStore = 0, kEpiDup = 1, kEpiVideo = 2 };
+
+struct ConvArgs {
+  ConvTap taps[kMaxTaps];
+  int n_taps;
+  int total_kb;
+  // grid = tiles_n * tiles_x * tiles_y * frames * batches CTAs (n fastest)
+  int tiles_n, tiles_x, tiles_y, frames, batches;
+  int box_w, box_h;      // spatial tile, box_w * box_h == 128
+  int H, W;              // output spatial size (equal to the A sources')
+  int src_f0[2];         // frame coordinate of output frame 0 in each A source
+  int b_per_frame;       // 1: B's third coordinate is b * b_gstride + output frame (batched GEMMs)
+  int b_gstride;
+  int N;                 // valid output channels
+  const float* bias;     // [N] fp32, or null
+  // output element (b, frame, y, x, n) at
+  //   out + b*out_bs + (out_f0 + f*out_fmul + hi)*out_fs + (y*W + x)*out_ldc + n'
+  // where, if interleave_c > 0, channels n >= interleave_c go to the next
+  // frame (hi = 1) as n' = n - interleave_c.
+  void* out;
+  int out_f32;
+  long long out_bs, out_fs;
+  int out_ldc, out_f0, out_fmul, interleave_c;
+  // kEpiStore: optional residual added at the same (b, y, x, n), frame res_f0 + f
+  const void* res;
+  int res_f32;
+  long long res_bs, res_fs;
+  int res_ldc, res_f0;
+  // kEpiDup: DupUp3D of a half-resolution source, added to the output
+  const void* dup;
+  long long dup_bs, dup_fs;
+  int dup_ldc, dup_W;
+  int dup_ft;            // frames per source frame (2 with temporal upsampling, else 1)
+  int dup_first;         // first chunk: the first ft-1 copies of frame 0 are dropped
+  int dup_pairs;         // 1: channel c reads source 2c + (row & 1) (r = 2); 0: channel c (r = 4ft)
+  // kEpiVideo: out = video [B][3][F][2H][2W]; channel 4k + 2j + i -> colour k,
+  // row 2y + i, column 2x + j; clamped to [-1, 1]; preclamp is the fp32 copy
+  // before the clamp (optional).
+  float* preclamp;
+  long long vid_bs, vid_cs;
+  int* err;              // device error word (kDev* codes)
+};
+
+struct ConvLaunch {
+  CUtensorMap a0, a1, b;
+  ConvArgs args;
+  int bn;      // 16, 32, 64, 128 or 256
+  int epi;     // EpiMode
+};
+
+cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream);
+size_t conv_smem_bytes(int bn);
+
+// ---------------------------------------------------------------------------
+// Memory-bound kernels (channels-last bf16 unless stated).
+// A "frame view" addresses element (b, f, p, c) of a tensor as
+//   base + b*bs + (f0 + f)*fs + p*ldc + c.
+// ---------------------------------------------------------------------------
+struct FrameView {
+  void* base;
+  long long bs, fs;
+  int ldc, f0;
+};
+
+// y = x / max(||x||, 1e-12) * gs (gs = sqrt(C)*gamma, fp32), then SiLU if silu.
+cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, bool silu,
+                            cudaStream_t s);
+// nearest x2: out(b, f, 2y+i, 2x+j, c) = in(b, f, y, x, c); in is H x W.
+cudaError_t launch_upsample2x(FrameView in, FrameView out, int C, int B, int F, int H, int W, cudaStream_t s);
+// copy F frames of C channels
+cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F, int P, cudaStream_t s);
+// post_quant_conv: z [B][48][Tz][h][w] (fp32 or bf16, NCDHW), frames t0..t0+F-1
+// -> out(b, f, p, 0..47) bf16; channels 48..ldc-1 are written as zero.
+cudaError_t launch_post_quant(const void* z, int z_f32, int B, int Tz, int t0, int F, int P, const float* w /*48x48*/,
+                              const float* bias, FrameView out, int round_z_bf16, cudaStream_t s);
+// Row softmax of S [R][ld_s] fp32 (n valid columns) scaled by `scale`, into
+// P [R][ld_p] bf16.
+cudaError_t launch_softmax_rows(const float* S, long long ld_s, __nv_bfloat16* P, long long ld_p, int n, long long R,
+                                float scale, cudaStream_t s);
+// Vt[g][c][p] = src[g][p][c] (bf16), p < P, c < C; src row stride ld_src.
+cudaError_t launch_transpose(const __nv_bfloat16* src, long long src_gs, int ld_src, __nv_bfloat16* dst,
+                             long long dst_gs, int ld_dst, int G, int P, int C, cudaStream_t s);
+// Causal-cache shift: for each ring, slots (0, 1) <- slots (F, F + 1).
+struct RingShift {
+  __nv_bfloat16* base;
+  long long frame_elems;   // elements per frame slot
+  long long batch_stride;  // elements per batch item
+  int F;                   // current frames (slots 2 .. F+1)
+  int batches;
+};
+constexpr int kMaxRings = 48;
+cudaError_t launch_ring_shift(const RingShift* rings, int n, cudaStream_t s);
+// Weight packing: src [Co][Ci][taps] (fp32 or bf16, taps = kt*kh*kw) ->
+// dst[co][k0 + tap*ci_pad + ci] bf16 for co < Co, ci < Ci; dst has ld columns.
+cudaError_t launch_pack_weight(const void* src, int src_f32, int Co, int Ci, int taps, __nv_bfloat16* dst, int ld,
+                               int k0, int ci_pad, cudaStream_t s);
+// dst[i] = scale * r(src[i]) (+ r(src2[i]) if src2) as fp32; src fp32 or bf16;
+// r rounds to the nearest bf16 when round_bf16 is set.
+cudaError_t launch_to_f32(const void* src, int src_f32, const void* src2, int src2_f32, float* dst, int n,
+                          float scale, int round_bf16, cudaStream_t s);
+
+}  // namespace wan

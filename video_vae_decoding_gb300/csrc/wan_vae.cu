@@ -1,0 +1,1317 @@
+// Host side of the decode: the C ABI of include/wan_vae.h, weight packing,
+// the per-chunk launch sequence and the causal-cache ring buffers.
+//
+// The sequence follows the page "wan22_vae_decode/reference.py", module
+// docstring "What is computed" (post_quant_conv; conv_in; mid block; up
+// blocks 0-3; norm_out, SiLU, conv_out; unpatchify; clamp), sections
+// "The first latent frame yields one frame" and "Causal caches".  A chunk of
+// n latent frames runs every layer over all of its frames at once (the
+// whole-sequence form of section "Causal caches" restricted to the chunk),
+// the 3-frame causal convs reading their two history frames from the front
+// slots of a per-conv ring buffer.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "wan_vae.h"
+
+using bf16 = __nv_bfloat16;
+
+namespace wan {
+
+thread_local std::string g_last_error;
+
+static wan_status fail(wan_status s, const char* fmt, ...) {
+  char buf[1024];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+#define CUDA_TRY(expr)                                                                                     \
+  do {                                                                                                     \
+    cudaError_t e_ = (expr);                                                                               \
+    if (e_ != cudaSuccess)                                                                                 \
+      return ::wan::fail(e_ == cudaErrorMemoryAllocation ? WAN_ERR_OOM : WAN_ERR_CUDA, "%s: %s (%s:%d)", #expr, \
+                         cudaGetErrorString(e_), __FILE__, __LINE__);                                      \
+  } while (0)
+#define WAN_TRY(expr)                 \
+  do {                                \
+    wan_status s_ = (expr);           \
+    if (s_ != WAN_OK) return s_;      \
+  } while (0)
+
+static inline long long rup(long long a, long long b) { return (a + b - 1) / b * b; }
+static inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static wan_status init_encode() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  });
+  if (!g_encode) return fail(WAN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  return WAN_OK;
+}
+
+static wan_status encode(CUtensorMap* m, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
+                         const uint32_t* box) {
+  WAN_TRY(init_encode());
+  const uint32_t es[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
+                              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WAN_ERR_INTERNAL, "cuTensorMapEncodeTiled failed (%d), rank %d", (int)r, rank);
+  return WAN_OK;
+}
+
+// Channels-last bf16 activation tensor [B][F][H][W][ldc]; channels C..ldc-1
+// hold zeros.  ldc is a multiple of 64 for tensors that feed the tensor cores.
+struct Act {
+  bf16* p = nullptr;
+  int B = 0, F = 0, H = 0, W = 0, C = 0, ldc = 0;
+  long long fs() const { return (long long)H * W * ldc; }
+  long long bs() const { return (long long)F * fs(); }
+  size_t bytes() const { return (size_t)B * bs() * sizeof(bf16); }
+  FrameView view(int f0 = 0) const { return FrameView{p, bs(), fs(), ldc, f0}; }
+};
+
+// A-operand map over an activation tensor: dims (C, W, H, F, B), box
+// (64, bw, bh, 1, 1).
+static wan_status act_map(CUtensorMap* m, const bf16* base, int C, int ldc, int W, int H, int F, int B, long long fs,
+                          long long bs, int bw, int bh) {
+  const uint64_t dims[5] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)F, (uint64_t)B};
+  const uint64_t strides[4] = {(uint64_t)ldc * 2, (uint64_t)W * ldc * 2, (uint64_t)fs * 2, (uint64_t)bs * 2};
+  const uint32_t box[5] = {64, (uint32_t)bw, (uint32_t)bh, 1, 1};
+  return encode(m, 5, base, dims, strides, box);
+}
+static wan_status act_map(CUtensorMap* m, const Act& a, int bw = 16, int bh = 8) {
+  return act_map(m, a.p, a.ldc, a.ldc, a.W, a.H, a.F, a.B, a.fs(), a.bs(), bw, bh);
+}
+// B-operand map: dims (K, N, G), box (64, bn, 1).
+static wan_status b_map(CUtensorMap* m, const bf16* base, long long K, long long N, long long G, long long ldk,
+                        long long gs, int bn) {
+  const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)G};
+  const uint64_t strides[2] = {(uint64_t)ldk * 2, (uint64_t)gs * 2};
+  const uint32_t box[3] = {64, (uint32_t)bn, 1};
+  return encode(m, 3, base, dims, strides, box);
+}
+
+// -------------------------------------------------------------- allocation
+struct DevMem {
+  std::vector<void*> ptrs;
+  cudaStream_t async = nullptr;  // stream-ordered allocations when set
+  bool use_async = false;
+  bool dry = false;              // validation pass: check names and shapes only
+  wan_status alloc(void** p, size_t bytes) {
+    *p = nullptr;
+    if (bytes == 0) bytes = 256;
+    const cudaError_t e = use_async ? cudaMallocAsync(p, bytes, async) : cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(e == cudaErrorMemoryAllocation ? WAN_ERR_OOM : WAN_ERR_CUDA, "device allocation of %zu bytes: %s",
+                  bytes, cudaGetErrorString(e));
+    }
+    ptrs.push_back(*p);
+    return WAN_OK;
+  }
+  void release() {
+    for (void* p : ptrs) use_async ? cudaFreeAsync(p, async) : cudaFree(p);
+    ptrs.clear();
+  }
+};
+
+// ------------------------------------------------------------ packed convs
+struct ConvW {
+  bf16* w = nullptr;      // [co_pad][ktot], K = tap-major, 64-padded channel blocks per tap
+  float* bias = nullptr;  // [Co] (conv bias + shortcut bias)
+  int Co = 0, Ci = 0, kt = 1, kh = 1, kw = 1;
+  int ci_pad = 0, ktot = 0, co_pad = 0, bn = 0;
+  int sc_Ci = 0, sc_ci_pad = 0;  // appended 1x1x1 shortcut conv
+};
+
+static int choose_bn(int co) {
+  if (co >= 256) return 256;
+  int b = 16;
+  while (b < co) b *= 2;
+  return b;
+}
+
+struct WeightTable {
+  const wan_tensor* t;
+  int n;
+  const wan_tensor* find(const std::string& name) const {
+    for (int i = 0; i < n; ++i)
+      if (t[i].name && name == t[i].name) return &t[i];
+    return nullptr;
+  }
+};
+
+static wan_status get_tensor(const WeightTable& wt, const std::string& name, const wan_tensor** out) {
+  const wan_tensor* x = wt.find(name);
+  if (!x) return fail(WAN_ERR_MISSING_WEIGHT, "missing weight '%s'", name.c_str());
+  if (x->dtype != WAN_F32 && x->dtype != WAN_BF16)
+    return fail(WAN_ERR_DTYPE, "weight '%s': dtype %d is neither WAN_F32 nor WAN_BF16", name.c_str(), x->dtype);
+  if (!x->data) return fail(WAN_ERR_INVALID_ARG, "weight '%s': null data", name.c_str());
+  if (x->ndim < 1 || x->ndim > 5) return fail(WAN_ERR_SHAPE, "weight '%s': ndim %d", name.c_str(), x->ndim);
+  *out = x;
+  return WAN_OK;
+}
+
+static long long numel(const wan_tensor* t) {
+  long long n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+static wan_status check_shape(const wan_tensor* t, std::vector<long long> want) {
+  bool ok = t->ndim == (int)want.size();
+  for (int i = 0; ok && i < t->ndim; ++i) ok = t->shape[i] == want[i];
+  if (!ok) {
+    std::string got, exp;
+    for (int i = 0; i < t->ndim; ++i) got += std::to_string(t->shape[i]) + (i + 1 < t->ndim ? "," : "");
+    for (size_t i = 0; i < want.size(); ++i) exp += std::to_string(want[i]) + (i + 1 < want.size() ? "," : "");
+    return fail(WAN_ERR_SHAPE, "weight '%s': shape [%s], expected [%s]", t->name, got.c_str(), exp.c_str());
+  }
+  return WAN_OK;
+}
+
+// Packs `name` (conv3d [Co,Ci,kt,kh,kw] or conv2d [Co,Ci,kh,kw]) and, if
+// given, a 1x1x1 shortcut conv appended along K.
+static wan_status pack_conv(const WeightTable& wt, const std::string& name, int Co, int Ci, int kt, int kh, int kw,
+                            bool conv2d, const std::string& sc_name, int sc_Ci, ConvW& cw, DevMem& mem,
+                            cudaStream_t s) {
+  const wan_tensor *W, *Bi;
+  WAN_TRY(get_tensor(wt, name + ".weight", &W));
+  WAN_TRY(get_tensor(wt, name + ".bias", &Bi));
+  if (conv2d)
+    WAN_TRY(check_shape(W, {Co, Ci, kh, kw}));
+  else
+    WAN_TRY(check_shape(W, {Co, Ci, kt, kh, kw}));
+  WAN_TRY(check_shape(Bi, {Co}));
+  const wan_tensor *Ws = nullptr, *Bs = nullptr;
+  if (!sc_name.empty()) {
+    WAN_TRY(get_tensor(wt, sc_name + ".weight", &Ws));
+    WAN_TRY(get_tensor(wt, sc_name + ".bias", &Bs));
+    WAN_TRY(check_shape(Ws, {Co, sc_Ci, 1, 1, 1}));
+    WAN_TRY(check_shape(Bs, {Co}));
+  }
+  if (mem.dry) return WAN_OK;
+  cw.Co = Co;
+  cw.Ci = Ci;
+  cw.kt = kt;
+  cw.kh = kh;
+  cw.kw = kw;
+  cw.ci_pad = (int)rup(Ci, 64);
+  cw.sc_Ci = Ws ? sc_Ci : 0;
+  cw.sc_ci_pad = Ws ? (int)rup(sc_Ci, 64) : 0;
+  const int taps = kt * kh * kw;
+  cw.ktot = taps * cw.ci_pad + cw.sc_ci_pad;
+  cw.bn = choose_bn(Co);
+  cw.co_pad = (int)rup(Co, cw.bn);
+  void* p;
+  WAN_TRY(mem.alloc(&p, (size_t)cw.co_pad * cw.ktot * sizeof(bf16)));
+  cw.w = (bf16*)p;
+  CUDA_TRY(cudaMemsetAsync(cw.w, 0, (size_t)cw.co_pad * cw.ktot * sizeof(bf16), s));
+  CUDA_TRY(launch_pack_weight(W->data, W->dtype == WAN_F32, Co, Ci, taps, cw.w, cw.ktot, 0, cw.ci_pad, s));
+  if (Ws)
+    CUDA_TRY(launch_pack_weight(Ws->data, Ws->dtype == WAN_F32, Co, sc_Ci, 1, cw.w, cw.ktot, taps * cw.ci_pad,
+                                cw.sc_ci_pad, s));
+  WAN_TRY(mem.alloc(&p, (size_t)Co * sizeof(float)));
+  cw.bias = (float*)p;
+  CUDA_TRY(launch_to_f32(Bi->data, Bi->dtype == WAN_F32, Bs ? Bs->data : nullptr, Bs ? Bs->dtype == WAN_F32 : 0,
+                         cw.bias, Co, 1.0f, 1, s));
+  return WAN_OK;
+}
+
+// sqrt(C) * gamma in fp32
+static wan_status pack_gamma(const WeightTable& wt, const std::string& name, int C, float** out, DevMem& mem,
+                             cudaStream_t s) {
+  const wan_tensor* g;
+  WAN_TRY(get_tensor(wt, name, &g));
+  if (numel(g) != C) return fail(WAN_ERR_SHAPE, "weight '%s': %lld values, expected %d", name.c_str(), numel(g), C);
+  if (mem.dry) return WAN_OK;
+  void* p;
+  WAN_TRY(mem.alloc(&p, (size_t)C * sizeof(float)));
+  *out = (float*)p;
+  CUDA_TRY(launch_to_f32(g->data, g->dtype == WAN_F32, nullptr, 0, *out, C, std::sqrt((float)C), 1, s));
+  return WAN_OK;
+}
+
+}  // namespace wan
+
+using namespace wan;
+
+struct Resnet {
+  ConvW c1, c2;  // c2 carries the shortcut when ci != co
+  float* g1 = nullptr;
+  float* g2 = nullptr;
+  int ci = 0, co = 0;
+};
+
+struct wan_vae_model {
+  int base = 0, dtype = WAN_BF16;
+  float* pq_w = nullptr;
+  float* pq_b = nullptr;
+  ConvW conv_in;
+  Resnet mid[2];
+  float* attn_g = nullptr;
+  ConvW qkv, proj;
+  Resnet up[4][3];
+  ConvW tconv[2];
+  ConvW resample[3];
+  float* out_g = nullptr;
+  ConvW conv_out;
+  DevMem mem;
+};
+
+// (in, out, temporal, spatial) of the up blocks in units of the base dim
+// (page "What is computed": channels 4b, 4b, 4b -> 2b, 2b -> b).
+static const int kUp[4][4] = {{4, 4, 1, 1}, {4, 4, 1, 1}, {4, 2, 0, 1}, {2, 1, 0, 0}};
+static const int kZdim = 48;
+
+static wan_status pack_resnet(const WeightTable& wt, const std::string& name, int ci, int co, Resnet& r, DevMem& mem,
+                              cudaStream_t s) {
+  r.ci = ci;
+  r.co = co;
+  WAN_TRY(pack_gamma(wt, name + ".norm1.gamma", ci, &r.g1, mem, s));
+  WAN_TRY(pack_gamma(wt, name + ".norm2.gamma", co, &r.g2, mem, s));
+  WAN_TRY(pack_conv(wt, name + ".conv1", co, ci, 3, 3, 3, false, "", 0, r.c1, mem, s));
+  WAN_TRY(pack_conv(wt, name + ".conv2", co, co, 3, 3, 3, false, ci != co ? name + ".conv_shortcut" : "", ci, r.c2,
+                    mem, s));
+  return WAN_OK;
+}
+
+static wan_status model_build(const wan_tensor* weights, int n, int dtype, cudaStream_t s, wan_vae_model* m) {
+  if (!weights || n <= 0) return fail(WAN_ERR_INVALID_ARG, "empty weight table");
+  if (dtype != WAN_F32 && dtype != WAN_BF16) return fail(WAN_ERR_DTYPE, "dtype must be WAN_F32 or WAN_BF16, not %d", dtype);
+  if (dtype == WAN_F32) return fail(WAN_ERR_NOT_IMPLEMENTED, "the fp32 decode is not implemented in this build");
+  WeightTable wt{weights, n};
+  const wan_tensor* ci;
+  WAN_TRY(get_tensor(wt, "decoder.conv_in.weight", &ci));
+  if (ci->ndim != 5 || ci->shape[0] % 4 || ci->shape[0] <= 0)
+    return fail(WAN_ERR_SHAPE, "decoder.conv_in.weight must be [4b, 48, 3, 3, 3]");
+  const int b = (int)(ci->shape[0] / 4);
+  if (b % 8 || 4 * b > 1024)
+    return fail(WAN_ERR_UNSUPPORTED, "decoder base dim %d: must be a multiple of 8 and at most 256", b);
+  m->base = b;
+  m->dtype = dtype;
+  DevMem& mem = m->mem;
+  // post_quant_conv 48 -> 48 (fp32, CUDA-core kernel)
+  {
+    const wan_tensor *w, *bb;
+    WAN_TRY(get_tensor(wt, "post_quant_conv.weight", &w));
+    WAN_TRY(get_tensor(wt, "post_quant_conv.bias", &bb));
+    WAN_TRY(check_shape(w, {kZdim, kZdim, 1, 1, 1}));
+    WAN_TRY(check_shape(bb, {kZdim}));
+    if (!mem.dry) {
+    void* p;
+    WAN_TRY(mem.alloc(&p, kZdim * kZdim * sizeof(float)));
+    m->pq_w = (float*)p;
+    WAN_TRY(mem.alloc(&p, kZdim * sizeof(float)));
+    m->pq_b = (float*)p;
+    CUDA_TRY(launch_to_f32(w->data, w->dtype == WAN_F32, nullptr, 0, m->pq_w, kZdim * kZdim, 1.0f, 1, s));
+    CUDA_TRY(launch_to_f32(bb->data, bb->dtype == WAN_F32, nullptr, 0, m->pq_b, kZdim, 1.0f, 1, s));
+    }
+  }
+  const int c4 = 4 * b;
+  WAN_TRY(pack_conv(wt, "decoder.conv_in", c4, kZdim, 3, 3, 3, false, "", 0, m->conv_in, mem, s));
+  WAN_TRY(pack_resnet(wt, "decoder.mid_block.resnets.0", c4, c4, m->mid[0], mem, s));
+  WAN_TRY(pack_resnet(wt, "decoder.mid_block.resnets.1", c4, c4, m->mid[1], mem, s));
+  WAN_TRY(pack_gamma(wt, "decoder.mid_block.attentions.0.norm.gamma", c4, &m->attn_g, mem, s));
+  WAN_TRY(pack_conv(wt, "decoder.mid_block.attentions.0.to_qkv", 3 * c4, c4, 1, 1, 1, true, "", 0, m->qkv, mem, s));
+  WAN_TRY(pack_conv(wt, "decoder.mid_block.attentions.0.proj", c4, c4, 1, 1, 1, true, "", 0, m->proj, mem, s));
+  for (int i = 0; i < 4; ++i) {
+    const int cin = kUp[i][0] * b, cout = kUp[i][1] * b;
+    const std::string nm = "decoder.up_blocks." + std::to_string(i);
+    for (int j = 0; j < 3; ++j)
+      WAN_TRY(pack_resnet(wt, nm + ".resnets." + std::to_string(j), j == 0 ? cin : cout, cout, m->up[i][j], mem, s));
+    if (kUp[i][2])
+      WAN_TRY(pack_conv(wt, nm + ".upsampler.time_conv", 2 * cout, cout, 3, 1, 1, false, "", 0, m->tconv[i], mem, s));
+    if (kUp[i][3])
+      WAN_TRY(pack_conv(wt, nm + ".upsampler.resample.1", cout, cout, 1, 3, 3, true, "", 0, m->resample[i], mem, s));
+  }
+  WAN_TRY(pack_gamma(wt, "decoder.norm_out.gamma", b, &m->out_g, mem, s));
+  WAN_TRY(pack_conv(wt, "decoder.conv_out", 12, b, 3, 3, 3, false, "", 0, m->conv_out, mem, s));
+  if (!mem.dry) CUDA_TRY(cudaGetLastError());
+  return WAN_OK;
+}
+
+// Checks every name and shape first (no CUDA call), then packs.
+static wan_status model_build_checked(const wan_tensor* weights, int n, int dtype, cudaStream_t s, wan_vae_model* m) {
+  m->mem.dry = true;
+  const wan_status v = model_build(weights, n, dtype, s, m);
+  m->mem.dry = false;
+  if (v != WAN_OK) return v;
+  return model_build(weights, n, dtype, s, m);
+}
+
+// ======================================================================
+// Stream state: workspace, rings, launch sequence
+// ======================================================================
+struct AttnBufs {
+  Act an, qkv, O;
+  float* S = nullptr;
+  bf16* P = nullptr;
+  bf16* Vt = nullptr;
+  int HW = 0, HWs = 0, HWp = 0, Fmax = 0, B = 0, C = 0;
+  long long s_bs() const { return (long long)Fmax * HW * HWs; }
+  long long p_bs() const { return (long long)Fmax * HW * HWp; }
+  long long vt_fs() const { return (long long)C * HWp; }
+  long long vt_bs() const { return (long long)Fmax * vt_fs(); }
+};
+
+struct wan_vae_stream {
+  const wan_vae_model* m = nullptr;
+  int B = 0, h = 0, w = 0, nmax = 0;
+  bool first = true;
+  DevMem mem;
+  char* ws = nullptr;
+  size_t ws_bytes = 0, ws_used = 0;
+  int* err_dev = nullptr;
+  int* err_host = nullptr;
+  cudaEvent_t err_ev = nullptr;
+  bool err_pending = false;
+  // level A (h x w)
+  Act ringIn, RA[3], HA, ringA[10], tcA, tuA;
+  AttnBufs at;
+  // level B (2h x 2w)
+  Act upB, RB[3], HB, ringB[6], tcB, tuB;
+  // level C (4h x 4w)
+  Act upC, RC[3], HC, ringC[6];
+  // level D (8h x 8w)
+  Act upD, RD[3], HD, ringD[6], ringOut;
+  std::vector<Act*> rings;
+  std::vector<RingShift> shifts;
+};
+
+static wan_status ws_take(wan_vae_stream* st, size_t bytes, void** p) {
+  const size_t off = rup(st->ws_used, 256);
+  if (off + bytes > st->ws_bytes) return fail(WAN_ERR_INTERNAL, "workspace plan overflow");
+  *p = st->ws + off;
+  st->ws_used = off + bytes;
+  return WAN_OK;
+}
+
+// Declares (plan pass, ws == null) or places an activation tensor.
+static wan_status make_act(wan_vae_stream* st, Act& a, int F, int H, int W, int C, int ldc_mult = 64) {
+  a.B = st->B;
+  a.F = F;
+  a.H = H;
+  a.W = W;
+  a.C = C;
+  a.ldc = (int)rup(C, ldc_mult);
+  if (!st->ws) {
+    st->ws_used = rup(st->ws_used, 256) + a.bytes();
+    return WAN_OK;
+  }
+  void* p;
+  WAN_TRY(ws_take(st, a.bytes(), &p));
+  a.p = (bf16*)p;
+  return WAN_OK;
+}
+static wan_status make_raw(wan_vae_stream* st, size_t bytes, void** p) {
+  if (!st->ws) {
+    st->ws_used = rup(st->ws_used, 256) + bytes;
+    *p = nullptr;
+    return WAN_OK;
+  }
+  return ws_take(st, bytes, p);
+}
+
+static wan_status plan_buffers(wan_vae_stream* st) {
+  const int b = st->m->base, c4 = 4 * b, c2 = 2 * b, c1 = b, n = st->nmax;
+  const int hA = st->h, wA = st->w;
+  st->rings.clear();
+  auto ring = [&](Act& a, int F, int H, int W, int C) -> wan_status {
+    WAN_TRY(make_act(st, a, 2 + F, H, W, C));
+    st->rings.push_back(&a);
+    return WAN_OK;
+  };
+  // level A
+  WAN_TRY(ring(st->ringIn, n, hA, wA, kZdim));
+  for (auto& a : st->RA) WAN_TRY(make_act(st, a, n, hA, wA, c4));
+  WAN_TRY(make_act(st, st->HA, n, hA, wA, c4));
+  for (auto& a : st->ringA) WAN_TRY(ring(a, n, hA, wA, c4));
+  WAN_TRY(ring(st->tcA, n, hA, wA, c4));
+  WAN_TRY(make_act(st, st->tuA, 2 * n, hA, wA, c4));
+  // attention
+  AttnBufs& at = st->at;
+  at.HW = hA * wA;
+  at.HWs = (int)rup(at.HW, 16);
+  at.HWp = (int)rup(at.HW, 64);
+  at.Fmax = n;
+  at.B = st->B;
+  at.C = c4;
+  WAN_TRY(make_act(st, at.an, n, 1, at.HW, c4));
+  WAN_TRY(make_act(st, at.qkv, n, 1, at.HW, 3 * c4));
+  WAN_TRY(make_act(st, at.O, n, 1, at.HW, c4));
+  void* p;
+  WAN_TRY(make_raw(st, (size_t)st->B * at.s_bs() * sizeof(float), &p));
+  at.S = (float*)p;
+  WAN_TRY(make_raw(st, (size_t)st->B * at.p_bs() * sizeof(bf16), &p));
+  at.P = (bf16*)p;
+  WAN_TRY(make_raw(st, (size_t)st->B * at.vt_bs() * sizeof(bf16), &p));
+  at.Vt = (bf16*)p;
+  // level B
+  const int hB = 2 * hA, wB = 2 * wA;
+  WAN_TRY(make_act(st, st->upB, 2 * n, hB, wB, c4));
+  for (auto& a : st->RB) WAN_TRY(make_act(st, a, 2 * n, hB, wB, c4));
+  WAN_TRY(make_act(st, st->HB, 2 * n, hB, wB, c4));
+  for (auto& a : st->ringB) WAN_TRY(ring(a, 2 * n, hB, wB, c4));
+  WAN_TRY(ring(st->tcB, 2 * n, hB, wB, c4));
+  WAN_TRY(make_act(st, st->tuB, 4 * n, hB, wB, c4));
+  // level C
+  const int hC = 4 * hA, wC = 4 * wA;
+  WAN_TRY(make_act(st, st->upC, 4 * n, hC, wC, c4));
+  WAN_TRY(make_act(st, st->RC[0], 4 * n, hC, wC, c4));
+  WAN_TRY(make_act(st, st->RC[1], 4 * n, hC, wC, c2));
+  WAN_TRY(make_act(st, st->RC[2], 4 * n, hC, wC, c2));
+  WAN_TRY(make_act(st, st->HC, 4 * n, hC, wC, c2));
+  WAN_TRY(ring(st->ringC[0], 4 * n, hC, wC, c4));
+  for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringC[i], 4 * n, hC, wC, c2));
+  // level D
+  const int hD = 8 * hA, wD = 8 * wA;
+  WAN_TRY(make_act(st, st->upD, 4 * n, hD, wD, c2));
+  WAN_TRY(make_act(st, st->RD[0], 4 * n, hD, wD, c2));
+  WAN_TRY(make_act(st, st->RD[1], 4 * n, hD, wD, c1));
+  WAN_TRY(make_act(st, st->RD[2], 4 * n, hD, wD, c1));
+  WAN_TRY(make_act(st, st->HD, 4 * n, hD, wD, c1));
+  WAN_TRY(ring(st->ringD[0], 4 * n, hD, wD, c2));
+  for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringD[i], 4 * n, hD, wD, c1));
+  WAN_TRY(ring(st->ringOut, 4 * n, hD, wD, c1));
+  return WAN_OK;
+}
+
+// ------------------------------------------------------------ conv launches
+struct OutSpec {
+  void* p = nullptr;
+  int f32 = 0;
+  long long bs = 0, fs = 0;
+  int ldc = 0, f0 = 0, fmul = 1, interleave = 0;
+};
+static OutSpec out_of(const Act& a, int f0 = 0) {
+  OutSpec o;
+  o.p = a.p;
+  o.bs = a.bs();
+  o.fs = a.fs();
+  o.ldc = a.ldc;
+  o.f0 = f0;
+  return o;
+}
+
+// Fills the launch for conv `cw` reading A source 0 (`a0`, output frame 0 at
+// frame coordinate a0_f0 for dt = 0) and optionally the shortcut source a1.
+static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Act* a1, int a1_f0, int F, ConvLaunch& L) {
+  memset(&L, 0, sizeof(L));
+  ConvArgs& A = L.args;
+  if (a0.ldc < cw.ci_pad || (a1 && a1->ldc < cw.sc_ci_pad))
+    return fail(WAN_ERR_INTERNAL, "conv source narrower than its packed channels");
+  WAN_TRY(act_map(&L.a0, a0));
+  if (a1)
+    WAN_TRY(act_map(&L.a1, *a1));
+  else
+    L.a1 = L.a0;
+  WAN_TRY(b_map(&L.b, cw.w, cw.ktot, cw.co_pad, 1, cw.ktot, (long long)cw.ktot * cw.co_pad, cw.bn));
+  int nt = 0, k = 0;
+  for (int dt = 0; dt < cw.kt; ++dt)
+    for (int dy = 0; dy < cw.kh; ++dy)
+      for (int dx = 0; dx < cw.kw; ++dx) {
+        ConvTap& t = A.taps[nt++];
+        t.src = 0;
+        t.dt = (int8_t)dt;
+        t.dy = (int8_t)(dy - cw.kh / 2);
+        t.dx = (int8_t)(dx - cw.kw / 2);
+        t.a_c0 = 0;
+        t.nkb = (int16_t)(cw.ci_pad / 64);
+        t.b_k0 = k;
+        k += cw.ci_pad;
+      }
+  if (cw.sc_ci_pad) {
+    if (!a1) return fail(WAN_ERR_INTERNAL, "shortcut conv without its source");
+    ConvTap& t = A.taps[nt++];
+    t.src = 1;
+    t.dt = 0;
+    t.dy = t.dx = 0;
+    t.a_c0 = 0;
+    t.nkb = (int16_t)(cw.sc_ci_pad / 64);
+    t.b_k0 = k;
+    k += cw.sc_ci_pad;
+  }
+  A.n_taps = nt;
+  A.total_kb = k / 64;
+  A.box_w = 16;
+  A.box_h = 8;
+  A.H = a0.H;
+  A.W = a0.W;
+  A.tiles_x = (int)cdiv(a0.W, 16);
+  A.tiles_y = (int)cdiv(a0.H, 8);
+  A.tiles_n = cw.co_pad / cw.bn;
+  A.frames = F;
+  A.batches = a0.B;
+  A.src_f0[0] = a0_f0;
+  A.src_f0[1] = a1_f0;
+  A.N = cw.Co;
+  A.bias = cw.bias;
+  L.bn = cw.bn;
+  L.epi = kEpiStore;
+  return WAN_OK;
+}
+
+static void set_out(ConvArgs& A, const OutSpec& o) {
+  A.out = o.p;
+  A.out_f32 = o.f32;
+  A.out_bs = o.bs;
+  A.out_fs = o.fs;
+  A.out_ldc = o.ldc;
+  A.out_f0 = o.f0;
+  A.out_fmul = o.fmul;
+  A.interleave_c = o.interleave;
+}
+
+static wan_status run(ConvLaunch& L, int* err, cudaStream_t s) {
+  L.args.err = err;
+  if (L.args.N % 16 && L.epi != kEpiVideo) return fail(WAN_ERR_INTERNAL, "conv output channels not a multiple of 16");
+  CUDA_TRY(launch_conv(L, s));
+  return WAN_OK;
+}
+
+// 3-frame causal conv over ring `in` (F current frames) into `out`.
+static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F, const OutSpec& o, const Act* res,
+                            const Act* sc, cudaStream_t s) {
+  ConvLaunch L;
+  WAN_TRY(conv_setup(cw, in, 0, sc, 0, F, L));
+  set_out(L.args, o);
+  if (res) {
+    L.args.res = res->p;
+    L.args.res_bs = res->bs();
+    L.args.res_fs = res->fs();
+    L.args.res_ldc = res->ldc;
+  }
+  WAN_TRY(run(L, st->err_dev, s));
+  st->shifts.push_back(RingShift{in.p, in.fs(), in.bs(), F, in.B});
+  return WAN_OK;
+}
+
+// Residual block: x (F frames) -> y.
+static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act& ring1, Act& ring2, Act& Ht, Act& y,
+                         int F, cudaStream_t s) {
+  const int P = x.H * x.W;
+  CUDA_TRY(launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s));
+  WAN_TRY(ring_conv(st, r.c1, ring1, F, out_of(Ht), nullptr, nullptr, s));
+  CUDA_TRY(launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s));
+  if (r.ci != r.co)
+    WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), nullptr, &x, s));
+  else
+    WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), &x, nullptr, s));
+  return WAN_OK;
+}
+
+// Plain batched GEMM launch: A = activation rows (HW positions per frame), B = `bmap`.
+static wan_status gemm_setup(ConvLaunch& L, const bf16* a_base, int a_C, int a_ldc, int HW, int Fmax, int B,
+                             long long a_fs, long long a_bs, int K, int N_tiles_n, int bn, int F) {
+  memset(&L.args, 0, sizeof(L.args));
+  WAN_TRY(act_map(&L.a0, a_base, a_C, a_ldc, HW, 1, Fmax, B, a_fs, a_bs, 128, 1));
+  L.a1 = L.a0;
+  ConvArgs& A = L.args;
+  ConvTap& t = A.taps[0];
+  t.src = 0;
+  t.dt = 0;
+  t.dy = t.dx = 0;
+  t.a_c0 = 0;
+  t.nkb = (int16_t)(K / 64);
+  t.b_k0 = 0;
+  A.n_taps = 1;
+  A.total_kb = K / 64;
+  A.box_w = 128;
+  A.box_h = 1;
+  A.H = 1;
+  A.W = HW;
+  A.tiles_x = (int)cdiv(HW, 128);
+  A.tiles_y = 1;
+  A.tiles_n = N_tiles_n;
+  A.frames = F;
+  A.batches = B;
+  L.bn = bn;
+  L.epi = kEpiStore;
+  return WAN_OK;
+}
+
+// Mid-block attention over F frames of x (level A) into y = attn(x) + x.
+static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj, AttnBufs& at, const Act& x, Act& y,
+                            int F, int* err, cudaStream_t s) {
+  const int C = at.C, HW = at.HW, B = at.B;
+  if (HW < 16) return fail(WAN_ERR_UNSUPPORTED, "attention over %d positions (at least 16 supported)", HW);
+  // n = RMS norm of x (no SiLU), rows = positions
+  CUDA_TRY(launch_rms_norm(x.view(0), at.an.view(0), g, C, B, F, HW, false, s));
+  ConvLaunch L;
+  // qkv = n @ Wqkv^T + b
+  WAN_TRY(gemm_setup(L, at.an.p, at.an.ldc, at.an.ldc, HW, at.an.F, B, at.an.fs(), at.an.bs(), qkv.ci_pad,
+                     qkv.co_pad / qkv.bn, qkv.bn, F));
+  WAN_TRY(b_map(&L.b, qkv.w, qkv.ktot, qkv.co_pad, 1, qkv.ktot, (long long)qkv.ktot * qkv.co_pad, qkv.bn));
+  L.args.N = qkv.Co;
+  L.args.bias = qkv.bias;
+  set_out(L.args, out_of(at.qkv));
+  WAN_TRY(run(L, err, s));
+  // S = q k^T per frame (fp32)
+  int bnS = 16;  // largest power of two <= min(HW, 256): the K-operand box stays inside the tensor
+  while (bnS * 2 <= std::min(HW, 256)) bnS *= 2;
+  WAN_TRY(gemm_setup(L, at.qkv.p, C, at.qkv.ldc, HW, at.qkv.F, B, at.qkv.fs(), at.qkv.bs(), C,
+                     (int)cdiv(at.HWs, bnS), bnS, F));
+  WAN_TRY(b_map(&L.b, at.qkv.p + C, C, HW, (long long)B * at.Fmax, at.qkv.ldc, at.qkv.fs(), bnS));
+  L.args.b_per_frame = 1;
+  L.args.b_gstride = at.Fmax;
+  L.args.N = at.HWs;
+  {
+    OutSpec o;
+    o.p = at.S;
+    o.f32 = 1;
+    o.bs = at.s_bs();
+    o.fs = (long long)HW * at.HWs;
+    o.ldc = at.HWs;
+    set_out(L.args, o);
+  }
+  WAN_TRY(run(L, err, s));
+  // P = softmax(S / sqrt(C)), V^T
+  const float scale = 1.0f / std::sqrt((float)C);
+  for (int b = 0; b < B; ++b) {
+    CUDA_TRY(launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.HWp, HW, (long long)F * HW,
+                                 scale, s));
+    CUDA_TRY(launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C, at.qkv.fs(), at.qkv.ldc, at.Vt + b * at.vt_bs(),
+                              at.vt_fs(), at.HWp, F, HW, C, s));
+  }
+  // O = P V per frame
+  const int bnC = choose_bn(C);
+  WAN_TRY(gemm_setup(L, at.P, at.HWp, at.HWp, HW, at.Fmax, B, (long long)HW * at.HWp, at.p_bs(), at.HWp,
+                     (int)cdiv(C, bnC), bnC, F));
+  WAN_TRY(b_map(&L.b, at.Vt, at.HWp, C, (long long)B * at.Fmax, at.HWp, at.vt_fs(), bnC));
+  L.args.b_per_frame = 1;
+  L.args.b_gstride = at.Fmax;
+  L.args.N = C;
+  set_out(L.args, out_of(at.O));
+  WAN_TRY(run(L, err, s));
+  // y = O Wp^T + b + x
+  WAN_TRY(gemm_setup(L, at.O.p, at.O.ldc, at.O.ldc, HW, at.O.F, B, at.O.fs(), at.O.bs(), proj.ci_pad,
+                     proj.co_pad / proj.bn, proj.bn, F));
+  WAN_TRY(b_map(&L.b, proj.w, proj.ktot, proj.co_pad, 1, proj.ktot, (long long)proj.ktot * proj.co_pad, proj.bn));
+  L.args.N = proj.Co;
+  L.args.bias = proj.bias;
+  OutSpec o = out_of(y);
+  set_out(L.args, o);
+  L.args.res = x.p;
+  L.args.res_bs = x.bs();
+  L.args.res_fs = x.fs();
+  L.args.res_ldc = x.ldc;
+  WAN_TRY(run(L, err, s));
+  return WAN_OK;
+}
+
+// ---------------------------------------------------------------- the chunk
+static wan_status copy_frames(const Act& src, int sf0, const Act& dst, int df0, int F, cudaStream_t s) {
+  CUDA_TRY(launch_copy_frames(src.view(sf0), dst.view(df0), src.C, src.B, F, src.H * src.W, s));
+  return WAN_OK;
+}
+
+// upsample3d's time conv (page "The parts", fifth bullet; "The first latent
+// frame yields one frame"): x has Fin frames; tu receives 2*Fin frames, or
+// 2*Fin - 1 on the first chunk, whose first frame passes through.
+static wan_status time_upsample(wan_vae_stream* st, const ConvW& tc, const Act& x, Act& ring, Act& tu, int Fin,
+                                bool first, cudaStream_t s) {
+  const int C = x.C;
+  int fx0 = 0, fout0 = 0, Ft = Fin;
+  if (first) {
+    WAN_TRY(copy_frames(x, 0, tu, 0, 1, s));
+    fx0 = 1;
+    fout0 = 1;
+    Ft = Fin - 1;
+  }
+  if (Ft <= 0) return WAN_OK;
+  WAN_TRY(copy_frames(x, fx0, ring, 2, Ft, s));
+  OutSpec o = out_of(tu, fout0);
+  o.fmul = 2;
+  o.interleave = C;
+  return ring_conv(st, tc, ring, Ft, o, nullptr, nullptr, s);
+}
+
+// upsample2d's 3x3 conv on the nearest-x2 input `up` (F frames) plus DupUp3D
+// of the up block's input `blk` (page "The parts", fifth and sixth bullets).
+static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& up, const Act& blk, int ft, bool first,
+                           Act& y, int F, cudaStream_t s) {
+  ConvLaunch L;
+  WAN_TRY(conv_setup(cw, up, 0, nullptr, 0, F, L));
+  set_out(L.args, out_of(y));
+  L.epi = kEpiDup;
+  L.args.dup = blk.p;
+  L.args.dup_bs = blk.bs();
+  L.args.dup_fs = blk.fs();
+  L.args.dup_ldc = blk.ldc;
+  L.args.dup_W = blk.W;
+  L.args.dup_ft = ft;
+  L.args.dup_first = first ? 1 : 0;
+  // r = out * ft * 4 / in: 4ft means channel c copies source channel c; r = 2
+  // (ft = 1, in = 2 out) means source channel 2c + row parity.
+  const int r = cw.Co * ft * 4 / blk.C;
+  if (r == 4 * ft && blk.C == cw.Co)
+    L.args.dup_pairs = 0;
+  else if (ft == 1 && r == 2 && blk.C == 2 * cw.Co)
+    L.args.dup_pairs = 1;
+  else
+    return fail(WAN_ERR_UNSUPPORTED, "DupUp3D with %d -> %d channels, ft %d", blk.C, cw.Co, ft);
+  return run(L, st->err_dev, s);
+}
+
+static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long long Tz, long long t0, int n, void* out,
+                            int out_f32, long long out_frames, long long out_f0, float* pre, cudaStream_t s) {
+  const wan_vae_model* m = st->m;
+  const bool first = st->first;
+  const int FA = n, FB = first ? 2 * n - 1 : 2 * n, FC = first ? 4 * n - 3 : 4 * n;
+  const int P = st->h * st->w;
+  st->shifts.clear();
+  // 1. post_quant_conv into conv_in's ring
+  CUDA_TRY(launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, st->ringIn.view(2), 1, s));
+  // 2. conv_in, mid block
+  WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s));
+  WAN_TRY(resnet(st, m->mid[0], st->RA[0], st->ringA[0], st->ringA[1], st->HA, st->RA[1], FA, s));
+  WAN_TRY(attention(m->attn_g, m->qkv, m->proj, st->at, st->RA[1], st->RA[2], FA, st->err_dev, s));
+  WAN_TRY(resnet(st, m->mid[1], st->RA[2], st->ringA[2], st->ringA[3], st->HA, st->RA[0], FA, s));
+  // up block 0 (level A -> B); block input RA[0]
+  WAN_TRY(resnet(st, m->up[0][0], st->RA[0], st->ringA[4], st->ringA[5], st->HA, st->RA[1], FA, s));
+  WAN_TRY(resnet(st, m->up[0][1], st->RA[1], st->ringA[6], st->ringA[7], st->HA, st->RA[2], FA, s));
+  WAN_TRY(resnet(st, m->up[0][2], st->RA[2], st->ringA[8], st->ringA[9], st->HA, st->RA[1], FA, s));
+  WAN_TRY(time_upsample(st, m->tconv[0], st->RA[1], st->tcA, st->tuA, FA, first, s));
+  CUDA_TRY(launch_upsample2x(st->tuA.view(0), st->upB.view(0), st->tuA.C, st->B, FB, st->tuA.H, st->tuA.W, s));
+  WAN_TRY(resample(st, m->resample[0], st->upB, st->RA[0], 2, first, st->RB[0], FB, s));
+  // up block 1 (level B -> C); block input RB[0]
+  WAN_TRY(resnet(st, m->up[1][0], st->RB[0], st->ringB[0], st->ringB[1], st->HB, st->RB[1], FB, s));
+  WAN_TRY(resnet(st, m->up[1][1], st->RB[1], st->ringB[2], st->ringB[3], st->HB, st->RB[2], FB, s));
+  WAN_TRY(resnet(st, m->up[1][2], st->RB[2], st->ringB[4], st->ringB[5], st->HB, st->RB[1], FB, s));
+  WAN_TRY(time_upsample(st, m->tconv[1], st->RB[1], st->tcB, st->tuB, FB, first, s));
+  CUDA_TRY(launch_upsample2x(st->tuB.view(0), st->upC.view(0), st->tuB.C, st->B, FC, st->tuB.H, st->tuB.W, s));
+  WAN_TRY(resample(st, m->resample[1], st->upC, st->RB[0], 2, first, st->RC[0], FC, s));
+  // up block 2 (level C -> D); block input RC[0]
+  WAN_TRY(resnet(st, m->up[2][0], st->RC[0], st->ringC[0], st->ringC[1], st->HC, st->RC[1], FC, s));
+  WAN_TRY(resnet(st, m->up[2][1], st->RC[1], st->ringC[2], st->ringC[3], st->HC, st->RC[2], FC, s));
+  WAN_TRY(resnet(st, m->up[2][2], st->RC[2], st->ringC[4], st->ringC[5], st->HC, st->RC[1], FC, s));
+  CUDA_TRY(launch_upsample2x(st->RC[1].view(0), st->upD.view(0), st->RC[1].C, st->B, FC, st->RC[1].H, st->RC[1].W, s));
+  WAN_TRY(resample(st, m->resample[2], st->upD, st->RC[0], 1, first, st->RD[0], FC, s));
+  // up block 3 (level D)
+  WAN_TRY(resnet(st, m->up[3][0], st->RD[0], st->ringD[0], st->ringD[1], st->HD, st->RD[1], FC, s));
+  WAN_TRY(resnet(st, m->up[3][1], st->RD[1], st->ringD[2], st->ringD[3], st->HD, st->RD[2], FC, s));
+  WAN_TRY(resnet(st, m->up[3][2], st->RD[2], st->ringD[4], st->ringD[5], st->HD, st->RD[1], FC, s));
+  // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
+  CUDA_TRY(launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
+                           st->RD[1].H * st->RD[1].W, true, s));
+  {
+    ConvLaunch L;
+    WAN_TRY(conv_setup(m->conv_out, st->ringOut, 0, nullptr, 0, FC, L));
+    L.epi = kEpiVideo;
+    L.args.out = out;
+    L.args.out_f32 = out_f32;
+    L.args.out_f0 = (int)out_f0;
+    L.args.preclamp = pre;
+    L.args.vid_cs = out_frames * 4LL * st->ringOut.H * st->ringOut.W;
+    L.args.vid_bs = 3 * L.args.vid_cs;
+    WAN_TRY(run(L, st->err_dev, s));
+    st->shifts.push_back(RingShift{st->ringOut.p, st->ringOut.fs(), st->ringOut.bs(), FC, st->B});
+  }
+  // 3. the causal caches: each ring keeps the last two frames it convolved
+  CUDA_TRY(launch_ring_shift(st->shifts.data(), (int)st->shifts.size(), s));
+  st->first = false;
+  if (st->err_host) {
+    CUDA_TRY(cudaMemcpyAsync(st->err_host, st->err_dev, sizeof(int), cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaEventRecord(st->err_ev, s));
+    st->err_pending = true;
+  }
+  return WAN_OK;
+}
+
+static wan_status stream_build(const wan_vae_model* m, int B, int h, int w, int nmax, bool async, cudaStream_t s,
+                               wan_vae_stream* st) {
+  st->m = m;
+  st->B = B;
+  st->h = h;
+  st->w = w;
+  st->nmax = nmax;
+  st->mem.use_async = async;
+  st->mem.async = s;
+  st->ws = nullptr;
+  st->ws_used = 0;
+  WAN_TRY(plan_buffers(st));
+  st->ws_bytes = rup(st->ws_used, 256) + 256;
+  void* p;
+  WAN_TRY(st->mem.alloc(&p, st->ws_bytes));
+  st->ws = (char*)p;
+  st->ws_used = 0;
+  WAN_TRY(plan_buffers(st));
+  WAN_TRY(st->mem.alloc(&p, 256));
+  st->err_dev = (int*)p;
+  if (async) {
+    CUDA_TRY(cudaMemsetAsync(st->ws, 0, st->ws_bytes, s));
+    CUDA_TRY(cudaMemsetAsync(st->err_dev, 0, 256, s));
+  } else {
+    CUDA_TRY(cudaMemset(st->ws, 0, st->ws_bytes));
+    CUDA_TRY(cudaMemset(st->err_dev, 0, 256));
+    CUDA_TRY(cudaMallocHost((void**)&st->err_host, sizeof(int)));
+    *st->err_host = 0;
+    CUDA_TRY(cudaEventCreateWithFlags(&st->err_ev, cudaEventDisableTiming));
+    CUDA_TRY(cudaDeviceSynchronize());
+  }
+  st->first = true;
+  return WAN_OK;
+}
+
+static void stream_free(wan_vae_stream* st) {
+  if (!st) return;
+  if (!st->mem.use_async) cudaDeviceSynchronize();
+  st->mem.release();
+  if (st->err_host) cudaFreeHost(st->err_host);
+  if (st->err_ev) cudaEventDestroy(st->err_ev);
+  delete st;
+}
+
+static wan_status check_pending_error(wan_vae_stream* st, bool block) {
+  if (!st->err_pending) return WAN_OK;
+  if (block) {
+    CUDA_TRY(cudaEventSynchronize(st->err_ev));
+  } else {
+    const cudaError_t q = cudaEventQuery(st->err_ev);
+    if (q == cudaErrorNotReady) return WAN_OK;
+    if (q != cudaSuccess) return fail(WAN_ERR_CUDA, "earlier decode failed: %s", cudaGetErrorString(q));
+  }
+  st->err_pending = false;
+  if (*st->err_host != 0)
+    return fail(WAN_ERR_INTERNAL, "a decode kernel reported error %d (a bounded wait expired)", *st->err_host);
+  return WAN_OK;
+}
+
+static wan_status dtype_ok(int d, const char* what) {
+  if (d != WAN_F32 && d != WAN_BF16) return fail(WAN_ERR_DTYPE, "%s: dtype must be WAN_F32 or WAN_BF16, not %d", what, d);
+  return WAN_OK;
+}
+
+static wan_status decode_chunk_impl(wan_vae_stream* st, const void* z, int z_dtype, long long z_frames, long long t0,
+                                    int n, void* out, int out_dtype, long long out_frames, long long out_f0,
+                                    float* pre, cudaStream_t s) {
+  if (!st) return fail(WAN_ERR_INVALID_ARG, "null stream state");
+  if (!z || !out) return fail(WAN_ERR_INVALID_ARG, "null latents or output");
+  WAN_TRY(dtype_ok(z_dtype, "latents"));
+  WAN_TRY(dtype_ok(out_dtype, "output"));
+  if (n < 1 || n > st->nmax) return fail(WAN_ERR_INVALID_ARG, "chunk of %d frames (1..%d allowed)", n, st->nmax);
+  if (t0 < 0 || t0 + n > z_frames) return fail(WAN_ERR_INVALID_ARG, "frames %lld..%lld outside z", t0, t0 + n - 1);
+  const long long nf = st->first ? 4LL * n - 3 : 4LL * n;
+  if (out_f0 < 0 || out_f0 + nf > out_frames)
+    return fail(WAN_ERR_INVALID_ARG, "output frames %lld..%lld outside out (%lld frames)", out_f0, out_f0 + nf - 1,
+                out_frames);
+  WAN_TRY(check_pending_error(st, false));
+  return run_chunk(st, z, z_dtype == WAN_F32, z_frames, t0, n, out, out_dtype == WAN_F32, out_frames, out_f0, pre, s);
+}
+
+static wan_status reset_impl(wan_vae_stream* st, cudaStream_t s) {
+  for (Act* r : st->rings)
+    for (int b = 0; b < r->B; ++b) CUDA_TRY(cudaMemsetAsync(r->p + b * r->bs(), 0, 2 * r->fs() * sizeof(bf16), s));
+  st->first = true;
+  return WAN_OK;
+}
+
+static wan_status clip_impl(wan_vae_stream* st, const void* z, int z_dtype, int T, void* out, int out_dtype,
+                            float* pre, cudaStream_t s) {
+  if (!st) return fail(WAN_ERR_INVALID_ARG, "null stream state");
+  if (T < 1) return fail(WAN_ERR_INVALID_ARG, "T = %d", T);
+  WAN_TRY(reset_impl(st, s));
+  const long long F = 4LL * T - 3;
+  long long f0 = 0;
+  for (int t0 = 0; t0 < T;) {
+    const int n = std::min(st->nmax, T - t0);
+    WAN_TRY(decode_chunk_impl(st, z, z_dtype, T, t0, n, out, out_dtype, F, f0, pre, s));
+    f0 += (t0 == 0) ? 4LL * n - 3 : 4LL * n;
+    t0 += n;
+  }
+  return WAN_OK;
+}
+
+// ------------------------------------------------------------- C ABI
+#define API_GUARD(...)                                               \
+  try {                                                              \
+    __VA_ARGS__                                                      \
+  } catch (const std::bad_alloc&) {                                  \
+    return fail(WAN_ERR_OOM, "host allocation failed");              \
+  } catch (...) {                                                    \
+    return fail(WAN_ERR_INTERNAL, "unexpected C++ exception");       \
+  }
+
+extern "C" {
+
+int64_t wan_vae_out_frames(int64_t T) { return T >= 1 ? 4 * T - 3 : 0; }
+
+const char* wan_vae_last_error(void) { return g_last_error.c_str(); }
+
+const char* wan_vae_status_string(int32_t s) {
+  switch (s) {
+    case WAN_OK: return "WAN_OK";
+    case WAN_ERR_INVALID_ARG: return "WAN_ERR_INVALID_ARG";
+    case WAN_ERR_DTYPE: return "WAN_ERR_DTYPE";
+    case WAN_ERR_MISSING_WEIGHT: return "WAN_ERR_MISSING_WEIGHT";
+    case WAN_ERR_SHAPE: return "WAN_ERR_SHAPE";
+    case WAN_ERR_UNSUPPORTED: return "WAN_ERR_UNSUPPORTED";
+    case WAN_ERR_OOM: return "WAN_ERR_OOM";
+    case WAN_ERR_CUDA: return "WAN_ERR_CUDA";
+    case WAN_ERR_STATE: return "WAN_ERR_STATE";
+    case WAN_ERR_INTERNAL: return "WAN_ERR_INTERNAL";
+    case WAN_ERR_NOT_IMPLEMENTED: return "WAN_ERR_NOT_IMPLEMENTED";
+  }
+  return "unknown status";
+}
+
+wan_status wan_vae_model_create(const wan_tensor* weights, int32_t n_weights, int32_t dtype, wan_cuda_stream stream,
+                                wan_vae_model** model) {
+  API_GUARD({
+    if (!model) return fail(WAN_ERR_INVALID_ARG, "null model output pointer");
+    *model = nullptr;
+    wan_vae_model* m = new wan_vae_model();
+    const wan_status st = model_build_checked(weights, n_weights, dtype, (cudaStream_t)stream, m);
+    if (st != WAN_OK) {
+      if (!m->mem.ptrs.empty()) cudaStreamSynchronize((cudaStream_t)stream);
+      m->mem.release();
+      delete m;
+      return st;
+    }
+    *model = m;
+    return WAN_OK;
+  })
+}
+
+void wan_vae_model_destroy(wan_vae_model* model) {
+  if (!model) return;
+  cudaDeviceSynchronize();
+  model->mem.release();
+  delete model;
+}
+
+int32_t wan_vae_model_base_dim(const wan_vae_model* model) { return model ? model->base : -1; }
+
+wan_status wan_vae_stream_create(const wan_vae_model* model, int32_t B, int32_t h, int32_t w, int32_t max_chunk,
+                                 wan_vae_stream** out) {
+  API_GUARD({
+    if (!out) return fail(WAN_ERR_INVALID_ARG, "null stream output pointer");
+    *out = nullptr;
+    if (!model) return fail(WAN_ERR_INVALID_ARG, "null model");
+    if (B < 1 || h < 1 || w < 1 || max_chunk < 1)
+      return fail(WAN_ERR_INVALID_ARG, "B=%d h=%d w=%d max_chunk=%d must be positive", B, h, w, max_chunk);
+    if ((long long)8 * h > 65535 || (long long)8 * w > 65535 || max_chunk > 64 || B > 64)
+      return fail(WAN_ERR_UNSUPPORTED, "latent %dx%d, batch %d, chunk %d too large", h, w, B, max_chunk);
+    wan_vae_stream* st = new wan_vae_stream();
+    const wan_status s = stream_build(model, B, h, w, max_chunk, false, nullptr, st);
+    if (s != WAN_OK) {
+      stream_free(st);
+      return s;
+    }
+    *out = st;
+    return WAN_OK;
+  })
+}
+
+wan_status wan_vae_stream_reset(wan_vae_stream* st, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!st) return fail(WAN_ERR_INVALID_ARG, "null stream state");
+    return reset_impl(st, (cudaStream_t)stream);
+  })
+}
+
+void wan_vae_stream_destroy(wan_vae_stream* st) { stream_free(st); }
+
+int64_t wan_vae_stream_workspace_bytes(const wan_vae_stream* st) { return st ? (int64_t)st->ws_bytes : 0; }
+
+wan_status wan_vae_stream_sync_status(wan_vae_stream* st, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!st) return fail(WAN_ERR_INVALID_ARG, "null stream state");
+    CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+    CUDA_TRY(cudaGetLastError());
+    return check_pending_error(st, true);
+  })
+}
+
+wan_status wan_vae_decode_chunk(wan_vae_stream* st, const void* z, int32_t z_dtype, int64_t z_frames, int64_t t0,
+                                int32_t n, void* out, int32_t out_dtype, int64_t out_frames, int64_t out_f0,
+                                float* preclamp, wan_cuda_stream stream) {
+  API_GUARD({
+    return decode_chunk_impl(st, z, z_dtype, z_frames, t0, n, out, out_dtype, out_frames, out_f0, preclamp,
+                             (cudaStream_t)stream);
+  })
+}
+
+wan_status wan_vae_decode_clip(wan_vae_stream* st, const void* z, int32_t z_dtype, int32_t T, void* out,
+                               int32_t out_dtype, float* preclamp, wan_cuda_stream stream) {
+  API_GUARD({ return clip_impl(st, z, z_dtype, T, out, out_dtype, preclamp, (cudaStream_t)stream); })
+}
+
+wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int32_t z_dtype, int32_t T,
+                                    void* out_host, int32_t out_dtype, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!st || !z_host || !out_host) return fail(WAN_ERR_INVALID_ARG, "null argument");
+    WAN_TRY(dtype_ok(z_dtype, "latents"));
+    WAN_TRY(dtype_ok(out_dtype, "output"));
+    if (T < 1) return fail(WAN_ERR_INVALID_ARG, "T = %d", T);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t zes = z_dtype == WAN_F32 ? 4 : 2, oes = out_dtype == WAN_F32 ? 4 : 2;
+    const long long P = (long long)st->h * st->w, HW = 256LL * P;
+    const int n = st->nmax;
+    const long long nfmax = 4LL * n;
+    // staging: two latent chunks and two video chunks (allocated once per stream)
+    static_assert(sizeof(void*) == 8, "");
+    void *zb[2], *vb[2];
+    for (int k = 0; k < 2; ++k) {
+      WAN_TRY(st->mem.alloc(&zb[k], (size_t)st->B * kZdim * n * P * zes));
+      WAN_TRY(st->mem.alloc(&vb[k], (size_t)st->B * 3 * nfmax * HW * oes));
+    }
+    cudaStream_t cs;
+    cudaEvent_t dec_ev[2], d2h_ev[2];
+    CUDA_TRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    for (int k = 0; k < 2; ++k) {
+      CUDA_TRY(cudaEventCreateWithFlags(&dec_ev[k], cudaEventDisableTiming));
+      CUDA_TRY(cudaEventCreateWithFlags(&d2h_ev[k], cudaEventDisableTiming));
+    }
+    wan_status result = reset_impl(st, s);
+    const long long F = 4LL * T - 3;
+    long long f0 = 0;
+    int i = 0;
+    for (int t0 = 0; t0 < T && result == WAN_OK; ++i) {
+      const int k = i & 1;
+      const int nn = std::min(n, T - t0);
+      const long long nf = t0 == 0 ? 4LL * nn - 3 : 4LL * nn;
+      if (i >= 2 && cudaStreamWaitEvent(s, d2h_ev[k], 0) != cudaSuccess) {
+        result = fail(WAN_ERR_CUDA, "cudaStreamWaitEvent failed");
+        break;
+      }
+      // latents of this chunk: rows (b, c) of nn*P values
+      if (cudaMemcpy2DAsync(zb[k], nn * P * zes, (const char*)z_host + t0 * P * zes, (size_t)T * P * zes,
+                            nn * P * zes, (size_t)st->B * kZdim, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        result = fail(WAN_ERR_CUDA, "latent upload failed");
+        break;
+      }
+      result = decode_chunk_impl(st, zb[k], z_dtype, nn, 0, nn, vb[k], out_dtype, nfmax, 0, nullptr, s);
+      if (result != WAN_OK) break;
+      if (cudaEventRecord(dec_ev[k], s) != cudaSuccess || cudaStreamWaitEvent(cs, dec_ev[k], 0) != cudaSuccess ||
+          cudaMemcpy2DAsync((char*)out_host + f0 * HW * oes, (size_t)F * HW * oes, vb[k], nfmax * HW * oes,
+                            nf * HW * oes, (size_t)st->B * 3, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+          cudaEventRecord(d2h_ev[k], cs) != cudaSuccess) {
+        result = fail(WAN_ERR_CUDA, "video download failed");
+        break;
+      }
+      f0 += nf;
+      t0 += nn;
+    }
+    cudaStreamSynchronize(cs);
+    cudaStreamSynchronize(s);
+    for (int k = 0; k < 2; ++k) {
+      cudaEventDestroy(dec_ev[k]);
+      cudaEventDestroy(d2h_ev[k]);
+    }
+    cudaStreamDestroy(cs);
+    // release the staging buffers
+    for (int k = 0; k < 2; ++k) {
+      for (void** pp : {&zb[k], &vb[k]}) {
+        auto it = std::find(st->mem.ptrs.begin(), st->mem.ptrs.end(), *pp);
+        if (it != st->mem.ptrs.end()) st->mem.ptrs.erase(it);
+        cudaFree(*pp);
+      }
+    }
+    if (result != WAN_OK) return result;
+    return check_pending_error(st, true);
+  })
+}
+
+wan_status wan_vae_decode(const void* z, int32_t z_dtype, int32_t B, int32_t T, int32_t h, int32_t w,
+                          const wan_tensor* weights, int32_t n_weights, void* out, int32_t dtype,
+                          wan_cuda_stream stream) {
+  API_GUARD({
+    WAN_TRY(dtype_ok(dtype, "decode"));
+    WAN_TRY(dtype_ok(z_dtype, "latents"));
+    if (!z || !out) return fail(WAN_ERR_INVALID_ARG, "null latents or output");
+    if (B < 1 || T < 1 || h < 1 || w < 1) return fail(WAN_ERR_INVALID_ARG, "B=%d T=%d h=%d w=%d", B, T, h, w);
+    cudaStream_t s = (cudaStream_t)stream;
+    wan_vae_model m;
+    m.mem.use_async = true;
+    m.mem.async = s;
+    wan_status r = model_build_checked(weights, n_weights, dtype, s, &m);
+    wan_vae_stream* st = nullptr;
+    if (r == WAN_OK) {
+      st = new wan_vae_stream();
+      r = stream_build(&m, B, h, w, std::min(T, 4), true, s, st);
+      if (r == WAN_OK) r = clip_impl(st, z, z_dtype, T, out, dtype, nullptr, s);
+      st->mem.release();
+      delete st;
+    }
+    m.mem.release();
+    return r;
+  })
+}
+
+wan_status wan_attention_block(const void* x, int32_t N, int32_t H, int32_t W, int32_t C, const wan_tensor* weights,
+                               int32_t n_weights, void* out, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!x || !out || !weights) return fail(WAN_ERR_INVALID_ARG, "null argument");
+    if (N < 1 || H < 1 || W < 1) return fail(WAN_ERR_INVALID_ARG, "N=%d H=%d W=%d", N, H, W);
+    if (C % 64 || C < 64 || C > 1024) return fail(WAN_ERR_UNSUPPORTED, "C=%d (multiple of 64, <= 1024)", C);
+    cudaStream_t s = (cudaStream_t)stream;
+    // pick the five tensors by suffix
+    std::vector<wan_tensor> t;
+    const char* suff[5] = {"norm.gamma", "to_qkv.weight", "to_qkv.bias", "proj.weight", "proj.bias"};
+    for (const char* sfx : suff) {
+      const wan_tensor* hit = nullptr;
+      for (int i = 0; i < n_weights; ++i) {
+        const char* nm = weights[i].name;
+        if (!nm) continue;
+        const size_t L = strlen(nm), Ls = strlen(sfx);
+        if (L >= Ls && strcmp(nm + L - Ls, sfx) == 0) hit = &weights[i];
+      }
+      if (!hit) return fail(WAN_ERR_MISSING_WEIGHT, "missing weight '*%s'", sfx);
+      wan_tensor c = *hit;
+      c.name = sfx;
+      t.push_back(c);
+    }
+    WeightTable wt{t.data(), (int)t.size()};
+    DevMem mem;
+    mem.use_async = true;
+    mem.async = s;
+    wan_status r = WAN_OK;
+    float* g = nullptr;
+    ConvW qkv, proj;
+    do {
+      if ((r = pack_gamma(wt, "norm.gamma", C, &g, mem, s)) != WAN_OK) break;
+      if ((r = pack_conv(wt, "to_qkv", 3 * C, C, 1, 1, 1, true, "", 0, qkv, mem, s)) != WAN_OK) break;
+      if ((r = pack_conv(wt, "proj", C, C, 1, 1, 1, true, "", 0, proj, mem, s)) != WAN_OK) break;
+      AttnBufs at;
+      at.HW = H * W;
+      at.HWs = (int)rup(at.HW, 16);
+      at.HWp = (int)rup(at.HW, 64);
+      at.Fmax = N;
+      at.B = 1;
+      at.C = C;
+      auto mk = [&](Act& a, int ch) -> wan_status {
+        a.B = 1;
+        a.F = N;
+        a.H = 1;
+        a.W = at.HW;
+        a.C = ch;
+        a.ldc = ch;
+        void* p;
+        WAN_TRY(mem.alloc(&p, a.bytes()));
+        a.p = (bf16*)p;
+        return WAN_OK;
+      };
+      if ((r = mk(at.an, C)) != WAN_OK || (r = mk(at.qkv, 3 * C)) != WAN_OK || (r = mk(at.O, C)) != WAN_OK) break;
+      void* p;
+      if ((r = mem.alloc(&p, (size_t)at.s_bs() * sizeof(float))) != WAN_OK) break;
+      at.S = (float*)p;
+      if ((r = mem.alloc(&p, (size_t)at.p_bs() * sizeof(bf16))) != WAN_OK) break;
+      at.P = (bf16*)p;
+      if ((r = mem.alloc(&p, (size_t)at.vt_bs() * sizeof(bf16))) != WAN_OK) break;
+      at.Vt = (bf16*)p;
+      int* err;
+      if ((r = mem.alloc((void**)&err, 256)) != WAN_OK) break;
+      if (cudaMemsetAsync(at.P, 0, (size_t)at.p_bs() * sizeof(bf16), s) != cudaSuccess ||
+          cudaMemsetAsync(at.Vt, 0, (size_t)at.vt_bs() * sizeof(bf16), s) != cudaSuccess ||
+          cudaMemsetAsync(err, 0, 256, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "memset failed");
+        break;
+      }
+      Act xa, ya;
+      xa.p = (bf16*)x;
+      ya.p = (bf16*)out;
+      for (Act* a : {&xa, &ya}) {
+        a->B = 1;
+        a->F = N;
+        a->H = 1;
+        a->W = at.HW;
+        a->C = C;
+        a->ldc = C;
+      }
+      r = attention(g, qkv, proj, at, xa, ya, N, err, s);
+    } while (false);
+    mem.release();
+    return r;
+  })
+}
+
+wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F, int32_t H, int32_t W, int32_t Cin,
+                             const void* weight, const void* bias, int32_t w_dtype, int32_t Cout, int32_t kt,
+                             int32_t kh, int32_t kw, void* out, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!x || !weight || !bias || !out) return fail(WAN_ERR_INVALID_ARG, "null argument");
+    WAN_TRY(dtype_ok(w_dtype, "weights"));
+    if (B < 1 || F < 1 || H < 1 || W < 1 || Cin < 8 || Cout < 16 || n_hist < 0 || n_hist > 2)
+      return fail(WAN_ERR_INVALID_ARG, "B=%d F=%d H=%d W=%d Cin=%d Cout=%d n_hist=%d", B, F, H, W, Cin, Cout, n_hist);
+    if (Cin % 8 || Cout % 16 || Cin > 4096 || Cout > 4096)
+      return fail(WAN_ERR_UNSUPPORTED, "Cin %% 8 and Cout %% 16 must be 0 (Cin=%d Cout=%d)", Cin, Cout);
+    for (int k : {kt, kh, kw})
+      if (k != 1 && k != 3) return fail(WAN_ERR_UNSUPPORTED, "kernel extents must be 1 or 3");
+    if (kt * kh * kw * (((Cin + 63) / 64)) > 0 && kt * kh * kw > kMaxTaps)
+      return fail(WAN_ERR_UNSUPPORTED, "too many taps");
+    cudaStream_t s = (cudaStream_t)stream;
+    wan_tensor t[2] = {{"c.weight", weight, w_dtype, 5, {Cout, Cin, kt, kh, kw}}, {"c.bias", bias, w_dtype, 1, {Cout}}};
+    WeightTable wt{t, 2};
+    DevMem mem;
+    mem.use_async = true;
+    mem.async = s;
+    wan_status r = WAN_OK;
+    do {
+      ConvW cw;
+      if ((r = pack_conv(wt, "c", Cout, Cin, kt, kh, kw, false, "", 0, cw, mem, s)) != WAN_OK) break;
+      // the input with two history slots in front, channels padded to 64
+      Act xr;
+      xr.B = B;
+      xr.F = 2 + F;
+      xr.H = H;
+      xr.W = W;
+      xr.C = Cin;
+      xr.ldc = (int)rup(Cin, 64);
+      void* p;
+      if ((r = mem.alloc(&p, xr.bytes())) != WAN_OK) break;
+      xr.p = (bf16*)p;
+      int* err;
+      if ((r = mem.alloc((void**)&err, 256)) != WAN_OK) break;
+      if (cudaMemsetAsync(xr.p, 0, xr.bytes(), s) != cudaSuccess || cudaMemsetAsync(err, 0, 256, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "memset failed");
+        break;
+      }
+      const long long fs_in = (long long)H * W * Cin;
+      FrameView vin{const_cast<void*>(x), (long long)(n_hist + F) * fs_in, fs_in, Cin, 0};
+      if (launch_copy_frames(vin, xr.view(2 - n_hist), Cin, B, n_hist + F, H * W, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "copy failed");
+        break;
+      }
+      ConvLaunch L;
+      if ((r = conv_setup(cw, xr, kt == 3 ? 0 : 2, nullptr, 0, F, L)) != WAN_OK) break;
+      OutSpec o;
+      o.p = out;
+      o.fs = (long long)H * W * Cout;
+      o.bs = (long long)F * o.fs;
+      o.ldc = Cout;
+      set_out(L.args, o);
+      r = run(L, err, s);
+    } while (false);
+    mem.release();
+    return r;
+  })
+}
+
+}  // extern "C"
