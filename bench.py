@@ -1,0 +1,294 @@
+#!/usr/bin/env python3
+"""Benchmark of the Wan2.2-TI2V-5B VAE decode on GB300.
+
+One step = one whole 720p clip: latents [1, 48, 31, 44, 80] (device-resident
+when the timed region starts) decoded to a [1, 3, 121, 704, 1280] bf16 video
+through the library's stream API (causal chunks of --chunk latent frames).
+Weights are seeded random init of the full-width TI2V-5B decoder, latents
+~ N(0, 1); weight packing happens before the timed region.
+
+Prints one JSON line (rank 0).  With --gpus N under torchrun every rank
+decodes its own clip (independent samples; no collective on the data path:
+weak scaling); the timing barrier and the max over ranks use the process
+group.  `--impl reference` times the CPU oracle instead, on a bounded crop of
+the same workload, on this machine's host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import wan_synth  # noqa: E402
+
+WORKLOAD = wan_synth.CONFIGS["720p"]
+B, Z, T, H_LAT, W_LAT = WORKLOAD["latents"]
+FRAMES = 4 * T - 3
+H_OUT, W_OUT = 16 * H_LAT, 16 * W_LAT
+METRIC = "decoded frames/s (704x1280, bf16)"
+UNIT = "frames/s"
+# bounded sample for the CPU oracle: the first 2 latent frames of a 11x20 crop
+# of the 720p latents (1/16 of the area): 5 video frames of 176x320
+CPU_SAMPLE = dict(T=2, h=11, w=20)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d["bf16_tflops_sustained"], d["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = sorted({n for r in rows for n, v in zip(self.NAMES, r[5:9]) if v.lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def cpu_oracle_sample(z_full):
+    """The CPU oracle (fp32 NumPy, frame loop) on the bounded crop; returns
+    (seconds, 720p-equivalent frames, description)."""
+    import oracle
+    s = CPU_SAMPLE
+    z = np.ascontiguousarray(z_full[:, :, :s["T"], :s["h"], :s["w"]])
+    w = wan_synth.make_weights(base=WORKLOAD["base"], seed=WORKLOAD["weight_seed"])
+    t0 = time.perf_counter()
+    v = oracle.decode(z, w)
+    dt = time.perf_counter() - t0
+    frames_equiv = v.shape[2] * (v.shape[3] * v.shape[4]) / float(H_OUT * W_OUT)
+    desc = (f"oracle frame loop on latents [:, :, :{s['T']}, :{s['h']}, :{s['w']}] of the 720p latents "
+            f"-> {v.shape[2]} frames of {v.shape[3]}x{v.shape[4]} = {frames_equiv:.4f} frames of 704x1280")
+    return dt, frames_equiv, desc
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    z = wan_synth.make_latents(WORKLOAD["latents"], WORKLOAD["latent_seed"])
+    times, fe, desc = [], 0.0, ""
+    for i in range(args.warmup + args.steps):
+        dt, fe, desc = cpu_oracle_sample(z)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1000.0 * statistics.mean(times)
+    value = fe / (ms / 1000.0)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280]; each step a bounded crop",
+                   "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--chunk", type=int, default=4, help="latent frames per causal chunk")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    ws, rank, local = _dist()
+    if ws != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {ws}")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from video_vae_decoding_gb300 import build as _build
+    _build.build()
+    import video_vae_decoding_gb300 as wv
+
+    stream = torch.cuda.current_stream()
+    w = wan_synth.make_weights(base=WORKLOAD["base"], seed=WORKLOAD["weight_seed"])
+    wdev = {k: torch.from_numpy(np.array(v)).to(dev) for k, v in w.items()}
+    model = wv.Model(wdev, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    del wdev
+    z_np = wan_synth.make_latents(WORKLOAD["latents"], WORKLOAD["latent_seed"] + rank)
+    z = torch.from_numpy(z_np).to(dev)
+    st = wv.DecodeStream(model, B, H_LAT, W_LAT, max_chunk=args.chunk)
+    out = torch.empty((B, 3, FRAMES, H_OUT, W_OUT), device=dev, dtype=torch.bfloat16)
+
+    for _ in range(args.warmup):
+        st.decode_clip(z, out)
+    st.sync_status()
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
+
+    # ---- timed region: K clips, device-resident inputs
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    st.profile_begin()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        st.decode_clip(z, out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = st.profile_end()
+    clocks = sampler.stop()
+    if pg:
+        pg.barrier()
+    st.sync_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    value = ws * B * FRAMES / (ms / 1000.0)
+    burst, sustained, hbm, peak_src = _peaks()
+    flops_step = prof["tc_flops"] / args.steps
+    achieved = prof["tc_flops"] / (prof["tc_ms"] / 1000.0) / 1e12 if prof["tc_ms"] > 0 else 0.0
+
+    # ---- end to end: host latents in, host video out, through the C ABI
+    e2e = None
+    if not args.no_e2e:
+        z_host = torch.from_numpy(z_np).pin_memory()
+        v_host = torch.empty((B, 3, FRAMES, H_OUT, W_OUT), dtype=torch.bfloat16).pin_memory()
+        st.decode_clip_host(z_host, v_host)
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            st.decode_clip_host(z_host, v_host)
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        if pg:
+            t = torch.tensor([e2e_s], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": ws * B * FRAMES / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": z_host.numel() * z_host.element_size(),
+               "d2h_bytes_per_step": v_host.numel() * v_host.element_size()}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        dt, fe, desc = cpu_oracle_sample(z_np)
+        cpu = {"value": fe / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        kinds = {k: {"ms_per_step": v["ms"] / args.steps, "tflops": (v["flops"] / (v["ms"] / 1000.0) / 1e12)
+                     if v["ms"] > 0 else None, "launches_per_step": v["launches"] / args.steps}
+                 for k, v in prof["kinds"].items()}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded random-init TI2V-5B decoder weights, N(0,1) latents",
+            "config": {"workload": "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280] bf16",
+                       "chunk_latent_frames": args.chunk, "batch_per_gpu": B,
+                       "l2": "working set larger than L2 (1.1 GB packed weights; GB-scale activations per chunk)"},
+            "mpix_per_s": value * H_OUT * W_OUT / 1e6,
+            "nominal_tflop_per_step": flops_step / 1e12,
+            "tflops_nominal": flops_step / (ms / 1000.0) / 1e12,
+            "frac_of_bf16_peak": {"burst": flops_step / (ms / 1000.0) / 1e12 / burst,
+                                  "sustained": flops_step / (ms / 1000.0) / 1e12 / sustained, "source": peak_src},
+            "roofline": {"bound": "tensor", "kernel": "conv_gemm_kernel (tcgen05 implicit GEMM, all launches)",
+                         "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
+                         "frac": achieved / sustained, "peak_kind": f"bf16 sustained ({peak_src})",
+                         "traffic": None},
+            "tensor_core_ms_per_step": prof["tc_ms"] / args.steps,
+            "by_kind": kinds,
+            "gpu_launches": prof["launches"],
+            "workspace_gb": st.workspace_bytes / 1e9,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

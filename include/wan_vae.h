@@ -83,8 +83,9 @@ const char* wan_vae_last_error(void);
 const char* wan_vae_status_string(int32_t status);
 
 /* Packs the 110 decoder + post_quant_conv tensors into a library-owned model
- * (weights rounded to bf16 for the tensor cores, K-major, per-tap channel
- * blocks padded to 64; biases and sqrt(C)*gamma kept in fp32).  The
+ * (every tensor rounded to bf16, as the bf16 contract rounds the weights;
+ * conv weights K-major with per-tap channel blocks padded to 64; biases and
+ * sqrt(C)*gamma held as fp32).  The
  * architecture (decoder base dim b, channels 4b/4b/2b/b) is inferred from
  * decoder.conv_in.weight [4b, 48, 3, 3, 3]; every other shape is checked
  * against it.  `dtype` is the decode precision: WAN_BF16 computes with bf16
@@ -118,6 +119,25 @@ int64_t wan_vae_stream_workspace_bytes(const wan_vae_stream* st);
 /* Blocks until the stream's enqueued work is done and reports any error a
  * kernel recorded (WAN_ERR_INTERNAL with a message) or a CUDA error. */
 wan_status wan_vae_stream_sync_status(wan_vae_stream* st, wan_cuda_stream stream);
+
+/* Device-side timing of the stream's work (for benchmarks).  Between
+ * profile_begin and profile_end every tensor-core (implicit-GEMM) launch is
+ * bracketed by CUDA events on the launching stream; profile_end waits for the
+ * stream, sums the events and reports, with the launch counts, the nominal
+ * FLOPs of those launches (2*M*N*K per conv, zero-padded taps included).
+ * kind index: 0 causal 3x3x3 convs (conv_in, residual blocks), 1 time convs,
+ * 2 upsample2d convs (+DupUp3D), 3 attention GEMMs, 4 conv_out. */
+typedef struct {
+  int64_t launches;          /* all kernel launches enqueued */
+  int64_t tc_launches;       /* tensor-core launches among them */
+  double tc_ms;              /* their summed device time */
+  double tc_flops;           /* their nominal FLOPs */
+  double kind_ms[5];
+  double kind_flops[5];
+  int64_t kind_launches[5];
+} wan_vae_profile;
+wan_status wan_vae_stream_profile_begin(wan_vae_stream* st);
+wan_status wan_vae_stream_profile_end(wan_vae_stream* st, wan_cuda_stream stream, wan_vae_profile* out);
 
 /* Decodes latent frames t0 .. t0+n-1 of z [B, 48, z_frames, h, w] (device,
  * NCDHW, z_dtype) as the next chunk of the stream (page functions decode /

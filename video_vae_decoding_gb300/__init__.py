@@ -12,7 +12,7 @@ import ctypes
 
 import torch
 
-from ._lib import WAN_BF16, WAN_F32, WanError, WanTensor, check, load  # noqa: F401
+from ._lib import PROFILE_KINDS, WAN_BF16, WAN_F32, WanError, WanProfile, WanTensor, check, load  # noqa: F401
 
 __all__ = ["Model", "DecodeStream", "decode", "attention_block", "causal_conv3d", "out_frames", "WanError"]
 
@@ -114,6 +114,20 @@ class DecodeStream:
 
     def sync_status(self, stream=None):
         check(load().wan_vae_stream_sync_status(self._s, _stream(stream)))
+
+    def profile_begin(self):
+        check(load().wan_vae_stream_profile_begin(self._s))
+
+    def profile_end(self, stream=None) -> dict:
+        """Waits for the stream; returns launch counts and the summed device
+        time and nominal FLOPs of the tensor-core launches since profile_begin."""
+        p = WanProfile()
+        check(load().wan_vae_stream_profile_end(self._s, _stream(stream), ctypes.byref(p)))
+        return {
+            "launches": p.launches, "tc_launches": p.tc_launches, "tc_ms": p.tc_ms, "tc_flops": p.tc_flops,
+            "kinds": {k: {"ms": p.kind_ms[i], "flops": p.kind_flops[i], "launches": p.kind_launches[i]}
+                      for i, k in enumerate(PROFILE_KINDS)},
+        }
 
     def decode_chunk(self, z, t0, n, out, out_f0, preclamp=None, stream=None):
         p = 0 if preclamp is None else _dev(preclamp, "preclamp")

@@ -27,6 +27,20 @@ class WanTensor(ctypes.Structure):
     ]
 
 
+class WanProfile(ctypes.Structure):
+    _fields_ = [
+        ("launches", ctypes.c_int64),
+        ("tc_launches", ctypes.c_int64),
+        ("tc_ms", ctypes.c_double),
+        ("tc_flops", ctypes.c_double),
+        ("kind_ms", ctypes.c_double * 5),
+        ("kind_flops", ctypes.c_double * 5),
+        ("kind_launches", ctypes.c_int64 * 5),
+    ]
+
+
+PROFILE_KINDS = ("conv3x3x3", "time_conv", "upsample2d_conv", "attention_gemm", "conv_out")
+
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
 
 # name -> (restype, argtypes)
@@ -42,6 +56,8 @@ SIGNATURES = {
     "wan_vae_stream_destroy": (None, [_vp]),
     "wan_vae_stream_workspace_bytes": (_i64, [_vp]),
     "wan_vae_stream_sync_status": (_i32, [_vp, _vp]),
+    "wan_vae_stream_profile_begin": (_i32, [_vp]),
+    "wan_vae_stream_profile_end": (_i32, [_vp, _vp, ctypes.POINTER(WanProfile)]),
     "wan_vae_decode_chunk": (_i32, [_vp, _vp, _i32, _i64, _i64, _i32, _vp, _i32, _i64, _i64, _vp, _vp]),
     "wan_vae_decode_clip": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]),
     "wan_vae_decode_clip_host": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp]),

@@ -140,6 +140,24 @@ struct DevMem {
   }
 };
 
+// ----------------------------------------------------------- profiling
+// Kinds of tensor-core launches, for the per-kind breakdown.
+enum LaunchKind { kKindConv333 = 0, kKindTimeConv = 1, kKindResample = 2, kKindAttention = 3, kKindConvOut = 4 };
+struct Prof {
+  bool on = false;
+  long long launches = 0;                  // every kernel launch enqueued
+  std::vector<cudaEvent_t> ev;             // start/end pairs of tensor-core launches
+  std::vector<std::pair<int, double>> rec; // (kind, nominal FLOPs) per tensor-core launch
+  ~Prof() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+};
+#define ELT(prof, expr)                  \
+  do {                                   \
+    CUDA_TRY(expr);                      \
+    if (prof) (prof)->launches++;        \
+  } while (0)
+
 // ------------------------------------------------------------ packed convs
 struct ConvW {
   bf16* w = nullptr;      // [co_pad][ktot], K = tap-major, 64-padded channel blocks per tap
@@ -382,6 +400,7 @@ struct AttnBufs {
 
 struct wan_vae_stream {
   const wan_vae_model* m = nullptr;
+  Prof prof;
   int B = 0, h = 0, w = 0, nmax = 0;
   bool first = true;
   DevMem mem;
@@ -588,16 +607,39 @@ static void set_out(ConvArgs& A, const OutSpec& o) {
   A.interleave_c = o.interleave;
 }
 
-static wan_status run(ConvLaunch& L, int* err, cudaStream_t s) {
+// Enqueues a tensor-core launch; when profiling, brackets it with CUDA events
+// on the same stream and records its nominal FLOPs (2 * M * N * K with the
+// zero-padded taps included).
+static wan_status run(ConvLaunch& L, Prof* prof, int kind, double flops, int* err, cudaStream_t s) {
   L.args.err = err;
   if (L.args.N % 16 && L.epi != kEpiVideo) return fail(WAN_ERR_INTERNAL, "conv output channels not a multiple of 16");
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (prof && prof->on) {
+    const size_t i = prof->rec.size();
+    while (prof->ev.size() < 2 * (i + 1)) {
+      cudaEvent_t e;
+      CUDA_TRY(cudaEventCreate(&e));
+      prof->ev.push_back(e);
+    }
+    e0 = prof->ev[2 * i];
+    e1 = prof->ev[2 * i + 1];
+    prof->rec.push_back({kind, flops});
+    CUDA_TRY(cudaEventRecord(e0, s));
+  }
   CUDA_TRY(launch_conv(L, s));
+  if (e1) CUDA_TRY(cudaEventRecord(e1, s));
+  if (prof) prof->launches++;
   return WAN_OK;
+}
+
+static double conv_flops(const ConvW& cw, const Act& a0, int F) {
+  const double M = (double)a0.B * F * a0.H * a0.W;
+  return 2.0 * M * cw.Co * ((double)cw.kt * cw.kh * cw.kw * cw.Ci + cw.sc_Ci);
 }
 
 // 3-frame causal conv over ring `in` (F current frames) into `out`.
 static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F, const OutSpec& o, const Act* res,
-                            const Act* sc, cudaStream_t s) {
+                            const Act* sc, cudaStream_t s, int kind = kKindConv333) {
   ConvLaunch L;
   WAN_TRY(conv_setup(cw, in, 0, sc, 0, F, L));
   set_out(L.args, o);
@@ -607,7 +649,7 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
     L.args.res_fs = res->fs();
     L.args.res_ldc = res->ldc;
   }
-  WAN_TRY(run(L, st->err_dev, s));
+  WAN_TRY(run(L, &st->prof, kind, conv_flops(cw, in, F), st->err_dev, s));
   st->shifts.push_back(RingShift{in.p, in.fs(), in.bs(), F, in.B});
   return WAN_OK;
 }
@@ -616,9 +658,9 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
 static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act& ring1, Act& ring2, Act& Ht, Act& y,
                          int F, cudaStream_t s) {
   const int P = x.H * x.W;
-  CUDA_TRY(launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s));
+  ELT(&st->prof, launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s));
   WAN_TRY(ring_conv(st, r.c1, ring1, F, out_of(Ht), nullptr, nullptr, s));
-  CUDA_TRY(launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s));
+  ELT(&st->prof, launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s));
   if (r.ci != r.co)
     WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), nullptr, &x, s));
   else
@@ -658,11 +700,12 @@ static wan_status gemm_setup(ConvLaunch& L, const bf16* a_base, int a_C, int a_l
 
 // Mid-block attention over F frames of x (level A) into y = attn(x) + x.
 static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj, AttnBufs& at, const Act& x, Act& y,
-                            int F, int* err, cudaStream_t s) {
+                            int F, Prof* prof, int* err, cudaStream_t s) {
+  const double M = (double)at.B * F * at.HW;
   const int C = at.C, HW = at.HW, B = at.B;
   if (HW < 16) return fail(WAN_ERR_UNSUPPORTED, "attention over %d positions (at least 16 supported)", HW);
   // n = RMS norm of x (no SiLU), rows = positions
-  CUDA_TRY(launch_rms_norm(x.view(0), at.an.view(0), g, C, B, F, HW, false, s));
+  ELT(prof, launch_rms_norm(x.view(0), at.an.view(0), g, C, B, F, HW, false, s));
   ConvLaunch L;
   // qkv = n @ Wqkv^T + b
   WAN_TRY(gemm_setup(L, at.an.p, at.an.ldc, at.an.ldc, HW, at.an.F, B, at.an.fs(), at.an.bs(), qkv.ci_pad,
@@ -671,7 +714,7 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
   L.args.N = qkv.Co;
   L.args.bias = qkv.bias;
   set_out(L.args, out_of(at.qkv));
-  WAN_TRY(run(L, err, s));
+  WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * 3 * C * C, err, s));
   // S = q k^T per frame (fp32)
   int bnS = 16;  // largest power of two <= min(HW, 256): the K-operand box stays inside the tensor
   while (bnS * 2 <= std::min(HW, 256)) bnS *= 2;
@@ -690,13 +733,13 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
     o.ldc = at.HWs;
     set_out(L.args, o);
   }
-  WAN_TRY(run(L, err, s));
+  WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * HW * C, err, s));
   // P = softmax(S / sqrt(C)), V^T
   const float scale = 1.0f / std::sqrt((float)C);
   for (int b = 0; b < B; ++b) {
-    CUDA_TRY(launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.HWp, HW, (long long)F * HW,
+    ELT(prof, launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.HWp, HW, (long long)F * HW,
                                  scale, s));
-    CUDA_TRY(launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C, at.qkv.fs(), at.qkv.ldc, at.Vt + b * at.vt_bs(),
+    ELT(prof, launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C, at.qkv.fs(), at.qkv.ldc, at.Vt + b * at.vt_bs(),
                               at.vt_fs(), at.HWp, F, HW, C, s));
   }
   // O = P V per frame
@@ -708,7 +751,7 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
   L.args.b_gstride = at.Fmax;
   L.args.N = C;
   set_out(L.args, out_of(at.O));
-  WAN_TRY(run(L, err, s));
+  WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * HW * C, err, s));
   // y = O Wp^T + b + x
   WAN_TRY(gemm_setup(L, at.O.p, at.O.ldc, at.O.ldc, HW, at.O.F, B, at.O.fs(), at.O.bs(), proj.ci_pad,
                      proj.co_pad / proj.bn, proj.bn, F));
@@ -721,13 +764,13 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
   L.args.res_bs = x.bs();
   L.args.res_fs = x.fs();
   L.args.res_ldc = x.ldc;
-  WAN_TRY(run(L, err, s));
+  WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * C * C, err, s));
   return WAN_OK;
 }
 
 // ---------------------------------------------------------------- the chunk
-static wan_status copy_frames(const Act& src, int sf0, const Act& dst, int df0, int F, cudaStream_t s) {
-  CUDA_TRY(launch_copy_frames(src.view(sf0), dst.view(df0), src.C, src.B, F, src.H * src.W, s));
+static wan_status copy_frames(const Act& src, int sf0, const Act& dst, int df0, int F, Prof* prof, cudaStream_t s) {
+  ELT(prof, launch_copy_frames(src.view(sf0), dst.view(df0), src.C, src.B, F, src.H * src.W, s));
   return WAN_OK;
 }
 
@@ -739,17 +782,17 @@ static wan_status time_upsample(wan_vae_stream* st, const ConvW& tc, const Act& 
   const int C = x.C;
   int fx0 = 0, fout0 = 0, Ft = Fin;
   if (first) {
-    WAN_TRY(copy_frames(x, 0, tu, 0, 1, s));
+    WAN_TRY(copy_frames(x, 0, tu, 0, 1, &st->prof, s));
     fx0 = 1;
     fout0 = 1;
     Ft = Fin - 1;
   }
   if (Ft <= 0) return WAN_OK;
-  WAN_TRY(copy_frames(x, fx0, ring, 2, Ft, s));
+  WAN_TRY(copy_frames(x, fx0, ring, 2, Ft, &st->prof, s));
   OutSpec o = out_of(tu, fout0);
   o.fmul = 2;
   o.interleave = C;
-  return ring_conv(st, tc, ring, Ft, o, nullptr, nullptr, s);
+  return ring_conv(st, tc, ring, Ft, o, nullptr, nullptr, s, kKindTimeConv);
 }
 
 // upsample2d's 3x3 conv on the nearest-x2 input `up` (F frames) plus DupUp3D
@@ -776,7 +819,7 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& up, c
     L.args.dup_pairs = 1;
   else
     return fail(WAN_ERR_UNSUPPORTED, "DupUp3D with %d -> %d channels, ft %d", blk.C, cw.Co, ft);
-  return run(L, st->err_dev, s);
+  return run(L, &st->prof, kKindResample, conv_flops(cw, up, F), st->err_dev, s);
 }
 
 static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long long Tz, long long t0, int n, void* out,
@@ -787,38 +830,38 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   const int P = st->h * st->w;
   st->shifts.clear();
   // 1. post_quant_conv into conv_in's ring
-  CUDA_TRY(launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, st->ringIn.view(2), 1, s));
+  ELT(&st->prof, launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, st->ringIn.view(2), 1, s));
   // 2. conv_in, mid block
   WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s));
   WAN_TRY(resnet(st, m->mid[0], st->RA[0], st->ringA[0], st->ringA[1], st->HA, st->RA[1], FA, s));
-  WAN_TRY(attention(m->attn_g, m->qkv, m->proj, st->at, st->RA[1], st->RA[2], FA, st->err_dev, s));
+  WAN_TRY(attention(m->attn_g, m->qkv, m->proj, st->at, st->RA[1], st->RA[2], FA, &st->prof, st->err_dev, s));
   WAN_TRY(resnet(st, m->mid[1], st->RA[2], st->ringA[2], st->ringA[3], st->HA, st->RA[0], FA, s));
   // up block 0 (level A -> B); block input RA[0]
   WAN_TRY(resnet(st, m->up[0][0], st->RA[0], st->ringA[4], st->ringA[5], st->HA, st->RA[1], FA, s));
   WAN_TRY(resnet(st, m->up[0][1], st->RA[1], st->ringA[6], st->ringA[7], st->HA, st->RA[2], FA, s));
   WAN_TRY(resnet(st, m->up[0][2], st->RA[2], st->ringA[8], st->ringA[9], st->HA, st->RA[1], FA, s));
   WAN_TRY(time_upsample(st, m->tconv[0], st->RA[1], st->tcA, st->tuA, FA, first, s));
-  CUDA_TRY(launch_upsample2x(st->tuA.view(0), st->upB.view(0), st->tuA.C, st->B, FB, st->tuA.H, st->tuA.W, s));
+  ELT(&st->prof, launch_upsample2x(st->tuA.view(0), st->upB.view(0), st->tuA.C, st->B, FB, st->tuA.H, st->tuA.W, s));
   WAN_TRY(resample(st, m->resample[0], st->upB, st->RA[0], 2, first, st->RB[0], FB, s));
   // up block 1 (level B -> C); block input RB[0]
   WAN_TRY(resnet(st, m->up[1][0], st->RB[0], st->ringB[0], st->ringB[1], st->HB, st->RB[1], FB, s));
   WAN_TRY(resnet(st, m->up[1][1], st->RB[1], st->ringB[2], st->ringB[3], st->HB, st->RB[2], FB, s));
   WAN_TRY(resnet(st, m->up[1][2], st->RB[2], st->ringB[4], st->ringB[5], st->HB, st->RB[1], FB, s));
   WAN_TRY(time_upsample(st, m->tconv[1], st->RB[1], st->tcB, st->tuB, FB, first, s));
-  CUDA_TRY(launch_upsample2x(st->tuB.view(0), st->upC.view(0), st->tuB.C, st->B, FC, st->tuB.H, st->tuB.W, s));
+  ELT(&st->prof, launch_upsample2x(st->tuB.view(0), st->upC.view(0), st->tuB.C, st->B, FC, st->tuB.H, st->tuB.W, s));
   WAN_TRY(resample(st, m->resample[1], st->upC, st->RB[0], 2, first, st->RC[0], FC, s));
   // up block 2 (level C -> D); block input RC[0]
   WAN_TRY(resnet(st, m->up[2][0], st->RC[0], st->ringC[0], st->ringC[1], st->HC, st->RC[1], FC, s));
   WAN_TRY(resnet(st, m->up[2][1], st->RC[1], st->ringC[2], st->ringC[3], st->HC, st->RC[2], FC, s));
   WAN_TRY(resnet(st, m->up[2][2], st->RC[2], st->ringC[4], st->ringC[5], st->HC, st->RC[1], FC, s));
-  CUDA_TRY(launch_upsample2x(st->RC[1].view(0), st->upD.view(0), st->RC[1].C, st->B, FC, st->RC[1].H, st->RC[1].W, s));
+  ELT(&st->prof, launch_upsample2x(st->RC[1].view(0), st->upD.view(0), st->RC[1].C, st->B, FC, st->RC[1].H, st->RC[1].W, s));
   WAN_TRY(resample(st, m->resample[2], st->upD, st->RC[0], 1, first, st->RD[0], FC, s));
   // up block 3 (level D)
   WAN_TRY(resnet(st, m->up[3][0], st->RD[0], st->ringD[0], st->ringD[1], st->HD, st->RD[1], FC, s));
   WAN_TRY(resnet(st, m->up[3][1], st->RD[1], st->ringD[2], st->ringD[3], st->HD, st->RD[2], FC, s));
   WAN_TRY(resnet(st, m->up[3][2], st->RD[2], st->ringD[4], st->ringD[5], st->HD, st->RD[1], FC, s));
   // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
-  CUDA_TRY(launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
+  ELT(&st->prof, launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
                            st->RD[1].H * st->RD[1].W, true, s));
   {
     ConvLaunch L;
@@ -830,11 +873,11 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
     L.args.preclamp = pre;
     L.args.vid_cs = out_frames * 4LL * st->ringOut.H * st->ringOut.W;
     L.args.vid_bs = 3 * L.args.vid_cs;
-    WAN_TRY(run(L, st->err_dev, s));
+    WAN_TRY(run(L, &st->prof, kKindConvOut, conv_flops(m->conv_out, st->ringOut, FC), st->err_dev, s));
     st->shifts.push_back(RingShift{st->ringOut.p, st->ringOut.fs(), st->ringOut.bs(), FC, st->B});
   }
   // 3. the causal caches: each ring keeps the last two frames it convolved
-  CUDA_TRY(launch_ring_shift(st->shifts.data(), (int)st->shifts.size(), s));
+  ELT(&st->prof, launch_ring_shift(st->shifts.data(), (int)st->shifts.size(), s));
   st->first = false;
   if (st->err_host) {
     CUDA_TRY(cudaMemcpyAsync(st->err_host, st->err_dev, sizeof(int), cudaMemcpyDeviceToHost, s));
@@ -1049,6 +1092,46 @@ wan_status wan_vae_stream_sync_status(wan_vae_stream* st, wan_cuda_stream stream
   })
 }
 
+wan_status wan_vae_stream_profile_begin(wan_vae_stream* st) {
+  API_GUARD({
+    if (!st) return fail(WAN_ERR_INVALID_ARG, "null stream state");
+    st->prof.on = true;
+    st->prof.launches = 0;
+    st->prof.rec.clear();
+    return WAN_OK;
+  })
+}
+
+wan_status wan_vae_stream_profile_end(wan_vae_stream* st, wan_cuda_stream stream, wan_vae_profile* out) {
+  API_GUARD({
+    if (!st) return fail(WAN_ERR_INVALID_ARG, "null stream state");
+    Prof& p = st->prof;
+    wan_vae_profile r;
+    memset(&r, 0, sizeof(r));
+    r.launches = p.launches;
+    r.tc_launches = (int64_t)p.rec.size();
+    if (p.on && !p.rec.empty()) {
+      CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+      for (size_t i = 0; i < p.rec.size(); ++i) {
+        float ms = 0.f;
+        CUDA_TRY(cudaEventElapsedTime(&ms, p.ev[2 * i], p.ev[2 * i + 1]));
+        const int k = p.rec[i].first;
+        r.tc_ms += ms;
+        r.tc_flops += p.rec[i].second;
+        if (k >= 0 && k < 5) {
+          r.kind_ms[k] += ms;
+          r.kind_flops[k] += p.rec[i].second;
+          r.kind_launches[k] += 1;
+        }
+      }
+    }
+    p.on = false;
+    p.rec.clear();
+    if (out) *out = r;
+    return WAN_OK;
+  })
+}
+
 wan_status wan_vae_decode_chunk(wan_vae_stream* st, const void* z, int32_t z_dtype, int64_t z_frames, int64_t t0,
                                 int32_t n, void* out, int32_t out_dtype, int64_t out_frames, int64_t out_f0,
                                 float* preclamp, wan_cuda_stream stream) {
@@ -1245,7 +1328,7 @@ wan_status wan_attention_block(const void* x, int32_t N, int32_t H, int32_t W, i
         a->C = C;
         a->ldc = C;
       }
-      r = attention(g, qkv, proj, at, xa, ya, N, err, s);
+      r = attention(g, qkv, proj, at, xa, ya, N, nullptr, err, s);
     } while (false);
     mem.release();
     return r;
@@ -1307,7 +1390,7 @@ wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F
       o.bs = (long long)F * o.fs;
       o.ldc = Cout;
       set_out(L.args, o);
-      r = run(L, err, s);
+      r = run(L, nullptr, 0, 0.0, err, s);
     } while (false);
     mem.release();
     return r;
