@@ -195,6 +195,27 @@ wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F
                              const void* weight, const void* bias, int32_t w_dtype, int32_t Cout, int32_t kt,
                              int32_t kh, int32_t kw, void* out, wan_cuda_stream stream);
 
+/* wan_causal_conv3d without any device allocation.  The pages have no
+ * counterpart: this is for callers that must not allocate device memory --
+ * code that runs while a host framework owns all GPU memory through its own
+ * pool, or that must not pay cudaMalloc's implicit device-wide
+ * synchronisation on a latency-critical path.  Same arguments, layout and
+ * result as wan_causal_conv3d; the caller still provides x, the weights and
+ * out.  The scratch (packed weights, bias, a copy of x behind two history
+ * slots, an error word) lives in one fixed 32 MiB device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits; a conv whose scratch exceeds 32 MiB is rejected with
+ * WAN_ERR_UNSUPPORTED before any work is enqueued.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * All calls share the array: each call clears the parts that must start at
+ * zero, and calls whose work overlaps on the GPU (different streams, or
+ * devices sharing one context) race on it -- serialise them. */
+wan_status wan_causal_conv3d_noalloc(const void* x, int32_t B, int32_t n_hist, int32_t F, int32_t H, int32_t W,
+                                     int32_t Cin, const void* weight, const void* bias, int32_t w_dtype,
+                                     int32_t Cout, int32_t kt, int32_t kh, int32_t kw, void* out,
+                                     wan_cuda_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1398,3 +1398,109 @@ wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F
 }
 
 }  // extern "C"
+
+// ======================================================================
+// wan_causal_conv3d_noalloc: the causal conv with its scratch (packed
+// weights, bias, the input copied behind two history slots, the error word)
+// carved from a fixed device array instead of the stream-ordered allocator.
+// ======================================================================
+namespace {
+
+// Scratch limit of the allocation-free entry point.  Every device that loads
+// the library holds this array until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The array's
+// name is only a host-side stand-in, so the address is looked up once per
+// device, with that device current.
+wan_status noalloc_scratch(char** out) {
+  int dev = -1;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(WAN_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(WAN_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s", cudaGetErrorString(e));
+    g_noalloc_addr[dev] = p;
+  }
+  *out = static_cast<char*>(g_noalloc_addr[dev]);
+  return WAN_OK;
+}
+
+}  // namespace
+
+extern "C" wan_status wan_causal_conv3d_noalloc(const void* x, int32_t B, int32_t n_hist, int32_t F, int32_t H,
+                                                int32_t W, int32_t Cin, const void* weight, const void* bias,
+                                                int32_t w_dtype, int32_t Cout, int32_t kt, int32_t kh, int32_t kw,
+                                                void* out, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!x || !weight || !bias || !out) return fail(WAN_ERR_INVALID_ARG, "null argument");
+    WAN_TRY(dtype_ok(w_dtype, "weights"));
+    if (B < 1 || F < 1 || H < 1 || W < 1 || Cin < 8 || Cout < 16 || n_hist < 0 || n_hist > 2)
+      return fail(WAN_ERR_INVALID_ARG, "B=%d F=%d H=%d W=%d Cin=%d Cout=%d n_hist=%d", B, F, H, W, Cin, Cout, n_hist);
+    if (Cin % 8 || Cout % 16 || Cin > 4096 || Cout > 4096)
+      return fail(WAN_ERR_UNSUPPORTED, "Cin %% 8 and Cout %% 16 must be 0 (Cin=%d Cout=%d)", Cin, Cout);
+    for (int k : {kt, kh, kw})
+      if (k != 1 && k != 3) return fail(WAN_ERR_UNSUPPORTED, "kernel extents must be 1 or 3");
+    cudaStream_t s = (cudaStream_t)stream;
+    // scratch plan: packed weights | bias | input with history slots | error word
+    ConvW cw;
+    cw.Co = Cout;
+    cw.Ci = Cin;
+    cw.kt = kt;
+    cw.kh = kh;
+    cw.kw = kw;
+    cw.ci_pad = (int)rup(Cin, 64);
+    const int taps = kt * kh * kw;
+    cw.ktot = taps * cw.ci_pad;
+    cw.bn = choose_bn(Cout);
+    cw.co_pad = (int)rup(Cout, cw.bn);
+    Act xr;
+    xr.B = B;
+    xr.F = 2 + F;
+    xr.H = H;
+    xr.W = W;
+    xr.C = Cin;
+    xr.ldc = cw.ci_pad;
+    const size_t w_bytes = (size_t)cw.co_pad * cw.ktot * sizeof(bf16);
+    const size_t off_b = rup(w_bytes, 256);
+    const size_t off_x = off_b + rup((size_t)Cout * sizeof(float), 256);
+    const size_t off_e = off_x + rup(xr.bytes(), 256);
+    const size_t need = off_e + 256;
+    if (need > kNoAllocScratchBytes)
+      return fail(WAN_ERR_UNSUPPORTED, "this conv needs %zu bytes of scratch; the allocation-free entry point has %zu",
+                  need, kNoAllocScratchBytes);
+    char* base = nullptr;
+    WAN_TRY(noalloc_scratch(&base));
+    cw.w = reinterpret_cast<bf16*>(base);
+    cw.bias = reinterpret_cast<float*>(base + off_b);
+    xr.p = reinterpret_cast<bf16*>(base + off_x);
+    int* err = reinterpret_cast<int*>(base + off_e);
+    // The array keeps the previous call's contents: clear what must start at
+    // zero (weight padding, history slots and channel padding, error word).
+    CUDA_TRY(cudaMemsetAsync(cw.w, 0, w_bytes, s));
+    CUDA_TRY(cudaMemsetAsync(xr.p, 0, xr.bytes(), s));
+    CUDA_TRY(cudaMemsetAsync(err, 0, 256, s));
+    CUDA_TRY(launch_pack_weight(weight, w_dtype == WAN_F32, Cout, Cin, taps, cw.w, cw.ktot, 0, cw.ci_pad, s));
+    CUDA_TRY(launch_to_f32(bias, w_dtype == WAN_F32, nullptr, 0, cw.bias, Cout, 1.0f, 1, s));
+    const long long fs_in = (long long)H * W * Cin;
+    FrameView vin{const_cast<void*>(x), (long long)(n_hist + F) * fs_in, fs_in, Cin, 0};
+    CUDA_TRY(launch_copy_frames(vin, xr.view(2 - n_hist), Cin, B, n_hist + F, H * W, s));
+    ConvLaunch L;
+    WAN_TRY(conv_setup(cw, xr, kt == 3 ? 0 : 2, nullptr, 0, F, L));
+    OutSpec o;
+    o.p = out;
+    o.fs = (long long)H * W * Cout;
+    o.bs = (long long)F * o.fs;
+    o.ldc = Cout;
+    set_out(L.args, o);
+    return run(L, nullptr, 0, 0.0, err, s);
+  })
+}
