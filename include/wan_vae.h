@@ -83,14 +83,18 @@ const char* wan_vae_last_error(void);
 const char* wan_vae_status_string(int32_t status);
 
 /* Packs the 110 decoder + post_quant_conv tensors into a library-owned model
- * (every tensor rounded to bf16, as the bf16 contract rounds the weights;
- * conv weights K-major with per-tap channel blocks padded to 64; biases and
- * sqrt(C)*gamma held as fp32).  The
+ * (conv weights K-major with per-tap channel blocks padded to 64; biases and
+ * sqrt(C)*gamma held as fp32; in WAN_BF16 mode every tensor is first rounded
+ * to bf16, as the page's bf16 contract rounds the weights).  The
  * architecture (decoder base dim b, channels 4b/4b/2b/b) is inferred from
  * decoder.conv_in.weight [4b, 48, 3, 3, 3]; every other shape is checked
  * against it.  `dtype` is the decode precision: WAN_BF16 computes with bf16
  * operands and fp32 accumulation (the page's section "Precision", bf16
- * mode).  WAN_F32 returns WAN_ERR_NOT_IMPLEMENTED in this build.
+ * mode; every weight is rounded to bf16 first).  WAN_F32 keeps fp32 values
+ * throughout: each weight and activation is held as a pair of bf16 halves
+ * (hi = bf16(v), lo = bf16(v - hi)) and every product is formed as
+ * hi*hi + hi*lo + lo*hi on the tensor cores with fp32 accumulation, about
+ * 16 significant bits per operand (three times the MMA work of WAN_BF16).
  * The caller's tensors may be freed once the work enqueued on `stream` is
  * done.  Errors: WAN_ERR_INVALID_ARG, WAN_ERR_DTYPE, WAN_ERR_MISSING_WEIGHT,
  * WAN_ERR_SHAPE, WAN_ERR_OOM, WAN_ERR_CUDA. */

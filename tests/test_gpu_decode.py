@@ -15,6 +15,7 @@ from tests.gpu_util import lib_ready, rounded, to_dev, weights_dev
 
 pytestmark = pytest.mark.gpu
 TOL, PSNR_MIN = 4e-2, 40.0
+TOL_F32 = 2e-3
 
 
 @pytest.fixture(scope="module")
@@ -131,3 +132,41 @@ def test_full_width_small_decode(wv, small, small_ref, chunk):
     z, ref = small_ref
     model = wv.Model(wd, dtype=torch.bfloat16)
     _check(_decode(wv, model, z, chunk), ref)
+
+
+# ------------------------------------------------------------------ fp32
+def _check_f32(got, pre, ref_clamped, ref_pre):
+    e1 = float(np.abs(got - ref_clamped).max())
+    e2 = float(np.abs(pre - ref_pre).max())
+    assert e1 <= TOL_F32 and e2 <= TOL_F32, (e1, e2)
+    return e1, e2
+
+
+def _decode_f32(wv, model, z, chunk):
+    B, _, T, h, w = z.shape
+    st = wv.DecodeStream(model, B, h, w, max_chunk=chunk)
+    pre = torch.empty((B, 3, 4 * T - 3, 16 * h, 16 * w), device="cuda")
+    v = st.decode_clip(to_dev(z), out_dtype=torch.float32, preclamp=pre)
+    st.sync_status()
+    return v.cpu().numpy(), pre.cpu().numpy()
+
+
+@pytest.mark.parametrize("chunk", [1, 2])
+def test_tiny_decode_fp32(wv, tiny, chunk):
+    """fp32 decode (bf16 hi/lo pairs on the tensor cores) against the fp32
+    oracle on the unrounded inputs: within 2e-3 before and after the clamp."""
+    w, wd = tiny
+    z = wan_synth.make_latents((2, 48, 3, 4, 5), seed=11)
+    model = wv.Model(wd, dtype=torch.float32)
+    got, pre = _decode_f32(wv, model, z, chunk)
+    ref, ref_pre = oracle.decode(z, w, return_preclamp=True)
+    _check_f32(got, pre, ref, ref_pre)
+
+
+def test_full_width_small_decode_fp32(wv, small):
+    w, wd = small
+    z = wan_synth.make_latents((1, 48, 3, 16, 16), seed=1)
+    model = wv.Model(wd, dtype=torch.float32)
+    got, pre = _decode_f32(wv, model, z, 2)
+    ref, ref_pre = oracle.decode(z, w, return_preclamp=True)
+    _check_f32(got, pre, ref, ref_pre)

@@ -26,7 +26,25 @@ struct ConvCfg {
   static constexpr size_t kSmem = 1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 1) + 16;
 };
 
-__device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16]) {
+__device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16], int lo = 0) {
+  if (lo) {
+    // split format: hi at dst, lo = v - hi at dst + lo
+    float h[16], l[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+      l[i] = v[i] - h[i];
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    uint4* e = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + lo);
+    d[0] = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+    d[1] = make_uint4(pack_bf16x2(h[8], h[9]), pack_bf16x2(h[10], h[11]), pack_bf16x2(h[12], h[13]),
+                      pack_bf16x2(h[14], h[15]));
+    e[0] = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
+    e[1] = make_uint4(pack_bf16x2(l[8], l[9]), pack_bf16x2(l[10], l[11]), pack_bf16x2(l[12], l[13]),
+                      pack_bf16x2(l[14], l[15]));
+    return;
+  }
   if (f32) {
     float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -40,7 +58,8 @@ __device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16]
   }
 }
 
-__device__ __forceinline__ void add16(const void* src, int f32, float (&v)[16]) {
+__device__ __forceinline__ void add16(const void* src, int f32, float (&v)[16], int lo = 0) {
+  if (lo) add16(static_cast<const __nv_bfloat16*>(src) + lo, 0, v, 0);
   if (f32) {
     const float4* s = reinterpret_cast<const float4*>(src);
 #pragma unroll
@@ -207,7 +226,7 @@ __global__ void __launch_bounds__(256, 1)
                 (long long)b * args.res_bs + (long long)(args.res_f0 + f) * args.res_fs + pos * args.res_ldc + n0;
             const void* rp = args.res_f32 ? (const void*)(static_cast<const float*>(args.res) + ro)
                                           : (const void*)(static_cast<const __nv_bfloat16*>(args.res) + ro);
-            add16(rp, args.res_f32, v);
+            add16(rp, args.res_f32, v, args.res_lo);
           }
         } else {  // kEpiDup
           const int sf = (f + (args.dup_first ? args.dup_ft - 1 : 0)) / args.dup_ft;
@@ -217,17 +236,19 @@ __global__ void __launch_bounds__(256, 1)
               sp * args.dup_ldc;
           if (args.dup_pairs) {
             // channel c reads source channel 2c + (row & 1)
-            const uint4* s4 = reinterpret_cast<const uint4*>(src + 2 * n0);
             const int odd = yy & 1;
+            for (int part = 0; part < (args.dup_lo ? 2 : 1); ++part) {
+              const uint4* s4 = reinterpret_cast<const uint4*>(src + 2 * n0 + (part ? args.dup_lo : 0));
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const uint4 a = s4[h];
-              const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+              for (int h = 0; h < 4; ++h) {
+                const uint4 a = s4[h];
+                const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-              for (int i = 0; i < 4; ++i) v[4 * h + i] += odd ? bf16_hi(w[i]) : bf16_lo(w[i]);
+                for (int i = 0; i < 4; ++i) v[4 * h + i] += odd ? bf16_hi(w[i]) : bf16_lo(w[i]);
+              }
             }
           } else {
-            add16(src + n0, 0, v);
+            add16(src + n0, 0, v, args.dup_lo);
           }
         }
         int fo = args.out_f0 + f * args.out_fmul;
@@ -239,7 +260,7 @@ __global__ void __launch_bounds__(256, 1)
         const long long oo = (long long)b * args.out_bs + (long long)fo * args.out_fs + pos * args.out_ldc + no;
         void* op = args.out_f32 ? (void*)(static_cast<float*>(args.out) + oo)
                                 : (void*)(static_cast<__nv_bfloat16*>(args.out) + oo);
-        store16(op, args.out_f32, v);
+        store16(op, args.out_f32, v, args.out_lo);
       }
     }
   }

@@ -22,7 +22,7 @@ inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + 
 constexpr int kNormMaxC = 1024;
 template <bool SILU>
 __global__ void rms_norm_kernel(FrameView in, FrameView out, const float* __restrict__ gs, int C, int F, int P,
-                                long long rows) {
+                                long long rows, int in_lo, int out_lo) {
   const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -32,20 +32,30 @@ __global__ void rms_norm_kernel(FrameView in, FrameView out, const float* __rest
   const __nv_bfloat16* src = at(in, b, f, p);
   __nv_bfloat16* dst = at_mut(out, b, f, p);
   constexpr int kMaxChunks = kNormMaxC / 256;
-  uint4 x[kMaxChunks];
+  float x[kMaxChunks][8];
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxChunks; ++j) {
     const int c = lane * 8 + j * 256;
     if (c < C) {
-      x[j] = *reinterpret_cast<const uint4*>(src + c);
-      const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+      const uint4 a4 = *reinterpret_cast<const uint4*>(src + c);
+      const uint32_t w[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float a = bf16_lo(w[i]), bb = bf16_hi(w[i]);
-        ss = fmaf(a, a, ss);
-        ss = fmaf(bb, bb, ss);
+        x[j][2 * i] = bf16_lo(w[i]);
+        x[j][2 * i + 1] = bf16_hi(w[i]);
       }
+      if (in_lo) {  // split format: value = hi + lo
+        const uint4 b4 = *reinterpret_cast<const uint4*>(src + in_lo + c);
+        const uint32_t u[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[j][2 * i] += bf16_lo(u[i]);
+          x[j][2 * i + 1] += bf16_hi(u[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(x[j][i], x[j][i], ss);
     }
   }
 #pragma unroll
@@ -55,22 +65,30 @@ __global__ void rms_norm_kernel(FrameView in, FrameView out, const float* __rest
   for (int j = 0; j < kMaxChunks; ++j) {
     const int c = lane * 8 + j * 256;
     if (c < C) {
-      const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
       const float4 g0 = *reinterpret_cast<const float4*>(gs + c);
       const float4 g1 = *reinterpret_cast<const float4*>(gs + c + 4);
       const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      uint32_t o[4];
+      float y[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float a = bf16_lo(w[i]) * rinv * g[2 * i];
-        float bb = bf16_hi(w[i]) * rinv * g[2 * i + 1];
-        if (SILU) {
-          a = a / (1.0f + expf(-a));
-          bb = bb / (1.0f + expf(-bb));
-        }
-        o[i] = pack_bf16x2(a, bb);
+      for (int i = 0; i < 8; ++i) {
+        y[i] = x[j][i] * rinv * g[i];
+        if (SILU) y[i] = y[i] / (1.0f + expf(-y[i]));
       }
-      *reinterpret_cast<uint4*>(dst + c) = make_uint4(o[0], o[1], o[2], o[3]);
+      if (out_lo) {
+        float h[8], l[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          h[i] = __bfloat162float(__float2bfloat16_rn(y[i]));
+          l[i] = y[i] - h[i];
+        }
+        *reinterpret_cast<uint4*>(dst + c) = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]),
+                                                        pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+        *reinterpret_cast<uint4*>(dst + out_lo + c) = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]),
+                                                                 pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
+      } else {
+        *reinterpret_cast<uint4*>(dst + c) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                        pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+      }
     }
   }
 }
@@ -106,7 +124,7 @@ __global__ void copy_frames_kernel(FrameView in, FrameView out, int C8, int F, i
 constexpr int kZ = 48;
 __global__ void post_quant_kernel(const void* __restrict__ z, int z_f32, int Tz, int t0, int F, int P,
                                   const float* __restrict__ w, const float* __restrict__ bias, FrameView out,
-                                  long long n, int round_z) {
+                                  long long n, int round_z, int out_lo) {
   __shared__ float sw[kZ * kZ];
   __shared__ float sb[kZ];
   for (int i = threadIdx.x; i < kZ * kZ; i += blockDim.x) sw[i] = w[i];
@@ -136,15 +154,23 @@ __global__ void post_quant_kernel(const void* __restrict__ z, int z_f32, int Tz,
       for (int c = 0; c < kZ; ++c) s = fmaf(sw[(co + k) * kZ + c], zin[c], s);
       acc[k] = s;
     }
-    *reinterpret_cast<uint4*>(dst + co) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    float h[8], l[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      h[k] = out_lo ? __bfloat162float(__float2bfloat16_rn(acc[k])) : acc[k];
+      l[k] = acc[k] - h[k];
+    }
+    *reinterpret_cast<uint4*>(dst + co) = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]),
+                                                     pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+    if (out_lo)
+      *reinterpret_cast<uint4*>(dst + out_lo + co) = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]),
+                                                                pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
   }
-  for (int c = kZ; c < out.ldc; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
 }
 
 // One 256-thread block per row.
 __global__ void softmax_rows_kernel(const float* __restrict__ S, long long ld_s, __nv_bfloat16* __restrict__ Pm,
-                                    long long ld_p, int n, float scale) {
+                                    long long ld_p, int n, float scale, int p_lo) {
   const float* s = S + (long long)blockIdx.x * ld_s;
   __nv_bfloat16* p = Pm + (long long)blockIdx.x * ld_p;
   __shared__ float red[32];
@@ -177,7 +203,12 @@ __global__ void softmax_rows_kernel(const float* __restrict__ S, long long ld_s,
   }
   __syncthreads();
   const float inv = 1.0f / red[0];
-  for (int j = threadIdx.x; j < n; j += blockDim.x) p[j] = __float2bfloat16_rn(expf((s[j] - mx) * scale) * inv);
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const float v = expf((s[j] - mx) * scale) * inv;
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    p[j] = h;
+    if (p_lo) p[p_lo + j] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
 }
 
 // 32 x 32 tiles through shared memory.
@@ -221,14 +252,15 @@ __global__ void ring_shift_kernel(const __grid_constant__ RingTable t) {
 }
 
 __global__ void pack_weight_kernel(const void* __restrict__ src, int src_f32, int Co, int Ci, int taps,
-                                   __nv_bfloat16* __restrict__ dst, int ld, int k0, int ci_pad, long long n) {
+                                   __nv_bfloat16* __restrict__ dst, int ld, int k0, int ci_pad, long long n, int lo) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const int tap = (int)(i % taps);
   const int ci = (int)((i / taps) % Ci);
   const int co = (int)(i / ((long long)taps * Ci));
   const float v = src_f32 ? static_cast<const float*>(src)[i] : __bfloat162float(static_cast<const __nv_bfloat16*>(src)[i]);
-  dst[(long long)co * ld + k0 + (long long)tap * ci_pad + ci] = __float2bfloat16_rn(v);
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  dst[(long long)co * ld + k0 + (long long)tap * ci_pad + ci] = lo ? __float2bfloat16_rn(v - __bfloat162float(h)) : h;
 }
 
 __device__ __forceinline__ float load_any(const void* p, int f32, int i, int rnd) {
@@ -248,15 +280,15 @@ __global__ void to_f32_kernel(const void* __restrict__ src, int src_f32, const v
 }  // namespace
 
 cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, bool silu,
-                            cudaStream_t s) {
+                            cudaStream_t s, int in_lo, int out_lo) {
   if (C > kNormMaxC || C % 8) return cudaErrorInvalidValue;
   const long long rows = (long long)B * F * P;
   if (rows == 0) return cudaSuccess;
   const unsigned grid = blocks_for(rows, 8);
   if (silu)
-    rms_norm_kernel<true><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows);
+    rms_norm_kernel<true><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
   else
-    rms_norm_kernel<false><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows);
+    rms_norm_kernel<false><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
   return cudaGetLastError();
 }
 
@@ -277,19 +309,19 @@ cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F,
 }
 
 cudaError_t launch_post_quant(const void* z, int z_f32, int B, int Tz, int t0, int F, int P, const float* w,
-                              const float* bias, FrameView out, int round_z_bf16, cudaStream_t s) {
+                              const float* bias, FrameView out, int round_z_bf16, cudaStream_t s, int out_lo) {
   if (out.ldc % 8 || out.ldc < kZ) return cudaErrorInvalidValue;
   const long long n = (long long)B * F * P;
   if (n == 0) return cudaSuccess;
-  post_quant_kernel<<<blocks_for(n, 128), 128, 0, s>>>(z, z_f32, Tz, t0, F, P, w, bias, out, n, round_z_bf16);
+  post_quant_kernel<<<blocks_for(n, 128), 128, 0, s>>>(z, z_f32, Tz, t0, F, P, w, bias, out, n, round_z_bf16, out_lo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_softmax_rows(const float* S, long long ld_s, __nv_bfloat16* P, long long ld_p, int n, long long R,
-                                float scale, cudaStream_t s) {
+                                float scale, cudaStream_t s, int p_lo) {
   if (R == 0) return cudaSuccess;
   if (R > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  softmax_rows_kernel<<<(unsigned)R, 256, 0, s>>>(S, ld_s, P, ld_p, n, scale);
+  softmax_rows_kernel<<<(unsigned)R, 256, 0, s>>>(S, ld_s, P, ld_p, n, scale, p_lo);
   return cudaGetLastError();
 }
 
@@ -318,10 +350,10 @@ cudaError_t launch_ring_shift(const RingShift* rings, int n, cudaStream_t s) {
 }
 
 cudaError_t launch_pack_weight(const void* src, int src_f32, int Co, int Ci, int taps, __nv_bfloat16* dst, int ld,
-                               int k0, int ci_pad, cudaStream_t s) {
+                               int k0, int ci_pad, cudaStream_t s, int lo) {
   const long long n = (long long)Co * Ci * taps;
   if (n == 0) return cudaSuccess;
-  pack_weight_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, src_f32, Co, Ci, taps, dst, ld, k0, ci_pad, n);
+  pack_weight_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, src_f32, Co, Ci, taps, dst, ld, k0, ci_pad, n, lo);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,9 @@ struct ConvArgs {
   int out_f32;
   long long out_bs, out_fs;
   int out_ldc, out_f0, out_fmul, interleave_c;
+  // Split format (fp32 decode): a value v is stored as bf16 hi = bf16(v) at
+  // channel n and bf16 lo = bf16(v - hi) at channel n + *_lo; 0 = plain.
+  int out_lo, res_lo, dup_lo;
   // kEpiStore: optional residual added at the same (b, y, x, n), frame res_f0 + f
   const void* res;
   int res_f32;
@@ -98,8 +101,9 @@ struct FrameView {
 };
 
 // y = x / max(||x||, 1e-12) * gs (gs = sqrt(C)*gamma, fp32), then SiLU if silu.
+// in_lo / out_lo: split-format offsets of the low halves (0 = plain bf16).
 cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, bool silu,
-                            cudaStream_t s);
+                            cudaStream_t s, int in_lo = 0, int out_lo = 0);
 // nearest x2: out(b, f, 2y+i, 2x+j, c) = in(b, f, y, x, c); in is H x W.
 cudaError_t launch_upsample2x(FrameView in, FrameView out, int C, int B, int F, int H, int W, cudaStream_t s);
 // copy F frames of C channels
@@ -107,11 +111,11 @@ cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F,
 // post_quant_conv: z [B][48][Tz][h][w] (fp32 or bf16, NCDHW), frames t0..t0+F-1
 // -> out(b, f, p, 0..47) bf16; channels 48..ldc-1 are written as zero.
 cudaError_t launch_post_quant(const void* z, int z_f32, int B, int Tz, int t0, int F, int P, const float* w /*48x48*/,
-                              const float* bias, FrameView out, int round_z_bf16, cudaStream_t s);
+                              const float* bias, FrameView out, int round_z_bf16, cudaStream_t s, int out_lo = 0);
 // Row softmax of S [R][ld_s] fp32 (n valid columns) scaled by `scale`, into
 // P [R][ld_p] bf16.
 cudaError_t launch_softmax_rows(const float* S, long long ld_s, __nv_bfloat16* P, long long ld_p, int n, long long R,
-                                float scale, cudaStream_t s);
+                                float scale, cudaStream_t s, int p_lo = 0);
 // Vt[g][c][p] = src[g][p][c] (bf16), p < P, c < C; src row stride ld_src.
 cudaError_t launch_transpose(const __nv_bfloat16* src, long long src_gs, int ld_src, __nv_bfloat16* dst,
                              long long dst_gs, int ld_dst, int G, int P, int C, cudaStream_t s);
@@ -127,8 +131,9 @@ constexpr int kMaxRings = 48;
 cudaError_t launch_ring_shift(const RingShift* rings, int n, cudaStream_t s);
 // Weight packing: src [Co][Ci][taps] (fp32 or bf16, taps = kt*kh*kw) ->
 // dst[co][k0 + tap*ci_pad + ci] bf16 for co < Co, ci < Ci; dst has ld columns.
+// lo = 1 packs the low half bf16(w - bf16(w)) of the split format instead.
 cudaError_t launch_pack_weight(const void* src, int src_f32, int Co, int Ci, int taps, __nv_bfloat16* dst, int ld,
-                               int k0, int ci_pad, cudaStream_t s);
+                               int k0, int ci_pad, cudaStream_t s, int lo = 0);
 // dst[i] = scale * r(src[i]) (+ r(src2[i]) if src2) as fp32; src fp32 or bf16;
 // r rounds to the nearest bf16 when round_bf16 is set.
 cudaError_t launch_to_f32(const void* src, int src_f32, const void* src2, int src2_f32, float* dst, int n,

@@ -89,6 +89,8 @@ static wan_status encode(CUtensorMap* m, int rank, const void* base, const uint6
 struct Act {
   bf16* p = nullptr;
   int B = 0, F = 0, H = 0, W = 0, C = 0, ldc = 0;
+  int lo = 0;  // split format: low halves at channel offset lo (0: plain bf16)
+  int chans() const { return lo ? ldc : C; }  // channels a copy must move
   long long fs() const { return (long long)H * W * ldc; }
   long long bs() const { return (long long)F * fs(); }
   size_t bytes() const { return (size_t)B * bs() * sizeof(bf16); }
@@ -165,6 +167,7 @@ struct ConvW {
   int Co = 0, Ci = 0, kt = 1, kh = 1, kw = 1;
   int ci_pad = 0, ktot = 0, co_pad = 0, bn = 0;
   int sc_Ci = 0, sc_ci_pad = 0;  // appended 1x1x1 shortcut conv
+  int split = 0;                 // hi/lo weight halves per tap (fp32 decode)
 };
 
 static int choose_bn(int co) {
@@ -215,9 +218,11 @@ static wan_status check_shape(const wan_tensor* t, std::vector<long long> want) 
 
 // Packs `name` (conv3d [Co,Ci,kt,kh,kw] or conv2d [Co,Ci,kh,kw]) and, if
 // given, a 1x1x1 shortcut conv appended along K.
+// Split mode (fp32 decode): each tap holds the weights' bf16 high halves
+// followed by their low halves, K = taps * 2 * ci_pad (+ 2 * sc_ci_pad).
 static wan_status pack_conv(const WeightTable& wt, const std::string& name, int Co, int Ci, int kt, int kh, int kw,
                             bool conv2d, const std::string& sc_name, int sc_Ci, ConvW& cw, DevMem& mem,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool split = false) {
   const wan_tensor *W, *Bi;
   WAN_TRY(get_tensor(wt, name + ".weight", &W));
   WAN_TRY(get_tensor(wt, name + ".bias", &Bi));
@@ -243,27 +248,32 @@ static wan_status pack_conv(const WeightTable& wt, const std::string& name, int 
   cw.sc_Ci = Ws ? sc_Ci : 0;
   cw.sc_ci_pad = Ws ? (int)rup(sc_Ci, 64) : 0;
   const int taps = kt * kh * kw;
-  cw.ktot = taps * cw.ci_pad + cw.sc_ci_pad;
+  const int sp = split ? 2 : 1;
+  cw.split = split ? 1 : 0;
+  cw.ktot = sp * (taps * cw.ci_pad + cw.sc_ci_pad);
   cw.bn = choose_bn(Co);
   cw.co_pad = (int)rup(Co, cw.bn);
   void* p;
   WAN_TRY(mem.alloc(&p, (size_t)cw.co_pad * cw.ktot * sizeof(bf16)));
   cw.w = (bf16*)p;
   CUDA_TRY(cudaMemsetAsync(cw.w, 0, (size_t)cw.co_pad * cw.ktot * sizeof(bf16), s));
-  CUDA_TRY(launch_pack_weight(W->data, W->dtype == WAN_F32, Co, Ci, taps, cw.w, cw.ktot, 0, cw.ci_pad, s));
-  if (Ws)
-    CUDA_TRY(launch_pack_weight(Ws->data, Ws->dtype == WAN_F32, Co, sc_Ci, 1, cw.w, cw.ktot, taps * cw.ci_pad,
-                                cw.sc_ci_pad, s));
+  for (int part = 0; part < sp; ++part) {
+    CUDA_TRY(launch_pack_weight(W->data, W->dtype == WAN_F32, Co, Ci, taps, cw.w, cw.ktot, part * cw.ci_pad,
+                                sp * cw.ci_pad, s, part));
+    if (Ws)
+      CUDA_TRY(launch_pack_weight(Ws->data, Ws->dtype == WAN_F32, Co, sc_Ci, 1, cw.w, cw.ktot,
+                                  sp * taps * cw.ci_pad + part * cw.sc_ci_pad, cw.sc_ci_pad, s, part));
+  }
   WAN_TRY(mem.alloc(&p, (size_t)Co * sizeof(float)));
   cw.bias = (float*)p;
   CUDA_TRY(launch_to_f32(Bi->data, Bi->dtype == WAN_F32, Bs ? Bs->data : nullptr, Bs ? Bs->dtype == WAN_F32 : 0,
-                         cw.bias, Co, 1.0f, 1, s));
+                         cw.bias, Co, 1.0f, split ? 0 : 1, s));
   return WAN_OK;
 }
 
 // sqrt(C) * gamma in fp32
 static wan_status pack_gamma(const WeightTable& wt, const std::string& name, int C, float** out, DevMem& mem,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool split = false) {
   const wan_tensor* g;
   WAN_TRY(get_tensor(wt, name, &g));
   if (numel(g) != C) return fail(WAN_ERR_SHAPE, "weight '%s': %lld values, expected %d", name.c_str(), numel(g), C);
@@ -271,7 +281,7 @@ static wan_status pack_gamma(const WeightTable& wt, const std::string& name, int
   void* p;
   WAN_TRY(mem.alloc(&p, (size_t)C * sizeof(float)));
   *out = (float*)p;
-  CUDA_TRY(launch_to_f32(g->data, g->dtype == WAN_F32, nullptr, 0, *out, C, std::sqrt((float)C), 1, s));
+  CUDA_TRY(launch_to_f32(g->data, g->dtype == WAN_F32, nullptr, 0, *out, C, std::sqrt((float)C), split ? 0 : 1, s));
   return WAN_OK;
 }
 
@@ -288,6 +298,7 @@ struct Resnet {
 
 struct wan_vae_model {
   int base = 0, dtype = WAN_BF16;
+  bool split = false;  // fp32 decode: activations and weights as bf16 hi/lo pairs
   float* pq_w = nullptr;
   float* pq_b = nullptr;
   ConvW conv_in;
@@ -308,21 +319,20 @@ static const int kUp[4][4] = {{4, 4, 1, 1}, {4, 4, 1, 1}, {4, 2, 0, 1}, {2, 1, 0
 static const int kZdim = 48;
 
 static wan_status pack_resnet(const WeightTable& wt, const std::string& name, int ci, int co, Resnet& r, DevMem& mem,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool split) {
   r.ci = ci;
   r.co = co;
-  WAN_TRY(pack_gamma(wt, name + ".norm1.gamma", ci, &r.g1, mem, s));
-  WAN_TRY(pack_gamma(wt, name + ".norm2.gamma", co, &r.g2, mem, s));
-  WAN_TRY(pack_conv(wt, name + ".conv1", co, ci, 3, 3, 3, false, "", 0, r.c1, mem, s));
+  WAN_TRY(pack_gamma(wt, name + ".norm1.gamma", ci, &r.g1, mem, s, split));
+  WAN_TRY(pack_gamma(wt, name + ".norm2.gamma", co, &r.g2, mem, s, split));
+  WAN_TRY(pack_conv(wt, name + ".conv1", co, ci, 3, 3, 3, false, "", 0, r.c1, mem, s, split));
   WAN_TRY(pack_conv(wt, name + ".conv2", co, co, 3, 3, 3, false, ci != co ? name + ".conv_shortcut" : "", ci, r.c2,
-                    mem, s));
+                    mem, s, split));
   return WAN_OK;
 }
 
 static wan_status model_build(const wan_tensor* weights, int n, int dtype, cudaStream_t s, wan_vae_model* m) {
   if (!weights || n <= 0) return fail(WAN_ERR_INVALID_ARG, "empty weight table");
   if (dtype != WAN_F32 && dtype != WAN_BF16) return fail(WAN_ERR_DTYPE, "dtype must be WAN_F32 or WAN_BF16, not %d", dtype);
-  if (dtype == WAN_F32) return fail(WAN_ERR_NOT_IMPLEMENTED, "the fp32 decode is not implemented in this build");
   WeightTable wt{weights, n};
   const wan_tensor* ci;
   WAN_TRY(get_tensor(wt, "decoder.conv_in.weight", &ci));
@@ -333,6 +343,8 @@ static wan_status model_build(const wan_tensor* weights, int n, int dtype, cudaS
     return fail(WAN_ERR_UNSUPPORTED, "decoder base dim %d: must be a multiple of 8 and at most 256", b);
   m->base = b;
   m->dtype = dtype;
+  m->split = dtype == WAN_F32;
+  const bool sp = m->split;
   DevMem& mem = m->mem;
   // post_quant_conv 48 -> 48 (fp32, CUDA-core kernel)
   {
@@ -347,29 +359,32 @@ static wan_status model_build(const wan_tensor* weights, int n, int dtype, cudaS
     m->pq_w = (float*)p;
     WAN_TRY(mem.alloc(&p, kZdim * sizeof(float)));
     m->pq_b = (float*)p;
-    CUDA_TRY(launch_to_f32(w->data, w->dtype == WAN_F32, nullptr, 0, m->pq_w, kZdim * kZdim, 1.0f, 1, s));
-    CUDA_TRY(launch_to_f32(bb->data, bb->dtype == WAN_F32, nullptr, 0, m->pq_b, kZdim, 1.0f, 1, s));
+    CUDA_TRY(launch_to_f32(w->data, w->dtype == WAN_F32, nullptr, 0, m->pq_w, kZdim * kZdim, 1.0f, sp ? 0 : 1, s));
+    CUDA_TRY(launch_to_f32(bb->data, bb->dtype == WAN_F32, nullptr, 0, m->pq_b, kZdim, 1.0f, sp ? 0 : 1, s));
     }
   }
   const int c4 = 4 * b;
-  WAN_TRY(pack_conv(wt, "decoder.conv_in", c4, kZdim, 3, 3, 3, false, "", 0, m->conv_in, mem, s));
-  WAN_TRY(pack_resnet(wt, "decoder.mid_block.resnets.0", c4, c4, m->mid[0], mem, s));
-  WAN_TRY(pack_resnet(wt, "decoder.mid_block.resnets.1", c4, c4, m->mid[1], mem, s));
-  WAN_TRY(pack_gamma(wt, "decoder.mid_block.attentions.0.norm.gamma", c4, &m->attn_g, mem, s));
-  WAN_TRY(pack_conv(wt, "decoder.mid_block.attentions.0.to_qkv", 3 * c4, c4, 1, 1, 1, true, "", 0, m->qkv, mem, s));
-  WAN_TRY(pack_conv(wt, "decoder.mid_block.attentions.0.proj", c4, c4, 1, 1, 1, true, "", 0, m->proj, mem, s));
+  WAN_TRY(pack_conv(wt, "decoder.conv_in", c4, kZdim, 3, 3, 3, false, "", 0, m->conv_in, mem, s, sp));
+  WAN_TRY(pack_resnet(wt, "decoder.mid_block.resnets.0", c4, c4, m->mid[0], mem, s, sp));
+  WAN_TRY(pack_resnet(wt, "decoder.mid_block.resnets.1", c4, c4, m->mid[1], mem, s, sp));
+  WAN_TRY(pack_gamma(wt, "decoder.mid_block.attentions.0.norm.gamma", c4, &m->attn_g, mem, s, sp));
+  WAN_TRY(pack_conv(wt, "decoder.mid_block.attentions.0.to_qkv", 3 * c4, c4, 1, 1, 1, true, "", 0, m->qkv, mem, s, sp));
+  WAN_TRY(pack_conv(wt, "decoder.mid_block.attentions.0.proj", c4, c4, 1, 1, 1, true, "", 0, m->proj, mem, s, sp));
   for (int i = 0; i < 4; ++i) {
     const int cin = kUp[i][0] * b, cout = kUp[i][1] * b;
     const std::string nm = "decoder.up_blocks." + std::to_string(i);
     for (int j = 0; j < 3; ++j)
-      WAN_TRY(pack_resnet(wt, nm + ".resnets." + std::to_string(j), j == 0 ? cin : cout, cout, m->up[i][j], mem, s));
+      WAN_TRY(pack_resnet(wt, nm + ".resnets." + std::to_string(j), j == 0 ? cin : cout, cout, m->up[i][j], mem, s,
+                          sp));
     if (kUp[i][2])
-      WAN_TRY(pack_conv(wt, nm + ".upsampler.time_conv", 2 * cout, cout, 3, 1, 1, false, "", 0, m->tconv[i], mem, s));
+      WAN_TRY(pack_conv(wt, nm + ".upsampler.time_conv", 2 * cout, cout, 3, 1, 1, false, "", 0, m->tconv[i], mem, s,
+                        sp));
     if (kUp[i][3])
-      WAN_TRY(pack_conv(wt, nm + ".upsampler.resample.1", cout, cout, 1, 3, 3, true, "", 0, m->resample[i], mem, s));
+      WAN_TRY(pack_conv(wt, nm + ".upsampler.resample.1", cout, cout, 1, 3, 3, true, "", 0, m->resample[i], mem, s,
+                        sp));
   }
-  WAN_TRY(pack_gamma(wt, "decoder.norm_out.gamma", b, &m->out_g, mem, s));
-  WAN_TRY(pack_conv(wt, "decoder.conv_out", 12, b, 3, 3, 3, false, "", 0, m->conv_out, mem, s));
+  WAN_TRY(pack_gamma(wt, "decoder.norm_out.gamma", b, &m->out_g, mem, s, sp));
+  WAN_TRY(pack_conv(wt, "decoder.conv_out", 12, b, 3, 3, 3, false, "", 0, m->conv_out, mem, s, sp));
   if (!mem.dry) CUDA_TRY(cudaGetLastError());
   return WAN_OK;
 }
@@ -392,9 +407,11 @@ struct AttnBufs {
   bf16* P = nullptr;
   bf16* Vt = nullptr;
   int HW = 0, HWs = 0, HWp = 0, Fmax = 0, B = 0, C = 0;
+  int sp = 1;  // 2 in split mode: P and V^T rows hold [hi HWp | lo HWp]
+  long long ldp() const { return (long long)sp * HWp; }
   long long s_bs() const { return (long long)Fmax * HW * HWs; }
-  long long p_bs() const { return (long long)Fmax * HW * HWp; }
-  long long vt_fs() const { return (long long)C * HWp; }
+  long long p_bs() const { return (long long)Fmax * HW * ldp(); }
+  long long vt_fs() const { return (long long)C * ldp(); }
   long long vt_bs() const { return (long long)Fmax * vt_fs(); }
 };
 
@@ -439,6 +456,11 @@ static wan_status make_act(wan_vae_stream* st, Act& a, int F, int H, int W, int 
   a.W = W;
   a.C = C;
   a.ldc = (int)rup(C, ldc_mult);
+  a.lo = 0;
+  if (st->m->split) {  // [hi | lo] halves per position
+    a.lo = a.ldc;
+    a.ldc *= 2;
+  }
   if (!st->ws) {
     st->ws_used = rup(st->ws_used, 256) + a.bytes();
     return WAN_OK;
@@ -481,6 +503,7 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   at.Fmax = n;
   at.B = st->B;
   at.C = c4;
+  at.sp = st->m->split ? 2 : 1;
   WAN_TRY(make_act(st, at.an, n, 1, at.HW, c4));
   WAN_TRY(make_act(st, at.qkv, n, 1, at.HW, 3 * c4));
   WAN_TRY(make_act(st, at.O, n, 1, at.HW, c4));
@@ -526,16 +549,40 @@ struct OutSpec {
   void* p = nullptr;
   int f32 = 0;
   long long bs = 0, fs = 0;
-  int ldc = 0, f0 = 0, fmul = 1, interleave = 0;
+  int ldc = 0, f0 = 0, fmul = 1, interleave = 0, lo = 0;
 };
 static OutSpec out_of(const Act& a, int f0 = 0) {
   OutSpec o;
   o.p = a.p;
+  o.lo = a.lo;
   o.bs = a.bs();
   o.fs = a.fs();
   o.ldc = a.ldc;
   o.f0 = f0;
   return o;
+}
+
+// Appends the K slices of one kernel tap: cpad input channels of source
+// `src` against B columns kb..kb+cpad.  In split mode a value is hi + lo in
+// both operands and the tap becomes three slices, hi*hi + hi*lo + lo*hi
+// (B's lo half follows its hi half at kb + cpad; A's at channel a_lo); the
+// dropped lo*lo term is below 2^-16 of the product.
+static wan_status add_tap(ConvArgs& A, int& nt, int src, int dt, int dy, int dx, int cpad, int a_lo, int kb,
+                          int split) {
+  const int parts = split ? 3 : 1;
+  if (nt + parts > kMaxTaps) return fail(WAN_ERR_INTERNAL, "too many K slices");
+  for (int q = 0; q < parts; ++q) {
+    ConvTap& t = A.taps[nt++];
+    t.src = (int8_t)src;
+    t.dt = (int8_t)dt;
+    t.dy = (int8_t)dy;
+    t.dx = (int8_t)dx;
+    t.a_c0 = (int16_t)(q == 2 ? a_lo : 0);
+    t.nkb = (int16_t)(cpad / 64);
+    t.b_k0 = kb + (q == 1 ? cpad : 0);
+    A.total_kb += cpad / 64;
+  }
+  return WAN_OK;
 }
 
 // Fills the launch for conv `cw` reading A source 0 (`a0`, output frame 0 at
@@ -551,33 +598,20 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   else
     L.a1 = L.a0;
   WAN_TRY(b_map(&L.b, cw.w, cw.ktot, cw.co_pad, 1, cw.ktot, (long long)cw.ktot * cw.co_pad, cw.bn));
+  if (cw.split && (!a0.lo || (a1 && !a1->lo))) return fail(WAN_ERR_INTERNAL, "split conv on a plain tensor");
   int nt = 0, k = 0;
   for (int dt = 0; dt < cw.kt; ++dt)
     for (int dy = 0; dy < cw.kh; ++dy)
       for (int dx = 0; dx < cw.kw; ++dx) {
-        ConvTap& t = A.taps[nt++];
-        t.src = 0;
-        t.dt = (int8_t)dt;
-        t.dy = (int8_t)(dy - cw.kh / 2);
-        t.dx = (int8_t)(dx - cw.kw / 2);
-        t.a_c0 = 0;
-        t.nkb = (int16_t)(cw.ci_pad / 64);
-        t.b_k0 = k;
-        k += cw.ci_pad;
+        WAN_TRY(add_tap(A, nt, 0, dt, dy - cw.kh / 2, dx - cw.kw / 2, cw.ci_pad, a0.lo, k, cw.split));
+        k += (cw.split ? 2 : 1) * cw.ci_pad;
       }
   if (cw.sc_ci_pad) {
     if (!a1) return fail(WAN_ERR_INTERNAL, "shortcut conv without its source");
-    ConvTap& t = A.taps[nt++];
-    t.src = 1;
-    t.dt = 0;
-    t.dy = t.dx = 0;
-    t.a_c0 = 0;
-    t.nkb = (int16_t)(cw.sc_ci_pad / 64);
-    t.b_k0 = k;
-    k += cw.sc_ci_pad;
+    WAN_TRY(add_tap(A, nt, 1, 0, 0, 0, cw.sc_ci_pad, a1->lo, k, cw.split));
+    k += (cw.split ? 2 : 1) * cw.sc_ci_pad;
   }
   A.n_taps = nt;
-  A.total_kb = k / 64;
   A.box_w = 16;
   A.box_h = 8;
   A.H = a0.H;
@@ -605,6 +639,7 @@ static void set_out(ConvArgs& A, const OutSpec& o) {
   A.out_f0 = o.f0;
   A.out_fmul = o.fmul;
   A.interleave_c = o.interleave;
+  A.out_lo = o.lo;
 }
 
 // Enqueues a tensor-core launch; when profiling, brackets it with CUDA events
@@ -648,6 +683,7 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
     L.args.res_bs = res->bs();
     L.args.res_fs = res->fs();
     L.args.res_ldc = res->ldc;
+    L.args.res_lo = res->lo;
   }
   WAN_TRY(run(L, &st->prof, kind, conv_flops(cw, in, F), st->err_dev, s));
   st->shifts.push_back(RingShift{in.p, in.fs(), in.bs(), F, in.B});
@@ -658,9 +694,9 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
 static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act& ring1, Act& ring2, Act& Ht, Act& y,
                          int F, cudaStream_t s) {
   const int P = x.H * x.W;
-  ELT(&st->prof, launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s));
+  ELT(&st->prof, launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s, x.lo, ring1.lo));
   WAN_TRY(ring_conv(st, r.c1, ring1, F, out_of(Ht), nullptr, nullptr, s));
-  ELT(&st->prof, launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s));
+  ELT(&st->prof, launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s, Ht.lo, ring2.lo));
   if (r.ci != r.co)
     WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), nullptr, &x, s));
   else
@@ -668,22 +704,27 @@ static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act&
   return WAN_OK;
 }
 
-// Plain batched GEMM launch: A = activation rows (HW positions per frame), B = `bmap`.
-static wan_status gemm_setup(ConvLaunch& L, const bf16* a_base, int a_C, int a_ldc, int HW, int Fmax, int B,
-                             long long a_fs, long long a_bs, int K, int N_tiles_n, int bn, int F) {
+// Batched GEMM launch: A = rows of an activation tensor (HW positions per
+// frame, `a_ldc` channels of which `K` are read, low halves at a_lo), B = a
+// K-major operand whose columns b0.. (low halves at b0 + b_lo) are read.
+static wan_status gemm_setup(ConvLaunch& L, const bf16* a_base, int a_ldc, int a_lo, int HW, int Fmax, int B,
+                             long long a_fs, long long a_bs, int K, int b0, int b_lo, int split, int N_tiles_n, int bn,
+                             int F) {
   memset(&L.args, 0, sizeof(L.args));
-  WAN_TRY(act_map(&L.a0, a_base, a_C, a_ldc, HW, 1, Fmax, B, a_fs, a_bs, 128, 1));
+  WAN_TRY(act_map(&L.a0, a_base, a_ldc, a_ldc, HW, 1, Fmax, B, a_fs, a_bs, 128, 1));
   L.a1 = L.a0;
   ConvArgs& A = L.args;
-  ConvTap& t = A.taps[0];
-  t.src = 0;
-  t.dt = 0;
-  t.dy = t.dx = 0;
-  t.a_c0 = 0;
-  t.nkb = (int16_t)(K / 64);
-  t.b_k0 = 0;
-  A.n_taps = 1;
-  A.total_kb = K / 64;
+  int nt = 0;
+  if (split) {
+    // hi*hi + hi*lo + lo*hi, with B's low half at b0 + b_lo
+    WAN_TRY(add_tap(A, nt, 0, 0, 0, 0, K, a_lo, b0, 0));
+    WAN_TRY(add_tap(A, nt, 0, 0, 0, 0, K, a_lo, b0 + b_lo, 0));
+    WAN_TRY(add_tap(A, nt, 0, 0, 0, 0, K, a_lo, b0, 0));
+    A.taps[2].a_c0 = (int16_t)a_lo;
+  } else {
+    WAN_TRY(add_tap(A, nt, 0, 0, 0, 0, K, 0, b0, 0));
+  }
+  A.n_taps = nt;
   A.box_w = 128;
   A.box_h = 1;
   A.H = 1;
@@ -698,29 +739,30 @@ static wan_status gemm_setup(ConvLaunch& L, const bf16* a_base, int a_C, int a_l
   return WAN_OK;
 }
 
-// Mid-block attention over F frames of x (level A) into y = attn(x) + x.
+// Mid-block attention over F frames of x (level A) into y = attn(x) + x
+// (page "The parts", fourth bullet): RMS norm; qkv = 1x1 conv C -> 3C;
+// S = q k^T per frame (fp32); P = softmax(S / sqrt(C)); O = P v; y = proj(O) + x.
 static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj, AttnBufs& at, const Act& x, Act& y,
                             int F, Prof* prof, int* err, cudaStream_t s) {
   const double M = (double)at.B * F * at.HW;
-  const int C = at.C, HW = at.HW, B = at.B;
+  const int C = at.C, HW = at.HW, B = at.B, sp = at.sp - 1;
   if (HW < 16) return fail(WAN_ERR_UNSUPPORTED, "attention over %d positions (at least 16 supported)", HW);
-  // n = RMS norm of x (no SiLU), rows = positions
-  ELT(prof, launch_rms_norm(x.view(0), at.an.view(0), g, C, B, F, HW, false, s));
+  ELT(prof, launch_rms_norm(x.view(0), at.an.view(0), g, C, B, F, HW, false, s, x.lo, at.an.lo));
   ConvLaunch L;
-  // qkv = n @ Wqkv^T + b
-  WAN_TRY(gemm_setup(L, at.an.p, at.an.ldc, at.an.ldc, HW, at.an.F, B, at.an.fs(), at.an.bs(), qkv.ci_pad,
-                     qkv.co_pad / qkv.bn, qkv.bn, F));
+  // qkv = n Wqkv^T + b; split weights keep their low halves ci_pad after the high ones
+  WAN_TRY(gemm_setup(L, at.an.p, at.an.ldc, at.an.lo, HW, at.an.F, B, at.an.fs(), at.an.bs(), qkv.ci_pad, 0,
+                     qkv.ci_pad, sp, qkv.co_pad / qkv.bn, qkv.bn, F));
   WAN_TRY(b_map(&L.b, qkv.w, qkv.ktot, qkv.co_pad, 1, qkv.ktot, (long long)qkv.ktot * qkv.co_pad, qkv.bn));
   L.args.N = qkv.Co;
   L.args.bias = qkv.bias;
   set_out(L.args, out_of(at.qkv));
   WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * 3 * C * C, err, s));
-  // S = q k^T per frame (fp32)
+  // S = q k^T: q = channels [0, C) of qkv, k = [C, 2C) (low halves 3C further on)
   int bnS = 16;  // largest power of two <= min(HW, 256): the K-operand box stays inside the tensor
   while (bnS * 2 <= std::min(HW, 256)) bnS *= 2;
-  WAN_TRY(gemm_setup(L, at.qkv.p, C, at.qkv.ldc, HW, at.qkv.F, B, at.qkv.fs(), at.qkv.bs(), C,
-                     (int)cdiv(at.HWs, bnS), bnS, F));
-  WAN_TRY(b_map(&L.b, at.qkv.p + C, C, HW, (long long)B * at.Fmax, at.qkv.ldc, at.qkv.fs(), bnS));
+  WAN_TRY(gemm_setup(L, at.qkv.p, at.qkv.ldc, at.qkv.lo, HW, at.qkv.F, B, at.qkv.fs(), at.qkv.bs(), C, C, at.qkv.lo,
+                     sp, (int)cdiv(at.HWs, bnS), bnS, F));
+  WAN_TRY(b_map(&L.b, at.qkv.p, at.qkv.ldc, HW, (long long)B * at.Fmax, at.qkv.ldc, at.qkv.fs(), bnS));
   L.args.b_per_frame = 1;
   L.args.b_gstride = at.Fmax;
   L.args.N = at.HWs;
@@ -734,43 +776,44 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
     set_out(L.args, o);
   }
   WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * HW * C, err, s));
-  // P = softmax(S / sqrt(C)), V^T
+  // P = softmax(S / sqrt(C)); V^T per frame
   const float scale = 1.0f / std::sqrt((float)C);
   for (int b = 0; b < B; ++b) {
-    ELT(prof, launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.HWp, HW, (long long)F * HW,
-                                 scale, s));
-    ELT(prof, launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C, at.qkv.fs(), at.qkv.ldc, at.Vt + b * at.vt_bs(),
-                              at.vt_fs(), at.HWp, F, HW, C, s));
+    ELT(prof, launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.ldp(), HW, (long long)F * HW,
+                                  scale, s, sp ? at.HWp : 0));
+    for (int part = 0; part <= sp; ++part)
+      ELT(prof, launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C + part * at.qkv.lo, at.qkv.fs(), at.qkv.ldc,
+                                 at.Vt + b * at.vt_bs() + part * at.HWp, at.vt_fs(), (int)at.ldp(), F, HW, C, s));
   }
-  // O = P V per frame
+  // O = P V
   const int bnC = choose_bn(C);
-  WAN_TRY(gemm_setup(L, at.P, at.HWp, at.HWp, HW, at.Fmax, B, (long long)HW * at.HWp, at.p_bs(), at.HWp,
-                     (int)cdiv(C, bnC), bnC, F));
-  WAN_TRY(b_map(&L.b, at.Vt, at.HWp, C, (long long)B * at.Fmax, at.HWp, at.vt_fs(), bnC));
+  WAN_TRY(gemm_setup(L, at.P, (int)at.ldp(), sp ? at.HWp : 0, HW, at.Fmax, B, (long long)HW * at.ldp(), at.p_bs(),
+                     at.HWp, 0, at.HWp, sp, (int)cdiv(C, bnC), bnC, F));
+  WAN_TRY(b_map(&L.b, at.Vt, at.ldp(), C, (long long)B * at.Fmax, at.ldp(), at.vt_fs(), bnC));
   L.args.b_per_frame = 1;
   L.args.b_gstride = at.Fmax;
   L.args.N = C;
   set_out(L.args, out_of(at.O));
   WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * HW * C, err, s));
   // y = O Wp^T + b + x
-  WAN_TRY(gemm_setup(L, at.O.p, at.O.ldc, at.O.ldc, HW, at.O.F, B, at.O.fs(), at.O.bs(), proj.ci_pad,
-                     proj.co_pad / proj.bn, proj.bn, F));
+  WAN_TRY(gemm_setup(L, at.O.p, at.O.ldc, at.O.lo, HW, at.O.F, B, at.O.fs(), at.O.bs(), proj.ci_pad, 0, proj.ci_pad,
+                     sp, proj.co_pad / proj.bn, proj.bn, F));
   WAN_TRY(b_map(&L.b, proj.w, proj.ktot, proj.co_pad, 1, proj.ktot, (long long)proj.ktot * proj.co_pad, proj.bn));
   L.args.N = proj.Co;
   L.args.bias = proj.bias;
-  OutSpec o = out_of(y);
-  set_out(L.args, o);
+  set_out(L.args, out_of(y));
   L.args.res = x.p;
   L.args.res_bs = x.bs();
   L.args.res_fs = x.fs();
   L.args.res_ldc = x.ldc;
+  L.args.res_lo = x.lo;
   WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * C * C, err, s));
   return WAN_OK;
 }
 
 // ---------------------------------------------------------------- the chunk
 static wan_status copy_frames(const Act& src, int sf0, const Act& dst, int df0, int F, Prof* prof, cudaStream_t s) {
-  ELT(prof, launch_copy_frames(src.view(sf0), dst.view(df0), src.C, src.B, F, src.H * src.W, s));
+  ELT(prof, launch_copy_frames(src.view(sf0), dst.view(df0), src.chans(), src.B, F, src.H * src.W, s));
   return WAN_OK;
 }
 
@@ -810,6 +853,7 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& up, c
   L.args.dup_W = blk.W;
   L.args.dup_ft = ft;
   L.args.dup_first = first ? 1 : 0;
+  L.args.dup_lo = blk.lo;
   // r = out * ft * 4 / in: 4ft means channel c copies source channel c; r = 2
   // (ft = 1, in = 2 out) means source channel 2c + row parity.
   const int r = cw.Co * ft * 4 / blk.C;
@@ -830,7 +874,8 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   const int P = st->h * st->w;
   st->shifts.clear();
   // 1. post_quant_conv into conv_in's ring
-  ELT(&st->prof, launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, st->ringIn.view(2), 1, s));
+  ELT(&st->prof, launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, st->ringIn.view(2),
+                                   m->split ? 0 : 1, s, st->ringIn.lo));
   // 2. conv_in, mid block
   WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s));
   WAN_TRY(resnet(st, m->mid[0], st->RA[0], st->ringA[0], st->ringA[1], st->HA, st->RA[1], FA, s));
@@ -841,20 +886,20 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   WAN_TRY(resnet(st, m->up[0][1], st->RA[1], st->ringA[6], st->ringA[7], st->HA, st->RA[2], FA, s));
   WAN_TRY(resnet(st, m->up[0][2], st->RA[2], st->ringA[8], st->ringA[9], st->HA, st->RA[1], FA, s));
   WAN_TRY(time_upsample(st, m->tconv[0], st->RA[1], st->tcA, st->tuA, FA, first, s));
-  ELT(&st->prof, launch_upsample2x(st->tuA.view(0), st->upB.view(0), st->tuA.C, st->B, FB, st->tuA.H, st->tuA.W, s));
+  ELT(&st->prof, launch_upsample2x(st->tuA.view(0), st->upB.view(0), st->tuA.chans(), st->B, FB, st->tuA.H, st->tuA.W, s));
   WAN_TRY(resample(st, m->resample[0], st->upB, st->RA[0], 2, first, st->RB[0], FB, s));
   // up block 1 (level B -> C); block input RB[0]
   WAN_TRY(resnet(st, m->up[1][0], st->RB[0], st->ringB[0], st->ringB[1], st->HB, st->RB[1], FB, s));
   WAN_TRY(resnet(st, m->up[1][1], st->RB[1], st->ringB[2], st->ringB[3], st->HB, st->RB[2], FB, s));
   WAN_TRY(resnet(st, m->up[1][2], st->RB[2], st->ringB[4], st->ringB[5], st->HB, st->RB[1], FB, s));
   WAN_TRY(time_upsample(st, m->tconv[1], st->RB[1], st->tcB, st->tuB, FB, first, s));
-  ELT(&st->prof, launch_upsample2x(st->tuB.view(0), st->upC.view(0), st->tuB.C, st->B, FC, st->tuB.H, st->tuB.W, s));
+  ELT(&st->prof, launch_upsample2x(st->tuB.view(0), st->upC.view(0), st->tuB.chans(), st->B, FC, st->tuB.H, st->tuB.W, s));
   WAN_TRY(resample(st, m->resample[1], st->upC, st->RB[0], 2, first, st->RC[0], FC, s));
   // up block 2 (level C -> D); block input RC[0]
   WAN_TRY(resnet(st, m->up[2][0], st->RC[0], st->ringC[0], st->ringC[1], st->HC, st->RC[1], FC, s));
   WAN_TRY(resnet(st, m->up[2][1], st->RC[1], st->ringC[2], st->ringC[3], st->HC, st->RC[2], FC, s));
   WAN_TRY(resnet(st, m->up[2][2], st->RC[2], st->ringC[4], st->ringC[5], st->HC, st->RC[1], FC, s));
-  ELT(&st->prof, launch_upsample2x(st->RC[1].view(0), st->upD.view(0), st->RC[1].C, st->B, FC, st->RC[1].H, st->RC[1].W, s));
+  ELT(&st->prof, launch_upsample2x(st->RC[1].view(0), st->upD.view(0), st->RC[1].chans(), st->B, FC, st->RC[1].H, st->RC[1].W, s));
   WAN_TRY(resample(st, m->resample[2], st->upD, st->RC[0], 1, first, st->RD[0], FC, s));
   // up block 3 (level D)
   WAN_TRY(resnet(st, m->up[3][0], st->RD[0], st->ringD[0], st->ringD[1], st->HD, st->RD[1], FC, s));
@@ -862,7 +907,7 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   WAN_TRY(resnet(st, m->up[3][2], st->RD[2], st->ringD[4], st->ringD[5], st->HD, st->RD[1], FC, s));
   // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
   ELT(&st->prof, launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
-                           st->RD[1].H * st->RD[1].W, true, s));
+                                 st->RD[1].H * st->RD[1].W, true, s, st->RD[1].lo, st->ringOut.lo));
   {
     ConvLaunch L;
     WAN_TRY(conv_setup(m->conv_out, st->ringOut, 0, nullptr, 0, FC, L));
