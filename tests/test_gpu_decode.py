@@ -12,6 +12,7 @@ import torch
 import oracle
 import wan_synth
 from tests.gpu_util import lib_ready, rounded, to_dev, weights_dev
+from tests.parity_log import record
 
 pytestmark = pytest.mark.gpu
 TOL, PSNR_MIN = 4e-2, 40.0
@@ -39,9 +40,11 @@ def _ref(z, w):
     return oracle.decode(oracle.round_bf16(z), rounded(w))
 
 
-def _check(got, ref):
+def _check(got, ref, case=None):
     err = float(np.abs(got - ref).max())
     p = oracle.psnr(got, ref)
+    if case:
+        record(case, err, p)
     assert err <= TOL and p >= PSNR_MIN, (err, p)
     return err, p
 
@@ -59,7 +62,7 @@ def test_tiny_decode(wv, tiny, chunk):
     w, wd = tiny
     z = wan_synth.make_latents((1, 48, 2, 4, 4), seed=1)
     model = wv.Model(wd, dtype=torch.bfloat16)
-    _check(_decode(wv, model, z, chunk), _ref(z, w))
+    _check(_decode(wv, model, z, chunk), _ref(z, w), f"tiny [1,48,2,4,4] bf16 chunk {chunk}")
 
 
 def test_tiny_ragged_batch_and_first_chunk_rules(wv, tiny):
@@ -70,7 +73,7 @@ def test_tiny_ragged_batch_and_first_chunk_rules(wv, tiny):
     model = wv.Model(wd, dtype=torch.bfloat16)
     got = _decode(wv, model, z, 2)
     assert got.shape == (2, 3, 9, 80, 96)
-    _check(got, _ref(z, w))
+    _check(got, _ref(z, w), "tiny [2,48,3,5,6] bf16 chunk 2")
     # batch independence: each sample alone gives the same frames bit for bit
     one = _decode(wv, model, z[1:2], 2)
     np.testing.assert_array_equal(one, got[1:2])
@@ -131,13 +134,15 @@ def test_full_width_small_decode(wv, small, small_ref, chunk):
     _, wd = small
     z, ref = small_ref
     model = wv.Model(wd, dtype=torch.bfloat16)
-    _check(_decode(wv, model, z, chunk), ref)
+    _check(_decode(wv, model, z, chunk), ref, f"full-width [1,48,3,16,16] bf16 chunk {chunk}")
 
 
 # ------------------------------------------------------------------ fp32
-def _check_f32(got, pre, ref_clamped, ref_pre):
+def _check_f32(got, pre, ref_clamped, ref_pre, case=None):
     e1 = float(np.abs(got - ref_clamped).max())
     e2 = float(np.abs(pre - ref_pre).max())
+    if case:
+        record(case, e1, oracle.psnr(got, ref_clamped), preclamp_max_abs=e2)
     assert e1 <= TOL_F32 and e2 <= TOL_F32, (e1, e2)
     return e1, e2
 
@@ -160,7 +165,7 @@ def test_tiny_decode_fp32(wv, tiny, chunk):
     model = wv.Model(wd, dtype=torch.float32)
     got, pre = _decode_f32(wv, model, z, chunk)
     ref, ref_pre = oracle.decode(z, w, return_preclamp=True)
-    _check_f32(got, pre, ref, ref_pre)
+    _check_f32(got, pre, ref, ref_pre, f"tiny [2,48,3,4,5] fp32 chunk {chunk}")
 
 
 def test_full_width_small_decode_fp32(wv, small):
@@ -169,4 +174,4 @@ def test_full_width_small_decode_fp32(wv, small):
     model = wv.Model(wd, dtype=torch.float32)
     got, pre = _decode_f32(wv, model, z, 2)
     ref, ref_pre = oracle.decode(z, w, return_preclamp=True)
-    _check_f32(got, pre, ref, ref_pre)
+    _check_f32(got, pre, ref, ref_pre, "full-width [1,48,3,16,16] fp32 chunk 2")

@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from tests.gpu_util import lib_ready, to_dev
+from tests.parity_log import record
 
 pytestmark = pytest.mark.gpu
 RNG = np.random.default_rng(77)
@@ -74,6 +75,7 @@ def _attention_check(wv, N, C, H, W, frames, seed):
         ref = oracle.attention(xf, w, "a")[0, :, 0].transpose(1, 2, 0).reshape(H * W, C)
         err = np.abs(got[f] - ref)
         rel = np.linalg.norm(got[f] - ref) / np.linalg.norm(ref)
+        record(f"attention block C={C} {H}x{W} frame {f} (bf16)", float(err.max()), None, rel_l2=float(rel))
         assert err.max() <= 4e-2 and rel <= 1e-2, (f, float(err.max()), float(rel))
 
 
