@@ -105,6 +105,12 @@ __global__ void __launch_bounds__(256, 1)
   int t = blockIdx.x;
   const int tn = t % args.tiles_n;
   t /= args.tiles_n;
+  int phase = 0;
+  if (args.subpix) {
+    phase = t & 3;
+    t >>= 2;
+  }
+  const int pi = phase >> 1, pj = phase & 1;
   const int tx = t % args.tiles_x;
   t /= args.tiles_x;
   const int ty = t % args.tiles_y;
@@ -136,13 +142,14 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ producer
     int it = 0;
     bool ok = true;
-    const int gB = args.b_per_frame ? (b * args.b_gstride + f) : 0;
+    const int gB = args.b_per_frame ? (b * args.b_gstride + f) : phase;
+    const int sy = args.subpix ? pi - 1 : 0, sx = args.subpix ? pj - 1 : 0;
     for (int ti = 0; ti < args.n_taps && ok; ++ti) {
       const ConvTap tp = args.taps[ti];
       const CUtensorMap* am = tp.src ? &mapA1 : &mapA0;
       const int fr = args.src_f0[tp.src] + f + tp.dt;
-      const int x0 = tx * args.box_w + tp.dx;
-      const int y0 = ty * args.box_h + tp.dy;
+      const int x0 = tx * args.box_w + tp.dx + sx;
+      const int y0 = ty * args.box_h + tp.dy + sy;
       for (int kb = 0; kb < tp.nkb; ++kb, ++it) {
         const int s = it % S;
         const int r = it / S;
@@ -183,7 +190,8 @@ __global__ void __launch_bounds__(256, 1)
     const int yy = ty * args.box_h + m / args.box_w;
     const int xx = tx * args.box_w + m % args.box_w;
     const bool valid = got && yy < args.H && xx < args.W;
-    const long long pos = (long long)yy * args.W + xx;
+    const long long pos = args.subpix ? (long long)(2 * yy + pi) * (2 * args.W) + (2 * xx + pj)
+                                      : (long long)yy * args.W + xx;
     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
     for (int c = 0; c < BN / 16; ++c) {
@@ -230,13 +238,16 @@ __global__ void __launch_bounds__(256, 1)
           }
         } else {  // kEpiDup
           const int sf = (f + (args.dup_first ? args.dup_ft - 1 : 0)) / args.dup_ft;
-          const long long sp = (long long)(yy >> 1) * args.dup_W + (xx >> 1);
+          // source position of output (Y, X) is (Y >> 1, X >> 1): in the
+          // sub-pixel form that is the tile position itself
+          const long long sp = args.subpix ? (long long)yy * args.dup_W + xx
+                                           : (long long)(yy >> 1) * args.dup_W + (xx >> 1);
           const __nv_bfloat16* src =
               static_cast<const __nv_bfloat16*>(args.dup) + (long long)b * args.dup_bs + (long long)sf * args.dup_fs +
               sp * args.dup_ldc;
           if (args.dup_pairs) {
             // channel c reads source channel 2c + (row & 1)
-            const int odd = yy & 1;
+            const int odd = args.subpix ? pi : (yy & 1);
             for (int part = 0; part < (args.dup_lo ? 2 : 1); ++part) {
               const uint4* s4 = reinterpret_cast<const uint4*>(src + 2 * n0 + (part ? args.dup_lo : 0));
 #pragma unroll
@@ -279,7 +290,8 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
   if (e != cudaSuccess) return e;
   const ConvArgs& a = L.args;
-  const long long grid = (long long)a.tiles_n * a.tiles_x * a.tiles_y * a.frames * a.batches;
+  const long long grid =
+      (long long)a.tiles_n * (a.subpix ? 4 : 1) * a.tiles_x * a.tiles_y * a.frames * a.batches;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)grid, 256, Cfg::kSmem, stream>>>(L.a0, L.a1, L.b, a);

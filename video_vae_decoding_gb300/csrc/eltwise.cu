@@ -93,21 +93,6 @@ __global__ void rms_norm_kernel(FrameView in, FrameView out, const float* __rest
   }
 }
 
-__global__ void upsample2x_kernel(FrameView in, FrameView out, int C8, int F, int H, int W, long long n) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const int c = (int)(i % C8) * 8;
-  long long r = i / C8;
-  const int X = (int)(r % (2 * W));
-  r /= 2 * W;
-  const int Y = (int)(r % (2 * H));
-  r /= 2 * H;
-  const int f = (int)(r % F);
-  const int b = (int)(r / F);
-  const uint4 v = *reinterpret_cast<const uint4*>(at(in, b, f, (long long)(Y >> 1) * W + (X >> 1)) + c);
-  *reinterpret_cast<uint4*>(at_mut(out, b, f, (long long)Y * (2 * W) + X) + c) = v;
-}
-
 __global__ void copy_frames_kernel(FrameView in, FrameView out, int C8, int F, int P, long long n) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
@@ -268,6 +253,37 @@ __device__ __forceinline__ float load_any(const void* p, int f32, int i, int rnd
   return rnd ? __bfloat162float(__float2bfloat16_rn(v)) : v;
 }
 
+// rows dy of a 3-row kernel that land on source offset a for output phase i
+__device__ __forceinline__ bool subpix_tap(int i, int a, int d) {
+  return i == 0 ? (a == 0 ? d == 0 : d >= 1) : (a == 0 ? d <= 1 : d == 2);
+}
+
+__global__ void pack_subpixel_kernel(const void* __restrict__ src, int src_f32, int Co, int Ci,
+                                     __nv_bfloat16* __restrict__ dst, int ld, int co_pad, int k0, int tap_stride,
+                                     int round_src, int lo, long long n) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n) return;  // n = 4 phases * Co * Ci * 4 taps
+  const int ab = (int)(idx % 4);
+  const int ci = (int)((idx / 4) % Ci);
+  const int co = (int)((idx / (4LL * Ci)) % Co);
+  const int p = (int)(idx / (4LL * Ci * Co));
+  const int i = p >> 1, j = p & 1, a = ab >> 1, b = ab & 1;
+  float v = 0.f;
+  for (int dy = 0; dy < 3; ++dy) {
+    if (!subpix_tap(i, a, dy)) continue;
+    for (int dx = 0; dx < 3; ++dx) {
+      if (!subpix_tap(j, b, dx)) continue;
+      const long long o = (((long long)co * Ci + ci) * 3 + dy) * 3 + dx;
+      float w = src_f32 ? static_cast<const float*>(src)[o] : __bfloat162float(static_cast<const __nv_bfloat16*>(src)[o]);
+      if (round_src) w = __bfloat162float(__float2bfloat16_rn(w));
+      v += w;
+    }
+  }
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  dst[((long long)p * co_pad + co) * ld + k0 + (long long)ab * tap_stride + ci] =
+      lo ? __float2bfloat16_rn(v - __bfloat162float(h)) : h;
+}
+
 __global__ void to_f32_kernel(const void* __restrict__ src, int src_f32, const void* __restrict__ src2, int src2_f32,
                               float* __restrict__ dst, int n, float scale, int rnd) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -289,14 +305,6 @@ cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C,
     rms_norm_kernel<true><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
   else
     rms_norm_kernel<false><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_upsample2x(FrameView in, FrameView out, int C, int B, int F, int H, int W, cudaStream_t s) {
-  if (C % 8) return cudaErrorInvalidValue;
-  const long long n = (long long)B * F * 4 * H * W * (C / 8);
-  if (n == 0) return cudaSuccess;
-  upsample2x_kernel<<<blocks_for(n, 256), 256, 0, s>>>(in, out, C / 8, F, H, W, n);
   return cudaGetLastError();
 }
 
@@ -354,6 +362,15 @@ cudaError_t launch_pack_weight(const void* src, int src_f32, int Co, int Ci, int
   const long long n = (long long)Co * Ci * taps;
   if (n == 0) return cudaSuccess;
   pack_weight_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, src_f32, Co, Ci, taps, dst, ld, k0, ci_pad, n, lo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_subpixel(const void* src, int src_f32, int Co, int Ci, __nv_bfloat16* dst, int ld, int co_pad,
+                                 int k0, int tap_stride, int round_src, int lo, cudaStream_t s) {
+  const long long n = 16LL * Co * Ci;
+  if (n == 0) return cudaSuccess;
+  pack_subpixel_kernel<<<blocks_for(n, 256), 256, 0, s>>>(src, src_f32, Co, Ci, dst, ld, co_pad, k0, tap_stride,
+                                                          round_src, lo, n);
   return cudaGetLastError();
 }
 

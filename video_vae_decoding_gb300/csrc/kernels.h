@@ -46,6 +46,11 @@ struct ConvArgs {
   int src_f0[2];         // frame coordinate of output frame 0 in each A source
   int b_per_frame;       // 1: B's third coordinate is b * b_gstride + output frame (batched GEMMs)
   int b_gstride;
+  // Sub-pixel form of nearest-x2 + 3x3 conv: the grid carries a phase
+  // p = 2i + j (i, j in {0, 1}) per tile; the taps' spatial offsets are
+  // shifted by (i - 1, j - 1), B's third coordinate is p, and the output of
+  // low-resolution position (y, x) goes to (2y + i, 2x + j) of a 2H x 2W frame.
+  int subpix;
   int N;                 // valid output channels
   const float* bias;     // [N] fp32, or null
   // output element (b, frame, y, x, n) at
@@ -104,8 +109,6 @@ struct FrameView {
 // in_lo / out_lo: split-format offsets of the low halves (0 = plain bf16).
 cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, bool silu,
                             cudaStream_t s, int in_lo = 0, int out_lo = 0);
-// nearest x2: out(b, f, 2y+i, 2x+j, c) = in(b, f, y, x, c); in is H x W.
-cudaError_t launch_upsample2x(FrameView in, FrameView out, int C, int B, int F, int H, int W, cudaStream_t s);
 // copy F frames of C channels
 cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F, int P, cudaStream_t s);
 // post_quant_conv: z [B][48][Tz][h][w] (fp32 or bf16, NCDHW), frames t0..t0+F-1
@@ -134,6 +137,15 @@ cudaError_t launch_ring_shift(const RingShift* rings, int n, cudaStream_t s);
 // lo = 1 packs the low half bf16(w - bf16(w)) of the split format instead.
 cudaError_t launch_pack_weight(const void* src, int src_f32, int Co, int Ci, int taps, __nv_bfloat16* dst, int ld,
                                int k0, int ci_pad, cudaStream_t s, int lo = 0);
+// Sub-pixel weights of nearest-x2 + 3x3 conv: src [Co][Ci][3][3] ->
+// dst[p][co][k0 + (2a + b)*tap_stride + ci] = sum of src[co][ci][dy][dx] over the
+// kernel rows dy that land on source row offset a for output row phase i
+// (i = 0: {0} | {1, 2}; i = 1: {0, 1} | {2}) and likewise columns dx for phase
+// j, p = 2i + j.  round_src rounds each weight to bf16 before the sum; lo
+// packs the low half of the split format.  dst has ld columns and co_pad rows
+// per phase.
+cudaError_t launch_pack_subpixel(const void* src, int src_f32, int Co, int Ci, __nv_bfloat16* dst, int ld, int co_pad,
+                                 int k0, int tap_stride, int round_src, int lo, cudaStream_t s);
 // dst[i] = scale * r(src[i]) (+ r(src2[i]) if src2) as fp32; src fp32 or bf16;
 // r rounds to the nearest bf16 when round_bf16 is set.
 cudaError_t launch_to_f32(const void* src, int src_f32, const void* src2, int src2_f32, float* dst, int n,

@@ -168,6 +168,7 @@ struct ConvW {
   int ci_pad = 0, ktot = 0, co_pad = 0, bn = 0;
   int sc_Ci = 0, sc_ci_pad = 0;  // appended 1x1x1 shortcut conv
   int split = 0;                 // hi/lo weight halves per tap (fp32 decode)
+  int subpix = 0;                // 4 phases of 2x2 taps (nearest-x2 + 3x3 conv)
 };
 
 static int choose_bn(int co) {
@@ -285,6 +286,46 @@ static wan_status pack_gamma(const WeightTable& wt, const std::string& name, int
   return WAN_OK;
 }
 
+// upsample2d's 3x3 conv (conv2d [C, C, 3, 3]) on the nearest-x2 input, in
+// its sub-pixel form: four 2x2 convs on the low-resolution input, one per
+// output phase (row parity i, column parity j), whose weights sum the 3x3
+// taps that read the same source pixel (page "The parts", fifth bullet: the
+// upsampling only copies values, so the conv of the copies is the conv of
+// the source with the taps merged).  K per phase = 4 taps * ci_pad (x2 split).
+static wan_status pack_subpix_conv(const WeightTable& wt, const std::string& name, int C, ConvW& cw, DevMem& mem,
+                                   cudaStream_t s, bool split) {
+  const wan_tensor *W, *Bi;
+  WAN_TRY(get_tensor(wt, name + ".weight", &W));
+  WAN_TRY(get_tensor(wt, name + ".bias", &Bi));
+  WAN_TRY(check_shape(W, {C, C, 3, 3}));
+  WAN_TRY(check_shape(Bi, {C}));
+  if (mem.dry) return WAN_OK;
+  const int sp = split ? 2 : 1;
+  cw.Co = C;
+  cw.Ci = C;
+  cw.kt = 1;
+  cw.kh = 2;
+  cw.kw = 2;
+  cw.subpix = 1;
+  cw.split = split ? 1 : 0;
+  cw.ci_pad = (int)rup(C, 64);
+  cw.ktot = sp * 4 * cw.ci_pad;
+  cw.bn = choose_bn(C);
+  cw.co_pad = (int)rup(C, cw.bn);
+  void* p;
+  const size_t bytes = (size_t)4 * cw.co_pad * cw.ktot * sizeof(bf16);
+  WAN_TRY(mem.alloc(&p, bytes));
+  cw.w = (bf16*)p;
+  CUDA_TRY(cudaMemsetAsync(cw.w, 0, bytes, s));
+  for (int part = 0; part < sp; ++part)
+    CUDA_TRY(launch_pack_subpixel(W->data, W->dtype == WAN_F32, C, C, cw.w, cw.ktot, cw.co_pad, part * cw.ci_pad,
+                                  sp * cw.ci_pad, split ? 0 : 1, part, s));
+  WAN_TRY(mem.alloc(&p, (size_t)C * sizeof(float)));
+  cw.bias = (float*)p;
+  CUDA_TRY(launch_to_f32(Bi->data, Bi->dtype == WAN_F32, nullptr, 0, cw.bias, C, 1.0f, split ? 0 : 1, s));
+  return WAN_OK;
+}
+
 }  // namespace wan
 
 using namespace wan;
@@ -379,9 +420,7 @@ static wan_status model_build(const wan_tensor* weights, int n, int dtype, cudaS
     if (kUp[i][2])
       WAN_TRY(pack_conv(wt, nm + ".upsampler.time_conv", 2 * cout, cout, 3, 1, 1, false, "", 0, m->tconv[i], mem, s,
                         sp));
-    if (kUp[i][3])
-      WAN_TRY(pack_conv(wt, nm + ".upsampler.resample.1", cout, cout, 1, 3, 3, true, "", 0, m->resample[i], mem, s,
-                        sp));
+    if (kUp[i][3]) WAN_TRY(pack_subpix_conv(wt, nm + ".upsampler.resample.1", cout, m->resample[i], mem, s, sp));
   }
   WAN_TRY(pack_gamma(wt, "decoder.norm_out.gamma", b, &m->out_g, mem, s, sp));
   WAN_TRY(pack_conv(wt, "decoder.conv_out", 12, b, 3, 3, 3, false, "", 0, m->conv_out, mem, s, sp));
@@ -431,11 +470,11 @@ struct wan_vae_stream {
   Act ringIn, RA[3], HA, ringA[10], tcA, tuA;
   AttnBufs at;
   // level B (2h x 2w)
-  Act upB, RB[3], HB, ringB[6], tcB, tuB;
+  Act RB[3], HB, ringB[6], tcB, tuB;
   // level C (4h x 4w)
-  Act upC, RC[3], HC, ringC[6];
+  Act RC[3], HC, ringC[6];
   // level D (8h x 8w)
-  Act upD, RD[3], HD, ringD[6], ringOut;
+  Act RD[3], HD, ringD[6], ringOut;
   std::vector<Act*> rings;
   std::vector<RingShift> shifts;
 };
@@ -516,7 +555,6 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   at.Vt = (bf16*)p;
   // level B
   const int hB = 2 * hA, wB = 2 * wA;
-  WAN_TRY(make_act(st, st->upB, 2 * n, hB, wB, c4));
   for (auto& a : st->RB) WAN_TRY(make_act(st, a, 2 * n, hB, wB, c4));
   WAN_TRY(make_act(st, st->HB, 2 * n, hB, wB, c4));
   for (auto& a : st->ringB) WAN_TRY(ring(a, 2 * n, hB, wB, c4));
@@ -524,7 +562,6 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   WAN_TRY(make_act(st, st->tuB, 4 * n, hB, wB, c4));
   // level C
   const int hC = 4 * hA, wC = 4 * wA;
-  WAN_TRY(make_act(st, st->upC, 4 * n, hC, wC, c4));
   WAN_TRY(make_act(st, st->RC[0], 4 * n, hC, wC, c4));
   WAN_TRY(make_act(st, st->RC[1], 4 * n, hC, wC, c2));
   WAN_TRY(make_act(st, st->RC[2], 4 * n, hC, wC, c2));
@@ -533,7 +570,6 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringC[i], 4 * n, hC, wC, c2));
   // level D
   const int hD = 8 * hA, wD = 8 * wA;
-  WAN_TRY(make_act(st, st->upD, 4 * n, hD, wD, c2));
   WAN_TRY(make_act(st, st->RD[0], 4 * n, hD, wD, c2));
   WAN_TRY(make_act(st, st->RD[1], 4 * n, hD, wD, c1));
   WAN_TRY(make_act(st, st->RD[2], 4 * n, hD, wD, c1));
@@ -597,13 +633,16 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
     WAN_TRY(act_map(&L.a1, *a1));
   else
     L.a1 = L.a0;
-  WAN_TRY(b_map(&L.b, cw.w, cw.ktot, cw.co_pad, 1, cw.ktot, (long long)cw.ktot * cw.co_pad, cw.bn));
+  WAN_TRY(b_map(&L.b, cw.w, cw.ktot, cw.co_pad, cw.subpix ? 4 : 1, cw.ktot, (long long)cw.ktot * cw.co_pad, cw.bn));
   if (cw.split && (!a0.lo || (a1 && !a1->lo))) return fail(WAN_ERR_INTERNAL, "split conv on a plain tensor");
+  A.subpix = cw.subpix;
   int nt = 0, k = 0;
   for (int dt = 0; dt < cw.kt; ++dt)
     for (int dy = 0; dy < cw.kh; ++dy)
       for (int dx = 0; dx < cw.kw; ++dx) {
-        WAN_TRY(add_tap(A, nt, 0, dt, dy - cw.kh / 2, dx - cw.kw / 2, cw.ci_pad, a0.lo, k, cw.split));
+        // sub-pixel taps carry source offsets 0/1; the kernel adds the phase's (i - 1, j - 1)
+        const int oy = cw.subpix ? dy : dy - cw.kh / 2, ox = cw.subpix ? dx : dx - cw.kw / 2;
+        WAN_TRY(add_tap(A, nt, 0, dt, oy, ox, cw.ci_pad, a0.lo, k, cw.split));
         k += (cw.split ? 2 : 1) * cw.ci_pad;
       }
   if (cw.sc_ci_pad) {
@@ -838,12 +877,14 @@ static wan_status time_upsample(wan_vae_stream* st, const ConvW& tc, const Act& 
   return ring_conv(st, tc, ring, Ft, o, nullptr, nullptr, s, kKindTimeConv);
 }
 
-// upsample2d's 3x3 conv on the nearest-x2 input `up` (F frames) plus DupUp3D
-// of the up block's input `blk` (page "The parts", fifth and sixth bullets).
-static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& up, const Act& blk, int ft, bool first,
+// upsample2d (nearest x2, 3x3 conv) of the low-resolution `x` (F frames),
+// in the sub-pixel form, plus DupUp3D of the up block's input `blk` (page
+// "The parts", fifth and sixth bullets); y is at twice x's resolution.
+static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, const Act& blk, int ft, bool first,
                            Act& y, int F, cudaStream_t s) {
   ConvLaunch L;
-  WAN_TRY(conv_setup(cw, up, 0, nullptr, 0, F, L));
+  if (!cw.subpix || y.H != 2 * x.H || y.W != 2 * x.W) return fail(WAN_ERR_INTERNAL, "resample shapes");
+  WAN_TRY(conv_setup(cw, x, 0, nullptr, 0, F, L));
   set_out(L.args, out_of(y));
   L.epi = kEpiDup;
   L.args.dup = blk.p;
@@ -863,7 +904,9 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& up, c
     L.args.dup_pairs = 1;
   else
     return fail(WAN_ERR_UNSUPPORTED, "DupUp3D with %d -> %d channels, ft %d", blk.C, cw.Co, ft);
-  return run(L, &st->prof, kKindResample, conv_flops(cw, up, F), st->err_dev, s);
+  // nominal FLOPs: the 3x3 conv at the upsampled resolution (4/9 of it is executed)
+  const double nominal = 2.0 * x.B * F * 4.0 * x.H * x.W * cw.Co * 9.0 * cw.Ci;
+  return run(L, &st->prof, kKindResample, nominal, st->err_dev, s);
 }
 
 static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long long Tz, long long t0, int n, void* out,
@@ -886,21 +929,18 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   WAN_TRY(resnet(st, m->up[0][1], st->RA[1], st->ringA[6], st->ringA[7], st->HA, st->RA[2], FA, s));
   WAN_TRY(resnet(st, m->up[0][2], st->RA[2], st->ringA[8], st->ringA[9], st->HA, st->RA[1], FA, s));
   WAN_TRY(time_upsample(st, m->tconv[0], st->RA[1], st->tcA, st->tuA, FA, first, s));
-  ELT(&st->prof, launch_upsample2x(st->tuA.view(0), st->upB.view(0), st->tuA.chans(), st->B, FB, st->tuA.H, st->tuA.W, s));
-  WAN_TRY(resample(st, m->resample[0], st->upB, st->RA[0], 2, first, st->RB[0], FB, s));
+  WAN_TRY(resample(st, m->resample[0], st->tuA, st->RA[0], 2, first, st->RB[0], FB, s));
   // up block 1 (level B -> C); block input RB[0]
   WAN_TRY(resnet(st, m->up[1][0], st->RB[0], st->ringB[0], st->ringB[1], st->HB, st->RB[1], FB, s));
   WAN_TRY(resnet(st, m->up[1][1], st->RB[1], st->ringB[2], st->ringB[3], st->HB, st->RB[2], FB, s));
   WAN_TRY(resnet(st, m->up[1][2], st->RB[2], st->ringB[4], st->ringB[5], st->HB, st->RB[1], FB, s));
   WAN_TRY(time_upsample(st, m->tconv[1], st->RB[1], st->tcB, st->tuB, FB, first, s));
-  ELT(&st->prof, launch_upsample2x(st->tuB.view(0), st->upC.view(0), st->tuB.chans(), st->B, FC, st->tuB.H, st->tuB.W, s));
-  WAN_TRY(resample(st, m->resample[1], st->upC, st->RB[0], 2, first, st->RC[0], FC, s));
+  WAN_TRY(resample(st, m->resample[1], st->tuB, st->RB[0], 2, first, st->RC[0], FC, s));
   // up block 2 (level C -> D); block input RC[0]
   WAN_TRY(resnet(st, m->up[2][0], st->RC[0], st->ringC[0], st->ringC[1], st->HC, st->RC[1], FC, s));
   WAN_TRY(resnet(st, m->up[2][1], st->RC[1], st->ringC[2], st->ringC[3], st->HC, st->RC[2], FC, s));
   WAN_TRY(resnet(st, m->up[2][2], st->RC[2], st->ringC[4], st->ringC[5], st->HC, st->RC[1], FC, s));
-  ELT(&st->prof, launch_upsample2x(st->RC[1].view(0), st->upD.view(0), st->RC[1].chans(), st->B, FC, st->RC[1].H, st->RC[1].W, s));
-  WAN_TRY(resample(st, m->resample[2], st->upD, st->RC[0], 1, first, st->RD[0], FC, s));
+  WAN_TRY(resample(st, m->resample[2], st->RC[1], st->RC[0], 1, first, st->RD[0], FC, s));
   // up block 3 (level D)
   WAN_TRY(resnet(st, m->up[3][0], st->RD[0], st->ringD[0], st->ringD[1], st->HD, st->RD[1], FC, s));
   WAN_TRY(resnet(st, m->up[3][1], st->RD[1], st->ringD[2], st->ringD[3], st->HD, st->RD[2], FC, s));
