@@ -22,8 +22,8 @@ struct ConvCfg {
   static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
   static constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
   static constexpr int kBBytes = BN * kBlockK * 2;
-  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 1) + 16;
+  static constexpr int kAccCols = BN < 32 ? 32 : BN;  // one accumulator buffer; two are allocated
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 5) + 16;
 };
 
 __device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16], int lo = 0) {
@@ -58,8 +58,22 @@ __device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16]
   }
 }
 
+__device__ __forceinline__ void add16_bf16(const __nv_bfloat16* src, float (&v)[16]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 a = s[h];
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[8 * h + 2 * i] += bf16_lo(w[i]);
+      v[8 * h + 2 * i + 1] += bf16_hi(w[i]);
+    }
+  }
+}
+
+// v += src[0..15] (fp32, bf16, or split bf16 with the low halves at src + lo)
 __device__ __forceinline__ void add16(const void* src, int f32, float (&v)[16], int lo = 0) {
-  if (lo) add16(static_cast<const __nv_bfloat16*>(src) + lo, 0, v, 0);
   if (f32) {
     const float4* s = reinterpret_cast<const float4*>(src);
 #pragma unroll
@@ -70,67 +84,176 @@ __device__ __forceinline__ void add16(const void* src, int f32, float (&v)[16], 
       v[4 * i + 2] += a.z;
       v[4 * i + 3] += a.w;
     }
-  } else {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
+    return;
+  }
+  add16_bf16(static_cast<const __nv_bfloat16*>(src), v);
+  if (lo) add16_bf16(static_cast<const __nv_bfloat16*>(src) + lo, v);
+}
+
+// Output tile coordinates of linear tile index t (n fastest, then the
+// sub-pixel phase, x, y, frame, batch).
+struct TileCoord {
+  int tn, phase, tx, ty, f, b;
+};
+__device__ __forceinline__ TileCoord tile_coord(const ConvArgs& a, int t) {
+  TileCoord c;
+  c.tn = t % a.tiles_n;
+  t /= a.tiles_n;
+  c.phase = 0;
+  if (a.subpix) {
+    c.phase = t & 3;
+    t >>= 2;
+  }
+  c.tx = t % a.tiles_x;
+  t /= a.tiles_x;
+  c.ty = t % a.tiles_y;
+  t /= a.tiles_y;
+  c.f = t % a.frames;
+  c.b = t / a.frames;
+  return c;
+}
+
+// Epilogue of one tile: 4 warps, thread q*32 + lane owns accumulator row
+// (TMEM lane) q*32 + lane, i.e. one output position, and walks its BN columns
+// 16 at a time.
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tacc, const TileCoord& tc, int q,
+                                              int lane, bool got) {
+  const int m = q * 32 + lane;
+  const int pi = tc.phase >> 1, pj = tc.phase & 1;
+  const int yy = tc.ty * args.box_h + m / args.box_w;
+  const int xx = tc.tx * args.box_w + m % args.box_w;
+  const bool valid = got && yy < args.H && xx < args.W;
+  const int f = tc.f, b = tc.b;
+  const long long pos = args.subpix ? (long long)(2 * yy + pi) * (2 * args.W) + (2 * xx + pj)
+                                    : (long long)yy * args.W + xx;
+  const uint32_t tbase = tacc + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+  for (int c = 0; c < BN / 16; ++c) {
+    const int n0 = tc.tn * BN + c * 16;
+    if (n0 >= args.N) break;  // warp-uniform
+    __syncwarp();               // tcgen05.ld is .sync.aligned: all 32 lanes together
+    uint32_t r[16];
+    tmem_ld16(tbase + c * 16, r);
+    tmem_ld_wait();
+    float v[16];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 a = s[h];
-      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    if (args.bias) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[8 * h + 2 * i] += bf16_lo(w[i]);
-        v[8 * h + 2 * i + 1] += bf16_hi(w[i]);
+      for (int i = 0; i < 16; ++i)
+        if (n0 + i < args.N) v[i] += __ldg(args.bias + n0 + i);
+    }
+    if (!valid) continue;       // lanes re-converge at the __syncwarp above
+    if constexpr (EPI == kEpiVideo) {
+      const long long base = (long long)b * args.vid_bs + (long long)(args.out_f0 + f) * (4LL * args.H * args.W);
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float a0 = v[4 * k + i], a1 = v[4 * k + 2 + i];  // column offsets j = 0, 1
+          const long long off = base + k * args.vid_cs + (long long)(2 * yy + i) * (2LL * args.W) + 2LL * xx;
+          if (args.preclamp) *reinterpret_cast<float2*>(args.preclamp + off) = make_float2(a0, a1);
+          const float c0 = fminf(fmaxf(a0, -1.f), 1.f), c1 = fminf(fmaxf(a1, -1.f), 1.f);
+          if (args.out_f32)
+            *reinterpret_cast<float2*>(static_cast<float*>(args.out) + off) = make_float2(c0, c1);
+          else
+            *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(args.out) + off) = pack_bf16x2(c0, c1);
+        }
       }
+    } else {
+      if constexpr (EPI == kEpiStore) {
+        if (args.res) {
+          const long long ro =
+              (long long)b * args.res_bs + (long long)(args.res_f0 + f) * args.res_fs + pos * args.res_ldc + n0;
+          const void* rp = args.res_f32 ? (const void*)(static_cast<const float*>(args.res) + ro)
+                                        : (const void*)(static_cast<const __nv_bfloat16*>(args.res) + ro);
+          add16(rp, args.res_f32, v, args.res_lo);
+        }
+      } else {  // kEpiDup
+        const int sf = (f + (args.dup_first ? args.dup_ft - 1 : 0)) / args.dup_ft;
+        // source position of output (Y, X) is (Y >> 1, X >> 1): in the
+        // sub-pixel form that is the tile position itself
+        const long long sp = args.subpix ? (long long)yy * args.dup_W + xx
+                                         : (long long)(yy >> 1) * args.dup_W + (xx >> 1);
+        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(args.dup) + (long long)b * args.dup_bs +
+                                   (long long)sf * args.dup_fs + sp * args.dup_ldc;
+        if (args.dup_pairs) {
+          // channel c reads source channel 2c + (row & 1)
+          const int odd = args.subpix ? pi : (yy & 1);
+          for (int part = 0; part < (args.dup_lo ? 2 : 1); ++part) {
+            const uint4* s4 = reinterpret_cast<const uint4*>(src + 2 * n0 + (part ? args.dup_lo : 0));
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const uint4 a = s4[h];
+              const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[4 * h + i] += odd ? bf16_hi(w[i]) : bf16_lo(w[i]);
+            }
+          }
+        } else {
+          add16(src + n0, 0, v, args.dup_lo);
+        }
+      }
+      int fo = args.out_f0 + f * args.out_fmul;
+      int no = n0;
+      if (args.interleave_c > 0 && n0 >= args.interleave_c) {
+        fo += 1;
+        no -= args.interleave_c;
+      }
+      const long long oo = (long long)b * args.out_bs + (long long)fo * args.out_fs + pos * args.out_ldc + no;
+      void* op = args.out_f32 ? (void*)(static_cast<float*>(args.out) + oo)
+                              : (void*)(static_cast<__nv_bfloat16*>(args.out) + oo);
+      store16(op, args.out_f32, v, args.out_lo);
     }
   }
 }
 
+// Persistent kernel: each CTA walks tiles blockIdx.x, + gridDim.x, ...  The
+// accumulator is double-buffered in TMEM (2 x BN columns), so the epilogue
+// warps drain tile i while the MMA issuer accumulates tile i + 1.
 template <int BN, int EPI>
 __global__ void __launch_bounds__(256, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                      const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
   using Cfg = ConvCfg<BN>;
   constexpr int S = Cfg::kStages;
+  constexpr uint32_t kAccCols = Cfg::kAccCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * Cfg::kABytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * Cfg::kBBytes);
   uint64_t* empty = full + S;
-  uint64_t* accum = empty + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* tfull = empty + S;   // [2] accumulator ready (MMA -> epilogue)
+  uint64_t* tempty = tfull + 2;  // [2] accumulator drained (epilogue -> MMA)
+  uint64_t* done = tempty + 2;   // all MMAs of this CTA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int t = blockIdx.x;
-  const int tn = t % args.tiles_n;
-  t /= args.tiles_n;
-  int phase = 0;
-  if (args.subpix) {
-    phase = t & 3;
-    t >>= 2;
-  }
-  const int pi = phase >> 1, pj = phase & 1;
-  const int tx = t % args.tiles_x;
-  t /= args.tiles_x;
-  const int ty = t % args.tiles_y;
-  t /= args.tiles_y;
-  const int f = t % args.frames;
-  const int b = t / args.frames;
+  const int num_tiles =
+      args.tiles_n * (args.subpix ? 4 : 1) * args.tiles_x * args.tiles_y * args.frames * args.batches;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    mbar_init(smem_u32(accum), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&tfull[i]), 1);
+      mbar_init(smem_u32(&tempty[i]), 128);
+    }
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_map(&mapA0);
     tma_prefetch_map(&mapA1);
     tma_prefetch_map(&mapB);
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), 2 * kAccCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -142,25 +265,33 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ producer
     int it = 0;
     bool ok = true;
-    const int gB = args.b_per_frame ? (b * args.b_gstride + f) : phase;
-    const int sy = args.subpix ? pi - 1 : 0, sx = args.subpix ? pj - 1 : 0;
-    for (int ti = 0; ti < args.n_taps && ok; ++ti) {
-      const ConvTap tp = args.taps[ti];
-      const CUtensorMap* am = tp.src ? &mapA1 : &mapA0;
-      const int fr = args.src_f0[tp.src] + f + tp.dt;
-      const int x0 = tx * args.box_w + tp.dx + sx;
-      const int y0 = ty * args.box_h + tp.dy + sy;
-      for (int kb = 0; kb < tp.nkb; ++kb, ++it) {
-        const int s = it % S;
-        const int r = it / S;
-        if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty)) {
-          ok = false;
-          break;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const TileCoord tc = tile_coord(args, tile);
+      const int gB = args.b_per_frame ? (tc.b * args.b_gstride + tc.f) : tc.phase;
+      const int sy = args.subpix ? (tc.phase >> 1) - 1 : 0, sx = args.subpix ? (tc.phase & 1) - 1 : 0;
+      for (int ti = 0; ti < args.n_taps && ok; ++ti) {
+        const ConvTap tp = args.taps[ti];
+        const CUtensorMap* am = tp.src ? &mapA1 : &mapA0;
+        const int fr = args.src_f0[tp.src] + tc.f + tp.dt;
+        const int x0 = tc.tx * args.box_w + tp.dx + sx;
+        const int y0 = tc.ty * args.box_h + tp.dy + sy;
+        for (int kb = 0; kb < tp.nkb; ++kb, ++it) {
+          const int s = it % S;
+          const int r = it / S;
+          if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty)) {
+            ok = false;
+            *abort_flag = 1;
+            break;
+          }
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
+          tma_load_5d(smem_u32(sA + s * Cfg::kABytes), am, fb, tp.a_c0 + kb * kBlockK, x0, y0, fr, tc.b);
+          tma_load_3d(smem_u32(sB + s * Cfg::kBBytes), &mapB, fb, tp.b_k0 + kb * kBlockK, tc.tn * BN, gB);
         }
-        const uint32_t fb = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
-        tma_load_5d(smem_u32(sA + s * Cfg::kABytes), am, fb, tp.a_c0 + kb * kBlockK, x0, y0, fr, b);
-        tma_load_3d(smem_u32(sB + s * Cfg::kBBytes), &mapB, fb, tp.b_k0 + kb * kBlockK, tn * BN, gB);
       }
     }
     // Do not leave while copies into this CTA's shared memory are in flight.
@@ -169,117 +300,57 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
-    for (int it = 0; it < args.total_kb; ++it) {
-      const int s = it % S;
-      if (!mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull)) break;
+    int it = 0, lt = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++lt) {
+      const int buf = lt & 1, use = lt >> 1;
+      if (use > 0 && !mbar_wait_bounded(smem_u32(&tempty[buf]), (use - 1) & 1, args.err, kDevTimeoutAccum)) {
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_after();
-      const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
-      const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+      const uint32_t d = tmem + buf * kAccCols;
+      for (int kk = 0; kk < args.total_kb; ++kk, ++it) {
+        const int s = it % S;
+        if (*abort_flag || !mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
+        const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
 #pragma unroll
-      for (int k = 0; k < kBlockK / 16; ++k)
-        umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
-      umma_commit(smem_u32(&empty[s]));
+        for (int k = 0; k < kBlockK / 16; ++k)
+          umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
+        umma_commit(smem_u32(&empty[s]));
+      }
+      umma_commit(smem_u32(&tfull[buf]));
     }
-    umma_commit(smem_u32(accum));  // also on an aborted loop: tracks the MMAs in flight
+    // wait for every MMA of this CTA before the TMEM can be released
+    umma_commit(smem_u32(done));
+    mbar_wait_bounded(smem_u32(done), 0, args.err, kDevTimeoutAccum);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const bool got = mbar_wait_bounded(smem_u32(accum), 0, args.err, kDevTimeoutAccum);
-    tc_fence_after();
     const int q = warp - 4;
-    const int m = q * 32 + lane;
-    const int yy = ty * args.box_h + m / args.box_w;
-    const int xx = tx * args.box_w + m % args.box_w;
-    const bool valid = got && yy < args.H && xx < args.W;
-    const long long pos = args.subpix ? (long long)(2 * yy + pi) * (2 * args.W) + (2 * xx + pj)
-                                      : (long long)yy * args.W + xx;
-    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-    for (int c = 0; c < BN / 16; ++c) {
-      const int n0 = tn * BN + c * 16;
-      if (n0 >= args.N) break;  // warp-uniform
-      __syncwarp();               // tcgen05.ld is .sync.aligned: all 32 lanes together
-      uint32_t r[16];
-      tmem_ld16(tbase + c * 16, r);
-      tmem_ld_wait();
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-      if (args.bias) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (n0 + i < args.N) v[i] += __ldg(args.bias + n0 + i);
-      }
-      if (!valid) continue;       // lanes re-converge at the __syncwarp above
-      if constexpr (EPI == kEpiVideo) {
-        const long long base = (long long)b * args.vid_bs + (long long)(args.out_f0 + f) * (4LL * args.H * args.W);
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const float a0 = v[4 * k + i], a1 = v[4 * k + 2 + i];  // column offsets j = 0, 1
-            const long long off =
-                base + k * args.vid_cs + (long long)(2 * yy + i) * (2LL * args.W) + 2LL * xx;
-            if (args.preclamp) *reinterpret_cast<float2*>(args.preclamp + off) = make_float2(a0, a1);
-            const float c0 = fminf(fmaxf(a0, -1.f), 1.f), c1 = fminf(fmaxf(a1, -1.f), 1.f);
-            if (args.out_f32)
-              *reinterpret_cast<float2*>(static_cast<float*>(args.out) + off) = make_float2(c0, c1);
-            else
-              *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(args.out) + off) = pack_bf16x2(c0, c1);
-          }
-        }
-      } else {
-        if constexpr (EPI == kEpiStore) {
-          if (args.res) {
-            const long long ro =
-                (long long)b * args.res_bs + (long long)(args.res_f0 + f) * args.res_fs + pos * args.res_ldc + n0;
-            const void* rp = args.res_f32 ? (const void*)(static_cast<const float*>(args.res) + ro)
-                                          : (const void*)(static_cast<const __nv_bfloat16*>(args.res) + ro);
-            add16(rp, args.res_f32, v, args.res_lo);
-          }
-        } else {  // kEpiDup
-          const int sf = (f + (args.dup_first ? args.dup_ft - 1 : 0)) / args.dup_ft;
-          // source position of output (Y, X) is (Y >> 1, X >> 1): in the
-          // sub-pixel form that is the tile position itself
-          const long long sp = args.subpix ? (long long)yy * args.dup_W + xx
-                                           : (long long)(yy >> 1) * args.dup_W + (xx >> 1);
-          const __nv_bfloat16* src =
-              static_cast<const __nv_bfloat16*>(args.dup) + (long long)b * args.dup_bs + (long long)sf * args.dup_fs +
-              sp * args.dup_ldc;
-          if (args.dup_pairs) {
-            // channel c reads source channel 2c + (row & 1)
-            const int odd = args.subpix ? pi : (yy & 1);
-            for (int part = 0; part < (args.dup_lo ? 2 : 1); ++part) {
-              const uint4* s4 = reinterpret_cast<const uint4*>(src + 2 * n0 + (part ? args.dup_lo : 0));
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const uint4 a = s4[h];
-                const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) v[4 * h + i] += odd ? bf16_hi(w[i]) : bf16_lo(w[i]);
-              }
-            }
-          } else {
-            add16(src + n0, 0, v, args.dup_lo);
-          }
-        }
-        int fo = args.out_f0 + f * args.out_fmul;
-        int no = n0;
-        if (args.interleave_c > 0 && n0 >= args.interleave_c) {
-          fo += 1;
-          no -= args.interleave_c;
-        }
-        const long long oo = (long long)b * args.out_bs + (long long)fo * args.out_fs + pos * args.out_ldc + no;
-        void* op = args.out_f32 ? (void*)(static_cast<float*>(args.out) + oo)
-                                : (void*)(static_cast<__nv_bfloat16*>(args.out) + oo);
-        store16(op, args.out_f32, v, args.out_lo);
-      }
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+      const int buf = lt & 1, use = lt >> 1;
+      const bool got =
+          !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum);
+      if (!got) *abort_flag = 1;
+      tc_fence_after();
+      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tile_coord(args, tile), q, lane, got);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&tempty[buf]));
+      if (!got) break;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg::kTmemCols);
+    tmem_dealloc(tmem, 2 * kAccCols);
   }
 }
 
@@ -290,10 +361,15 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
   if (e != cudaSuccess) return e;
   const ConvArgs& a = L.args;
-  const long long grid =
+  const long long tiles =
       (long long)a.tiles_n * (a.subpix ? 4 : 1) * a.tiles_x * a.tiles_y * a.frames * a.batches;
-  if (grid <= 0) return cudaSuccess;
-  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  if (tiles <= 0) return cudaSuccess;
+  if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long grid = tiles < sms ? tiles : sms;  // one persistent CTA per SM
   kern<<<(unsigned)grid, 256, Cfg::kSmem, stream>>>(L.a0, L.a1, L.b, a);
   return cudaGetLastError();
 }
