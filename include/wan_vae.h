@@ -125,20 +125,23 @@ int64_t wan_vae_stream_workspace_bytes(const wan_vae_stream* st);
 wan_status wan_vae_stream_sync_status(wan_vae_stream* st, wan_cuda_stream stream);
 
 /* Device-side timing of the stream's work (for benchmarks).  Between
- * profile_begin and profile_end every tensor-core (implicit-GEMM) launch is
- * bracketed by CUDA events on the launching stream; profile_end waits for the
- * stream, sums the events and reports, with the launch counts, the nominal
- * FLOPs of those launches (2*M*N*K per conv, zero-padded taps included).
+ * profile_begin and profile_end every launch is bracketed by CUDA events on
+ * the launching stream; profile_end waits for the stream, sums the events and
+ * reports them by kind with their algorithmic work: nominal FLOPs for the
+ * tensor-core (implicit-GEMM) kinds (2*M*N*K per conv, zero-padded taps
+ * included), bytes read + written for the memory-bound kinds.
  * kind index: 0 causal 3x3x3 convs (conv_in, residual blocks), 1 time convs,
- * 2 upsample2d convs (+DupUp3D), 3 attention GEMMs, 4 conv_out. */
+ * 2 upsample2d convs (+DupUp3D), 3 attention GEMMs, 4 conv_out,
+ * 5 RMS norm (+SiLU), 6 other memory-bound kernels (post_quant_conv, softmax,
+ * transposes, frame copies, the cache ring shift). */
 typedef struct {
   int64_t launches;          /* all kernel launches enqueued */
   int64_t tc_launches;       /* tensor-core launches among them */
   double tc_ms;              /* their summed device time */
   double tc_flops;           /* their nominal FLOPs */
-  double kind_ms[5];
-  double kind_flops[5];
-  int64_t kind_launches[5];
+  double kind_ms[7];
+  double kind_work[7];       /* FLOPs (kinds 0-4) or bytes (kinds 5-6) */
+  int64_t kind_launches[7];
 } wan_vae_profile;
 wan_status wan_vae_stream_profile_begin(wan_vae_stream* st);
 wan_status wan_vae_stream_profile_end(wan_vae_stream* st, wan_cuda_stream stream, wan_vae_profile* out);

@@ -125,7 +125,8 @@ class DecodeStream:
         check(load().wan_vae_stream_profile_end(self._s, _stream(stream), ctypes.byref(p)))
         return {
             "launches": p.launches, "tc_launches": p.tc_launches, "tc_ms": p.tc_ms, "tc_flops": p.tc_flops,
-            "kinds": {k: {"ms": p.kind_ms[i], "flops": p.kind_flops[i], "launches": p.kind_launches[i]}
+            "kinds": {k: {"ms": p.kind_ms[i], ("flops" if i < 5 else "bytes"): p.kind_work[i],
+                          "launches": p.kind_launches[i]}
                       for i, k in enumerate(PROFILE_KINDS)},
         }
 

@@ -33,13 +33,14 @@ class WanProfile(ctypes.Structure):
         ("tc_launches", ctypes.c_int64),
         ("tc_ms", ctypes.c_double),
         ("tc_flops", ctypes.c_double),
-        ("kind_ms", ctypes.c_double * 5),
-        ("kind_flops", ctypes.c_double * 5),
-        ("kind_launches", ctypes.c_int64 * 5),
+        ("kind_ms", ctypes.c_double * 7),
+        ("kind_work", ctypes.c_double * 7),
+        ("kind_launches", ctypes.c_int64 * 7),
     ]
 
 
-PROFILE_KINDS = ("conv3x3x3", "time_conv", "upsample2d_conv", "attention_gemm", "conv_out")
+PROFILE_KINDS = ("conv3x3x3", "time_conv", "upsample2d_conv", "attention_gemm", "conv_out", "rms_norm", "misc_memory")
+PROFILE_TENSOR_KINDS = 5  # the first five report FLOPs, the rest bytes
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
 

@@ -18,61 +18,77 @@ __device__ __forceinline__ __nv_bfloat16* at_mut(const FrameView& v, int b, int 
 
 inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + per_block - 1) / per_block); }
 
-// One warp per position; up to kMaxChunks 8-channel chunks per lane.
+// RMS norm (+ SiLU) over channels.  A warp normalises R positions; lane l
+// holds channels l*8 + j*256 .. +7 (j < NCH) of each.  All R*NCH 16-byte loads
+// are issued before the first reduction, to keep enough bytes in flight.
 constexpr int kNormMaxC = 1024;
-template <bool SILU>
-__global__ void rms_norm_kernel(FrameView in, FrameView out, const float* __restrict__ gs, int C, int F, int P,
-                                long long rows, int in_lo, int out_lo) {
-  const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+template <bool SILU, int R, int NCH>
+__global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView out, const float* __restrict__ gs,
+                                                       int C, int F, int P, long long rows, int in_lo, int out_lo) {
+  const long long row0 = ((long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * R;
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const long long p = row % P;
-  const int f = (int)((row / P) % F);
-  const int b = (int)(row / ((long long)P * F));
-  const __nv_bfloat16* src = at(in, b, f, p);
-  __nv_bfloat16* dst = at_mut(out, b, f, p);
-  constexpr int kMaxChunks = kNormMaxC / 256;
-  float x[kMaxChunks][8];
-  float ss = 0.f;
+  if (row0 >= rows) return;  // warp-uniform
+  float x[R][NCH][8];
 #pragma unroll
-  for (int j = 0; j < kMaxChunks; ++j) {
-    const int c = lane * 8 + j * 256;
-    if (c < C) {
-      const uint4 a4 = *reinterpret_cast<const uint4*>(src + c);
-      const uint32_t w[4] = {a4.x, a4.y, a4.z, a4.w};
+  for (int r = 0; r < R; ++r) {
+    const long long row = row0 + r;
+    const bool ok = row < rows;
+    const long long p = ok ? row % P : 0;
+    const int f = ok ? (int)((row / P) % F) : 0;
+    const int b = ok ? (int)(row / ((long long)P * F)) : 0;
+    const __nv_bfloat16* src = at(in, b, f, p);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[j][2 * i] = bf16_lo(w[i]);
-        x[j][2 * i + 1] = bf16_hi(w[i]);
+    for (int j = 0; j < NCH; ++j) {
+      const int c = lane * 8 + j * 256;
+      uint4 a4 = make_uint4(0, 0, 0, 0), b4 = make_uint4(0, 0, 0, 0);
+      if (ok && c < C) {
+        a4 = __ldg(reinterpret_cast<const uint4*>(src + c));
+        if (in_lo) b4 = __ldg(reinterpret_cast<const uint4*>(src + in_lo + c));
       }
-      if (in_lo) {  // split format: value = hi + lo
-        const uint4 b4 = *reinterpret_cast<const uint4*>(src + in_lo + c);
-        const uint32_t u[4] = {b4.x, b4.y, b4.z, b4.w};
+      const uint32_t w[4] = {a4.x, a4.y, a4.z, a4.w}, u[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          x[j][2 * i] += bf16_lo(u[i]);
-          x[j][2 * i + 1] += bf16_hi(u[i]);
-        }
+      for (int i = 0; i < 4; ++i) {  // split format: value = hi + lo (lo is zero otherwise)
+        x[r][j][2 * i] = bf16_lo(w[i]) + bf16_lo(u[i]);
+        x[r][j][2 * i + 1] = bf16_hi(w[i]) + bf16_hi(u[i]);
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(x[j][i], x[j][i], ss);
     }
   }
+  float rinv[R];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float rinv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+  for (int r = 0; r < R; ++r) {
+    float ss = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxChunks; ++j) {
+    for (int j = 0; j < NCH; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(x[r][j][i], x[r][j][i], ss);
+    rinv[r] = ss;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < R; ++r) rinv[r] += __shfl_xor_sync(0xffffffffu, rinv[r], o);
+#pragma unroll
+  for (int r = 0; r < R; ++r) rinv[r] = 1.0f / fmaxf(sqrtf(rinv[r]), 1e-12f);
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
     const int c = lane * 8 + j * 256;
-    if (c < C) {
-      const float4 g0 = *reinterpret_cast<const float4*>(gs + c);
-      const float4 g1 = *reinterpret_cast<const float4*>(gs + c + 4);
-      const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    if (c >= C) continue;
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(gs + c));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(gs + c + 4));
+    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const long long row = row0 + r;
+      if (row >= rows) continue;
+      const long long p = row % P;
+      const int f = (int)((row / P) % F);
+      const int b = (int)(row / ((long long)P * F));
+      __nv_bfloat16* dst = at_mut(out, b, f, p);
       float y[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        y[i] = x[j][i] * rinv * g[i];
-        if (SILU) y[i] = y[i] / (1.0f + expf(-y[i]));
+        y[i] = x[r][j][i] * rinv[r] * g[i];
+        if (SILU) y[i] = y[i] / (1.0f + __expf(-y[i]));
       }
       if (out_lo) {
         float h[8], l[8];
@@ -295,16 +311,26 @@ __global__ void to_f32_kernel(const void* __restrict__ src, int src_f32, const v
 
 }  // namespace
 
+template <bool SILU>
+static void norm_dispatch(FrameView in, FrameView out, const float* gs, int C, int F, int P, long long rows, int in_lo,
+                          int out_lo, cudaStream_t s) {
+  if (C <= 256)
+    rms_norm_kernel<SILU, 4, 1><<<blocks_for(rows, 32), 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
+  else if (C <= 512)
+    rms_norm_kernel<SILU, 2, 2><<<blocks_for(rows, 16), 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
+  else
+    rms_norm_kernel<SILU, 1, 4><<<blocks_for(rows, 8), 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
+}
+
 cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, bool silu,
                             cudaStream_t s, int in_lo, int out_lo) {
   if (C > kNormMaxC || C % 8) return cudaErrorInvalidValue;
   const long long rows = (long long)B * F * P;
   if (rows == 0) return cudaSuccess;
-  const unsigned grid = blocks_for(rows, 8);
   if (silu)
-    rms_norm_kernel<true><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
+    norm_dispatch<true>(in, out, gs, C, F, P, rows, in_lo, out_lo, s);
   else
-    rms_norm_kernel<false><<<grid, 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
+    norm_dispatch<false>(in, out, gs, C, F, P, rows, in_lo, out_lo, s);
   return cudaGetLastError();
 }
 

@@ -144,20 +144,48 @@ struct DevMem {
 
 // ----------------------------------------------------------- profiling
 // Kinds of tensor-core launches, for the per-kind breakdown.
-enum LaunchKind { kKindConv333 = 0, kKindTimeConv = 1, kKindResample = 2, kKindAttention = 3, kKindConvOut = 4 };
+enum LaunchKind {
+  kKindConv333 = 0,
+  kKindTimeConv = 1,
+  kKindResample = 2,
+  kKindAttention = 3,
+  kKindConvOut = 4,
+  kKindNorm = 5,  // memory-bound kinds record algorithmic bytes instead of FLOPs
+  kKindMisc = 6,
+  kNumKinds = 7
+};
 struct Prof {
   bool on = false;
   long long launches = 0;                  // every kernel launch enqueued
-  std::vector<cudaEvent_t> ev;             // start/end pairs of tensor-core launches
-  std::vector<std::pair<int, double>> rec; // (kind, nominal FLOPs) per tensor-core launch
+  std::vector<cudaEvent_t> ev;             // start/end pairs of timed launches
+  std::vector<std::pair<int, double>> rec; // (kind, nominal FLOPs or bytes) per timed launch
   ~Prof() {
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
   }
+  // Events of the next timed launch (null when not profiling).
+  wan_status begin(int kind, double work, cudaStream_t s, cudaEvent_t* e1) {
+    *e1 = nullptr;
+    if (!on) return WAN_OK;
+    const size_t i = rec.size();
+    while (ev.size() < 2 * (i + 1)) {
+      cudaEvent_t e;
+      CUDA_TRY(cudaEventCreate(&e));
+      ev.push_back(e);
+    }
+    rec.push_back({kind, work});
+    *e1 = ev[2 * i + 1];
+    CUDA_TRY(cudaEventRecord(ev[2 * i], s));
+    return WAN_OK;
+  }
 };
-#define ELT(prof, expr)                  \
-  do {                                   \
-    CUDA_TRY(expr);                      \
-    if (prof) (prof)->launches++;        \
+// A memory-bound launch, timed when profiling, with its algorithmic bytes.
+#define ELT(prof, kind, bytes, expr)                                   \
+  do {                                                                 \
+    cudaEvent_t e1_ = nullptr;                                         \
+    if (prof) WAN_TRY((prof)->begin((kind), (double)(bytes), s, &e1_)); \
+    CUDA_TRY(expr);                                                    \
+    if (e1_) CUDA_TRY(cudaEventRecord(e1_, s));                        \
+    if (prof) (prof)->launches++;                                      \
   } while (0)
 
 // ------------------------------------------------------------ packed convs
@@ -687,19 +715,8 @@ static void set_out(ConvArgs& A, const OutSpec& o) {
 static wan_status run(ConvLaunch& L, Prof* prof, int kind, double flops, int* err, cudaStream_t s) {
   L.args.err = err;
   if (L.args.N % 16 && L.epi != kEpiVideo) return fail(WAN_ERR_INTERNAL, "conv output channels not a multiple of 16");
-  cudaEvent_t e0 = nullptr, e1 = nullptr;
-  if (prof && prof->on) {
-    const size_t i = prof->rec.size();
-    while (prof->ev.size() < 2 * (i + 1)) {
-      cudaEvent_t e;
-      CUDA_TRY(cudaEventCreate(&e));
-      prof->ev.push_back(e);
-    }
-    e0 = prof->ev[2 * i];
-    e1 = prof->ev[2 * i + 1];
-    prof->rec.push_back({kind, flops});
-    CUDA_TRY(cudaEventRecord(e0, s));
-  }
+  cudaEvent_t e1 = nullptr;
+  if (prof) WAN_TRY(prof->begin(kind, flops, s, &e1));
   CUDA_TRY(launch_conv(L, s));
   if (e1) CUDA_TRY(cudaEventRecord(e1, s));
   if (prof) prof->launches++;
@@ -733,9 +750,10 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
 static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act& ring1, Act& ring2, Act& Ht, Act& y,
                          int F, cudaStream_t s) {
   const int P = x.H * x.W;
-  ELT(&st->prof, launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s, x.lo, ring1.lo));
+  const double nb = 2.0 * 2 * x.B * F * (double)P * (x.lo ? 2 : 1);  // bytes per channel, read + write
+  ELT(&st->prof, kKindNorm, nb * r.ci, launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s, x.lo, ring1.lo));
   WAN_TRY(ring_conv(st, r.c1, ring1, F, out_of(Ht), nullptr, nullptr, s));
-  ELT(&st->prof, launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s, Ht.lo, ring2.lo));
+  ELT(&st->prof, kKindNorm, nb * r.co, launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s, Ht.lo, ring2.lo));
   if (r.ci != r.co)
     WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), nullptr, &x, s));
   else
@@ -786,7 +804,7 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
   const double M = (double)at.B * F * at.HW;
   const int C = at.C, HW = at.HW, B = at.B, sp = at.sp - 1;
   if (HW < 16) return fail(WAN_ERR_UNSUPPORTED, "attention over %d positions (at least 16 supported)", HW);
-  ELT(prof, launch_rms_norm(x.view(0), at.an.view(0), g, C, B, F, HW, false, s, x.lo, at.an.lo));
+  ELT(prof, kKindNorm, 4.0 * M * C * at.sp, launch_rms_norm(x.view(0), at.an.view(0), g, C, B, F, HW, false, s, x.lo, at.an.lo));
   ConvLaunch L;
   // qkv = n Wqkv^T + b; split weights keep their low halves ci_pad after the high ones
   WAN_TRY(gemm_setup(L, at.an.p, at.an.ldc, at.an.lo, HW, at.an.F, B, at.an.fs(), at.an.bs(), qkv.ci_pad, 0,
@@ -818,10 +836,10 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
   // P = softmax(S / sqrt(C)); V^T per frame
   const float scale = 1.0f / std::sqrt((float)C);
   for (int b = 0; b < B; ++b) {
-    ELT(prof, launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.ldp(), HW, (long long)F * HW,
+    ELT(prof, kKindMisc, (4.0 * at.HWs + 2.0 * at.ldp()) * F * HW, launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.ldp(), HW, (long long)F * HW,
                                   scale, s, sp ? at.HWp : 0));
     for (int part = 0; part <= sp; ++part)
-      ELT(prof, launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C + part * at.qkv.lo, at.qkv.fs(), at.qkv.ldc,
+      ELT(prof, kKindMisc, 4.0 * F * HW * C, launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C + part * at.qkv.lo, at.qkv.fs(), at.qkv.ldc,
                                  at.Vt + b * at.vt_bs() + part * at.HWp, at.vt_fs(), (int)at.ldp(), F, HW, C, s));
   }
   // O = P V
@@ -852,7 +870,8 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
 
 // ---------------------------------------------------------------- the chunk
 static wan_status copy_frames(const Act& src, int sf0, const Act& dst, int df0, int F, Prof* prof, cudaStream_t s) {
-  ELT(prof, launch_copy_frames(src.view(sf0), dst.view(df0), src.chans(), src.B, F, src.H * src.W, s));
+  ELT(prof, kKindMisc, 4.0 * src.chans() * src.B * F * src.H * src.W,
+      launch_copy_frames(src.view(sf0), dst.view(df0), src.chans(), src.B, F, src.H * src.W, s));
   return WAN_OK;
 }
 
@@ -917,7 +936,7 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   const int P = st->h * st->w;
   st->shifts.clear();
   // 1. post_quant_conv into conv_in's ring
-  ELT(&st->prof, launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, st->ringIn.view(2),
+  ELT(&st->prof, kKindMisc, (double)st->B * FA * P * (kZdim * (z_f32 ? 4 : 2) + 2 * st->ringIn.ldc), launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, st->ringIn.view(2),
                                    m->split ? 0 : 1, s, st->ringIn.lo));
   // 2. conv_in, mid block
   WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s));
@@ -946,7 +965,8 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   WAN_TRY(resnet(st, m->up[3][1], st->RD[1], st->ringD[2], st->ringD[3], st->HD, st->RD[2], FC, s));
   WAN_TRY(resnet(st, m->up[3][2], st->RD[2], st->ringD[4], st->ringD[5], st->HD, st->RD[1], FC, s));
   // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
-  ELT(&st->prof, launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
+  ELT(&st->prof, kKindNorm, 4.0 * st->B * FC * st->RD[1].H * st->RD[1].W * m->base * (m->split ? 2 : 1),
+      launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
                                  st->RD[1].H * st->RD[1].W, true, s, st->RD[1].lo, st->ringOut.lo));
   {
     ConvLaunch L;
@@ -962,7 +982,9 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
     st->shifts.push_back(RingShift{st->ringOut.p, st->ringOut.fs(), st->ringOut.bs(), FC, st->B});
   }
   // 3. the causal caches: each ring keeps the last two frames it convolved
-  ELT(&st->prof, launch_ring_shift(st->shifts.data(), (int)st->shifts.size(), s));
+  double shift_bytes = 0;
+  for (const RingShift& r : st->shifts) shift_bytes += 8.0 * r.frame_elems * r.batches;  // 2 slots, read + write
+  ELT(&st->prof, kKindMisc, shift_bytes, launch_ring_shift(st->shifts.data(), (int)st->shifts.size(), s));
   st->first = false;
   if (st->err_host) {
     CUDA_TRY(cudaMemcpyAsync(st->err_host, st->err_dev, sizeof(int), cudaMemcpyDeviceToHost, s));
@@ -1194,18 +1216,21 @@ wan_status wan_vae_stream_profile_end(wan_vae_stream* st, wan_cuda_stream stream
     wan_vae_profile r;
     memset(&r, 0, sizeof(r));
     r.launches = p.launches;
-    r.tc_launches = (int64_t)p.rec.size();
+
     if (p.on && !p.rec.empty()) {
       CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
       for (size_t i = 0; i < p.rec.size(); ++i) {
         float ms = 0.f;
         CUDA_TRY(cudaEventElapsedTime(&ms, p.ev[2 * i], p.ev[2 * i + 1]));
         const int k = p.rec[i].first;
-        r.tc_ms += ms;
-        r.tc_flops += p.rec[i].second;
-        if (k >= 0 && k < 5) {
+        if (k < kKindNorm) {
+          r.tc_ms += ms;
+          r.tc_flops += p.rec[i].second;
+          r.tc_launches += 1;
+        }
+        if (k >= 0 && k < kNumKinds) {
           r.kind_ms[k] += ms;
-          r.kind_flops[k] += p.rec[i].second;
+          r.kind_work[k] += p.rec[i].second;
           r.kind_launches[k] += 1;
         }
       }
