@@ -18,32 +18,31 @@ __device__ __forceinline__ __nv_bfloat16* at_mut(const FrameView& v, int b, int 
 
 inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + per_block - 1) / per_block); }
 
-// RMS norm (+ SiLU) over channels.  A warp normalises R positions; lane l
+// RMS norm (+ SiLU) over channels.  Grid: (position blocks, frames,
+// batch).  A warp normalises R consecutive positions of one frame; lane l
 // holds channels l*8 + j*256 .. +7 (j < NCH) of each.  All R*NCH 16-byte loads
 // are issued before the first reduction, to keep enough bytes in flight.
 constexpr int kNormMaxC = 1024;
 template <bool SILU, int R, int NCH>
 __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView out, const float* __restrict__ gs,
-                                                       int C, int F, int P, long long rows, int in_lo, int out_lo) {
-  const long long row0 = ((long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * R;
+                                                       int C, int P, int in_lo, int out_lo) {
+  const int p0 = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * R;
   const int lane = threadIdx.x & 31;
-  if (row0 >= rows) return;  // warp-uniform
+  if (p0 >= P) return;  // warp-uniform
+  const int f = blockIdx.y, b = blockIdx.z;
+  const __nv_bfloat16* src = at(in, b, f, p0);
+  __nv_bfloat16* dst0 = at_mut(out, b, f, p0);
   float x[R][NCH][8];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const long long row = row0 + r;
-    const bool ok = row < rows;
-    const long long p = ok ? row % P : 0;
-    const int f = ok ? (int)((row / P) % F) : 0;
-    const int b = ok ? (int)(row / ((long long)P * F)) : 0;
-    const __nv_bfloat16* src = at(in, b, f, p);
+    const bool ok = p0 + r < P;
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int c = lane * 8 + j * 256;
       uint4 a4 = make_uint4(0, 0, 0, 0), b4 = make_uint4(0, 0, 0, 0);
       if (ok && c < C) {
-        a4 = __ldg(reinterpret_cast<const uint4*>(src + c));
-        if (in_lo) b4 = __ldg(reinterpret_cast<const uint4*>(src + in_lo + c));
+        a4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * in.ldc + c));
+        if (in_lo) b4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * in.ldc + in_lo + c));
       }
       const uint32_t w[4] = {a4.x, a4.y, a4.z, a4.w}, u[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
@@ -78,17 +77,15 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView o
     const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const long long row = row0 + r;
-      if (row >= rows) continue;
-      const long long p = row % P;
-      const int f = (int)((row / P) % F);
-      const int b = (int)(row / ((long long)P * F));
-      __nv_bfloat16* dst = at_mut(out, b, f, p);
+      if (p0 + r >= P) continue;
+      __nv_bfloat16* dst = dst0 + (long long)r * out.ldc;
       float y[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        y[i] = x[r][j][i] * rinv[r] * g[i];
-        if (SILU) y[i] = y[i] / (1.0f + __expf(-y[i]));
+        y[i] = x[r][j][i] * (rinv[r] * g[i]);
+        // SiLU: y * sigmoid(y); for y << 0 the exponential overflows to +inf
+        // and the approximate division returns -0
+        if (SILU) y[i] = __fdividef(y[i], 1.0f + __expf(-y[i]));
       }
       if (out_lo) {
         float h[8], l[8];
@@ -312,25 +309,25 @@ __global__ void to_f32_kernel(const void* __restrict__ src, int src_f32, const v
 }  // namespace
 
 template <bool SILU>
-static void norm_dispatch(FrameView in, FrameView out, const float* gs, int C, int F, int P, long long rows, int in_lo,
+static void norm_dispatch(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, int in_lo,
                           int out_lo, cudaStream_t s) {
+  // 8 warps per block, R positions per warp
   if (C <= 256)
-    rms_norm_kernel<SILU, 4, 1><<<blocks_for(rows, 32), 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
+    rms_norm_kernel<SILU, 4, 1><<<dim3(blocks_for(P, 32), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
   else if (C <= 512)
-    rms_norm_kernel<SILU, 2, 2><<<blocks_for(rows, 16), 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
+    rms_norm_kernel<SILU, 2, 2><<<dim3(blocks_for(P, 16), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
   else
-    rms_norm_kernel<SILU, 1, 4><<<blocks_for(rows, 8), 256, 0, s>>>(in, out, gs, C, F, P, rows, in_lo, out_lo);
+    rms_norm_kernel<SILU, 1, 4><<<dim3(blocks_for(P, 8), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
 }
 
 cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, bool silu,
                             cudaStream_t s, int in_lo, int out_lo) {
-  if (C > kNormMaxC || C % 8) return cudaErrorInvalidValue;
-  const long long rows = (long long)B * F * P;
-  if (rows == 0) return cudaSuccess;
+  if (C > kNormMaxC || C % 8 || F > 65535 || B > 65535) return cudaErrorInvalidValue;
+  if ((long long)B * F * P == 0) return cudaSuccess;
   if (silu)
-    norm_dispatch<true>(in, out, gs, C, F, P, rows, in_lo, out_lo, s);
+    norm_dispatch<true>(in, out, gs, C, B, F, P, in_lo, out_lo, s);
   else
-    norm_dispatch<false>(in, out, gs, C, F, P, rows, in_lo, out_lo, s);
+    norm_dispatch<false>(in, out, gs, C, B, F, P, in_lo, out_lo, s);
   return cudaGetLastError();
 }
 
