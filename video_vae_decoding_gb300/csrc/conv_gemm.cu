@@ -113,6 +113,66 @@ __device__ __forceinline__ TileCoord tile_coord(const ConvArgs& a, int t) {
   return c;
 }
 
+// Epilogue of a tile that holds all N output channels, with the RMS norm of
+// the output fused in.  Pass 1: y = acc + bias (+ residual), its sum of
+// squares, and the raw y to `out` if requested.  Pass 2: y again, scaled by
+// 1 / max(||y||, 1e-12) and sqrt(C) * gamma, SiLU, to out2.
+template <int BN>
+__device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_t tbase, int f, int b, long long pos,
+                                                   bool valid) {
+  const void* rp = nullptr;
+  if (args.res) {
+    const long long ro = (long long)b * args.res_bs + (long long)(args.res_f0 + f) * args.res_fs + pos * args.res_ldc;
+    rp = args.res_f32 ? (const void*)(static_cast<const float*>(args.res) + ro)
+                      : (const void*)(static_cast<const __nv_bfloat16*>(args.res) + ro);
+  }
+  const int esz = args.res_f32 ? 4 : 2;
+  float ss = 0.f;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const float rinv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+#pragma unroll 1
+    for (int c = 0; c < BN / 16; ++c) {
+      const int n0 = c * 16;
+      if (n0 >= args.N) break;  // warp-uniform
+      __syncwarp();
+      uint32_t r[16];
+      tmem_ld16(tbase + c * 16, r);
+      tmem_ld_wait();
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+      if (args.bias) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] += __ldg(args.bias + n0 + i);
+      }
+      if (!valid) continue;
+      if (rp) add16(static_cast<const char*>(rp) + (long long)n0 * esz, args.res_f32, v, args.res_lo);
+      if (pass == 0) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
+        if (args.out) {
+          const long long oo = (long long)b * args.out_bs + (long long)(args.out_f0 + f * args.out_fmul) * args.out_fs +
+                               pos * args.out_ldc + n0;
+          void* op = args.out_f32 ? (void*)(static_cast<float*>(args.out) + oo)
+                                  : (void*)(static_cast<__nv_bfloat16*>(args.out) + oo);
+          store16(op, args.out_f32, v, args.out_lo);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float y = v[i] * (rinv * __ldg(args.norm_gs + n0 + i));
+          if (args.norm_silu) y = __fdividef(y, 1.0f + __expf(-y));
+          v[i] = y;
+        }
+        const long long oo =
+            (long long)b * args.out2_bs + (long long)(args.out2_f0 + f) * args.out2_fs + pos * args.out2_ldc + n0;
+        store16(static_cast<__nv_bfloat16*>(args.out2) + oo, 0, v, args.out2_lo);
+      }
+    }
+  }
+}
+
 // Epilogue of one tile: 4 warps, thread q*32 + lane owns accumulator row
 // (TMEM lane) q*32 + lane, i.e. one output position, and walks its BN columns
 // 16 at a time.
@@ -128,6 +188,12 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
   const long long pos = args.subpix ? (long long)(2 * yy + pi) * (2 * args.W) + (2 * xx + pj)
                                     : (long long)yy * args.W + xx;
   const uint32_t tbase = tacc + ((uint32_t)(q * 32) << 16);
+  if constexpr (EPI == kEpiStore) {
+    if (args.norm_gs) {
+      epilogue_norm_tile<BN>(args, tbase, f, b, pos, valid);
+      return;
+    }
+  }
 #pragma unroll 1
   for (int c = 0; c < BN / 16; ++c) {
     const int n0 = tc.tn * BN + c * 16;

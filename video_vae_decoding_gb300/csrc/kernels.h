@@ -81,6 +81,15 @@ struct ConvArgs {
   // before the clamp (optional).
   float* preclamp;
   long long vid_bs, vid_cs;
+  // Fused RMS norm (requires one N tile holding all N channels): y = acc +
+  // bias (+ residual) is also written normalised over its N channels,
+  // y / max(||y||, 1e-12) * norm_gs (then SiLU if norm_silu), to out2 at
+  // (b, out2_f0 + f, position); `out` may be null (only the normalised y).
+  const float* norm_gs;
+  int norm_silu;
+  void* out2;
+  long long out2_bs, out2_fs;
+  int out2_ldc, out2_f0, out2_lo;
   int* err;              // device error word (kDev* codes)
 };
 

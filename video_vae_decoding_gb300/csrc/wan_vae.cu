@@ -728,12 +728,33 @@ static double conv_flops(const ConvW& cw, const Act& a0, int F) {
   return 2.0 * M * cw.Co * ((double)cw.kt * cw.kh * cw.kw * cw.Ci + cw.sc_Ci);
 }
 
+// RMS norm (+ SiLU) of a conv's output fused into its epilogue, written to
+// the current-frame slots of `ring`.
+struct NormOut {
+  const float* gs = nullptr;  // sqrt(C) * gamma
+  bool silu = true;
+  const Act* ring = nullptr;
+};
+// One N tile holds every output channel: the epilogue can normalise.
+static bool single_tile(const ConvW& cw) { return cw.co_pad == cw.bn && !cw.subpix; }
+
 // 3-frame causal conv over ring `in` (F current frames) into `out`.
 static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F, const OutSpec& o, const Act* res,
-                            const Act* sc, cudaStream_t s, int kind = kKindConv333) {
+                            const Act* sc, cudaStream_t s, int kind = kKindConv333, const NormOut* nrm = nullptr) {
   ConvLaunch L;
   WAN_TRY(conv_setup(cw, in, 0, sc, 0, F, L));
   set_out(L.args, o);
+  if (nrm) {
+    if (!single_tile(cw)) return fail(WAN_ERR_INTERNAL, "fused norm over several N tiles");
+    L.args.norm_gs = nrm->gs;
+    L.args.norm_silu = nrm->silu ? 1 : 0;
+    L.args.out2 = nrm->ring->p;
+    L.args.out2_bs = nrm->ring->bs();
+    L.args.out2_fs = nrm->ring->fs();
+    L.args.out2_ldc = nrm->ring->ldc;
+    L.args.out2_f0 = 2;
+    L.args.out2_lo = nrm->ring->lo;
+  }
   if (res) {
     L.args.res = res->p;
     L.args.res_bs = res->bs();
@@ -746,18 +767,36 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
   return WAN_OK;
 }
 
-// Residual block: x (F frames) -> y.
+// Residual block (page "The parts", third bullet): x (F frames) -> y.
+// normed: ring1 already holds SiLU(norm1(x)), written by the producer of x.
+// next: the RMS norm that consumes y; when conv2 has one N tile it is fused
+// into conv2's epilogue and *next_done is set.
 static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act& ring1, Act& ring2, Act& Ht, Act& y,
-                         int F, cudaStream_t s) {
+                         int F, cudaStream_t s, bool normed = false, const NormOut* next = nullptr,
+                         bool* next_done = nullptr) {
   const int P = x.H * x.W;
   const double nb = 2.0 * 2 * x.B * F * (double)P * (x.lo ? 2 : 1);  // bytes per channel, read + write
-  ELT(&st->prof, kKindNorm, nb * r.ci, launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s, x.lo, ring1.lo));
-  WAN_TRY(ring_conv(st, r.c1, ring1, F, out_of(Ht), nullptr, nullptr, s));
-  ELT(&st->prof, kKindNorm, nb * r.co, launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s, Ht.lo, ring2.lo));
+  if (!normed)
+    ELT(&st->prof, kKindNorm, nb * r.ci,
+        launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s, x.lo, ring1.lo));
+  if (single_tile(r.c1)) {  // conv1 writes SiLU(norm2(h)) straight into conv2's ring
+    NormOut n2;
+    n2.gs = r.g2;
+    n2.ring = &ring2;
+    OutSpec none;
+    WAN_TRY(ring_conv(st, r.c1, ring1, F, none, nullptr, nullptr, s, kKindConv333, &n2));
+  } else {
+    WAN_TRY(ring_conv(st, r.c1, ring1, F, out_of(Ht), nullptr, nullptr, s));
+    ELT(&st->prof, kKindNorm, nb * r.co,
+        launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s, Ht.lo, ring2.lo));
+  }
+  const bool fuse_next = next && single_tile(r.c2);
+  if (next_done) *next_done = fuse_next;
+  const NormOut* nx = fuse_next ? next : nullptr;
   if (r.ci != r.co)
-    WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), nullptr, &x, s));
+    WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), nullptr, &x, s, kKindConv333, nx));
   else
-    WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), &x, nullptr, s));
+    WAN_TRY(ring_conv(st, r.c2, ring2, F, out_of(y), &x, nullptr, s, kKindConv333, nx));
   return WAN_OK;
 }
 
@@ -928,6 +967,32 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
   return run(L, &st->prof, kKindResample, nominal, st->err_dev, s);
 }
 
+// The three residual blocks of an up block: R[0] -> R[1] -> R[2] -> R[1]
+// (R[0], the block input, stays for DupUp3D), with each block's norm1 fused
+// into the previous block's conv2 where possible.  `last` optionally names
+// the norm that consumes the final output.
+static wan_status resnet_chain(wan_vae_stream* st, const Resnet* r, Act* R, Act* rings, Act& Ht, int F,
+                               const NormOut* last, cudaStream_t s, bool* last_done = nullptr) {
+  const int io[3][2] = {{0, 1}, {1, 2}, {2, 1}};
+  bool normed = false;
+  for (int j = 0; j < 3; ++j) {
+    NormOut nx;
+    const NormOut* next = nullptr;
+    if (j < 2) {
+      nx.gs = r[j + 1].g1;
+      nx.ring = &rings[2 * (j + 1)];
+      next = &nx;
+    } else {
+      next = last;
+    }
+    bool done = false;
+    WAN_TRY(resnet(st, r[j], R[io[j][0]], rings[2 * j], rings[2 * j + 1], Ht, R[io[j][1]], F, s, normed, next, &done));
+    normed = done;
+    if (j == 2 && last_done) *last_done = done;
+  }
+  return WAN_OK;
+}
+
 static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long long Tz, long long t0, int n, void* out,
                             int out_f32, long long out_frames, long long out_f0, float* pre, cudaStream_t s) {
   const wan_vae_model* m = st->m;
@@ -944,27 +1009,24 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   WAN_TRY(attention(m->attn_g, m->qkv, m->proj, st->at, st->RA[1], st->RA[2], FA, &st->prof, st->err_dev, s));
   WAN_TRY(resnet(st, m->mid[1], st->RA[2], st->ringA[2], st->ringA[3], st->HA, st->RA[0], FA, s));
   // up block 0 (level A -> B); block input RA[0]
-  WAN_TRY(resnet(st, m->up[0][0], st->RA[0], st->ringA[4], st->ringA[5], st->HA, st->RA[1], FA, s));
-  WAN_TRY(resnet(st, m->up[0][1], st->RA[1], st->ringA[6], st->ringA[7], st->HA, st->RA[2], FA, s));
-  WAN_TRY(resnet(st, m->up[0][2], st->RA[2], st->ringA[8], st->ringA[9], st->HA, st->RA[1], FA, s));
+  WAN_TRY(resnet_chain(st, m->up[0], st->RA, st->ringA + 4, st->HA, FA, nullptr, s));
   WAN_TRY(time_upsample(st, m->tconv[0], st->RA[1], st->tcA, st->tuA, FA, first, s));
   WAN_TRY(resample(st, m->resample[0], st->tuA, st->RA[0], 2, first, st->RB[0], FB, s));
   // up block 1 (level B -> C); block input RB[0]
-  WAN_TRY(resnet(st, m->up[1][0], st->RB[0], st->ringB[0], st->ringB[1], st->HB, st->RB[1], FB, s));
-  WAN_TRY(resnet(st, m->up[1][1], st->RB[1], st->ringB[2], st->ringB[3], st->HB, st->RB[2], FB, s));
-  WAN_TRY(resnet(st, m->up[1][2], st->RB[2], st->ringB[4], st->ringB[5], st->HB, st->RB[1], FB, s));
+  WAN_TRY(resnet_chain(st, m->up[1], st->RB, st->ringB, st->HB, FB, nullptr, s));
   WAN_TRY(time_upsample(st, m->tconv[1], st->RB[1], st->tcB, st->tuB, FB, first, s));
   WAN_TRY(resample(st, m->resample[1], st->tuB, st->RB[0], 2, first, st->RC[0], FC, s));
   // up block 2 (level C -> D); block input RC[0]
-  WAN_TRY(resnet(st, m->up[2][0], st->RC[0], st->ringC[0], st->ringC[1], st->HC, st->RC[1], FC, s));
-  WAN_TRY(resnet(st, m->up[2][1], st->RC[1], st->ringC[2], st->ringC[3], st->HC, st->RC[2], FC, s));
-  WAN_TRY(resnet(st, m->up[2][2], st->RC[2], st->ringC[4], st->ringC[5], st->HC, st->RC[1], FC, s));
+  WAN_TRY(resnet_chain(st, m->up[2], st->RC, st->ringC, st->HC, FC, nullptr, s));
   WAN_TRY(resample(st, m->resample[2], st->RC[1], st->RC[0], 1, first, st->RD[0], FC, s));
   // up block 3 (level D)
-  WAN_TRY(resnet(st, m->up[3][0], st->RD[0], st->ringD[0], st->ringD[1], st->HD, st->RD[1], FC, s));
-  WAN_TRY(resnet(st, m->up[3][1], st->RD[1], st->ringD[2], st->ringD[3], st->HD, st->RD[2], FC, s));
-  WAN_TRY(resnet(st, m->up[3][2], st->RD[2], st->ringD[4], st->ringD[5], st->HD, st->RD[1], FC, s));
+  NormOut nout;  // norm_out + SiLU, fused into the last conv2 when possible
+  nout.gs = m->out_g;
+  nout.ring = &st->ringOut;
+  bool out_done = false;
+  WAN_TRY(resnet_chain(st, m->up[3], st->RD, st->ringD, st->HD, FC, &nout, s, &out_done));
   // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
+  if (!out_done)
   ELT(&st->prof, kKindNorm, 4.0 * st->B * FC * st->RD[1].H * st->RD[1].W * m->base * (m->split ? 2 : 1),
       launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
                                  st->RD[1].H * st->RD[1].W, true, s, st->RD[1].lo, st->ringOut.lo));
