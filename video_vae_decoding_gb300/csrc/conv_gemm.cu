@@ -17,13 +17,20 @@
 
 namespace wan {
 
+// 12 warps: producer (0), MMA issuer (1), TMEM allocator (2), idle (3),
+// and 8 epilogue warps (4-11): warp w reads TMEM lanes 32*(w % 4) .. +31 and
+// the column half (w - 4) / 4 of the tile.
+constexpr int kThreads = 384;
+constexpr int kEpiThreads = 256;
+
 template <int BN>
 struct ConvCfg {
   static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
   static constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
   static constexpr int kBBytes = BN * kBlockK * 2;
   static constexpr int kAccCols = BN < 32 ? 32 : BN;  // one accumulator buffer; two are allocated
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 5) + 16;
+  static constexpr size_t kSmem =
+      1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 7) + 16 + 4 * 2 * 2 * 128;
 };
 
 __device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16], int lo = 0) {
@@ -119,7 +126,8 @@ __device__ __forceinline__ TileCoord tile_coord(const ConvArgs& a, int t) {
 // 1 / max(||y||, 1e-12) and sqrt(C) * gamma, SiLU, to out2.
 template <int BN>
 __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_t tbase, int f, int b, long long pos,
-                                                   bool valid) {
+                                                   bool valid, int c_begin, int c_end, float* red, int m, int h,
+                                                   uint32_t ssbar, uint32_t ss_parity) {
   const void* rp = nullptr;
   if (args.res) {
     const long long ro = (long long)b * args.res_bs + (long long)(args.res_f0 + f) * args.res_fs + pos * args.res_ldc;
@@ -128,11 +136,19 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
   }
   const int esz = args.res_f32 ? 4 : 2;
   float ss = 0.f;
+  float rinv = 0.f;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
-    const float rinv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+    if (pass == 1) {
+      // the other column half's partial sum of squares, through shared memory
+      red[h * 128 + m] = ss;
+      mbar_arrive(ssbar);
+      mbar_wait_bounded(ssbar, ss_parity, args.err, kDevTimeoutAccum);
+      ss += red[(1 - h) * 128 + m];
+      rinv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+    }
 #pragma unroll 1
-    for (int c = 0; c < BN / 16; ++c) {
+    for (int c = c_begin; c < c_end; ++c) {
       const int n0 = c * 16;
       if (n0 >= args.N) break;  // warp-uniform
       __syncwarp();
@@ -177,8 +193,8 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
 // (TMEM lane) q*32 + lane, i.e. one output position, and walks its BN columns
 // 16 at a time.
 template <int BN, int EPI>
-__device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tacc, const TileCoord& tc, int q,
-                                              int lane, bool got) {
+__device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tacc, const TileCoord& tc, int q, int h,
+                                              int lane, bool got, float* red, uint32_t ssbar, uint32_t ss_parity) {
   const int m = q * 32 + lane;
   const int pi = tc.phase >> 1, pj = tc.phase & 1;
   const int yy = tc.ty * args.box_h + m / args.box_w;
@@ -188,14 +204,16 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
   const long long pos = args.subpix ? (long long)(2 * yy + pi) * (2 * args.W) + (2 * xx + pj)
                                     : (long long)yy * args.W + xx;
   const uint32_t tbase = tacc + ((uint32_t)(q * 32) << 16);
+  constexpr int NC = BN / 16;  // 16-column chunks; half h takes [h*NC/2, (h+1)*NC/2)
+  const int c_begin = (h * NC) / 2, c_end = ((h + 1) * NC) / 2;
   if constexpr (EPI == kEpiStore) {
     if (args.norm_gs) {
-      epilogue_norm_tile<BN>(args, tbase, f, b, pos, valid);
+      epilogue_norm_tile<BN>(args, tbase, f, b, pos, valid, c_begin, c_end, red, m, h, ssbar, ss_parity);
       return;
     }
   }
 #pragma unroll 1
-  for (int c = 0; c < BN / 16; ++c) {
+  for (int c = c_begin; c < c_end; ++c) {
     const int n0 = tc.tn * BN + c * 16;
     if (n0 >= args.N) break;  // warp-uniform
     __syncwarp();               // tcgen05.ld is .sync.aligned: all 32 lanes together
@@ -279,7 +297,7 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
 // accumulator is double-buffered in TMEM (2 x BN columns), so the epilogue
 // warps drain tile i while the MMA issuer accumulates tile i + 1.
 template <int BN, int EPI>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                      const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
   using Cfg = ConvCfg<BN>;
@@ -294,8 +312,10 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* tfull = empty + S;   // [2] accumulator ready (MMA -> epilogue)
   uint64_t* tempty = tfull + 2;  // [2] accumulator drained (epilogue -> MMA)
   uint64_t* done = tempty + 2;   // all MMAs of this CTA complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* ssbar = done + 1;    // [2] fused norm: both column halves' partial sums written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ssbar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2 tiles][2 halves][128 rows]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -309,7 +329,8 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
-      mbar_init(smem_u32(&tempty[i]), 128);
+      mbar_init(smem_u32(&tempty[i]), kEpiThreads);
+      mbar_init(smem_u32(&ssbar[i]), kEpiThreads);
     }
     mbar_init(smem_u32(done), 1);
     *abort_flag = 0;
@@ -398,7 +419,7 @@ __global__ void __launch_bounds__(256, 1)
     mbar_wait_bounded(smem_u32(done), 0, args.err, kDevTimeoutAccum);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp - 4;
+    const int q = warp & 3, h = (warp - 4) >> 2;
     int lt = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
@@ -406,7 +427,8 @@ __global__ void __launch_bounds__(256, 1)
           !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum);
       if (!got) *abort_flag = 1;
       tc_fence_after();
-      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tile_coord(args, tile), q, lane, got);
+      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tile_coord(args, tile), q, h, lane, got,
+                             red + buf * 256, smem_u32(&ssbar[buf]), use & 1);
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[buf]));
       if (!got) break;
@@ -436,7 +458,7 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long grid = tiles < sms ? tiles : sms;  // one persistent CTA per SM
-  kern<<<(unsigned)grid, 256, Cfg::kSmem, stream>>>(L.a0, L.a1, L.b, a);
+  kern<<<(unsigned)grid, kThreads, Cfg::kSmem, stream>>>(L.a0, L.a1, L.b, a);
   return cudaGetLastError();
 }
 
