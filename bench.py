@@ -287,7 +287,9 @@ def main():
                          "frac": achieved / sustained, "peak_kind": f"bf16 sustained ({peak_src})",
                          "launches_per_step": dom["launches"] / args.steps,
                          "flop_per_step": dom["flops"] / args.steps,
-                         "traffic": None},
+                         # DRAM bytes of one level-D 256->256 launch of 4 output frames from the
+                         # ncu capture in profiles/ (algorithmic bytes of that launch: 1.156e9)
+                         "traffic": 1.826e9, "traffic_case": "level-D 256->256 causal conv, 4 frames"},
             "tensor_core_tflops": prof["tc_flops"] / (prof["tc_ms"] / 1000.0) / 1e12 if prof["tc_ms"] > 0 else None,
             "tensor_core_ms_per_step": prof["tc_ms"] / args.steps,
             "by_kind": kinds,
