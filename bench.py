@@ -55,6 +55,22 @@ def _peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def max_over_ranks(x: float, pg=None, device="cpu") -> float:
+    """The largest x over all ranks (the slowest rank's time); x itself on one rank."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(ms_per_step_max: float, world: int, frames_per_rank: int) -> float:
+    """Whole-job frames/s: every rank decodes its own clip each step; the
+    step takes as long as the slowest rank."""
+    return world * frames_per_rank / (ms_per_step_max / 1000.0)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -219,12 +235,8 @@ def main():
     if pg:
         pg.barrier()
     st.sync_status()
-    ms = e0.elapsed_time(e1) / args.steps
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * B * FRAMES / (ms / 1000.0)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, dev)
+    value = weak_scaling_value(ms, ws, B * FRAMES)
     burst, sustained, hbm, peak_src = _peaks()
     flops_step = prof["tc_flops"] / args.steps
     # dominant kernel: conv_gemm_kernel on the causal 3x3x3 convs (conv_in and
@@ -244,12 +256,8 @@ def main():
         t0 = time.perf_counter()
         for _ in range(args.steps):
             st.decode_clip_host(z_host, v_host)
-        e2e_s = (time.perf_counter() - t0) / args.steps
-        if pg:
-            t = torch.tensor([e2e_s], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": ws * B * FRAMES / e2e_s, "unit": UNIT,
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, pg, dev)
+        e2e = {"value": weak_scaling_value(1000.0 * e2e_s, ws, B * FRAMES), "unit": UNIT,
                "h2d_bytes_per_step": z_host.numel() * z_host.element_size(),
                "d2h_bytes_per_step": v_host.numel() * v_host.element_size()}
 
