@@ -102,7 +102,12 @@ __device__ __forceinline__ void add16(const void* src, int f32, float (&v)[16], 
 struct TileCoord {
   int tn, phase, tx, ty, f, b;
 };
-__device__ __forceinline__ TileCoord tile_coord(const ConvArgs& a, int t) {
+// With clusters of CL CTAs, a work unit is CL tiles side by side in x with
+// the same N tile; CTA `rank` of the cluster takes x tile unit.x * CL + rank
+// (past the frame's right edge when tiles_x is not a multiple of CL: an
+// all-out-of-range tile whose loads read zeros and whose stores are masked).
+__device__ __forceinline__ int tiles_x_units(const ConvArgs& a, int CL) { return (a.tiles_x + CL - 1) / CL; }
+__device__ __forceinline__ TileCoord tile_coord(const ConvArgs& a, int t, int CL = 1, int rank = 0) {
   TileCoord c;
   c.tn = t % a.tiles_n;
   t /= a.tiles_n;
@@ -111,8 +116,9 @@ __device__ __forceinline__ TileCoord tile_coord(const ConvArgs& a, int t) {
     c.phase = t & 3;
     t >>= 2;
   }
-  c.tx = t % a.tiles_x;
-  t /= a.tiles_x;
+  const int nx = tiles_x_units(a, CL);
+  c.tx = (t % nx) * CL + rank;
+  t /= nx;
   c.ty = t % a.tiles_y;
   t /= a.tiles_y;
   c.f = t % a.frames;
@@ -293,10 +299,14 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
   }
 }
 
-// Persistent kernel: each CTA walks tiles blockIdx.x, + gridDim.x, ...  The
-// accumulator is double-buffered in TMEM (2 x BN columns), so the epilogue
-// warps drain tile i while the MMA issuer accumulates tile i + 1.
-template <int BN, int EPI>
+// Persistent kernel: each cluster of CL CTAs walks work units
+// blockIdx.x / CL, + gridDim.x / CL, ...  The accumulator is double-buffered
+// in TMEM (2 x BN columns), so the epilogue warps drain tile i while the MMA
+// issuer accumulates tile i + 1.  With CL = 2 the two CTAs compute adjacent
+// x tiles of the same N tile: each loads half of the B block and multicasts
+// it to both, and each MMA issuer frees a shared-memory stage in both CTAs
+// (the stage's "empty" barrier counts both), so L2 delivers B once per pair.
+template <int BN, int EPI, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                      const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
@@ -319,13 +329,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles =
-      args.tiles_n * (args.subpix ? 4 : 1) * args.tiles_x * args.tiles_y * args.frames * args.batches;
+  const int num_units =
+      args.tiles_n * (args.subpix ? 4 : 1) * tiles_x_units(args, CL) * args.tiles_y * args.frames * args.batches;
+  const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+  const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
+  constexpr uint16_t kPairMask = (1u << CL) - 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), CL);  // one MMA commit per CTA of the cluster
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
@@ -346,14 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (CL > 1) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const TileCoord tc = tile_coord(args, tile);
+    for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
+      const TileCoord tc = tile_coord(args, unit, CL, rank);
       const int gB = args.b_per_frame ? (tc.b * args.b_gstride + tc.f) : tc.phase;
       const int sy = args.subpix ? (tc.phase >> 1) - 1 : 0, sx = args.subpix ? (tc.phase & 1) - 1 : 0;
       for (int ti = 0; ti < args.n_taps && ok; ++ti) {
@@ -377,7 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
           tma_load_5d(smem_u32(sA + s * Cfg::kABytes), am, fb, tp.a_c0 + kb * kBlockK, x0, y0, fr, tc.b);
-          tma_load_3d(smem_u32(sB + s * Cfg::kBBytes), &mapB, fb, tp.b_k0 + kb * kBlockK, tc.tn * BN, gB);
+          if constexpr (CL > 1)
+            tma_load_3d_multicast(smem_u32(sB + s * Cfg::kBBytes + rank * (Cfg::kBBytes / CL)), &mapB, fb,
+                                  tp.b_k0 + kb * kBlockK, tc.tn * BN + rank * (BN / CL), gB, kPairMask);
+          else
+            tma_load_3d(smem_u32(sB + s * Cfg::kBBytes), &mapB, fb, tp.b_k0 + kb * kBlockK, tc.tn * BN, gB);
         }
       }
     }
@@ -389,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
     int it = 0, lt = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++lt) {
+    for (int unit = unit0; unit < num_units && ok; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
       if (use > 0 && !mbar_wait_bounded(smem_u32(&tempty[buf]), (use - 1) & 1, args.err, kDevTimeoutAccum)) {
         *abort_flag = 1;
@@ -410,7 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kBlockK / 16; ++k)
           umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
-        umma_commit(smem_u32(&empty[s]));
+        if constexpr (CL > 1)
+          umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
+        else
+          umma_commit(smem_u32(&empty[s]));
       }
       umma_commit(smem_u32(&tfull[buf]));
     }
@@ -421,13 +442,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, h = (warp - 4) >> 2;
     int lt = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+    for (int unit = unit0; unit < num_units; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
       const bool got =
           !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum);
       if (!got) *abort_flag = 1;
       tc_fence_after();
-      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tile_coord(args, tile), q, h, lane, got,
+      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tile_coord(args, unit, CL, rank), q, h, lane, got,
                              red + buf * 256, smem_u32(&ssbar[buf]), use & 1);
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[buf]));
@@ -436,29 +457,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while its peer's MMA commits or multicast copies may still reach it
+  if constexpr (CL > 1) cluster_sync();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, 2 * kAccCols);
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int CL>
 static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
   using Cfg = ConvCfg<BN>;
-  auto kern = conv_gemm_kernel<BN, EPI>;
+  auto kern = conv_gemm_kernel<BN, EPI, CL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
   if (e != cudaSuccess) return e;
   const ConvArgs& a = L.args;
-  const long long tiles =
-      (long long)a.tiles_n * (a.subpix ? 4 : 1) * a.tiles_x * a.tiles_y * a.frames * a.batches;
-  if (tiles <= 0) return cudaSuccess;
-  if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long units = (long long)a.tiles_n * (a.subpix ? 4 : 1) * ((a.tiles_x + CL - 1) / CL) * a.tiles_y *
+                          a.frames * a.batches;
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = stream;
+  int resident = 0;  // CTAs (one per SM) or clusters that fit on the device at once
+  if (CL > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(CL);
+    e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
+  } else {
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&resident, cudaDevAttrMultiProcessorCount, dev);
+  }
   if (e != cudaSuccess) return e;
-  const long long grid = tiles < sms ? tiles : sms;  // one persistent CTA per SM
-  kern<<<(unsigned)grid, kThreads, Cfg::kSmem, stream>>>(L.a0, L.a1, L.b, a);
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  const long long groups = units < resident ? units : resident;  // persistent: one wave of CTAs / clusters
+  cfg.gridDim = dim3((unsigned)(groups * CL));
+  e = cudaLaunchKernelEx(&cfg, kern, L.a0, L.a1, L.b, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -473,27 +516,31 @@ size_t conv_smem_bytes(int bn) {
   return 0;
 }
 
+// Clusters of two CTAs share the B block when it is large (BN = 256); the
+// B tensor map's box must then hold BN / 2 rows (conv_b_box_rows).
+int conv_b_box_rows(int bn) { return bn >= 256 ? bn / 2 : bn; }
+
 cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
   if (L.epi == kEpiVideo) {
     if (L.bn != 16) return cudaErrorInvalidValue;
-    return launch_t<16, kEpiVideo>(L, stream);
+    return launch_t<16, kEpiVideo, 1>(L, stream);
   }
   if (L.epi == kEpiDup) {
     switch (L.bn) {
-      case 16: return launch_t<16, kEpiDup>(L, stream);
-      case 32: return launch_t<32, kEpiDup>(L, stream);
-      case 64: return launch_t<64, kEpiDup>(L, stream);
-      case 128: return launch_t<128, kEpiDup>(L, stream);
-      case 256: return launch_t<256, kEpiDup>(L, stream);
+      case 16: return launch_t<16, kEpiDup, 1>(L, stream);
+      case 32: return launch_t<32, kEpiDup, 1>(L, stream);
+      case 64: return launch_t<64, kEpiDup, 1>(L, stream);
+      case 128: return launch_t<128, kEpiDup, 1>(L, stream);
+      case 256: return launch_t<256, kEpiDup, 2>(L, stream);
     }
     return cudaErrorInvalidValue;
   }
   switch (L.bn) {
-    case 16: return launch_t<16, kEpiStore>(L, stream);
-    case 32: return launch_t<32, kEpiStore>(L, stream);
-    case 64: return launch_t<64, kEpiStore>(L, stream);
-    case 128: return launch_t<128, kEpiStore>(L, stream);
-    case 256: return launch_t<256, kEpiStore>(L, stream);
+    case 16: return launch_t<16, kEpiStore, 1>(L, stream);
+    case 32: return launch_t<32, kEpiStore, 1>(L, stream);
+    case 64: return launch_t<64, kEpiStore, 1>(L, stream);
+    case 128: return launch_t<128, kEpiStore, 1>(L, stream);
+    case 256: return launch_t<256, kEpiStore, 2>(L, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -109,12 +109,13 @@ static wan_status act_map(CUtensorMap* m, const bf16* base, int C, int ldc, int 
 static wan_status act_map(CUtensorMap* m, const Act& a, int bw = 16, int bh = 8) {
   return act_map(m, a.p, a.ldc, a.ldc, a.W, a.H, a.F, a.B, a.fs(), a.bs(), bw, bh);
 }
-// B-operand map: dims (K, N, G), box (64, bn, 1).
+// B-operand map for an N tile of bn: dims (K, N, G), box (64, rows, 1) with
+// rows = bn, or bn / 2 when two CTAs of a cluster each load half of the tile.
 static wan_status b_map(CUtensorMap* m, const bf16* base, long long K, long long N, long long G, long long ldk,
                         long long gs, int bn) {
   const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)G};
   const uint64_t strides[2] = {(uint64_t)ldk * 2, (uint64_t)gs * 2};
-  const uint32_t box[3] = {64, (uint32_t)bn, 1};
+  const uint32_t box[3] = {64, (uint32_t)conv_b_box_rows(bn), 1};
   return encode(m, 3, base, dims, strides, box);
 }
 
