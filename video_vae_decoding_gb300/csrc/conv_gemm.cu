@@ -23,11 +23,16 @@ namespace wan {
 constexpr int kThreads = 384;
 constexpr int kEpiThreads = 256;
 
-template <int BN>
+// Halo mode (3x3 spatial taps, small N): per (time tap, 64-channel block) a
+// stage holds three 16 x 10 A boxes (x offsets -1, 0, +1; rows y0-1 .. y0+8)
+// and the nine taps' B blocks; tap (dy, dx) reads box dx from row 16*dy on.
+constexpr int kHaloABox = 16 * kHaloBoxRows * 128;  // 20 KB
+
+template <int BN, bool HALO = false>
 struct ConvCfg {
-  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
-  static constexpr int kABytes = kTileM * kBlockK * 2;  // 16 KB
-  static constexpr int kBBytes = BN * kBlockK * 2;
+  static constexpr int kStages = HALO ? 2 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
+  static constexpr int kABytes = HALO ? 3 * kHaloABox : kTileM * kBlockK * 2;  // 60 KB : 16 KB
+  static constexpr int kBBytes = (HALO ? 9 : 1) * BN * kBlockK * 2;
   static constexpr int kAccCols = BN < 32 ? 32 : BN;  // one accumulator buffer; two are allocated
   static constexpr size_t kSmem =
       1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 7) + 16 + 4 * 2 * 2 * 128;
@@ -306,11 +311,11 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
 // x tiles of the same N tile: each loads half of the B block and multicasts
 // it to both, and each MMA issuer frees a shared-memory stage in both CTAs
 // (the stage's "empty" barrier counts both), so L2 delivers B once per pair.
-template <int BN, int EPI, int CL>
+template <int BN, int EPI, int CL, bool HALO>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                      const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
-  using Cfg = ConvCfg<BN>;
+  using Cfg = ConvCfg<BN, HALO>;
   constexpr int S = Cfg::kStages;
   constexpr uint32_t kAccCols = Cfg::kAccCols;
   extern __shared__ uint8_t smem_raw[];
@@ -368,6 +373,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
       const TileCoord tc = tile_coord(args, unit, CL, rank);
+      if constexpr (HALO) {
+        // K order: time tap dt, then 64-channel block kb; 9 spatial taps per stage
+        const int nkb = args.taps[0].nkb;
+        for (int dt = 0; dt < 3 && ok; ++dt) {
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
+            const int s = it % S;
+            const int r = it / S;
+            if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty)) {
+              ok = false;
+              *abort_flag = 1;
+              break;
+            }
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
+            const int fr = args.src_f0[0] + tc.f + dt;
+            for (int dx = 0; dx < 3; ++dx)
+              tma_load_5d(smem_u32(sA + s * Cfg::kABytes + dx * kHaloABox), &mapA0, fb, kb * kBlockK,
+                          tc.tx * args.box_w + dx - 1, tc.ty * args.box_h - 1, fr, tc.b);
+            // B: the 9 spatial taps of time tap dt, block kb (a 3-D box over the packed weights)
+            tma_load_3d(smem_u32(sB + s * Cfg::kBBytes), &mapB, fb, dt * 9 * args.taps[0].nkb * kBlockK + kb * kBlockK,
+                        tc.tn * BN, 0);
+          }
+        }
+        continue;
+      }
       const int gB = args.b_per_frame ? (tc.b * args.b_gstride + tc.f) : tc.phase;
       const int sy = args.subpix ? (tc.phase >> 1) - 1 : 0, sx = args.subpix ? (tc.phase & 1) - 1 : 0;
       for (int ti = 0; ti < args.n_taps && ok; ++ti) {
@@ -423,11 +457,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
-        const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+        if constexpr (HALO) {
+#pragma unroll 1
+          for (int t9 = 0; t9 < 9; ++t9) {
+            const int dy = t9 / 3, dx = t9 % 3;
+            // rows of tap (dy, dx): box dx from image row dy on (16 rows per image row, 2 KB)
+            const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes + dx * kHaloABox + dy * 16 * 128));
+            const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes + t9 * BN * 128));
 #pragma unroll
-        for (int k = 0; k < kBlockK / 16; ++k)
-          umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kBlockK / 16; ++k)
+              umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || t9 > 0 || k > 0) ? 1u : 0u);
+          }
+        } else {
+          const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
+          const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+#pragma unroll
+          for (int k = 0; k < kBlockK / 16; ++k)
+            umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
+        }
         if constexpr (CL > 1)
           umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
         else
@@ -465,10 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int EPI, int CL>
+template <int BN, int EPI, int CL, bool HALO = false>
 static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
-  using Cfg = ConvCfg<BN>;
-  auto kern = conv_gemm_kernel<BN, EPI, CL>;
+  using Cfg = ConvCfg<BN, HALO>;
+  auto kern = conv_gemm_kernel<BN, EPI, CL, HALO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
   if (e != cudaSuccess) return e;
   const ConvArgs& a = L.args;
@@ -507,7 +554,7 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
 
 size_t conv_smem_bytes(int bn) {
   switch (bn) {
-    case 16: return ConvCfg<16>::kSmem;
+    case 16: return ConvCfg<16, true>::kSmem > ConvCfg<16>::kSmem ? ConvCfg<16, true>::kSmem : ConvCfg<16>::kSmem;
     case 32: return ConvCfg<32>::kSmem;
     case 64: return ConvCfg<64>::kSmem;
     case 128: return ConvCfg<128>::kSmem;
@@ -523,7 +570,7 @@ int conv_b_box_rows(int bn) { return bn >= 256 ? bn / 2 : bn; }
 cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
   if (L.epi == kEpiVideo) {
     if (L.bn != 16) return cudaErrorInvalidValue;
-    return launch_t<16, kEpiVideo, 1>(L, stream);
+    return L.args.halo ? launch_t<16, kEpiVideo, 1, true>(L, stream) : launch_t<16, kEpiVideo, 1>(L, stream);
   }
   if (L.epi == kEpiDup) {
     switch (L.bn) {

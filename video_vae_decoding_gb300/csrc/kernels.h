@@ -21,6 +21,7 @@ namespace wan {
 // history frames in slots 0-1 in front of the current frames.
 // ---------------------------------------------------------------------------
 constexpr int kMaxTaps = 96;
+constexpr int kHaloBoxRows = 10;  // halo mode: A boxes of 16 x 10 positions (8 rows + 2 halo rows)
 constexpr int kTileM = 128;
 constexpr int kBlockK = 64;
 
@@ -51,6 +52,10 @@ struct ConvArgs {
   // shifted by (i - 1, j - 1), B's third coordinate is p, and the output of
   // low-resolution position (y, x) goes to (2y + i, 2x + j) of a 2H x 2W frame.
   int subpix;
+  // Halo mode (conv_out: causal 3x3x3, N = 16): the A tensor map's box is
+  // 64 x 16 x 10 and the B map is 3-D (K, N, 9 spatial taps with stride
+  // ci_pad); K iterates time taps then 64-channel blocks (taps[0].nkb of them).
+  int halo;
   int N;                 // valid output channels
   const float* bias;     // [N] fp32, or null
   // output element (b, frame, y, x, n) at

@@ -1033,7 +1033,20 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
                                  st->RD[1].H * st->RD[1].W, true, s, st->RD[1].lo, st->ringOut.lo));
   {
     ConvLaunch L;
-    WAN_TRY(conv_setup(m->conv_out, st->ringOut, 0, nullptr, 0, FC, L));
+    const ConvW& co = m->conv_out;
+    WAN_TRY(conv_setup(co, st->ringOut, 0, nullptr, 0, FC, L));
+    if (!co.split && co.bn == 16 && co.kt == 3 && co.kh == 3 && co.kw == 3) {
+      // halo mode: three 16 x 10 boxes per time tap and channel block serve all nine spatial taps
+      const Act& a = st->ringOut;
+      WAN_TRY(act_map(&L.a0, a.p, a.ldc, a.ldc, a.W, a.H, a.F, a.B, a.fs(), a.bs(), 16, kHaloBoxRows));
+      L.a1 = L.a0;
+      const uint64_t dims[3] = {(uint64_t)co.ktot, (uint64_t)co.co_pad, 9};
+      const uint64_t strides[2] = {(uint64_t)co.ktot * 2, (uint64_t)co.ci_pad * 2};
+      const uint32_t box[3] = {64, 16, 9};
+      WAN_TRY(encode(&L.b, 3, co.w, dims, strides, box));
+      L.args.halo = 1;
+      L.args.total_kb = 3 * (co.ci_pad / 64);
+    }
     L.epi = kEpiVideo;
     L.args.out = out;
     L.args.out_f32 = out_f32;
