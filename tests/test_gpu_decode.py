@@ -175,3 +175,53 @@ def test_full_width_small_decode_fp32(wv, small):
     got, pre = _decode_f32(wv, model, z, 2)
     ref, ref_pre = oracle.decode(z, w, return_preclamp=True)
     _check_f32(got, pre, ref, ref_pre, "full-width [1,48,3,16,16] fp32 chunk 2")
+
+
+# ------------------------------------------------------------- edge cases
+def test_single_latent_frame(wv, tiny):
+    """T = 1: one output frame, no time conv ever runs (first-chunk rule)."""
+    w, wd = tiny
+    z = wan_synth.make_latents((1, 48, 1, 4, 4), seed=21)
+    model = wv.Model(wd, dtype=torch.bfloat16)
+    got = _decode(wv, model, z, 4)
+    assert got.shape == (1, 3, 1, 64, 64)
+    _check(got, _ref(z, w), "tiny T=1 bf16")
+
+
+def test_stream_reuse_after_reset(wv, tiny):
+    """A stream decodes a second clip from scratch: bit-identical to a fresh stream."""
+    w, wd = tiny
+    za = wan_synth.make_latents((1, 48, 3, 4, 4), seed=22)
+    zb = wan_synth.make_latents((1, 48, 3, 4, 4), seed=23)
+    model = wv.Model(wd, dtype=torch.bfloat16)
+    st = wv.DecodeStream(model, 1, 4, 4, max_chunk=2)
+    st.decode_clip(to_dev(za), out_dtype=torch.float32)
+    second = st.decode_clip(to_dev(zb), out_dtype=torch.float32).cpu().numpy()
+    st.sync_status()
+    np.testing.assert_array_equal(second, _decode(wv, model, zb, 2))
+
+
+def test_chunk_argument_errors(wv, tiny):
+    _, wd = tiny
+    model = wv.Model(wd, dtype=torch.bfloat16)
+    st = wv.DecodeStream(model, 1, 4, 4, max_chunk=2)
+    z = to_dev(wan_synth.make_latents((1, 48, 3, 4, 4), seed=24))
+    out = torch.zeros((1, 3, 9, 64, 64), device="cuda")
+    st.reset()
+    with pytest.raises(wv.WanError) as e:
+        st.decode_chunk(z, 0, 3, out, 0)            # more frames than max_chunk
+    assert e.value.status == 1
+    with pytest.raises(wv.WanError):
+        st.decode_chunk(z, 2, 2, out, 0)            # frames past the end of z
+    with pytest.raises(wv.WanError):
+        st.decode_chunk(z, 0, 2, out, 8)            # output frames past the end of out
+    st.decode_chunk(z, 0, 2, out, 0)                # valid calls still work afterwards
+    st.sync_status()
+
+
+def test_one_shot_fp32(wv, tiny):
+    w, wd = tiny
+    z = wan_synth.make_latents((1, 48, 2, 4, 4), seed=25)
+    got = wv.decode(to_dev(z), wd, dtype=torch.float32).cpu().numpy()
+    ref = oracle.decode(z, w)
+    assert float(np.abs(got - ref).max()) <= TOL_F32
