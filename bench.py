@@ -175,6 +175,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--chunk", type=int, default=4, help="latent frames per causal chunk")
+    ap.add_argument("--latents", default=None,
+                    help="B,T,h,w of the latents (default: the 720p workload 1,31,44,80); other shapes are "
+                         "for profiling and report frames of their own size")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -182,6 +185,12 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    global B, T, H_LAT, W_LAT, FRAMES, H_OUT, W_OUT, METRIC
+    custom = args.latents is not None
+    if custom:
+        B, T, H_LAT, W_LAT = (int(v) for v in args.latents.split(","))
+        FRAMES, H_OUT, W_OUT = 4 * T - 3, 16 * H_LAT, 16 * W_LAT
+        METRIC = f"decoded frames/s ({H_OUT}x{W_OUT}, bf16)"
 
     import torch
     ws, rank, local = _dist()
@@ -205,7 +214,7 @@ def main():
     model = wv.Model(wdev, dtype=torch.bfloat16)
     torch.cuda.synchronize()
     del wdev
-    z_np = wan_synth.make_latents(WORKLOAD["latents"], WORKLOAD["latent_seed"] + rank)
+    z_np = wan_synth.make_latents((B, Z, T, H_LAT, W_LAT), WORKLOAD["latent_seed"] + rank)
     z = torch.from_numpy(z_np).to(dev)
     st = wv.DecodeStream(model, B, H_LAT, W_LAT, max_chunk=args.chunk)
     out = torch.empty((B, 3, FRAMES, H_OUT, W_OUT), device=dev, dtype=torch.bfloat16)
@@ -262,7 +271,7 @@ def main():
                "d2h_bytes_per_step": v_host.numel() * v_host.element_size()}
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not custom:
         dt, fe, desc = cpu_oracle_sample(z_np)
         cpu = {"value": fe / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": desc}
 
@@ -281,7 +290,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: seeded random-init TI2V-5B decoder weights, N(0,1) latents",
-            "config": {"workload": "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280] bf16",
+            "config": {"workload": (f"latents [{B},48,{T},{H_LAT},{W_LAT}] -> video [{B},3,{FRAMES},{H_OUT},{W_OUT}] bf16"
+                                    if custom else "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280] bf16"),
                        "chunk_latent_frames": args.chunk, "batch_per_gpu": B,
                        "l2": "working set larger than L2 (1.1 GB packed weights; GB-scale activations per chunk)"},
             "mpix_per_s": value * H_OUT * W_OUT / 1e6,
