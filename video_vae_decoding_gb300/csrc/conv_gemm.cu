@@ -70,6 +70,19 @@ __device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16]
   }
 }
 
+// v += bias[0..15]: four 16-byte loads (bias buffers are padded with zeros
+// to the N tile, 16-byte aligned).
+__device__ __forceinline__ void add_bias16(const float* bias, float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 b = __ldg(reinterpret_cast<const float4*>(bias) + i);
+    v[4 * i] += b.x;
+    v[4 * i + 1] += b.y;
+    v[4 * i + 2] += b.z;
+    v[4 * i + 3] += b.w;
+  }
+}
+
 __device__ __forceinline__ void add16_bf16(const __nv_bfloat16* src, float (&v)[16]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll
@@ -169,10 +182,7 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
       float v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-      if (args.bias) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] += __ldg(args.bias + n0 + i);
-      }
+      if (args.bias) add_bias16(args.bias + n0, v);
       if (!valid) continue;
       if (rp) add16(static_cast<const char*>(rp) + (long long)n0 * esz, args.res_f32, v, args.res_lo);
       if (pass == 0) {
@@ -187,8 +197,18 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
         }
       } else {
 #pragma unroll
+        float g[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 g4 = __ldg(reinterpret_cast<const float4*>(args.norm_gs + n0) + i);
+          g[4 * i] = g4.x;
+          g[4 * i + 1] = g4.y;
+          g[4 * i + 2] = g4.z;
+          g[4 * i + 3] = g4.w;
+        }
+#pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float y = v[i] * (rinv * __ldg(args.norm_gs + n0 + i));
+          float y = v[i] * (rinv * g[i]);
           if (args.norm_silu) y = __fdividef(y, 1.0f + __expf(-y));
           v[i] = y;
         }
@@ -234,11 +254,7 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
     float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-    if (args.bias) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (n0 + i < args.N) v[i] += __ldg(args.bias + n0 + i);
-    }
+    if (args.bias) add_bias16(args.bias + n0, v);
     if (!valid) continue;       // lanes re-converge at the __syncwarp above
     if constexpr (EPI == kEpiVideo) {
       const long long base = (long long)b * args.vid_bs + (long long)(args.out_f0 + f) * (4LL * args.H * args.W);

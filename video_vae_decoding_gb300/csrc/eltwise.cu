@@ -23,7 +23,7 @@ inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + 
 // holds channels l*8 + j*256 .. +7 (j < NCH) of each.  All R*NCH 16-byte loads
 // are issued before the first reduction, to keep enough bytes in flight.
 constexpr int kNormMaxC = 1024;
-template <bool SILU, int R, int NCH>
+template <bool SILU, int R, int NCH, bool SPLIT>
 __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView out, const float* __restrict__ gs,
                                                        int C, int P, int in_lo, int out_lo) {
   const int p0 = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * R;
@@ -42,13 +42,13 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView o
       uint4 a4 = make_uint4(0, 0, 0, 0), b4 = make_uint4(0, 0, 0, 0);
       if (ok && c < C) {
         a4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * in.ldc + c));
-        if (in_lo) b4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * in.ldc + in_lo + c));
+        if (SPLIT) b4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * in.ldc + in_lo + c));
       }
       const uint32_t w[4] = {a4.x, a4.y, a4.z, a4.w}, u[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {  // split format: value = hi + lo (lo is zero otherwise)
-        x[r][j][2 * i] = bf16_lo(w[i]) + bf16_lo(u[i]);
-        x[r][j][2 * i + 1] = bf16_hi(w[i]) + bf16_hi(u[i]);
+      for (int i = 0; i < 4; ++i) {  // split format: value = hi + lo
+        x[r][j][2 * i] = SPLIT ? bf16_lo(w[i]) + bf16_lo(u[i]) : bf16_lo(w[i]);
+        x[r][j][2 * i + 1] = SPLIT ? bf16_hi(w[i]) + bf16_hi(u[i]) : bf16_hi(w[i]);
       }
     }
   }
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView o
         // and the approximate division returns -0
         if (SILU) y[i] = __fdividef(y[i], 1.0f + __expf(-y[i]));
       }
-      if (out_lo) {
+      if (SPLIT) {
         float h[8], l[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -308,26 +308,34 @@ __global__ void to_f32_kernel(const void* __restrict__ src, int src_f32, const v
 
 }  // namespace
 
-template <bool SILU>
+template <bool SILU, bool SPLIT>
 static void norm_dispatch(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, int in_lo,
                           int out_lo, cudaStream_t s) {
   // 8 warps per block, R positions per warp
   if (C <= 256)
-    rms_norm_kernel<SILU, 4, 1><<<dim3(blocks_for(P, 32), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
+    rms_norm_kernel<SILU, 4, 1, SPLIT><<<dim3(blocks_for(P, 32), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
   else if (C <= 512)
-    rms_norm_kernel<SILU, 2, 2><<<dim3(blocks_for(P, 16), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
+    rms_norm_kernel<SILU, 2, 2, SPLIT><<<dim3(blocks_for(P, 16), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
   else
-    rms_norm_kernel<SILU, 1, 4><<<dim3(blocks_for(P, 8), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
+    rms_norm_kernel<SILU, 1, 4, SPLIT><<<dim3(blocks_for(P, 8), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
 }
 
 cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, bool silu,
                             cudaStream_t s, int in_lo, int out_lo) {
   if (C > kNormMaxC || C % 8 || F > 65535 || B > 65535) return cudaErrorInvalidValue;
   if ((long long)B * F * P == 0) return cudaSuccess;
-  if (silu)
-    norm_dispatch<true>(in, out, gs, C, B, F, P, in_lo, out_lo, s);
-  else
-    norm_dispatch<false>(in, out, gs, C, B, F, P, in_lo, out_lo, s);
+  if ((in_lo != 0) != (out_lo != 0)) return cudaErrorInvalidValue;  // both split or both plain
+  if (silu) {
+    if (in_lo)
+      norm_dispatch<true, true>(in, out, gs, C, B, F, P, in_lo, out_lo, s);
+    else
+      norm_dispatch<true, false>(in, out, gs, C, B, F, P, in_lo, out_lo, s);
+  } else {
+    if (in_lo)
+      norm_dispatch<false, true>(in, out, gs, C, B, F, P, in_lo, out_lo, s);
+    else
+      norm_dispatch<false, false>(in, out, gs, C, B, F, P, in_lo, out_lo, s);
+  }
   return cudaGetLastError();
 }
 

@@ -57,7 +57,7 @@ struct ConvArgs {
   // ci_pad); K iterates time taps then 64-channel blocks (taps[0].nkb of them).
   int halo;
   int N;                 // valid output channels
-  const float* bias;     // [N] fp32, or null
+  const float* bias;     // fp32, zero-padded to a multiple of 16 values past N, or null
   // output element (b, frame, y, x, n) at
   //   out + b*out_bs + (out_f0 + f*out_fmul + hi)*out_fs + (y*W + x)*out_ldc + n'
   // where, if interleave_c > 0, channels n >= interleave_c go to the next

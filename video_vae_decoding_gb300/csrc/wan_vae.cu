@@ -294,8 +294,9 @@ static wan_status pack_conv(const WeightTable& wt, const std::string& name, int 
       CUDA_TRY(launch_pack_weight(Ws->data, Ws->dtype == WAN_F32, Co, sc_Ci, 1, cw.w, cw.ktot,
                                   sp * taps * cw.ci_pad + part * cw.sc_ci_pad, cw.sc_ci_pad, s, part));
   }
-  WAN_TRY(mem.alloc(&p, (size_t)Co * sizeof(float)));
+  WAN_TRY(mem.alloc(&p, (size_t)cw.co_pad * sizeof(float)));  // zero-padded to the N tile
   cw.bias = (float*)p;
+  CUDA_TRY(cudaMemsetAsync(cw.bias, 0, (size_t)cw.co_pad * sizeof(float), s));
   CUDA_TRY(launch_to_f32(Bi->data, Bi->dtype == WAN_F32, Bs ? Bs->data : nullptr, Bs ? Bs->dtype == WAN_F32 : 0,
                          cw.bias, Co, 1.0f, split ? 0 : 1, s));
   return WAN_OK;
@@ -349,8 +350,9 @@ static wan_status pack_subpix_conv(const WeightTable& wt, const std::string& nam
   for (int part = 0; part < sp; ++part)
     CUDA_TRY(launch_pack_subpixel(W->data, W->dtype == WAN_F32, C, C, cw.w, cw.ktot, cw.co_pad, part * cw.ci_pad,
                                   sp * cw.ci_pad, split ? 0 : 1, part, s));
-  WAN_TRY(mem.alloc(&p, (size_t)C * sizeof(float)));
+  WAN_TRY(mem.alloc(&p, (size_t)cw.co_pad * sizeof(float)));  // zero-padded to the N tile
   cw.bias = (float*)p;
+  CUDA_TRY(cudaMemsetAsync(cw.bias, 0, (size_t)cw.co_pad * sizeof(float), s));
   CUDA_TRY(launch_to_f32(Bi->data, Bi->dtype == WAN_F32, nullptr, 0, cw.bias, C, 1.0f, split ? 0 : 1, s));
   return WAN_OK;
 }
