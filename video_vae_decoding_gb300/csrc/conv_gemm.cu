@@ -474,12 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         if constexpr (HALO) {
-#pragma unroll 1
+          // descriptors of the stage's first box and first B block; the taps
+          // add constant byte offsets (>> 4) to the start-address field
+          const uint64_t a0 = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
+          const uint64_t b0 = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+#pragma unroll
           for (int t9 = 0; t9 < 9; ++t9) {
             const int dy = t9 / 3, dx = t9 % 3;
             // rows of tap (dy, dx): box dx from image row dy on (16 rows per image row, 2 KB)
-            const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes + dx * kHaloABox + dy * 16 * 128));
-            const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes + t9 * BN * 128));
+            const uint64_t ad = a0 + (uint64_t)((dx * kHaloABox + dy * 16 * 128) >> 4);
+            const uint64_t bd = b0 + (uint64_t)((t9 * BN * 128) >> 4);
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k)
               umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || t9 > 0 || k > 0) ? 1u : 0u);
