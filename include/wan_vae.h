@@ -202,6 +202,17 @@ wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F
                              const void* weight, const void* bias, int32_t w_dtype, int32_t Cout, int32_t kt,
                              int32_t kh, int32_t kw, void* out, wan_cuda_stream stream);
 
+/* Failure-detection self test (the pages have no counterpart: it exercises
+ * this library's own bounded waits).  Runs one small causal conv (64 -> cout
+ * channels, cout 64 for the one-CTA kernel or 256 for the two-CTA cluster
+ * kernel) whose TMA producer withholds its first stage, with the wait limit
+ * shortened to about 10 ms: the MMA issuer's wait runs out, every role of the
+ * kernel drains its copies and exits, and the kernel leaves an error code in
+ * its device error word.  Blocks until done.  Returns WAN_ERR_INTERNAL and
+ * the code (1..3) in *device_code when the timeout was detected and reported,
+ * WAN_OK if it was not; the CUDA context stays usable either way. */
+wan_status wan_selftest_wait_timeout(int32_t cout, int32_t* device_code, wan_cuda_stream stream);
+
 /* wan_causal_conv3d without any device allocation.  The pages have no
  * counterpart: this is for callers that must not allocate device memory --
  * code that runs while a host framework owns all GPU memory through its own

@@ -159,6 +159,7 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
                       : (const void*)(static_cast<const __nv_bfloat16*>(args.res) + ro);
   }
   const int esz = args.res_f32 ? 4 : 2;
+  const long long lim = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
   float ss = 0.f;
   float rinv = 0.f;
 #pragma unroll 1
@@ -167,7 +168,7 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
       // the other column half's partial sum of squares, through shared memory
       red[h * 128 + m] = ss;
       mbar_arrive(ssbar);
-      mbar_wait_bounded(ssbar, ss_parity, args.err, kDevTimeoutAccum);
+      mbar_wait_bounded(ssbar, ss_parity, args.err, kDevTimeoutAccum, lim);
       ss += red[(1 - h) * 128 + m];
       rinv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
     }
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const long long lim = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
   const int num_units =
       args.tiles_n * (args.subpix ? 4 : 1) * tiles_x_units(args, CL) * args.tiles_y * args.frames * args.batches;
   const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kb = 0; kb < nkb; ++kb, ++it) {
             const int s = it % S;
             const int r = it / S;
-            if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty)) {
+            if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty, lim)) {
               ok = false;
               *abort_flag = 1;
               break;
@@ -405,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
+            if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
             const uint32_t fb = smem_u32(&full[s]);
             mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
             const int fr = args.src_f0[0] + tc.f + dt;
@@ -429,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < tp.nkb; ++kb, ++it) {
           const int s = it % S;
           const int r = it / S;
-          if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty)) {
+          if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty, lim)) {
             ok = false;
             *abort_flag = 1;
             break;
@@ -438,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
           tma_load_5d(smem_u32(sA + s * Cfg::kABytes), am, fb, tp.a_c0 + kb * kBlockK, x0, y0, fr, tc.b);
@@ -451,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Do not leave while copies into this CTA's shared memory are in flight.
     for (int j = (it > S ? it - S : 0); j < it; ++j)
-      mbar_wait_bounded(smem_u32(&full[j % S]), (j / S) & 1, args.err, kDevTimeoutFull);
+      mbar_wait_bounded(smem_u32(&full[j % S]), (j / S) & 1, args.err, kDevTimeoutFull, lim);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
-      if (use > 0 && !mbar_wait_bounded(smem_u32(&tempty[buf]), (use - 1) & 1, args.err, kDevTimeoutAccum)) {
+      if (use > 0 && !mbar_wait_bounded(smem_u32(&tempty[buf]), (use - 1) & 1, args.err, kDevTimeoutAccum, lim)) {
         *abort_flag = 1;
         break;
       }
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d = tmem + buf * kAccCols;
       for (int kk = 0; kk < args.total_kb; ++kk, ++it) {
         const int s = it % S;
-        if (*abort_flag || !mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull)) {
+        if (*abort_flag || !mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull, lim)) {
           *abort_flag = 1;
           ok = false;
           break;
@@ -504,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // wait for every MMA of this CTA before the TMEM can be released
     umma_commit(smem_u32(done));
-    mbar_wait_bounded(smem_u32(done), 0, args.err, kDevTimeoutAccum);
+    mbar_wait_bounded(smem_u32(done), 0, args.err, kDevTimeoutAccum, lim);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, h = (warp - 4) >> 2;
@@ -512,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int unit = unit0; unit < num_units; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
       const bool got =
-          !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum);
+          !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum, lim);
       if (!got) *abort_flag = 1;
       tc_fence_after();
       epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tile_coord(args, unit, CL, rank), q, h, lane, got,

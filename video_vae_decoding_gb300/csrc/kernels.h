@@ -96,6 +96,12 @@ struct ConvArgs {
   long long out2_bs, out2_fs;
   int out2_ldc, out2_f0, out2_lo;
   int* err;              // device error word (kDev* codes)
+  // Failure-detection self test: a bounded wait gives up after wait_limit
+  // SM clocks (0: the default of about 2 s), and the TMA producer withholds
+  // the loads of its K iteration number stall_at1 - 1 (0: none), so the MMA
+  // issuer's wait for that stage runs out.
+  long long wait_limit;
+  int stall_at1;
 };
 
 struct ConvLaunch {

@@ -52,12 +52,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 // Waits for the phase of `parity` to complete.  Returns false (and records
-// `code` in *err) if it has not completed within kWaitLimitCycles.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err, int code) {
+// `code` in *err) if it has not completed within `limit` SM clocks.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err, int code,
+                                                  long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       if (err) atomicCAS(err, 0, code);
       return false;
     }

@@ -1588,6 +1588,76 @@ wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F
 }  // extern "C"
 
 // ======================================================================
+// Failure-detection self test
+// ======================================================================
+extern "C" wan_status wan_selftest_wait_timeout(int32_t cout, int32_t* device_code, wan_cuda_stream stream) {
+  API_GUARD({
+    if (device_code) *device_code = 0;
+    if (cout != 64 && cout != 256) return fail(WAN_ERR_INVALID_ARG, "cout must be 64 or 256, not %d", cout);
+    cudaStream_t s = (cudaStream_t)stream;
+    DevMem mem;
+    mem.use_async = true;
+    mem.async = s;
+    wan_status r = WAN_OK;
+    int code = 0;
+    do {
+      // a causal 3x3x3 conv 64 -> cout over one 16 x 32 frame (two history slots of zeros)
+      ConvW cw;
+      cw.Co = cout;
+      cw.Ci = 64;
+      cw.kt = cw.kh = cw.kw = 3;
+      cw.ci_pad = 64;
+      cw.ktot = 27 * 64;
+      cw.bn = choose_bn(cout);
+      cw.co_pad = (int)rup(cout, cw.bn);
+      Act x;
+      x.B = 1;
+      x.F = 3;
+      x.H = 16;
+      x.W = 32;
+      x.C = 64;
+      x.ldc = 64;
+      void *pw, *pb, *px, *po, *pe;
+      const size_t wb = (size_t)cw.co_pad * cw.ktot * sizeof(bf16), bb = (size_t)cw.co_pad * sizeof(float);
+      const size_t ob = (size_t)x.H * x.W * cout * sizeof(bf16);
+      if ((r = mem.alloc(&pw, wb)) || (r = mem.alloc(&pb, bb)) || (r = mem.alloc(&px, x.bytes())) ||
+          (r = mem.alloc(&po, ob)) || (r = mem.alloc(&pe, 256)))
+        break;
+      if (cudaMemsetAsync(pw, 0, wb, s) || cudaMemsetAsync(pb, 0, bb, s) || cudaMemsetAsync(px, 0, x.bytes(), s) ||
+          cudaMemsetAsync(pe, 0, 256, s)) {
+        r = fail(WAN_ERR_CUDA, "memset failed");
+        break;
+      }
+      cw.w = (bf16*)pw;
+      cw.bias = (float*)pb;
+      x.p = (bf16*)px;
+      ConvLaunch L;
+      if ((r = conv_setup(cw, x, 0, nullptr, 0, 1, L)) != WAN_OK) break;
+      OutSpec o;
+      o.p = po;
+      o.fs = (long long)x.H * x.W * cout;
+      o.bs = o.fs;
+      o.ldc = cout;
+      set_out(L.args, o);
+      L.args.wait_limit = 20000000;  // about 10 ms
+      L.args.stall_at1 = 1;          // the first K stage is never loaded
+      if ((r = run(L, nullptr, 0, 0.0, (int*)pe, s)) != WAN_OK) break;
+      if (cudaMemcpyAsync(&code, pe, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+          cudaStreamSynchronize(s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "reading the error word failed: %s", cudaGetErrorString(cudaGetLastError()));
+        break;
+      }
+    } while (false);
+    mem.release();
+    if (r != WAN_OK) return r;
+    CUDA_TRY(cudaStreamSynchronize(s));
+    if (device_code) *device_code = code;
+    if (code) return fail(WAN_ERR_INTERNAL, "a conv kernel reported error %d (a bounded wait expired)", code);
+    return WAN_OK;
+  })
+}
+
+// ======================================================================
 // wan_causal_conv3d_noalloc: the causal conv with its scratch (packed
 // weights, bias, the input copied behind two history slots, the error word)
 // carved from a fixed device array instead of the stream-ordered allocator.
