@@ -168,6 +168,43 @@ def run_reference(args):
     return 0
 
 
+def run_attention(args):
+    """The isolated attention block: RMS norm, qkv 1x1 conv, softmax(q k^T / 32) v over
+    3520 positions per frame (one head, d = 1024), proj, + x; 8 frames, bf16."""
+    import torch
+    from video_vae_decoding_gb300 import build as _build
+    _build.build()
+    import video_vae_decoding_gb300 as wv
+    cfg = wan_synth.CONFIGS["attention"]
+    N, C, H, W = cfg["x"]
+    HW = H * W
+    w = wan_synth.make_weights(base=cfg["base"], seed=cfg["weight_seed"])
+    name = "decoder.mid_block.attentions.0"
+    wd = {k: torch.from_numpy(np.array(v)).cuda() for k, v in w.items() if k.startswith(name)}
+    x = torch.from_numpy(wan_synth.make_normal((N, C, H, W), cfg["x_seed"])).cuda()
+    x = x.permute(0, 2, 3, 1).reshape(N, HW, C).contiguous().to(torch.bfloat16)
+    for _ in range(args.warmup):
+        wv.attention_block(x, wd, H, W)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        wv.attention_block(x, wd, H, W)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = 2.0 * N * HW * (3 * C * C + 2 * HW * C + C * C)
+    burst, sustained, _, src = _peaks()
+    tf = flops / (ms / 1000.0) / 1e12
+    print(json.dumps({
+        "metric": "attention block TFLOP/s (x [8,1024,44,80], bf16)", "value": tf, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic", "config": {"workload": "isolated mid-block attention, 8 frames of 44x80, C 1024"},
+        "nominal_gflop_per_step": flops / 1e9, "frac_of_bf16_peak": {"burst": tf / burst, "sustained": tf / sustained,
+                                                                    "source": src}}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -178,6 +215,8 @@ def main():
     ap.add_argument("--latents", default=None,
                     help="B,T,h,w of the latents (default: the 720p workload 1,31,44,80); other shapes are "
                          "for profiling and report frames of their own size")
+    ap.add_argument("--workload", choices=("decode", "attention"), default="decode",
+                    help="attention: the isolated mid-block attention (x [8, 1024, 44, 80]) instead of the decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -185,6 +224,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "attention":
+        return run_attention(args)
     global B, T, H_LAT, W_LAT, FRAMES, H_OUT, W_OUT, METRIC
     custom = args.latents is not None
     if custom:

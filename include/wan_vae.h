@@ -124,6 +124,19 @@ int64_t wan_vae_stream_workspace_bytes(const wan_vae_stream* st);
  * kernel recorded (WAN_ERR_INTERNAL with a message) or a CUDA error. */
 wan_status wan_vae_stream_sync_status(wan_vae_stream* st, wan_cuda_stream stream);
 
+/* Checkpoint / resume of a decode.  A stream's state between chunks is the
+ * causal caches (page section "Causal caches": the last two input frames of
+ * every 3-frame conv) and whether the next chunk is a first chunk.
+ * state_bytes: size of a saved state.  save: copies it, stream-ordered, to
+ * `dst` (device or host memory, at least state_bytes).  load: restores a
+ * state saved from a stream of the same model precision, base dim, B, h, w
+ * (WAN_ERR_STATE otherwise); it blocks to read the header, then enqueues the
+ * copies on `stream`.  A decode continued after load produces the frames the
+ * saved stream would have produced. */
+int64_t wan_vae_stream_state_bytes(const wan_vae_stream* st);
+wan_status wan_vae_stream_save(wan_vae_stream* st, void* dst, int64_t bytes, wan_cuda_stream stream);
+wan_status wan_vae_stream_load(wan_vae_stream* st, const void* src, int64_t bytes, wan_cuda_stream stream);
+
 /* Device-side timing of the stream's work (for benchmarks).  Between
  * profile_begin and profile_end every launch is bracketed by CUDA events on
  * the launching stream; profile_end waits for the stream, sums the events and

@@ -115,6 +115,21 @@ class DecodeStream:
     def sync_status(self, stream=None):
         check(load().wan_vae_stream_sync_status(self._s, _stream(stream)))
 
+    @property
+    def state_bytes(self) -> int:
+        return int(load().wan_vae_stream_state_bytes(self._s))
+
+    def save_state(self, stream=None) -> torch.Tensor:
+        """The causal caches and chunk position, as a uint8 device tensor."""
+        buf = torch.empty(self.state_bytes, dtype=torch.uint8, device="cuda")
+        check(load().wan_vae_stream_save(self._s, buf.data_ptr(), buf.numel(), _stream(stream)))
+        return buf
+
+    def load_state(self, buf: torch.Tensor, stream=None):
+        if not buf.is_contiguous():
+            raise ValueError("state buffer must be contiguous")
+        check(load().wan_vae_stream_load(self._s, buf.data_ptr(), buf.numel(), _stream(stream)))
+
     def profile_begin(self):
         check(load().wan_vae_stream_profile_begin(self._s))
 

@@ -57,6 +57,9 @@ SIGNATURES = {
     "wan_vae_stream_destroy": (None, [_vp]),
     "wan_vae_stream_workspace_bytes": (_i64, [_vp]),
     "wan_vae_stream_sync_status": (_i32, [_vp, _vp]),
+    "wan_vae_stream_state_bytes": (_i64, [_vp]),
+    "wan_vae_stream_save": (_i32, [_vp, _vp, _i64, _vp]),
+    "wan_vae_stream_load": (_i32, [_vp, _vp, _i64, _vp]),
     "wan_vae_stream_profile_begin": (_i32, [_vp]),
     "wan_vae_stream_profile_end": (_i32, [_vp, _vp, ctypes.POINTER(WanProfile)]),
     "wan_vae_decode_chunk": (_i32, [_vp, _vp, _i32, _i64, _i64, _i32, _vp, _i32, _i64, _i64, _vp, _vp]),

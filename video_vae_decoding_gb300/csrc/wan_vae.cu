@@ -1277,6 +1277,70 @@ wan_status wan_vae_stream_sync_status(wan_vae_stream* st, wan_cuda_stream stream
   })
 }
 
+// ---- causal-cache checkpoint: header + the two history slots of every ring
+struct StateHeader {
+  uint64_t magic;
+  int32_t base, split, B, h, w, first, n_rings;
+  int64_t payload;
+};
+static const uint64_t kStateMagic = 0x57414e5641453031ULL;  // "WANVAE01"
+
+static int64_t state_payload(const wan_vae_stream* st) {
+  int64_t n = 0;
+  for (const Act* r : st->rings) n += (int64_t)r->B * 2 * r->fs() * (int64_t)sizeof(bf16);
+  return n;
+}
+
+int64_t wan_vae_stream_state_bytes(const wan_vae_stream* st) {
+  return st ? (int64_t)rup(sizeof(StateHeader), 256) + state_payload(st) : 0;
+}
+
+wan_status wan_vae_stream_save(wan_vae_stream* st, void* dst, int64_t bytes, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!st || !dst) return fail(WAN_ERR_INVALID_ARG, "null argument");
+    if (bytes < wan_vae_stream_state_bytes(st))
+      return fail(WAN_ERR_INVALID_ARG, "state buffer of %lld bytes, %lld needed", (long long)bytes,
+                  (long long)wan_vae_stream_state_bytes(st));
+    cudaStream_t s = (cudaStream_t)stream;
+    StateHeader hd{kStateMagic, st->m->base, st->m->split ? 1 : 0, st->B, st->h, st->w, st->first ? 1 : 0,
+                   (int32_t)st->rings.size(), state_payload(st)};
+    CUDA_TRY(cudaMemcpyAsync(dst, &hd, sizeof(hd), cudaMemcpyDefault, s));
+    char* o = static_cast<char*>(dst) + rup(sizeof(StateHeader), 256);
+    for (const Act* r : st->rings)
+      for (int b = 0; b < r->B; ++b) {
+        const size_t n = 2 * r->fs() * sizeof(bf16);
+        CUDA_TRY(cudaMemcpyAsync(o, r->p + b * r->bs(), n, cudaMemcpyDefault, s));
+        o += n;
+      }
+    return WAN_OK;
+  })
+}
+
+wan_status wan_vae_stream_load(wan_vae_stream* st, const void* src, int64_t bytes, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!st || !src) return fail(WAN_ERR_INVALID_ARG, "null argument");
+    if (bytes < (int64_t)sizeof(StateHeader)) return fail(WAN_ERR_INVALID_ARG, "state buffer too small");
+    cudaStream_t s = (cudaStream_t)stream;
+    StateHeader hd;
+    CUDA_TRY(cudaMemcpyAsync(&hd, src, sizeof(hd), cudaMemcpyDefault, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    if (hd.magic != kStateMagic) return fail(WAN_ERR_INVALID_ARG, "not a decode state");
+    if (hd.base != st->m->base || hd.split != (st->m->split ? 1 : 0) || hd.B != st->B || hd.h != st->h ||
+        hd.w != st->w || hd.n_rings != (int32_t)st->rings.size() || hd.payload != state_payload(st))
+      return fail(WAN_ERR_STATE, "state of a different model, dtype or shape");
+    if (bytes < wan_vae_stream_state_bytes(st)) return fail(WAN_ERR_INVALID_ARG, "state buffer truncated");
+    const char* o = static_cast<const char*>(src) + rup(sizeof(StateHeader), 256);
+    for (Act* r : st->rings)
+      for (int b = 0; b < r->B; ++b) {
+        const size_t n = 2 * r->fs() * sizeof(bf16);
+        CUDA_TRY(cudaMemcpyAsync(r->p + b * r->bs(), o, n, cudaMemcpyDefault, s));
+        o += n;
+      }
+    st->first = hd.first != 0;
+    return WAN_OK;
+  })
+}
+
 wan_status wan_vae_stream_profile_begin(wan_vae_stream* st) {
   API_GUARD({
     if (!st) return fail(WAN_ERR_INVALID_ARG, "null stream state");
