@@ -179,7 +179,9 @@ wan_status wan_vae_decode_clip(wan_vae_stream* st, const void* z, int32_t z_dtyp
 /* As wan_vae_decode_clip, with z and out in HOST memory (page-locked memory
  * is recommended): copies each chunk's latents in, decodes, and copies each
  * chunk's frames out while the next chunk decodes.  Blocks the host until the
- * video is in `out_host`. */
+ * video is in `out_host`.  The first call allocates two latent and two video
+ * staging chunks (fp32-sized, so either dtype fits) and a copy stream; the
+ * stream keeps them for later calls and frees them in wan_vae_stream_destroy. */
 wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int32_t z_dtype, int32_t T,
                                     void* out_host, int32_t out_dtype, wan_cuda_stream stream);
 

@@ -109,6 +109,14 @@ def test_tiny_one_shot_and_host_paths(wv, tiny):
     st.decode_clip_host(torch.from_numpy(z).pin_memory(), host)
     torch.cuda.synchronize()
     assert torch.equal(host, dev.cpu())          # same kernels, same chunking: bit-exact
+    # second call on the same stream: reused staging, three chunks (both
+    # buffers recycled), another clip length and fp32 output
+    z5 = wan_synth.make_latents((1, 48, 5, 4, 4), seed=2)
+    dev5 = st.decode_clip(to_dev(z5), out_dtype=torch.float32)
+    host5 = torch.empty((1, 3, 17, 64, 64), dtype=torch.float32).pin_memory()
+    st.decode_clip_host(torch.from_numpy(z5).pin_memory(), host5)
+    torch.cuda.synchronize()
+    assert torch.equal(host5, dev5.cpu())
 
 
 def test_determinism(wv, tiny):

@@ -576,17 +576,6 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-size_t conv_smem_bytes(int bn) {
-  switch (bn) {
-    case 16: return ConvCfg<16, true>::kSmem > ConvCfg<16>::kSmem ? ConvCfg<16, true>::kSmem : ConvCfg<16>::kSmem;
-    case 32: return ConvCfg<32>::kSmem;
-    case 64: return ConvCfg<64>::kSmem;
-    case 128: return ConvCfg<128>::kSmem;
-    case 256: return ConvCfg<256>::kSmem;
-  }
-  return 0;
-}
-
 // Clusters of two CTAs share the B block when it is large (BN = 256); the
 // B tensor map's box must then hold BN / 2 rows (conv_b_box_rows).
 int conv_b_box_rows(int bn) { return bn >= 256 ? bn / 2 : bn; }

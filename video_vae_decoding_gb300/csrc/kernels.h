@@ -115,7 +115,6 @@ cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream);
 // Rows of the B tensor map's box for an N tile of bn (half of it when a
 // cluster of two CTAs shares the B block).
 int conv_b_box_rows(int bn);
-size_t conv_smem_bytes(int bn);
 
 // ---------------------------------------------------------------------------
 // Memory-bound kernels (channels-last bf16 unless stated).

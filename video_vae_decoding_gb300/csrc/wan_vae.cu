@@ -508,6 +508,13 @@ struct wan_vae_stream {
   Act RD[3], HD, ringD[6], ringOut;
   std::vector<Act*> rings;
   std::vector<RingShift> shifts;
+  // decode_clip_host: double-buffered latent / video staging, a copy stream
+  // and its events, created on first use and kept until destroy
+  void* zb[2] = {nullptr, nullptr};
+  void* vb[2] = {nullptr, nullptr};
+  size_t zb_bytes = 0, vb_bytes = 0;
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t dec_ev[2] = {nullptr, nullptr}, d2h_ev[2] = {nullptr, nullptr};
 };
 
 static wan_status ws_take(wan_vae_stream* st, size_t bytes, void** p) {
@@ -1029,10 +1036,11 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   bool out_done = false;
   WAN_TRY(resnet_chain(st, m->up[3], st->RD, st->ringD, st->HD, FC, &nout, s, &out_done));
   // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
-  if (!out_done)
-  ELT(&st->prof, kKindNorm, 4.0 * st->B * FC * st->RD[1].H * st->RD[1].W * m->base * (m->split ? 2 : 1),
-      launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
-                                 st->RD[1].H * st->RD[1].W, true, s, st->RD[1].lo, st->ringOut.lo));
+  if (!out_done) {
+    ELT(&st->prof, kKindNorm, 4.0 * st->B * FC * st->RD[1].H * st->RD[1].W * m->base * (m->split ? 2 : 1),
+        launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
+                        st->RD[1].H * st->RD[1].W, true, s, st->RD[1].lo, st->ringOut.lo));
+  }
   {
     ConvLaunch L;
     const ConvW& co = m->conv_out;
@@ -1110,6 +1118,11 @@ static wan_status stream_build(const wan_vae_model* m, int B, int h, int w, int 
 static void stream_free(wan_vae_stream* st) {
   if (!st) return;
   if (!st->mem.use_async) cudaDeviceSynchronize();
+  for (int k = 0; k < 2; ++k) {
+    if (st->dec_ev[k]) cudaEventDestroy(st->dec_ev[k]);
+    if (st->d2h_ev[k]) cudaEventDestroy(st->d2h_ev[k]);
+  }
+  if (st->copy_stream) cudaStreamDestroy(st->copy_stream);
   st->mem.release();
   if (st->err_host) cudaFreeHost(st->err_host);
   if (st->err_ev) cudaEventDestroy(st->err_ev);
@@ -1410,20 +1423,24 @@ wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int3
     const long long P = (long long)st->h * st->w, HW = 256LL * P;
     const int n = st->nmax;
     const long long nfmax = 4LL * n;
-    // staging: two latent chunks and two video chunks (allocated once per stream)
-    static_assert(sizeof(void*) == 8, "");
-    void *zb[2], *vb[2];
-    for (int k = 0; k < 2; ++k) {
-      WAN_TRY(st->mem.alloc(&zb[k], (size_t)st->B * kZdim * n * P * zes));
-      WAN_TRY(st->mem.alloc(&vb[k], (size_t)st->B * 3 * nfmax * HW * oes));
+    // staging: two latent chunks and two video chunks, kept by the stream
+    const size_t zneed = (size_t)st->B * kZdim * n * P * 4, vneed = (size_t)st->B * 3 * nfmax * HW * 4;
+    if (st->zb_bytes < zneed || st->vb_bytes < vneed) {
+      for (int k = 0; k < 2; ++k) {
+        WAN_TRY(st->mem.alloc(&st->zb[k], zneed));
+        WAN_TRY(st->mem.alloc(&st->vb[k], vneed));
+      }
+      st->zb_bytes = zneed;
+      st->vb_bytes = vneed;
     }
-    cudaStream_t cs;
-    cudaEvent_t dec_ev[2], d2h_ev[2];
-    CUDA_TRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
-    for (int k = 0; k < 2; ++k) {
-      CUDA_TRY(cudaEventCreateWithFlags(&dec_ev[k], cudaEventDisableTiming));
-      CUDA_TRY(cudaEventCreateWithFlags(&d2h_ev[k], cudaEventDisableTiming));
+    if (!st->copy_stream) {
+      CUDA_TRY(cudaStreamCreateWithFlags(&st->copy_stream, cudaStreamNonBlocking));
+      for (int k = 0; k < 2; ++k) {
+        CUDA_TRY(cudaEventCreateWithFlags(&st->dec_ev[k], cudaEventDisableTiming));
+        CUDA_TRY(cudaEventCreateWithFlags(&st->d2h_ev[k], cudaEventDisableTiming));
+      }
     }
+    cudaStream_t cs = st->copy_stream;
     wan_status result = reset_impl(st, s);
     const long long F = 4LL * T - 3;
     long long f0 = 0;
@@ -1432,22 +1449,24 @@ wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int3
       const int k = i & 1;
       const int nn = std::min(n, T - t0);
       const long long nf = t0 == 0 ? 4LL * nn - 3 : 4LL * nn;
-      if (i >= 2 && cudaStreamWaitEvent(s, d2h_ev[k], 0) != cudaSuccess) {
+      // buffer k is free once the download of chunk i - 2 is done
+      if (i >= 2 && cudaStreamWaitEvent(s, st->d2h_ev[k], 0) != cudaSuccess) {
         result = fail(WAN_ERR_CUDA, "cudaStreamWaitEvent failed");
         break;
       }
       // latents of this chunk: rows (b, c) of nn*P values
-      if (cudaMemcpy2DAsync(zb[k], nn * P * zes, (const char*)z_host + t0 * P * zes, (size_t)T * P * zes,
+      if (cudaMemcpy2DAsync(st->zb[k], nn * P * zes, (const char*)z_host + t0 * P * zes, (size_t)T * P * zes,
                             nn * P * zes, (size_t)st->B * kZdim, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         result = fail(WAN_ERR_CUDA, "latent upload failed");
         break;
       }
-      result = decode_chunk_impl(st, zb[k], z_dtype, nn, 0, nn, vb[k], out_dtype, nfmax, 0, nullptr, s);
+      result = decode_chunk_impl(st, st->zb[k], z_dtype, nn, 0, nn, st->vb[k], out_dtype, nfmax, 0, nullptr, s);
       if (result != WAN_OK) break;
-      if (cudaEventRecord(dec_ev[k], s) != cudaSuccess || cudaStreamWaitEvent(cs, dec_ev[k], 0) != cudaSuccess ||
-          cudaMemcpy2DAsync((char*)out_host + f0 * HW * oes, (size_t)F * HW * oes, vb[k], nfmax * HW * oes,
+      // the download of this chunk's frames overlaps the next chunk's decode
+      if (cudaEventRecord(st->dec_ev[k], s) != cudaSuccess || cudaStreamWaitEvent(cs, st->dec_ev[k], 0) != cudaSuccess ||
+          cudaMemcpy2DAsync((char*)out_host + f0 * HW * oes, (size_t)F * HW * oes, st->vb[k], nfmax * HW * oes,
                             nf * HW * oes, (size_t)st->B * 3, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
-          cudaEventRecord(d2h_ev[k], cs) != cudaSuccess) {
+          cudaEventRecord(st->d2h_ev[k], cs) != cudaSuccess) {
         result = fail(WAN_ERR_CUDA, "video download failed");
         break;
       }
@@ -1456,19 +1475,6 @@ wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int3
     }
     cudaStreamSynchronize(cs);
     cudaStreamSynchronize(s);
-    for (int k = 0; k < 2; ++k) {
-      cudaEventDestroy(dec_ev[k]);
-      cudaEventDestroy(d2h_ev[k]);
-    }
-    cudaStreamDestroy(cs);
-    // release the staging buffers
-    for (int k = 0; k < 2; ++k) {
-      for (void** pp : {&zb[k], &vb[k]}) {
-        auto it = std::find(st->mem.ptrs.begin(), st->mem.ptrs.end(), *pp);
-        if (it != st->mem.ptrs.end()) st->mem.ptrs.erase(it);
-        cudaFree(*pp);
-      }
-    }
     if (result != WAN_OK) return result;
     return check_pending_error(st, true);
   })
