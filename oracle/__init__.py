@@ -14,6 +14,10 @@ frame-loop = whole-sequence agreement, causality, batch independence and a
 second, independently written whole-sequence composition from torch library
 ops; there are no printed output values for it, so parity beyond composition
 is unpinned.
+
+``wan_tiled`` adds the tiled decode (the page "[Feature] Implement tiled VAE
+encoding/decoding for Wan model. #11414"): per-tile ``decode`` plus seam
+blending, pinned by ``tests/test_oracle_tiled.py``.
 """
 
 from .wan_decode import (  # noqa: F401
@@ -37,3 +41,4 @@ from .wan_decode import (  # noqa: F401
     time_upsample,
     unpatchify,
 )
+from .wan_tiled import blend_tiles, decode_tiled, tile_origins  # noqa: F401
