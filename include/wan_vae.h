@@ -185,6 +185,37 @@ wan_status wan_vae_decode_clip(wan_vae_stream* st, const void* z, int32_t z_dtyp
 wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int32_t z_dtype, int32_t T,
                                     void* out_host, int32_t out_dtype, wan_cuda_stream stream);
 
+/* Tiled decode (the diffusers pull request "[Feature] Implement tiled VAE
+ * encoding/decoding for Wan model. #11414": opt-in spatial tiling, tiles of a
+ * sample-space size placed at a sample-space stride, defaults 256 and 192).
+ * Decodes z [B, 48, T, h, w] (device, z_dtype) into out [B, 3, 4T-3, 16h, 16w]
+ * (device, out_dtype) as overlapping tiles:
+ *   - along each axis tiles start at 0, stride, 2*stride, ... (every start
+ *     inside the frame) and hold min(tile, remaining) pixels;
+ *   - each tile's latents are decoded on their own, exactly as
+ *     wan_vae_decode_clip would decode them (own causal caches, chunks of
+ *     max_chunk latent frames, unpatchify and clamp), into fp32;
+ *   - in raster order each tile cross-fades its top rows with the tile above
+ *     and then its left columns with the tile to its left, over the e pixels
+ *     the two share: local row (column) k < e becomes
+ *     earlier * (e - k) / e + this * k / e;
+ *   - tile (i, j) supplies the pixels from its origin to the next origin.
+ * The pages fix the interface, not the blend; this is the plainest reading.
+ * tile_h, tile_w, stride_h, stride_w: video pixels, positive multiples of 16,
+ * stride <= tile (stride == tile: no blending).  tile_batch: tiles of equal
+ * size decoded together as one batch (0 = as many as fit in 64 samples);
+ * smaller values lower the peak workspace.  At most 1024 tiles.
+ * Memory: stream-ordered allocations released before return (fp32 tiles of
+ * the whole video, plus one decode workspace at a time); no host
+ * synchronisation.  `out` must be 16-byte aligned.  Errors: WAN_ERR_INVALID_ARG
+ * (sizes, null pointers, alignment; the
+ * tile arguments are checked first), WAN_ERR_DTYPE, WAN_ERR_UNSUPPORTED (too
+ * many tiles), WAN_ERR_OOM, WAN_ERR_CUDA. */
+wan_status wan_vae_decode_tiled(const wan_vae_model* model, const void* z, int32_t z_dtype, int32_t B, int32_t T,
+                                int32_t h, int32_t w, int32_t tile_h, int32_t tile_w, int32_t stride_h,
+                                int32_t stride_w, int32_t tile_batch, int32_t max_chunk, void* out, int32_t out_dtype,
+                                wan_cuda_stream stream);
+
 /* One-shot decode (the page's decode(z, weights, dtype)): packs the weights,
  * decodes z [B, 48, T, h, w] (device, z_dtype) into out [B, 3, 4T-3, 16h, 16w]
  * (device, `dtype`) and releases its temporaries, all stream-ordered

@@ -100,6 +100,17 @@ def test_call_validation_without_device(lib):
     assert lib.wan_causal_conv3d(vp(1), 1, 0, 1, 4, 4, 64, vp(1), vp(1), 0, 64, 3, 2, 3, vp(1), None) == 5
     assert lib.wan_causal_conv3d(vp(1), 1, 3, 1, 4, 4, 64, vp(1), vp(1), 0, 64, 3, 3, 3, vp(1), None) == 1
     assert lib.wan_attention_block(vp(1), 1, 4, 4, 48, None, 0, vp(1), None) == 1
+    # tiled decode: tile arguments are checked before anything else
+    tiled = lambda th, tw, sh, sw, tb=0, mc=4, zd=1, od=1: lib.wan_vae_decode_tiled(  # noqa: E731
+        None, vp(16), zd, 1, 1, 4, 4, th, tw, sh, sw, tb, mc, vp(16), od, None)
+    assert tiled(250, 256, 192, 192) == 1           # not a multiple of 16
+    assert tiled(256, 256, 256, 272) == 1           # stride larger than the tile
+    assert tiled(256, 256, 0, 192) == 1
+    assert tiled(256, 256, 192, 192, tb=-1) == 1
+    assert tiled(256, 256, 192, 192, mc=0) == 1
+    assert tiled(256, 256, 192, 192, zd=7) == 2
+    assert tiled(256, 256, 192, 192) == 1           # null model
+    assert b"model" in lib.wan_vae_last_error()
     from video_vae_decoding_gb300._lib import WanTensor
     assert lib.wan_attention_block(vp(1), 1, 4, 4, 48, (WanTensor * 1)(), 0, vp(1), None) == 5
 

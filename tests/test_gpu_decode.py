@@ -196,6 +196,24 @@ def test_single_latent_frame(wv, tiny):
     _check(got, _ref(z, w), "tiny T=1 bf16")
 
 
+@pytest.mark.parametrize("h,w", [(1, 1), (2, 3), (1, 5)])
+def test_frames_with_few_positions(wv, tiny, h, w):
+    """Latent frames of fewer than 16 positions (down to one): the attention's
+    score GEMM then covers more key rows than the frame has."""
+    wt, wd = tiny
+    z = wan_synth.make_latents((1, 48, 2, h, w), seed=22)
+    for dt in (torch.bfloat16, torch.float32):
+        model = wv.Model(wd, dtype=dt)
+        got = _decode(wv, model, z, 2)
+        assert got.shape == (1, 3, 5, 16 * h, 16 * w)
+        if dt == torch.bfloat16:
+            _check(got, _ref(z, wt), f"tiny {h}x{w} latents bf16")
+        else:
+            err = float(np.abs(got - oracle.decode(z, wt)).max())
+            record(f"tiny {h}x{w} latents fp32", err, None)
+            assert err <= TOL_F32, err
+
+
 def test_stream_reuse_after_reset(wv, tiny):
     """A stream decodes a second clip from scratch: bit-identical to a fresh stream."""
     w, wd = tiny

@@ -82,6 +82,19 @@ class Model:
     def base_dim(self) -> int:
         return int(load().wan_vae_model_base_dim(self._h))
 
+    def decode_tiled(self, z: torch.Tensor, tile=(256, 256), stride=(192, 192), out_dtype: torch.dtype = None,
+                     tile_batch: int = 0, max_chunk: int = 4, stream=None) -> torch.Tensor:
+        """Tiled decode (wan_vae_decode_tiled): z [B, 48, T, h, w] on the GPU ->
+        video [B, 3, 4T-3, 16h, 16w]; tile and stride are (height, width) in
+        video pixels, multiples of 16."""
+        B, _, T, h, w = z.shape
+        dt = self.dtype if out_dtype is None else out_dtype
+        out = torch.empty((B, 3, 4 * T - 3, 16 * h, 16 * w), device=z.device, dtype=dt)
+        check(load().wan_vae_decode_tiled(self._h, _dev(z, "z"), _code(z.dtype), B, T, h, w, tile[0], tile[1],
+                                          stride[0], stride[1], tile_batch, max_chunk, _dev(out, "out"), _code(dt),
+                                          _stream(stream)))
+        return out
+
     def close(self):
         if self._h:
             load().wan_vae_model_destroy(self._h)

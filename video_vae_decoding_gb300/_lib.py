@@ -66,6 +66,8 @@ SIGNATURES = {
     "wan_vae_decode_clip": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]),
     "wan_vae_decode_clip_host": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp]),
     "wan_vae_decode": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(WanTensor), _i32, _vp, _i32, _vp]),
+    "wan_vae_decode_tiled": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                    _vp, _i32, _vp]),
     "wan_attention_block": (_i32, [_vp, _i32, _i32, _i32, _i32, ctypes.POINTER(WanTensor), _i32, _vp, _vp]),
     "wan_causal_conv3d": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                  _vp, _vp]),

@@ -173,4 +173,36 @@ cudaError_t launch_pack_subpixel(const void* src, int src_f32, int Co, int Ci, _
 cudaError_t launch_to_f32(const void* src, int src_f32, const void* src2, int src2_f32, float* dst, int n,
                           float scale, int round_bf16, cudaStream_t s);
 
+// ---------------------------------------------------------------------------
+// Tiled decode (tiled.cu).  Decoded tiles are fp32 [B][3][F][h][w] each, at
+// element offset `off` of one buffer; the table lists them in raster order.
+// Passed by value as kernel parameters (kept under the 32 KB limit).
+// ---------------------------------------------------------------------------
+struct TileDesc {
+  long long off;  // element offset of the tile in the buffer (a multiple of 4)
+  int h, w;       // pixels (multiples of 16)
+};
+constexpr int kMaxTiles = 1024;
+struct TileTable {
+  int ni, nj;  // tile rows and columns
+  int sh, sw;  // stride in pixels: tile (i, j) starts at (i*sh, j*sw)
+  TileDesc t[kMaxTiles];
+};
+// One batch of latent tiles of equal size: zt[(k*B + b)][c][t][y][x] =
+// z[b][c][t][r0[k] + y][c0[k] + x], CT = 48 * T.
+constexpr int kMaxGather = 64;
+struct TileGather {
+  int n, B, h, w, th, tw;
+  long long CT;
+  int r0[kMaxGather], c0[kMaxGather];
+};
+// elem_bytes: 4 (fp32) or 2 (bf16), copied as is.
+cudaError_t launch_gather_tiles(const void* z, int elem_bytes, void* zt, const TileGather& g, cudaStream_t s);
+// Seam blending in place, one launch per anti-diagonal of tiles; planes =
+// B * 3 * F.
+cudaError_t launch_blend_tiles(float* buf, const TileTable& tab, long long planes, cudaStream_t s);
+// out [planes][H][W] (fp32 or bf16) from the blended tiles.
+cudaError_t launch_assemble_tiles(const float* buf, const TileTable& tab, void* out, int out_f32, long long planes,
+                                  int H, int W, cudaStream_t s);
+
 }  // namespace wan

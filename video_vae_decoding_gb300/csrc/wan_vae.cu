@@ -18,6 +18,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -852,7 +853,6 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
                             int F, Prof* prof, int* err, cudaStream_t s) {
   const double M = (double)at.B * F * at.HW;
   const int C = at.C, HW = at.HW, B = at.B, sp = at.sp - 1;
-  if (HW < 16) return fail(WAN_ERR_UNSUPPORTED, "attention over %d positions (at least 16 supported)", HW);
   ELT(prof, kKindNorm, 4.0 * M * C * at.sp, launch_rms_norm(x.view(0), at.an.view(0), g, C, B, F, HW, false, s, x.lo, at.an.lo));
   ConvLaunch L;
   // qkv = n Wqkv^T + b; split weights keep their low halves ci_pad after the high ones
@@ -864,7 +864,11 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
   set_out(L.args, out_of(at.qkv));
   WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * 3 * C * C, err, s));
   // S = q k^T: q = channels [0, C) of qkv, k = [C, 2C) (low halves 3C further on)
-  int bnS = 16;  // largest power of two <= min(HW, 256): the K-operand box stays inside the tensor
+  // N tile: the largest power of two <= min(HW, 256), at least 16.  With
+  // fewer than 16 positions the key box runs past the frame's rows: TMA reads
+  // zeros there, the extra columns of S are never read by the softmax (n =
+  // HW), and P and V^T keep zeros beyond HW from the workspace clear.
+  int bnS = 16;
   while (bnS * 2 <= std::min(HW, 256)) bnS *= 2;
   WAN_TRY(gemm_setup(L, at.qkv.p, at.qkv.ldc, at.qkv.lo, HW, at.qkv.F, B, at.qkv.fs(), at.qkv.bs(), C, C, at.qkv.lo,
                      sp, (int)cdiv(at.HWs, bnS), bnS, F));
@@ -1189,6 +1193,110 @@ static wan_status clip_impl(wan_vae_stream* st, const void* z, int z_dtype, int 
   return WAN_OK;
 }
 
+// ------------------------------------------------------------- tiled decode
+// Tiles of equal latent size are decoded together as one batch (up to 64
+// samples per stream); each batch's output lands in the tile buffer at the
+// offsets of its tiles, which are consecutive.  Then the seams are blended
+// and the blended tiles assembled into `out`.
+static wan_status tiled_impl(const wan_vae_model* m, const void* z, int z_dtype, int B, int T, int h, int w,
+                             int tile_h, int tile_w, int stride_h, int stride_w, int tile_batch, int max_chunk,
+                             void* out, int out_dtype, cudaStream_t s) {
+  constexpr int P = 16;  // pixels per latent
+  const int th = tile_h / P, tw = tile_w / P, sh = stride_h / P, sw = stride_w / P;
+  std::vector<std::pair<int, int>> rows, cols;  // (origin, size) in latents
+  for (int r = 0; r < h; r += sh) rows.push_back({r, std::min(th, h - r)});
+  for (int c = 0; c < w; c += sw) cols.push_back({c, std::min(tw, w - c)});
+  const int ni = (int)rows.size(), nj = (int)cols.size();
+  if ((long long)ni * nj > kMaxTiles) return fail(WAN_ERR_UNSUPPORTED, "%d x %d tiles (at most %d)", ni, nj, kMaxTiles);
+  const long long F = 4LL * T - 3, planes = 3LL * B * F;
+  // tiles grouped by size, raster order inside a group
+  std::vector<std::pair<std::pair<int, int>, int>> order;  // ((rows, cols), raster index)
+  for (int i = 0; i < ni; ++i)
+    for (int j = 0; j < nj; ++j) order.push_back({{rows[i].second, cols[j].second}, i * nj + j});
+  std::stable_sort(order.begin(), order.end(),
+                   [](const auto& a, const auto& b) { return a.first < b.first; });
+  std::unique_ptr<TileTable> tab(new TileTable());
+  tab->ni = ni;
+  tab->nj = nj;
+  tab->sh = stride_h;
+  tab->sw = stride_w;
+  long long total = 0;
+  size_t zt_elems = 0;
+  for (const auto& o : order) {
+    TileDesc& t = tab->t[o.second];
+    t.h = P * o.first.first;
+    t.w = P * o.first.second;
+    t.off = total;
+    total += planes * t.h * t.w;
+  }
+  const int per_batch = std::max(1, std::min(tile_batch > 0 ? tile_batch : kMaxGather, std::min(kMaxGather, 64 / B)));
+  for (const auto& o : order)
+    zt_elems = std::max(zt_elems, (size_t)per_batch * B * kZdim * T * o.first.first * o.first.second);
+  const int zes = z_dtype == WAN_F32 ? 4 : 2;
+  DevMem mem;
+  mem.use_async = true;
+  mem.async = s;
+  wan_status r = WAN_OK;
+  void *buf = nullptr, *zt = nullptr;
+  wan_vae_stream* st = nullptr;
+  auto drop_stream = [&]() {
+    if (st) {
+      st->mem.release();
+      delete st;
+      st = nullptr;
+    }
+  };
+  do {
+    if ((r = mem.alloc(&buf, (size_t)total * sizeof(float))) != WAN_OK) break;
+    if ((r = mem.alloc(&zt, zt_elems * zes)) != WAN_OK) break;
+    int sb = 0, sh_l = 0, sw_l = 0;  // the current stream's batch and tile size
+    for (size_t g0 = 0; g0 < order.size() && r == WAN_OK;) {
+      // the next batch: up to per_batch tiles of the same size
+      size_t g1 = g0 + 1;
+      while (g1 < order.size() && (int)(g1 - g0) < per_batch && order[g1].first == order[g0].first) ++g1;
+      const int n = (int)(g1 - g0), rh = order[g0].first.first, cw = order[g0].first.second;
+      if (!st || sb != n * B || sh_l != rh || sw_l != cw) {
+        drop_stream();
+        st = new wan_vae_stream();
+        if ((r = stream_build(m, n * B, rh, cw, std::min(T, max_chunk), true, s, st)) != WAN_OK) break;
+        sb = n * B;
+        sh_l = rh;
+        sw_l = cw;
+      }
+      TileGather gt;
+      gt.n = n;
+      gt.B = B;
+      gt.h = h;
+      gt.w = w;
+      gt.th = rh;
+      gt.tw = cw;
+      gt.CT = (long long)kZdim * T;
+      for (int k = 0; k < n; ++k) {
+        const int idx = order[g0 + k].second;
+        gt.r0[k] = rows[idx / nj].first;
+        gt.c0[k] = cols[idx % nj].first;
+      }
+      if (launch_gather_tiles(z, zes, zt, gt, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "tile gather launch failed");
+        break;
+      }
+      r = clip_impl(st, zt, z_dtype, T, (float*)buf + tab->t[order[g0].second].off, WAN_F32, nullptr, s);
+      g0 = g1;
+    }
+    if (r != WAN_OK) break;
+    if (launch_blend_tiles((float*)buf, *tab, planes, s) != cudaSuccess) {
+      r = fail(WAN_ERR_CUDA, "tile blend launch failed");
+      break;
+    }
+    if (launch_assemble_tiles((const float*)buf, *tab, out, out_dtype == WAN_F32, planes, P * h, P * w, s) !=
+        cudaSuccess)
+      r = fail(WAN_ERR_CUDA, "tile assembly launch failed");
+  } while (false);
+  drop_stream();
+  mem.release();
+  return r;
+}
+
 // ------------------------------------------------------------- C ABI
 #define API_GUARD(...)                                               \
   try {                                                              \
@@ -1503,6 +1611,34 @@ wan_status wan_vae_decode(const void* z, int32_t z_dtype, int32_t B, int32_t T, 
     }
     m.mem.release();
     return r;
+  })
+}
+
+wan_status wan_vae_decode_tiled(const wan_vae_model* model, const void* z, int32_t z_dtype, int32_t B, int32_t T,
+                                int32_t h, int32_t w, int32_t tile_h, int32_t tile_w, int32_t stride_h,
+                                int32_t stride_w, int32_t tile_batch, int32_t max_chunk, void* out, int32_t out_dtype,
+                                wan_cuda_stream stream) {
+  API_GUARD({
+    for (int v : {tile_h, tile_w, stride_h, stride_w})
+      if (v <= 0 || v % 16)
+        return fail(WAN_ERR_INVALID_ARG, "tile %dx%d, stride %dx%d: positive multiples of 16 pixels needed", tile_h,
+                    tile_w, stride_h, stride_w);
+    if (stride_h > tile_h || stride_w > tile_w)
+      return fail(WAN_ERR_INVALID_ARG, "tile stride %dx%d larger than the tile %dx%d", stride_h, stride_w, tile_h,
+                  tile_w);
+    if (tile_batch < 0 || max_chunk < 1)
+      return fail(WAN_ERR_INVALID_ARG, "tile_batch=%d (>= 0) max_chunk=%d (>= 1)", tile_batch, max_chunk);
+    WAN_TRY(dtype_ok(z_dtype, "latents"));
+    WAN_TRY(dtype_ok(out_dtype, "output"));
+    if (!model) return fail(WAN_ERR_INVALID_ARG, "null model");
+    if (!z || !out) return fail(WAN_ERR_INVALID_ARG, "null latents or output");
+    if ((uintptr_t)out % 16) return fail(WAN_ERR_INVALID_ARG, "output not 16-byte aligned");
+    if (B < 1 || B > 64 || T < 1 || h < 1 || w < 1 || max_chunk > 64)
+      return fail(WAN_ERR_INVALID_ARG, "B=%d (1..64) T=%d h=%d w=%d max_chunk=%d (<= 64)", B, T, h, w, max_chunk);
+    if ((long long)16 * h > 65535 || (long long)16 * w > 65535)
+      return fail(WAN_ERR_UNSUPPORTED, "frame of %dx%d latents too large", h, w);
+    return tiled_impl(model, z, z_dtype, B, T, h, w, tile_h, tile_w, stride_h, stride_w, tile_batch, max_chunk, out,
+                      out_dtype, (cudaStream_t)stream);
   })
 }
 
