@@ -205,6 +205,88 @@ def run_attention(args):
     return 0
 
 
+def _tile_origins(n, tile, stride):
+    return [(s, min(tile, n - s)) for s in range(0, n, stride)]
+
+
+def run_tiled(args):
+    """The 720p clip decoded as overlapping spatial tiles (wan_vae_decode_tiled),
+    default tiles of 256x256 pixels at a stride of 192; the untiled decode of
+    the same clip is timed beside it."""
+    import torch
+    from video_vae_decoding_gb300 import build as _build
+    _build.build()
+    import video_vae_decoding_gb300 as wv
+    th, tw = (int(v) for v in args.tile.split(","))
+    sh, sw = (int(v) for v in args.stride.split(","))
+    w = wan_synth.make_weights(base=WORKLOAD["base"], seed=WORKLOAD["weight_seed"])
+    wdev = {k: torch.from_numpy(np.array(v)).cuda() for k, v in w.items()}
+    model = wv.Model(wdev, dtype=torch.bfloat16)
+    del wdev
+    z = torch.from_numpy(wan_synth.make_latents((B, Z, T, H_LAT, W_LAT), WORKLOAD["latent_seed"])).cuda()
+    rows = _tile_origins(H_LAT, th // 16, sh // 16)
+    cols = _tile_origins(W_LAT, tw // 16, sw // 16)
+    shapes = {}
+    for _, rh in rows:
+        for _, cw in cols:
+            shapes[(rh, cw)] = shapes.get((rh, cw), 0) + 1
+    # nominal FLOPs of the tile decodes, counted by the library's profiler
+    flops = 0.0
+    for (rh, cw), n in shapes.items():
+        st = wv.DecodeStream(model, n * B, rh, cw, max_chunk=args.chunk)
+        st.profile_begin()
+        st.decode_clip(torch.zeros((n * B, Z, T, rh, cw), device="cuda"), out_dtype=torch.bfloat16)
+        flops += st.profile_end()["tc_flops"]
+        st.close()
+    torch.cuda.synchronize()
+
+    def tiled():
+        return model.decode_tiled(z, tile=(th, tw), stride=(sh, sw), max_chunk=args.chunk)
+
+    for _ in range(args.warmup):
+        tiled()
+    torch.cuda.synchronize()
+    gpu_uuid = str(torch.cuda.get_device_properties(0).uuid)
+    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        tiled()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    # the untiled decode of the same clip, same chunking
+    st = wv.DecodeStream(model, B, H_LAT, W_LAT, max_chunk=args.chunk)
+    out = torch.empty((B, 3, FRAMES, H_OUT, W_OUT), device="cuda", dtype=torch.bfloat16)
+    st.decode_clip(z, out)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        st.decode_clip(z, out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_untiled = e0.elapsed_time(e1) / args.steps
+    burst, sustained, _, src = _peaks()
+    tf = flops / (ms / 1000.0) / 1e12
+    area = sum(rh * cw * n for (rh, cw), n in shapes.items()) / (H_LAT * W_LAT)
+    print(json.dumps({
+        "metric": f"tiled decode frames/s (704x1280, bf16, tiles {th}x{tw} stride {sh}x{sw})",
+        "value": B * FRAMES / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic: seeded random-init TI2V-5B decoder weights, N(0,1) latents",
+        "config": {"workload": "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280] bf16, tiled",
+                   "tiles": f"{len(rows)}x{len(cols)}", "tile_shapes_latents": {f"{a}x{b}": n for (a, b), n in
+                                                                              sorted(shapes.items())},
+                   "tile_area_over_frame": area, "chunk_latent_frames": args.chunk},
+        "nominal_tflop_per_step": flops / 1e12, "tflops_nominal": tf,
+        "frac_of_bf16_peak": {"burst": tf / burst, "sustained": tf / sustained, "source": src},
+        "untiled_ms_per_step": ms_untiled, "tiled_over_untiled_time": ms / ms_untiled, "clocks": clocks}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -215,8 +297,11 @@ def main():
     ap.add_argument("--latents", default=None,
                     help="B,T,h,w of the latents (default: the 720p workload 1,31,44,80); other shapes are "
                          "for profiling and report frames of their own size")
-    ap.add_argument("--workload", choices=("decode", "attention"), default="decode",
-                    help="attention: the isolated mid-block attention (x [8, 1024, 44, 80]) instead of the decode")
+    ap.add_argument("--workload", choices=("decode", "attention", "tiled"), default="decode",
+                    help="attention: the isolated mid-block attention (x [8, 1024, 44, 80]) instead of the decode; "
+                         "tiled: the 720p clip decoded as overlapping spatial tiles")
+    ap.add_argument("--tile", default="256,256", help="tiled workload: tile height,width in pixels")
+    ap.add_argument("--stride", default="192,192", help="tiled workload: tile stride height,width in pixels")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -226,6 +311,8 @@ def main():
         return run_reference(args)
     if args.workload == "attention":
         return run_attention(args)
+    if args.workload == "tiled":
+        return run_tiled(args)
     global B, T, H_LAT, W_LAT, FRAMES, H_OUT, W_OUT, METRIC
     custom = args.latents is not None
     if custom:
