@@ -17,7 +17,9 @@ is unpinned.
 
 ``wan_tiled`` adds the tiled decode (the page "[Feature] Implement tiled VAE
 encoding/decoding for Wan model. #11414"): per-tile ``decode`` plus seam
-blending, pinned by ``tests/test_oracle_tiled.py``.
+blending, pinned by ``tests/test_oracle_tiled.py``.  ``wan_latents`` adds the
+latent de-normalisation in front of the decode, pinned by
+``tests/test_oracle_latents.py``.
 """
 
 from .wan_decode import (  # noqa: F401
@@ -42,3 +44,4 @@ from .wan_decode import (  # noqa: F401
     unpatchify,
 )
 from .wan_tiled import blend_tiles, decode_tiled, tile_origins  # noqa: F401
+from .wan_latents import decode_normalized, denormalize_latents  # noqa: F401
