@@ -105,6 +105,21 @@ void wan_vae_model_destroy(wan_vae_model* model);
 /* Decoder base dim b of a model (256 for TI2V-5B), or -1 for NULL. */
 int32_t wan_vae_model_base_dim(const wan_vae_model* model);
 
+/* Latent de-normalisation in front of the decode (the diffusers Wan VAE's
+ * per-channel `latents_mean` / `latents_std` configuration lists, page
+ * "[Feature] Implement tiled VAE encoding/decoding for Wan model. #11414";
+ * the page gives neither values nor formula).  With statistics set, every
+ * decode through this model (one-shot excepted: it has no model handle,
+ * streams and tiled decodes included) first maps each latent to
+ * z * std[c] + mean[c] in fp32, inside the post_quant_conv kernel, and then
+ * applies the decode's own input rounding (bf16 models round the result).
+ * mean, std_dev: HOST arrays of n = 48 finite fp32 values, copied before
+ * return (synchronous copy); both NULL switches it off again.  Call it between
+ * decodes, never while a decode that uses the model is in flight.
+ * Errors: WAN_ERR_INVALID_ARG (null model, one of the two NULL, a value not
+ * finite), WAN_ERR_SHAPE (n != 48), WAN_ERR_OOM, WAN_ERR_CUDA. */
+wan_status wan_vae_model_set_latent_stats(wan_vae_model* model, const float* mean, const float* std_dev, int32_t n);
+
 /* A decode stream: the causal caches (two frames per 3-frame conv, page
  * section "Causal caches") and the activation workspace for latents of
  * B x h x w, decoding at most `max_chunk` latent frames per call.  The

@@ -100,6 +100,8 @@ def test_call_validation_without_device(lib):
     assert lib.wan_causal_conv3d(vp(1), 1, 0, 1, 4, 4, 64, vp(1), vp(1), 0, 64, 3, 2, 3, vp(1), None) == 5
     assert lib.wan_causal_conv3d(vp(1), 1, 3, 1, 4, 4, 64, vp(1), vp(1), 0, 64, 3, 3, 3, vp(1), None) == 1
     assert lib.wan_attention_block(vp(1), 1, 4, 4, 48, None, 0, vp(1), None) == 1
+    f48 = (ctypes.c_float * 48)()
+    assert lib.wan_vae_model_set_latent_stats(None, f48, f48, 48) == 1
     # tiled decode: tile arguments are checked before anything else
     tiled = lambda th, tw, sh, sw, tb=0, mc=4, zd=1, od=1: lib.wan_vae_decode_tiled(  # noqa: E731
         None, vp(16), zd, 1, 1, 4, 4, th, tw, sh, sw, tb, mc, vp(16), od, None)

@@ -82,6 +82,19 @@ class Model:
     def base_dim(self) -> int:
         return int(load().wan_vae_model_base_dim(self._h))
 
+    def set_latent_stats(self, mean=None, std=None):
+        """Latent de-normalisation (wan_vae_model_set_latent_stats): later decodes
+        through this model map z to z * std + mean per latent channel first.
+        mean, std: 48 values each (sequence, array or tensor); both None: off."""
+        if mean is None and std is None:
+            check(load().wan_vae_model_set_latent_stats(self._h, None, None, 0))
+            return
+        m = torch.as_tensor(mean, dtype=torch.float32).detach().cpu().contiguous().reshape(-1)
+        s = torch.as_tensor(std, dtype=torch.float32).detach().cpu().contiguous().reshape(-1)
+        if m.numel() != s.numel():
+            raise ValueError(f"{m.numel()} means but {s.numel()} stds")
+        check(load().wan_vae_model_set_latent_stats(self._h, m.data_ptr(), s.data_ptr(), m.numel()))
+
     def decode_tiled(self, z: torch.Tensor, tile=(256, 256), stride=(192, 192), out_dtype: torch.dtype = None,
                      tile_batch: int = 0, max_chunk: int = 4, stream=None) -> torch.Tensor:
         """Tiled decode (wan_vae_decode_tiled): z [B, 48, T, h, w] on the GPU ->

@@ -119,14 +119,19 @@ __global__ void copy_frames_kernel(FrameView in, FrameView out, int C8, int F, i
 }
 
 // post_quant_conv (1x1x1, 48 -> 48) on NCDHW latents; one thread per position.
+// With zstat (mean[48] then std[48]) each latent is first de-normalised,
+// z * std[c] + mean[c], in fp32.
 constexpr int kZ = 48;
 __global__ void post_quant_kernel(const void* __restrict__ z, int z_f32, int Tz, int t0, int F, int P,
-                                  const float* __restrict__ w, const float* __restrict__ bias, FrameView out,
-                                  long long n, int round_z, int out_lo) {
+                                  const float* __restrict__ w, const float* __restrict__ bias,
+                                  const float* __restrict__ zstat, FrameView out, long long n, int round_z,
+                                  int out_lo) {
   __shared__ float sw[kZ * kZ];
   __shared__ float sb[kZ];
+  __shared__ float sst[2 * kZ];
   for (int i = threadIdx.x; i < kZ * kZ; i += blockDim.x) sw[i] = w[i];
   for (int i = threadIdx.x; i < kZ; i += blockDim.x) sb[i] = bias[i];
+  for (int i = threadIdx.x; i < 2 * kZ; i += blockDim.x) sst[i] = zstat ? zstat[i] : (i < kZ ? 0.f : 1.f);
   __syncthreads();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
@@ -140,6 +145,7 @@ __global__ void post_quant_kernel(const void* __restrict__ z, int z_f32, int Tz,
     const long long o = base + (long long)c * Tz * P;
     zin[c] = z_f32 ? static_cast<const float*>(z)[o]
                    : __bfloat162float(static_cast<const __nv_bfloat16*>(z)[o]);
+    if (zstat) zin[c] = fmaf(zin[c], sst[kZ + c], sst[c]);
     if (round_z) zin[c] = __bfloat162float(__float2bfloat16_rn(zin[c]));
   }
   __nv_bfloat16* dst = at_mut(out, b, f, p);
@@ -348,11 +354,13 @@ cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F,
 }
 
 cudaError_t launch_post_quant(const void* z, int z_f32, int B, int Tz, int t0, int F, int P, const float* w,
-                              const float* bias, FrameView out, int round_z_bf16, cudaStream_t s, int out_lo) {
+                              const float* bias, const float* zstat, FrameView out, int round_z_bf16, cudaStream_t s,
+                              int out_lo) {
   if (out.ldc % 8 || out.ldc < kZ) return cudaErrorInvalidValue;
   const long long n = (long long)B * F * P;
   if (n == 0) return cudaSuccess;
-  post_quant_kernel<<<blocks_for(n, 128), 128, 0, s>>>(z, z_f32, Tz, t0, F, P, w, bias, out, n, round_z_bf16, out_lo);
+  post_quant_kernel<<<blocks_for(n, 128), 128, 0, s>>>(z, z_f32, Tz, t0, F, P, w, bias, zstat, out, n, round_z_bf16,
+                                                       out_lo);
   return cudaGetLastError();
 }
 

@@ -135,8 +135,11 @@ cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C,
 cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F, int P, cudaStream_t s);
 // post_quant_conv: z [B][48][Tz][h][w] (fp32 or bf16, NCDHW), frames t0..t0+F-1
 // -> out(b, f, p, 0..47) bf16; channels 48..ldc-1 are written as zero.
+// zstat: NULL, or mean[48] then std[48] (fp32): the latents are first
+// de-normalised to z * std + mean (before the bf16 rounding of round_z_bf16).
 cudaError_t launch_post_quant(const void* z, int z_f32, int B, int Tz, int t0, int F, int P, const float* w /*48x48*/,
-                              const float* bias, FrameView out, int round_z_bf16, cudaStream_t s, int out_lo = 0);
+                              const float* bias, const float* zstat, FrameView out, int round_z_bf16, cudaStream_t s,
+                              int out_lo = 0);
 // Row softmax of S [R][ld_s] fp32 (n valid columns) scaled by `scale`, into
 // P [R][ld_p] bf16.
 cudaError_t launch_softmax_rows(const float* S, long long ld_s, __nv_bfloat16* P, long long ld_p, int n, long long R,

@@ -383,6 +383,9 @@ struct wan_vae_model {
   ConvW resample[3];
   float* out_g = nullptr;
   ConvW conv_out;
+  // latent de-normalisation in front of post_quant_conv: mean[48], std[48]
+  float* zstat = nullptr;
+  bool zstat_on = false;
   DevMem mem;
 };
 
@@ -1015,7 +1018,7 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   const int P = st->h * st->w;
   st->shifts.clear();
   // 1. post_quant_conv into conv_in's ring
-  ELT(&st->prof, kKindMisc, (double)st->B * FA * P * (kZdim * (z_f32 ? 4 : 2) + 2 * st->ringIn.ldc), launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, st->ringIn.view(2),
+  ELT(&st->prof, kKindMisc, (double)st->B * FA * P * (kZdim * (z_f32 ? 4 : 2) + 2 * st->ringIn.ldc), launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, m->zstat_on ? m->zstat : nullptr, st->ringIn.view(2),
                                    m->split ? 0 : 1, s, st->ringIn.lo));
   // 2. conv_in, mid block
   WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s));
@@ -1356,6 +1359,33 @@ void wan_vae_model_destroy(wan_vae_model* model) {
 }
 
 int32_t wan_vae_model_base_dim(const wan_vae_model* model) { return model ? model->base : -1; }
+
+wan_status wan_vae_model_set_latent_stats(wan_vae_model* model, const float* mean, const float* std_dev, int32_t n) {
+  API_GUARD({
+    if (!model) return fail(WAN_ERR_INVALID_ARG, "null model");
+    if (!mean && !std_dev) {
+      model->zstat_on = false;
+      return WAN_OK;
+    }
+    if (!mean || !std_dev) return fail(WAN_ERR_INVALID_ARG, "mean and std must both be given or both be NULL");
+    if (n != kZdim) return fail(WAN_ERR_SHAPE, "%d latent statistics given, %d expected", n, kZdim);
+    float h[2 * kZdim];
+    for (int c = 0; c < kZdim; ++c) {
+      h[c] = mean[c];
+      h[kZdim + c] = std_dev[c];
+      if (!std::isfinite(h[c]) || !std::isfinite(h[kZdim + c]))
+        return fail(WAN_ERR_INVALID_ARG, "latent statistic of channel %d is not finite", c);
+    }
+    if (!model->zstat) {
+      void* p;
+      WAN_TRY(model->mem.alloc(&p, sizeof(h)));
+      model->zstat = (float*)p;
+    }
+    CUDA_TRY(cudaMemcpy(model->zstat, h, sizeof(h), cudaMemcpyHostToDevice));
+    model->zstat_on = true;
+    return WAN_OK;
+  })
+}
 
 wan_status wan_vae_stream_create(const wan_vae_model* model, int32_t B, int32_t h, int32_t w, int32_t max_chunk,
                                  wan_vae_stream** out) {
