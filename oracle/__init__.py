@@ -41,6 +41,7 @@ from .wan_decode import (  # noqa: F401
     spatial_upsample,
     time_interleave,
     time_upsample,
+    is_wan21,
     unpatchify,
 )
 from .wan_tiled import blend_tiles, decode_tiled, tile_origins  # noqa: F401

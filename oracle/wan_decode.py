@@ -1,4 +1,5 @@
-"""The Wan2.2-TI2V-5B VAE decode, written out plainly in NumPy (CPU oracle).
+"""The Wan2.2-TI2V-5B VAE decode, written out plainly in NumPy (CPU oracle),
+and the Wan2.1 VAE decode that shares its parts.
 
 Test infrastructure only: the CUDA path never imports this module.
 
@@ -13,6 +14,21 @@ and sums are taken in fp64.  A bf16 decode is represented by feeding the oracle
 bf16-rounded latents and weights (``round_bf16``), the first step of the
 page's bf16 contract (section "Precision"); the oracle itself always computes
 in fp32.
+
+Wan2.1 VAE (``AutoencoderKLWan`` of the Wan 2.1 and Wan 2.2 A14B pipelines,
+page "Fix the Wan VAE attention block"): the page fixes z_dim 16, 8x spatial
+compression (720p latents of 90x160, attention over 14,400 positions per
+frame) and that its attention block is the same one-head block over a
+frame's positions.  The rest of its decoder is not on the pages; the reading
+taken here is that model's published configuration, built from the same
+parts: base dim 96, channel multipliers (1, 2, 4, 4), two residual blocks
+per level (three per up block), temporal upsampling in the first two up
+blocks, and resamplers whose conv halves the channels (C -> C/2) with no
+DupUp3D shortcut and no 2x2 patching; conv_out writes the 3 colours
+directly.  Its up blocks, for base dim b: 4b -> 4b (time and space), 2b ->
+4b (time and space), 2b -> 2b (space), b -> b; parameter names as in
+diffusers (``upsamplers.0.time_conv``, ``upsamplers.0.resample.1``).  The
+variant is read from the weights: post_quant_conv 16 -> 16 is Wan2.1.
 """
 
 from __future__ import annotations
@@ -212,7 +228,7 @@ def nearest_exact_up2(x: np.ndarray) -> np.ndarray:
 
 def spatial_upsample(x, weights, name):
     """upsample2d: per frame, nearest x2 in h and w, then a 3x3 conv2d C -> C
-    with zero padding 1 (``spatial_upsample``)."""
+    (C -> C/2 in the Wan2.1 decoder) with zero padding 1 (``spatial_upsample``)."""
     return conv2d(nearest_exact_up2(x), weights[f"{name}.weight"], weights[f"{name}.bias"])
 
 
@@ -235,9 +251,11 @@ def dup_up(x: np.ndarray, out_channels: int, ft: int, first: bool) -> np.ndarray
     return out[:, :, ft - 1:] if first else out
 
 
-def up_block(x, weights, i, cache, first, up_blocks):
+def up_block(x, weights, i, cache, first, up_blocks, wan21: bool = False):
     """WanResidualUpBlock i (``up_block``): three residual blocks, then for up
-    blocks 0-2 the resampler plus DupUp3D of the block's input.
+    blocks 0-2 the resampler plus DupUp3D of the block's input.  In the Wan2.1
+    decoder the resampler (``upsamplers.0``) halves the channels and there is
+    no DupUp3D.
 
     Section "The first latent frame yields one frame": on the first chunk the
     time conv is skipped for its first frame, which passes through as one
@@ -245,13 +263,14 @@ def up_block(x, weights, i, cache, first, up_blocks):
     """
     _, cout, temporal, spatial = up_blocks[i]
     name = f"decoder.up_blocks.{i}"
+    ups = f"{name}.upsamplers.0" if wan21 else f"{name}.upsampler"
     block_input = x
     for j in range(RESNETS_PER_UP_BLOCK):
         x = residual_block(x, weights, f"{name}.resnets.{j}", cache)
     if not spatial:
         return x
     if temporal:
-        tconv = f"{name}.upsampler.time_conv"
+        tconv = f"{ups}.time_conv"
         if first:
             rest = x[:, :, 1:]
             if rest.shape[2] > 0:
@@ -260,7 +279,9 @@ def up_block(x, weights, i, cache, first, up_blocks):
                 x = x[:, :, :1]
         else:
             x = time_upsample(x, weights, tconv, cache)
-    x = spatial_upsample(x, weights, f"{name}.upsampler.resample.1")
+    x = spatial_upsample(x, weights, f"{ups}.resample.1")
+    if wan21:
+        return x
     return (x + dup_up(block_input, cout, 2 if temporal else 1, first)).astype(F32)
 
 
@@ -271,20 +292,35 @@ def _up_blocks(base: int):
             (4 * base, 2 * base, False, True), (2 * base, base, False, False))
 
 
+def _up_blocks_wan21(base: int):
+    """The Wan2.1 decoder's (in, out, temporal, spatial) per up block; each
+    resampler halves its block's output channels, so the next block starts
+    from half of them."""
+    return ((4 * base, 4 * base, True, True), (2 * base, 4 * base, True, True),
+            (2 * base, 2 * base, False, True), (base, base, False, False))
+
+
+def is_wan21(weights) -> bool:
+    """The Wan2.1 VAE (z_dim 16) rather than TI2V-5B's (z_dim 48)."""
+    return np.asarray(weights["post_quant_conv.weight"]).shape[0] == 16
+
+
 def decode_chunk(x, weights, cache, first):
     """The decoder on a chunk of latent frames x [B, 48, n, h, w] (``decode_chunk``).
 
     conv_in, mid block (residual, attention, residual), up blocks 0-3, then
-    norm_out, SiLU and conv_out.  Returns [B, 12, 4n-3 (first) or 4n, 8h, 8w].
+    norm_out, SiLU and conv_out.  Returns [B, 12, 4n-3 (first) or 4n, 8h, 8w]
+    (Wan2.1: x [B, 16, n, h, w] -> [B, 3, ..., 8h, 8w]).
     """
     base = np.asarray(weights["decoder.conv_in.weight"]).shape[0] // 4
-    ups = _up_blocks(base)
+    wan21 = is_wan21(weights)
+    ups = _up_blocks_wan21(base) if wan21 else _up_blocks(base)
     x = cached_conv(x, weights, "decoder.conv_in", cache)
     x = residual_block(x, weights, "decoder.mid_block.resnets.0", cache)
     x = attention(x, weights, "decoder.mid_block.attentions.0")
     x = residual_block(x, weights, "decoder.mid_block.resnets.1", cache)
     for i in range(len(ups)):
-        x = up_block(x, weights, i, cache, first, ups)
+        x = up_block(x, weights, i, cache, first, ups, wan21)
     x = silu(rms_norm(x, weights["decoder.norm_out.gamma"]))
     return cached_conv(x, weights, "decoder.conv_out", cache)
 
@@ -304,6 +340,8 @@ def unpatchify(out: np.ndarray, p: int = PATCH_SIZE) -> np.ndarray:
 def decode(z, weights, chunk: int = 1, return_preclamp: bool = False):
     """decode(z, weights): latents [B, 48, T, h, w] -> video [B, 3, 4T-3, 16h, 16w]
     in [-1, 1] (function ``decode``; section "What is computed", items 1-4).
+    Wan2.1 weights: latents [B, 16, T, h, w] -> video [B, 3, 4T-3, 8h, 8w],
+    no unpatchify.
 
     post_quant_conv over all T frames at once, then the decoder chunk by chunk
     (``chunk`` latent frames per call, 1 being the page's frame loop) with the
@@ -316,7 +354,8 @@ def decode(z, weights, chunk: int = 1, return_preclamp: bool = False):
     T = x.shape[2]
     cache: dict = {}
     outs = [decode_chunk(x[:, :, i:i + chunk], w, cache, first=(i == 0)) for i in range(0, T, chunk)]
-    video = unpatchify(np.concatenate(outs, axis=2))
+    out = np.concatenate(outs, axis=2)
+    video = out if is_wan21(w) else unpatchify(out)
     clamped = np.clip(video, -1.0, 1.0).astype(F32)
     return (clamped, video) if return_preclamp else clamped
 

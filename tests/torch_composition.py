@@ -7,7 +7,9 @@ two zero frames in front, the time conv over the frames after the first,
 DupUp3D doubling every frame but the first.  Built from torch library ops
 (conv3d/conv2d, normalize, silu, scaled_dot_product_attention, interpolate)
 so that a composition slip in the oracle (a misplaced norm, a wrong shortcut,
-a swapped resampler order) shows up as a disagreement.
+a swapped resampler order) shows up as a disagreement.  Wan2.1 weights
+(post_quant_conv 16 -> 16): resamplers under ``upsamplers.0`` that halve the
+channels, no DupUp3D shortcut, conv_out giving the 3 colours directly.
 """
 
 import math
@@ -59,9 +61,11 @@ def decode_whole_torch(z, weights):
     x = resnet(x, "decoder.mid_block.resnets.0")
     x = attn(x, "decoder.mid_block.attentions.0")
     x = resnet(x, "decoder.mid_block.resnets.1")
+    wan21 = w["post_quant_conv.weight"].shape[0] == 16
     specs = [(True, True), (True, True), (False, True), (False, False)]
     for i, (temporal, spatial) in enumerate(specs):
         name = f"decoder.up_blocks.{i}"
+        ups = f"{name}.upsamplers.0" if wan21 else f"{name}.upsampler"
         inp = x
         for j in range(3):
             x = resnet(x, f"{name}.resnets.{j}")
@@ -69,10 +73,12 @@ def decode_whole_torch(z, weights):
             continue
         if temporal:
             B, C, T, H, W = x.shape
-            y = cconv(x[:, :, 1:], f"{name}.upsampler.time_conv")       # [B, 2C, T-1, H, W]
+            y = cconv(x[:, :, 1:], f"{ups}.time_conv")                  # [B, 2C, T-1, H, W]
             y = y.reshape(B, 2, C, T - 1, H, W).permute(0, 2, 3, 1, 4, 5).reshape(B, C, 2 * (T - 1), H, W)
             x = torch.cat([x[:, :, :1], y], dim=2)
-        x = up2d(x, f"{name}.upsampler.resample.1")
+        x = up2d(x, f"{ups}.resample.1")
+        if wan21:
+            continue
         if temporal:   # r = 8: nearest x2 in t, h, w, the first frame kept once
             d = inp.repeat_interleave(2, 2).repeat_interleave(2, 3).repeat_interleave(2, 4)[:, :, 1:]
         else:          # r = 2: channel pair (2c, 2c+1) becomes row pair, each value in two columns
@@ -82,6 +88,8 @@ def decode_whole_torch(z, weights):
         x = x + d
     x = F.silu(norm(x, "decoder.norm_out"))
     out = cconv(x, "decoder.conv_out")                                   # [B, 12, F, h, w]
+    if wan21:
+        return out.numpy()
     B, _, Fr, H, W = out.shape
     # channel 4k + 2j + i -> colour k, row offset i, column offset j
     v = out.reshape(B, 3, 2, 2, Fr, H, W).permute(0, 1, 4, 5, 3, 6, 2).reshape(B, 3, Fr, 2 * H, 2 * W)
