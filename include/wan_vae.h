@@ -14,6 +14,16 @@
  *      (item 3);
  *   4. clamp to [-1, 1] (item 4).
  *
+ * The same entry points decode with the Wan2.1 VAE (AutoencoderKLWan of the
+ * Wan 2.1 and Wan 2.2 A14B pipelines; page "Fix the Wan VAE attention
+ * block": z_dim 16, 8x spatial compression, the same attention block) when
+ * given its weights: z [B, 16, T, H/8, W/8] -> video [B, 3, 4T-3, H, W], no
+ * unpatchify.  Its remaining dimensions are not on the pages and follow that
+ * model's published configuration (base dim 96; up blocks 4b -> 4b,
+ * 2b -> 4b, 2b -> 2b, b -> b; resamplers halving the channels, no DupUp3D;
+ * conv_out to 3 colours).  Below, "48" and "16h" read "16" and "8h" for it
+ * (wan_vae_model_z_dim, wan_vae_model_scale).
+ *
  * Conventions (all entry points):
  *  - Pointers named as device pointers are CUDA device memory owned by the
  *    caller; they must stay valid until the work enqueued on `stream`
@@ -82,13 +92,15 @@ const char* wan_vae_last_error(void);
 /* Name of a status code. */
 const char* wan_vae_status_string(int32_t status);
 
-/* Packs the 110 decoder + post_quant_conv tensors into a library-owned model
+/* Packs the 110 decoder + post_quant_conv tensors (Wan2.1: its decoder's
+ * tensors, resamplers named up_blocks.i.upsamplers.0.*) into a library-owned model
  * (conv weights K-major with per-tap channel blocks padded to 64; biases and
  * sqrt(C)*gamma held as fp32; in WAN_BF16 mode every tensor is first rounded
  * to bf16, as the page's bf16 contract rounds the weights).  The
- * architecture (decoder base dim b, channels 4b/4b/2b/b) is inferred from
- * decoder.conv_in.weight [4b, 48, 3, 3, 3]; every other shape is checked
- * against it.  `dtype` is the decode precision: WAN_BF16 computes with bf16
+ * architecture is inferred from post_quant_conv.weight ([48, 48, 1, 1, 1]:
+ * TI2V-5B; [16, 16, 1, 1, 1]: Wan2.1) and decoder.conv_in.weight
+ * [4b, z, 3, 3, 3] (decoder base dim b); every other shape is checked
+ * against them.  `dtype` is the decode precision: WAN_BF16 computes with bf16
  * operands and fp32 accumulation (the page's section "Precision", bf16
  * mode; every weight is rounded to bf16 first).  WAN_F32 keeps fp32 values
  * throughout: each weight and activation is held as a pair of bf16 halves
@@ -102,8 +114,13 @@ wan_status wan_vae_model_create(const wan_tensor* weights, int32_t n_weights, in
                                 wan_cuda_stream stream, wan_vae_model** model);
 /* Frees the model (synchronises with the device; no work may be pending). */
 void wan_vae_model_destroy(wan_vae_model* model);
-/* Decoder base dim b of a model (256 for TI2V-5B), or -1 for NULL. */
+/* Decoder base dim b of a model (256 for TI2V-5B, 96 for Wan2.1), or -1 for NULL. */
 int32_t wan_vae_model_base_dim(const wan_vae_model* model);
+/* Latent channels of a model: 48 (TI2V-5B) or 16 (Wan2.1); -1 for NULL. */
+int32_t wan_vae_model_z_dim(const wan_vae_model* model);
+/* Video pixels per latent along each spatial axis: 16 (TI2V-5B: 8x decoder
+ * upsampling, then the 2x2 unpatchify) or 8 (Wan2.1); -1 for NULL. */
+int32_t wan_vae_model_scale(const wan_vae_model* model);
 
 /* Latent de-normalisation in front of the decode (the diffusers Wan VAE's
  * per-channel `latents_mean` / `latents_std` configuration lists, page
@@ -113,11 +130,11 @@ int32_t wan_vae_model_base_dim(const wan_vae_model* model);
  * streams and tiled decodes included) first maps each latent to
  * z * std[c] + mean[c] in fp32, inside the post_quant_conv kernel, and then
  * applies the decode's own input rounding (bf16 models round the result).
- * mean, std_dev: HOST arrays of n = 48 finite fp32 values, copied before
+ * mean, std_dev: HOST arrays of n = z_dim (48 or 16) finite fp32 values, copied before
  * return (synchronous copy); both NULL switches it off again.  Call it between
  * decodes, never while a decode that uses the model is in flight.
  * Errors: WAN_ERR_INVALID_ARG (null model, one of the two NULL, a value not
- * finite), WAN_ERR_SHAPE (n != 48), WAN_ERR_OOM, WAN_ERR_CUDA. */
+ * finite), WAN_ERR_SHAPE (n != z_dim), WAN_ERR_OOM, WAN_ERR_CUDA. */
 wan_status wan_vae_model_set_latent_stats(wan_vae_model* model, const float* mean, const float* std_dev, int32_t n);
 
 /* A decode stream: the causal caches (two frames per 3-frame conv, page

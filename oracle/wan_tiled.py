@@ -12,8 +12,9 @@ consistent with "tiles overlap by tile - stride and are blended":
 
 * Tile origins.  Along each spatial axis of N pixels, tiles start at 0,
   stride, 2*stride, ... (every start < N) and cover min(tile, N - start)
-  pixels.  In latents (16 pixels per latent) that is tile/16 latents at a
-  stride of stride/16 latents; both sizes must be multiples of 16.
+  pixels.  In latents (P = 16 video pixels per latent; P = 8 for the Wan2.1
+  decoder) that is tile/P latents at a stride of stride/P latents; both
+  sizes must be multiples of 16 pixels.
 * Each tile is decoded on its own by ``decode`` (all frames, its own causal
   caches, unpatchify and clamp included), as if it were the whole latent.
 * Blending, in raster order over the tiles, in place: tile (i, j) first
@@ -36,9 +37,11 @@ from __future__ import annotations
 
 import numpy as np
 
-from .wan_decode import decode
+from .wan_decode import decode, is_wan21
 
-PIXELS_PER_LATENT = 16  # 8x spatial upsampling in the decoder, then the 2x2 unpatchify
+# 8x spatial upsampling in the decoder, then the 2x2 unpatchify (TI2V-5B; the
+# Wan2.1 decoder has no unpatchify: 8).  Tile sizes are multiples of 16 for both.
+PIXELS_PER_LATENT = 16
 
 
 def tile_origins(n: int, tile: int, stride: int) -> list[tuple[int, int]]:
@@ -76,7 +79,8 @@ def blend_tiles(tiles, H: int, W: int, stride_h: int, stride_w: int) -> np.ndarr
 
 
 def decode_tiled(z, weights, tile=(256, 256), stride=(192, 192), chunk: int = 1) -> np.ndarray:
-    """Tiled decode of z [B, 48, T, h, w] -> video [B, 3, 4T-3, 16h, 16w].
+    """Tiled decode of z [B, 48, T, h, w] -> video [B, 3, 4T-3, 16h, 16w]
+    (Wan2.1: z [B, 16, T, h, w] -> [B, 3, 4T-3, 8h, 8w]).
 
     ``tile`` and ``stride`` are (height, width) in video pixels, multiples of
     16.  Each latent tile goes through ``decode`` (frame loop of ``chunk``
@@ -84,10 +88,11 @@ def decode_tiled(z, weights, tile=(256, 256), stride=(192, 192), chunk: int = 1)
     """
     z = np.asarray(z, np.float32)
     _, _, _, h, w = z.shape
-    P = PIXELS_PER_LATENT
     for v in (*tile, *stride):
-        if v <= 0 or v % P:
-            raise ValueError(f"tile and stride must be positive multiples of {P} pixels, got {tile}, {stride}")
+        if v <= 0 or v % PIXELS_PER_LATENT:
+            raise ValueError(f"tile and stride must be positive multiples of {PIXELS_PER_LATENT} pixels, "
+                             f"got {tile}, {stride}")
+    P = 8 if is_wan21(weights) else PIXELS_PER_LATENT  # video pixels per latent
     rows = tile_origins(h, tile[0] // P, stride[0] // P)
     cols = tile_origins(w, tile[1] // P, stride[1] // P)
     tiles = [[decode(z[..., r0:r0 + rh, c0:c0 + cw], weights, chunk=chunk) for c0, cw in cols] for r0, rh in rows]

@@ -82,10 +82,20 @@ class Model:
     def base_dim(self) -> int:
         return int(load().wan_vae_model_base_dim(self._h))
 
+    @property
+    def z_dim(self) -> int:
+        """Latent channels: 48 (TI2V-5B) or 16 (Wan2.1)."""
+        return int(load().wan_vae_model_z_dim(self._h))
+
+    @property
+    def scale(self) -> int:
+        """Video pixels per latent along h and w: 16 (TI2V-5B) or 8 (Wan2.1)."""
+        return int(load().wan_vae_model_scale(self._h))
+
     def set_latent_stats(self, mean=None, std=None):
         """Latent de-normalisation (wan_vae_model_set_latent_stats): later decodes
         through this model map z to z * std + mean per latent channel first.
-        mean, std: 48 values each (sequence, array or tensor); both None: off."""
+        mean, std: z_dim values each (sequence, array or tensor); both None: off."""
         if mean is None and std is None:
             check(load().wan_vae_model_set_latent_stats(self._h, None, None, 0))
             return
@@ -97,12 +107,13 @@ class Model:
 
     def decode_tiled(self, z: torch.Tensor, tile=(256, 256), stride=(192, 192), out_dtype: torch.dtype = None,
                      tile_batch: int = 0, max_chunk: int = 4, stream=None) -> torch.Tensor:
-        """Tiled decode (wan_vae_decode_tiled): z [B, 48, T, h, w] on the GPU ->
-        video [B, 3, 4T-3, 16h, 16w]; tile and stride are (height, width) in
-        video pixels, multiples of 16."""
+        """Tiled decode (wan_vae_decode_tiled): z [B, z_dim, T, h, w] on the GPU ->
+        video [B, 3, 4T-3, scale*h, scale*w]; tile and stride are (height,
+        width) in video pixels, multiples of `scale`."""
         B, _, T, h, w = z.shape
         dt = self.dtype if out_dtype is None else out_dtype
-        out = torch.empty((B, 3, 4 * T - 3, 16 * h, 16 * w), device=z.device, dtype=dt)
+        k = self.scale
+        out = torch.empty((B, 3, 4 * T - 3, k * h, k * w), device=z.device, dtype=dt)
         check(load().wan_vae_decode_tiled(self._h, _dev(z, "z"), _code(z.dtype), B, T, h, w, tile[0], tile[1],
                                           stride[0], stride[1], tile_batch, max_chunk, _dev(out, "out"), _code(dt),
                                           _stream(stream)))
@@ -179,7 +190,8 @@ class DecodeStream:
     def decode_clip(self, z, out=None, out_dtype=None, preclamp=None, stream=None):
         B, _, T, h, w = z.shape
         if out is None:
-            out = torch.empty((B, 3, 4 * T - 3, 16 * h, 16 * w), device=z.device,
+            k = self.model.scale
+            out = torch.empty((B, 3, 4 * T - 3, k * h, k * w), device=z.device,
                               dtype=out_dtype or self.model.dtype)
         p = 0 if preclamp is None else _dev(preclamp, "preclamp")
         check(load().wan_vae_decode_clip(self._s, _dev(z, "z"), _code(z.dtype), T, _dev(out, "out"), _code(out.dtype),
@@ -208,10 +220,12 @@ class DecodeStream:
 
 
 def decode(z: torch.Tensor, weights: "dict[str, torch.Tensor]", dtype: torch.dtype = torch.float32, stream=None):
-    """One-shot decode(z, weights, dtype) -> video [B, 3, 4T-3, 16h, 16w] of `dtype`."""
+    """One-shot decode(z, weights, dtype) -> video [B, 3, 4T-3, 16h, 16w] of `dtype`
+    (Wan2.1 weights, z [B, 16, T, h, w]: [B, 3, 4T-3, 8h, 8w])."""
     code = _code(dtype)
-    B, _, T, h, w = z.shape
-    out = torch.empty((B, 3, 4 * T - 3, 16 * h, 16 * w), device=z.device, dtype=dtype)
+    B, C, T, h, w = z.shape
+    k = 8 if C == 16 else 16
+    out = torch.empty((B, 3, 4 * T - 3, k * h, k * w), device=z.device, dtype=dtype)
     arr, keep = weight_table(weights)
     check(load().wan_vae_decode(_dev(z, "z"), _code(z.dtype), B, T, h, w, arr, len(keep) // 2, _dev(out, "out"), code,
                                 _stream(stream)))

@@ -52,6 +52,8 @@ SIGNATURES = {
     "wan_vae_model_create": (_i32, [ctypes.POINTER(WanTensor), _i32, _i32, _vp, ctypes.POINTER(_vp)]),
     "wan_vae_model_destroy": (None, [_vp]),
     "wan_vae_model_base_dim": (_i32, [_vp]),
+    "wan_vae_model_z_dim": (_i32, [_vp]),
+    "wan_vae_model_scale": (_i32, [_vp]),
     "wan_vae_model_set_latent_stats": (_i32, [_vp, _vp, _vp, _i32]),
     "wan_vae_stream_create": (_i32, [_vp, _i32, _i32, _i32, _i32, ctypes.POINTER(_vp)]),
     "wan_vae_stream_reset": (_i32, [_vp, _vp]),

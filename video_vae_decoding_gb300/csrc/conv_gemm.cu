@@ -258,6 +258,19 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
     if (args.bias) add_bias16(args.bias + n0, v);
     if (!valid) continue;       // lanes re-converge at the __syncwarp above
     if constexpr (EPI == kEpiVideo) {
+      if (args.vid_patch == 1) {  // three colour channels, no unpatchify
+        const long long off = (long long)b * args.vid_bs + (long long)(args.out_f0 + f) * args.H * args.W + pos;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          if (args.preclamp) args.preclamp[off + k * args.vid_cs] = v[k];
+          const float c = fminf(fmaxf(v[k], -1.f), 1.f);
+          if (args.out_f32)
+            static_cast<float*>(args.out)[off + k * args.vid_cs] = c;
+          else
+            static_cast<__nv_bfloat16*>(args.out)[off + k * args.vid_cs] = __float2bfloat16_rn(c);
+        }
+        continue;
+      }
       const long long base = (long long)b * args.vid_bs + (long long)(args.out_f0 + f) * (4LL * args.H * args.W);
 #pragma unroll
       for (int k = 0; k < 3; ++k) {

@@ -118,10 +118,10 @@ __global__ void copy_frames_kernel(FrameView in, FrameView out, int C8, int F, i
   *reinterpret_cast<uint4*>(at_mut(out, b, f, p) + c) = *reinterpret_cast<const uint4*>(at(in, b, f, p) + c);
 }
 
-// post_quant_conv (1x1x1, 48 -> 48) on NCDHW latents; one thread per position.
-// With zstat (mean[48] then std[48]) each latent is first de-normalised,
-// z * std[c] + mean[c], in fp32.
-constexpr int kZ = 48;
+// post_quant_conv (1x1x1, kZ -> kZ; kZ = 48 for TI2V-5B, 16 for Wan2.1) on
+// NCDHW latents; one thread per position.  With zstat (mean[kZ] then
+// std[kZ]) each latent is first de-normalised, z * std[c] + mean[c], in fp32.
+template <int kZ>
 __global__ void post_quant_kernel(const void* __restrict__ z, int z_f32, int Tz, int t0, int F, int P,
                                   const float* __restrict__ w, const float* __restrict__ bias,
                                   const float* __restrict__ zstat, FrameView out, long long n, int round_z,
@@ -353,14 +353,18 @@ cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F,
   return cudaGetLastError();
 }
 
-cudaError_t launch_post_quant(const void* z, int z_f32, int B, int Tz, int t0, int F, int P, const float* w,
+cudaError_t launch_post_quant(const void* z, int z_f32, int Z, int B, int Tz, int t0, int F, int P, const float* w,
                               const float* bias, const float* zstat, FrameView out, int round_z_bf16, cudaStream_t s,
                               int out_lo) {
-  if (out.ldc % 8 || out.ldc < kZ) return cudaErrorInvalidValue;
+  if (out.ldc % 8 || out.ldc < Z || (Z != 48 && Z != 16)) return cudaErrorInvalidValue;
   const long long n = (long long)B * F * P;
   if (n == 0) return cudaSuccess;
-  post_quant_kernel<<<blocks_for(n, 128), 128, 0, s>>>(z, z_f32, Tz, t0, F, P, w, bias, zstat, out, n, round_z_bf16,
-                                                       out_lo);
+  if (Z == 48)
+    post_quant_kernel<48><<<blocks_for(n, 128), 128, 0, s>>>(z, z_f32, Tz, t0, F, P, w, bias, zstat, out, n,
+                                                             round_z_bf16, out_lo);
+  else
+    post_quant_kernel<16><<<blocks_for(n, 128), 128, 0, s>>>(z, z_f32, Tz, t0, F, P, w, bias, zstat, out, n,
+                                                             round_z_bf16, out_lo);
   return cudaGetLastError();
 }
 

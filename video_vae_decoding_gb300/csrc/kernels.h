@@ -82,10 +82,12 @@ struct ConvArgs {
   int dup_first;         // first chunk: the first ft-1 copies of frame 0 are dropped
   int dup_pairs;         // 1: channel c reads source 2c + (row & 1) (r = 2); 0: channel c (r = 4ft)
   // kEpiVideo: out = video [B][3][F][2H][2W]; channel 4k + 2j + i -> colour k,
-  // row 2y + i, column 2x + j; clamped to [-1, 1]; preclamp is the fp32 copy
-  // before the clamp (optional).
+  // row 2y + i, column 2x + j (vid_patch 2); or video [B][3][F][H][W] from
+  // channels 0..2 (vid_patch 1); clamped to [-1, 1]; preclamp is the fp32
+  // copy before the clamp (optional).
   float* preclamp;
   long long vid_bs, vid_cs;
+  int vid_patch;
   // Fused RMS norm (requires one N tile holding all N channels): y = acc +
   // bias (+ residual) is also written normalised over its N channels,
   // y / max(||y||, 1e-12) * norm_gs (then SiLU if norm_silu), to out2 at
@@ -133,11 +135,12 @@ cudaError_t launch_rms_norm(FrameView in, FrameView out, const float* gs, int C,
                             cudaStream_t s, int in_lo = 0, int out_lo = 0);
 // copy F frames of C channels
 cudaError_t launch_copy_frames(FrameView in, FrameView out, int C, int B, int F, int P, cudaStream_t s);
-// post_quant_conv: z [B][48][Tz][h][w] (fp32 or bf16, NCDHW), frames t0..t0+F-1
-// -> out(b, f, p, 0..47) bf16; channels 48..ldc-1 are written as zero.
-// zstat: NULL, or mean[48] then std[48] (fp32): the latents are first
+// post_quant_conv: z [B][Z][Tz][h][w] (fp32 or bf16, NCDHW), frames t0..t0+F-1
+// -> out(b, f, p, 0..Z-1) bf16; channels Z..ldc-1 are left as they are (zero).
+// zstat: NULL, or mean[Z] then std[Z] (fp32): the latents are first
 // de-normalised to z * std + mean (before the bf16 rounding of round_z_bf16).
-cudaError_t launch_post_quant(const void* z, int z_f32, int B, int Tz, int t0, int F, int P, const float* w /*48x48*/,
+cudaError_t launch_post_quant(const void* z, int z_f32, int Z /*48 or 16*/, int B, int Tz, int t0, int F, int P,
+                              const float* w /*Z x Z*/,
                               const float* bias, const float* zstat, FrameView out, int round_z_bf16, cudaStream_t s,
                               int out_lo = 0);
 // Row softmax of S [R][ld_s] fp32 (n valid columns) scaled by `scale`, into
@@ -183,7 +186,7 @@ cudaError_t launch_to_f32(const void* src, int src_f32, const void* src2, int sr
 // ---------------------------------------------------------------------------
 struct TileDesc {
   long long off;  // element offset of the tile in the buffer (a multiple of 4)
-  int h, w;       // pixels (multiples of 16)
+  int h, w;       // pixels (multiples of 8)
 };
 constexpr int kMaxTiles = 1024;
 struct TileTable {

@@ -323,16 +323,16 @@ static wan_status pack_gamma(const WeightTable& wt, const std::string& name, int
 // taps that read the same source pixel (page "The parts", fifth bullet: the
 // upsampling only copies values, so the conv of the copies is the conv of
 // the source with the taps merged).  K per phase = 4 taps * ci_pad (x2 split).
-static wan_status pack_subpix_conv(const WeightTable& wt, const std::string& name, int C, ConvW& cw, DevMem& mem,
-                                   cudaStream_t s, bool split) {
+static wan_status pack_subpix_conv(const WeightTable& wt, const std::string& name, int C, int Co, ConvW& cw,
+                                   DevMem& mem, cudaStream_t s, bool split) {
   const wan_tensor *W, *Bi;
   WAN_TRY(get_tensor(wt, name + ".weight", &W));
   WAN_TRY(get_tensor(wt, name + ".bias", &Bi));
-  WAN_TRY(check_shape(W, {C, C, 3, 3}));
-  WAN_TRY(check_shape(Bi, {C}));
+  WAN_TRY(check_shape(W, {Co, C, 3, 3}));
+  WAN_TRY(check_shape(Bi, {Co}));
   if (mem.dry) return WAN_OK;
   const int sp = split ? 2 : 1;
-  cw.Co = C;
+  cw.Co = Co;
   cw.Ci = C;
   cw.kt = 1;
   cw.kh = 2;
@@ -341,20 +341,20 @@ static wan_status pack_subpix_conv(const WeightTable& wt, const std::string& nam
   cw.split = split ? 1 : 0;
   cw.ci_pad = (int)rup(C, 64);
   cw.ktot = sp * 4 * cw.ci_pad;
-  cw.bn = choose_bn(C);
-  cw.co_pad = (int)rup(C, cw.bn);
+  cw.bn = choose_bn(Co);
+  cw.co_pad = (int)rup(Co, cw.bn);
   void* p;
   const size_t bytes = (size_t)4 * cw.co_pad * cw.ktot * sizeof(bf16);
   WAN_TRY(mem.alloc(&p, bytes));
   cw.w = (bf16*)p;
   CUDA_TRY(cudaMemsetAsync(cw.w, 0, bytes, s));
   for (int part = 0; part < sp; ++part)
-    CUDA_TRY(launch_pack_subpixel(W->data, W->dtype == WAN_F32, C, C, cw.w, cw.ktot, cw.co_pad, part * cw.ci_pad,
+    CUDA_TRY(launch_pack_subpixel(W->data, W->dtype == WAN_F32, Co, C, cw.w, cw.ktot, cw.co_pad, part * cw.ci_pad,
                                   sp * cw.ci_pad, split ? 0 : 1, part, s));
   WAN_TRY(mem.alloc(&p, (size_t)cw.co_pad * sizeof(float)));  // zero-padded to the N tile
   cw.bias = (float*)p;
   CUDA_TRY(cudaMemsetAsync(cw.bias, 0, (size_t)cw.co_pad * sizeof(float), s));
-  CUDA_TRY(launch_to_f32(Bi->data, Bi->dtype == WAN_F32, nullptr, 0, cw.bias, C, 1.0f, split ? 0 : 1, s));
+  CUDA_TRY(launch_to_f32(Bi->data, Bi->dtype == WAN_F32, nullptr, 0, cw.bias, Co, 1.0f, split ? 0 : 1, s));
   return WAN_OK;
 }
 
@@ -371,6 +371,11 @@ struct Resnet {
 
 struct wan_vae_model {
   int base = 0, dtype = WAN_BF16;
+  // decoder variant: TI2V-5B (z 48, 2x2 patch, DupUp3D shortcuts, resamplers
+  // keep channels) or Wan2.1 (z 16, no patch, no DupUp3D, resamplers halve)
+  int zdim = 48, patch = 2;
+  bool wan21 = false;
+  int up[4][5] = {};  // per up block: cin, cout, temporal, spatial, resampler out (channels)
   bool split = false;  // fp32 decode: activations and weights as bf16 hi/lo pairs
   float* pq_w = nullptr;
   float* pq_b = nullptr;
@@ -378,7 +383,7 @@ struct wan_vae_model {
   Resnet mid[2];
   float* attn_g = nullptr;
   ConvW qkv, proj;
-  Resnet up[4][3];
+  Resnet ups[4][3];
   ConvW tconv[2];
   ConvW resample[3];
   float* out_g = nullptr;
@@ -389,10 +394,14 @@ struct wan_vae_model {
   DevMem mem;
 };
 
-// (in, out, temporal, spatial) of the up blocks in units of the base dim
-// (page "What is computed": channels 4b, 4b, 4b -> 2b, 2b -> b).
-static const int kUp[4][4] = {{4, 4, 1, 1}, {4, 4, 1, 1}, {4, 2, 0, 1}, {2, 1, 0, 0}};
-static const int kZdim = 48;
+// (in, out, temporal, spatial, resampler out) of the up blocks in units of the
+// base dim.  TI2V-5B (page "What is computed": channels 4b, 4b, 4b -> 2b,
+// 2b -> b; the resampler keeps the channels and DupUp3D adds the block
+// input); Wan2.1 (that model's published configuration: the resampler
+// halves the channels, the next block starts from half).
+static const int kUp[4][5] = {{4, 4, 1, 1, 4}, {4, 4, 1, 1, 4}, {4, 2, 0, 1, 2}, {2, 1, 0, 0, 0}};
+static const int kUpWan21[4][5] = {{4, 4, 1, 1, 2}, {2, 4, 1, 1, 2}, {2, 2, 0, 1, 1}, {1, 1, 0, 0, 0}};
+static const int kZdimMax = 48;
 
 static wan_status pack_resnet(const WeightTable& wt, const std::string& name, int ci, int co, Resnet& r, DevMem& mem,
                               cudaStream_t s, bool split) {
@@ -410,10 +419,17 @@ static wan_status model_build(const wan_tensor* weights, int n, int dtype, cudaS
   if (!weights || n <= 0) return fail(WAN_ERR_INVALID_ARG, "empty weight table");
   if (dtype != WAN_F32 && dtype != WAN_BF16) return fail(WAN_ERR_DTYPE, "dtype must be WAN_F32 or WAN_BF16, not %d", dtype);
   WeightTable wt{weights, n};
-  const wan_tensor* ci;
+  const wan_tensor *ci, *pq;
+  WAN_TRY(get_tensor(wt, "post_quant_conv.weight", &pq));
+  if (pq->ndim < 1 || (pq->shape[0] != 48 && pq->shape[0] != 16))
+    return fail(WAN_ERR_SHAPE, "post_quant_conv.weight must be [48, 48, 1, 1, 1] (TI2V-5B) or [16, 16, 1, 1, 1] (Wan2.1)");
+  const int zd = (int)pq->shape[0];
+  m->zdim = zd;
+  m->wan21 = zd == 16;
+  m->patch = m->wan21 ? 1 : 2;
   WAN_TRY(get_tensor(wt, "decoder.conv_in.weight", &ci));
   if (ci->ndim != 5 || ci->shape[0] % 4 || ci->shape[0] <= 0)
-    return fail(WAN_ERR_SHAPE, "decoder.conv_in.weight must be [4b, 48, 3, 3, 3]");
+    return fail(WAN_ERR_SHAPE, "decoder.conv_in.weight must be [4b, %d, 3, 3, 3]", zd);
   const int b = (int)(ci->shape[0] / 4);
   if (b % 8 || 4 * b > 1024)
     return fail(WAN_ERR_UNSUPPORTED, "decoder base dim %d: must be a multiple of 8 and at most 256", b);
@@ -427,38 +443,41 @@ static wan_status model_build(const wan_tensor* weights, int n, int dtype, cudaS
     const wan_tensor *w, *bb;
     WAN_TRY(get_tensor(wt, "post_quant_conv.weight", &w));
     WAN_TRY(get_tensor(wt, "post_quant_conv.bias", &bb));
-    WAN_TRY(check_shape(w, {kZdim, kZdim, 1, 1, 1}));
-    WAN_TRY(check_shape(bb, {kZdim}));
+    WAN_TRY(check_shape(w, {zd, zd, 1, 1, 1}));
+    WAN_TRY(check_shape(bb, {zd}));
     if (!mem.dry) {
     void* p;
-    WAN_TRY(mem.alloc(&p, kZdim * kZdim * sizeof(float)));
+    WAN_TRY(mem.alloc(&p, zd * zd * sizeof(float)));
     m->pq_w = (float*)p;
-    WAN_TRY(mem.alloc(&p, kZdim * sizeof(float)));
+    WAN_TRY(mem.alloc(&p, zd * sizeof(float)));
     m->pq_b = (float*)p;
-    CUDA_TRY(launch_to_f32(w->data, w->dtype == WAN_F32, nullptr, 0, m->pq_w, kZdim * kZdim, 1.0f, sp ? 0 : 1, s));
-    CUDA_TRY(launch_to_f32(bb->data, bb->dtype == WAN_F32, nullptr, 0, m->pq_b, kZdim, 1.0f, sp ? 0 : 1, s));
+    CUDA_TRY(launch_to_f32(w->data, w->dtype == WAN_F32, nullptr, 0, m->pq_w, zd * zd, 1.0f, sp ? 0 : 1, s));
+    CUDA_TRY(launch_to_f32(bb->data, bb->dtype == WAN_F32, nullptr, 0, m->pq_b, zd, 1.0f, sp ? 0 : 1, s));
     }
   }
   const int c4 = 4 * b;
-  WAN_TRY(pack_conv(wt, "decoder.conv_in", c4, kZdim, 3, 3, 3, false, "", 0, m->conv_in, mem, s, sp));
+  WAN_TRY(pack_conv(wt, "decoder.conv_in", c4, zd, 3, 3, 3, false, "", 0, m->conv_in, mem, s, sp));
   WAN_TRY(pack_resnet(wt, "decoder.mid_block.resnets.0", c4, c4, m->mid[0], mem, s, sp));
   WAN_TRY(pack_resnet(wt, "decoder.mid_block.resnets.1", c4, c4, m->mid[1], mem, s, sp));
   WAN_TRY(pack_gamma(wt, "decoder.mid_block.attentions.0.norm.gamma", c4, &m->attn_g, mem, s, sp));
   WAN_TRY(pack_conv(wt, "decoder.mid_block.attentions.0.to_qkv", 3 * c4, c4, 1, 1, 1, true, "", 0, m->qkv, mem, s, sp));
   WAN_TRY(pack_conv(wt, "decoder.mid_block.attentions.0.proj", c4, c4, 1, 1, 1, true, "", 0, m->proj, mem, s, sp));
   for (int i = 0; i < 4; ++i) {
-    const int cin = kUp[i][0] * b, cout = kUp[i][1] * b;
+    const int* u = m->wan21 ? kUpWan21[i] : kUp[i];
+    for (int k = 0; k < 5; ++k) m->up[i][k] = (k == 2 || k == 3) ? u[k] : u[k] * b;
+    const int cin = m->up[i][0], cout = m->up[i][1];
     const std::string nm = "decoder.up_blocks." + std::to_string(i);
+    const std::string ups = nm + (m->wan21 ? ".upsamplers.0" : ".upsampler");
     for (int j = 0; j < 3; ++j)
-      WAN_TRY(pack_resnet(wt, nm + ".resnets." + std::to_string(j), j == 0 ? cin : cout, cout, m->up[i][j], mem, s,
+      WAN_TRY(pack_resnet(wt, nm + ".resnets." + std::to_string(j), j == 0 ? cin : cout, cout, m->ups[i][j], mem, s,
                           sp));
-    if (kUp[i][2])
-      WAN_TRY(pack_conv(wt, nm + ".upsampler.time_conv", 2 * cout, cout, 3, 1, 1, false, "", 0, m->tconv[i], mem, s,
-                        sp));
-    if (kUp[i][3]) WAN_TRY(pack_subpix_conv(wt, nm + ".upsampler.resample.1", cout, m->resample[i], mem, s, sp));
+    if (u[2])
+      WAN_TRY(pack_conv(wt, ups + ".time_conv", 2 * cout, cout, 3, 1, 1, false, "", 0, m->tconv[i], mem, s, sp));
+    if (u[3]) WAN_TRY(pack_subpix_conv(wt, ups + ".resample.1", cout, m->up[i][4], m->resample[i], mem, s, sp));
   }
   WAN_TRY(pack_gamma(wt, "decoder.norm_out.gamma", b, &m->out_g, mem, s, sp));
-  WAN_TRY(pack_conv(wt, "decoder.conv_out", 12, b, 3, 3, 3, false, "", 0, m->conv_out, mem, s, sp));
+  WAN_TRY(pack_conv(wt, "decoder.conv_out", 3 * m->patch * m->patch, b, 3, 3, 3, false, "", 0, m->conv_out, mem, s,
+                    sp));
   if (!mem.dry) CUDA_TRY(cudaGetLastError());
   return WAN_OK;
 }
@@ -561,7 +580,7 @@ static wan_status make_raw(wan_vae_stream* st, size_t bytes, void** p) {
 }
 
 static wan_status plan_buffers(wan_vae_stream* st) {
-  const int b = st->m->base, c4 = 4 * b, c2 = 2 * b, c1 = b, n = st->nmax;
+  const int b = st->m->base, c4 = 4 * b, n = st->nmax;
   const int hA = st->h, wA = st->w;
   st->rings.clear();
   auto ring = [&](Act& a, int F, int H, int W, int C) -> wan_status {
@@ -569,8 +588,9 @@ static wan_status plan_buffers(wan_vae_stream* st) {
     st->rings.push_back(&a);
     return WAN_OK;
   };
+  const wan_vae_model* m = st->m;
   // level A
-  WAN_TRY(ring(st->ringIn, n, hA, wA, kZdim));
+  WAN_TRY(ring(st->ringIn, n, hA, wA, m->zdim));
   for (auto& a : st->RA) WAN_TRY(make_act(st, a, n, hA, wA, c4));
   WAN_TRY(make_act(st, st->HA, n, hA, wA, c4));
   for (auto& a : st->ringA) WAN_TRY(ring(a, n, hA, wA, c4));
@@ -597,28 +617,36 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   at.Vt = (bf16*)p;
   // level B
   const int hB = 2 * hA, wB = 2 * wA;
-  for (auto& a : st->RB) WAN_TRY(make_act(st, a, 2 * n, hB, wB, c4));
-  WAN_TRY(make_act(st, st->HB, 2 * n, hB, wB, c4));
-  for (auto& a : st->ringB) WAN_TRY(ring(a, 2 * n, hB, wB, c4));
-  WAN_TRY(ring(st->tcB, 2 * n, hB, wB, c4));
-  WAN_TRY(make_act(st, st->tuB, 4 * n, hB, wB, c4));
+  // levels B, C, D: R[0] holds the up block's input (the previous block's
+  // resampler output, cin channels), R[1], R[2] and H its resnets' outputs
+  // (cout); ring 0 feeds the first conv1 (cin), rings 1-5 the others (cout)
+  const int ciB = m->up[1][0], coB = m->up[1][1];
+  WAN_TRY(make_act(st, st->RB[0], 2 * n, hB, wB, ciB));
+  for (int i = 1; i < 3; ++i) WAN_TRY(make_act(st, st->RB[i], 2 * n, hB, wB, coB));
+  WAN_TRY(make_act(st, st->HB, 2 * n, hB, wB, coB));
+  WAN_TRY(ring(st->ringB[0], 2 * n, hB, wB, ciB));
+  for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringB[i], 2 * n, hB, wB, coB));
+  WAN_TRY(ring(st->tcB, 2 * n, hB, wB, coB));
+  WAN_TRY(make_act(st, st->tuB, 4 * n, hB, wB, coB));
   // level C
   const int hC = 4 * hA, wC = 4 * wA;
-  WAN_TRY(make_act(st, st->RC[0], 4 * n, hC, wC, c4));
-  WAN_TRY(make_act(st, st->RC[1], 4 * n, hC, wC, c2));
-  WAN_TRY(make_act(st, st->RC[2], 4 * n, hC, wC, c2));
-  WAN_TRY(make_act(st, st->HC, 4 * n, hC, wC, c2));
-  WAN_TRY(ring(st->ringC[0], 4 * n, hC, wC, c4));
-  for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringC[i], 4 * n, hC, wC, c2));
+  const int ciC = m->up[2][0], coC = m->up[2][1];
+  WAN_TRY(make_act(st, st->RC[0], 4 * n, hC, wC, ciC));
+  WAN_TRY(make_act(st, st->RC[1], 4 * n, hC, wC, coC));
+  WAN_TRY(make_act(st, st->RC[2], 4 * n, hC, wC, coC));
+  WAN_TRY(make_act(st, st->HC, 4 * n, hC, wC, coC));
+  WAN_TRY(ring(st->ringC[0], 4 * n, hC, wC, ciC));
+  for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringC[i], 4 * n, hC, wC, coC));
   // level D
   const int hD = 8 * hA, wD = 8 * wA;
-  WAN_TRY(make_act(st, st->RD[0], 4 * n, hD, wD, c2));
-  WAN_TRY(make_act(st, st->RD[1], 4 * n, hD, wD, c1));
-  WAN_TRY(make_act(st, st->RD[2], 4 * n, hD, wD, c1));
-  WAN_TRY(make_act(st, st->HD, 4 * n, hD, wD, c1));
-  WAN_TRY(ring(st->ringD[0], 4 * n, hD, wD, c2));
-  for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringD[i], 4 * n, hD, wD, c1));
-  WAN_TRY(ring(st->ringOut, 4 * n, hD, wD, c1));
+  const int ciD = m->up[3][0], coD = m->up[3][1];
+  WAN_TRY(make_act(st, st->RD[0], 4 * n, hD, wD, ciD));
+  WAN_TRY(make_act(st, st->RD[1], 4 * n, hD, wD, coD));
+  WAN_TRY(make_act(st, st->RD[2], 4 * n, hD, wD, coD));
+  WAN_TRY(make_act(st, st->HD, 4 * n, hD, wD, coD));
+  WAN_TRY(ring(st->ringD[0], 4 * n, hD, wD, ciD));
+  for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringD[i], 4 * n, hD, wD, coD));
+  WAN_TRY(ring(st->ringOut, 4 * n, hD, wD, coD));
   return WAN_OK;
 }
 
@@ -954,13 +982,17 @@ static wan_status time_upsample(wan_vae_stream* st, const ConvW& tc, const Act& 
 
 // upsample2d (nearest x2, 3x3 conv) of the low-resolution `x` (F frames),
 // in the sub-pixel form, plus DupUp3D of the up block's input `blk` (page
-// "The parts", fifth and sixth bullets); y is at twice x's resolution.
+// "The parts", fifth and sixth bullets); y is at twice x's resolution.  The
+// Wan2.1 decoder has no DupUp3D: the conv's result is stored as it is.
 static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, const Act& blk, int ft, bool first,
                            Act& y, int F, cudaStream_t s) {
   ConvLaunch L;
   if (!cw.subpix || y.H != 2 * x.H || y.W != 2 * x.W) return fail(WAN_ERR_INTERNAL, "resample shapes");
   WAN_TRY(conv_setup(cw, x, 0, nullptr, 0, F, L));
   set_out(L.args, out_of(y));
+  // nominal FLOPs: the 3x3 conv at the upsampled resolution (4/9 of it is executed)
+  const double nominal = 2.0 * x.B * F * 4.0 * x.H * x.W * cw.Co * 9.0 * cw.Ci;
+  if (st->m->wan21) return run(L, &st->prof, kKindResample, nominal, st->err_dev, s);
   L.epi = kEpiDup;
   L.args.dup = blk.p;
   L.args.dup_bs = blk.bs();
@@ -979,8 +1011,6 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
     L.args.dup_pairs = 1;
   else
     return fail(WAN_ERR_UNSUPPORTED, "DupUp3D with %d -> %d channels, ft %d", blk.C, cw.Co, ft);
-  // nominal FLOPs: the 3x3 conv at the upsampled resolution (4/9 of it is executed)
-  const double nominal = 2.0 * x.B * F * 4.0 * x.H * x.W * cw.Co * 9.0 * cw.Ci;
   return run(L, &st->prof, kKindResample, nominal, st->err_dev, s);
 }
 
@@ -1018,30 +1048,31 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   const int P = st->h * st->w;
   st->shifts.clear();
   // 1. post_quant_conv into conv_in's ring
-  ELT(&st->prof, kKindMisc, (double)st->B * FA * P * (kZdim * (z_f32 ? 4 : 2) + 2 * st->ringIn.ldc), launch_post_quant(z, z_f32, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b, m->zstat_on ? m->zstat : nullptr, st->ringIn.view(2),
-                                   m->split ? 0 : 1, s, st->ringIn.lo));
+  ELT(&st->prof, kKindMisc, (double)st->B * FA * P * (m->zdim * (z_f32 ? 4 : 2) + 2 * st->ringIn.ldc),
+      launch_post_quant(z, z_f32, m->zdim, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b,
+                        m->zstat_on ? m->zstat : nullptr, st->ringIn.view(2), m->split ? 0 : 1, s, st->ringIn.lo));
   // 2. conv_in, mid block
   WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s));
   WAN_TRY(resnet(st, m->mid[0], st->RA[0], st->ringA[0], st->ringA[1], st->HA, st->RA[1], FA, s));
   WAN_TRY(attention(m->attn_g, m->qkv, m->proj, st->at, st->RA[1], st->RA[2], FA, &st->prof, st->err_dev, s));
   WAN_TRY(resnet(st, m->mid[1], st->RA[2], st->ringA[2], st->ringA[3], st->HA, st->RA[0], FA, s));
   // up block 0 (level A -> B); block input RA[0]
-  WAN_TRY(resnet_chain(st, m->up[0], st->RA, st->ringA + 4, st->HA, FA, nullptr, s));
+  WAN_TRY(resnet_chain(st, m->ups[0], st->RA, st->ringA + 4, st->HA, FA, nullptr, s));
   WAN_TRY(time_upsample(st, m->tconv[0], st->RA[1], st->tcA, st->tuA, FA, first, s));
   WAN_TRY(resample(st, m->resample[0], st->tuA, st->RA[0], 2, first, st->RB[0], FB, s));
   // up block 1 (level B -> C); block input RB[0]
-  WAN_TRY(resnet_chain(st, m->up[1], st->RB, st->ringB, st->HB, FB, nullptr, s));
+  WAN_TRY(resnet_chain(st, m->ups[1], st->RB, st->ringB, st->HB, FB, nullptr, s));
   WAN_TRY(time_upsample(st, m->tconv[1], st->RB[1], st->tcB, st->tuB, FB, first, s));
   WAN_TRY(resample(st, m->resample[1], st->tuB, st->RB[0], 2, first, st->RC[0], FC, s));
   // up block 2 (level C -> D); block input RC[0]
-  WAN_TRY(resnet_chain(st, m->up[2], st->RC, st->ringC, st->HC, FC, nullptr, s));
+  WAN_TRY(resnet_chain(st, m->ups[2], st->RC, st->ringC, st->HC, FC, nullptr, s));
   WAN_TRY(resample(st, m->resample[2], st->RC[1], st->RC[0], 1, first, st->RD[0], FC, s));
   // up block 3 (level D)
   NormOut nout;  // norm_out + SiLU, fused into the last conv2 when possible
   nout.gs = m->out_g;
   nout.ring = &st->ringOut;
   bool out_done = false;
-  WAN_TRY(resnet_chain(st, m->up[3], st->RD, st->ringD, st->HD, FC, &nout, s, &out_done));
+  WAN_TRY(resnet_chain(st, m->ups[3], st->RD, st->ringD, st->HD, FC, &nout, s, &out_done));
   // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
   if (!out_done) {
     ELT(&st->prof, kKindNorm, 4.0 * st->B * FC * st->RD[1].H * st->RD[1].W * m->base * (m->split ? 2 : 1),
@@ -1069,7 +1100,8 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
     L.args.out_f32 = out_f32;
     L.args.out_f0 = (int)out_f0;
     L.args.preclamp = pre;
-    L.args.vid_cs = out_frames * 4LL * st->ringOut.H * st->ringOut.W;
+    L.args.vid_patch = m->patch;
+    L.args.vid_cs = out_frames * (long long)(m->patch * m->patch) * st->ringOut.H * st->ringOut.W;
     L.args.vid_bs = 3 * L.args.vid_cs;
     WAN_TRY(run(L, &st->prof, kKindConvOut, conv_flops(m->conv_out, st->ringOut, FC), st->err_dev, s));
     st->shifts.push_back(RingShift{st->ringOut.p, st->ringOut.fs(), st->ringOut.bs(), FC, st->B});
@@ -1204,7 +1236,7 @@ static wan_status clip_impl(wan_vae_stream* st, const void* z, int z_dtype, int 
 static wan_status tiled_impl(const wan_vae_model* m, const void* z, int z_dtype, int B, int T, int h, int w,
                              int tile_h, int tile_w, int stride_h, int stride_w, int tile_batch, int max_chunk,
                              void* out, int out_dtype, cudaStream_t s) {
-  constexpr int P = 16;  // pixels per latent
+  const int P = 8 * m->patch;  // pixels per latent
   const int th = tile_h / P, tw = tile_w / P, sh = stride_h / P, sw = stride_w / P;
   std::vector<std::pair<int, int>> rows, cols;  // (origin, size) in latents
   for (int r = 0; r < h; r += sh) rows.push_back({r, std::min(th, h - r)});
@@ -1234,7 +1266,7 @@ static wan_status tiled_impl(const wan_vae_model* m, const void* z, int z_dtype,
   }
   const int per_batch = std::max(1, std::min(tile_batch > 0 ? tile_batch : kMaxGather, std::min(kMaxGather, 64 / B)));
   for (const auto& o : order)
-    zt_elems = std::max(zt_elems, (size_t)per_batch * B * kZdim * T * o.first.first * o.first.second);
+    zt_elems = std::max(zt_elems, (size_t)per_batch * B * m->zdim * T * o.first.first * o.first.second);
   const int zes = z_dtype == WAN_F32 ? 4 : 2;
   DevMem mem;
   mem.use_async = true;
@@ -1273,7 +1305,7 @@ static wan_status tiled_impl(const wan_vae_model* m, const void* z, int z_dtype,
       gt.w = w;
       gt.th = rh;
       gt.tw = cw;
-      gt.CT = (long long)kZdim * T;
+      gt.CT = (long long)m->zdim * T;
       for (int k = 0; k < n; ++k) {
         const int idx = order[g0 + k].second;
         gt.r0[k] = rows[idx / nj].first;
@@ -1359,6 +1391,8 @@ void wan_vae_model_destroy(wan_vae_model* model) {
 }
 
 int32_t wan_vae_model_base_dim(const wan_vae_model* model) { return model ? model->base : -1; }
+int32_t wan_vae_model_z_dim(const wan_vae_model* model) { return model ? model->zdim : -1; }
+int32_t wan_vae_model_scale(const wan_vae_model* model) { return model ? 8 * model->patch : -1; }
 
 wan_status wan_vae_model_set_latent_stats(wan_vae_model* model, const float* mean, const float* std_dev, int32_t n) {
   API_GUARD({
@@ -1368,12 +1402,13 @@ wan_status wan_vae_model_set_latent_stats(wan_vae_model* model, const float* mea
       return WAN_OK;
     }
     if (!mean || !std_dev) return fail(WAN_ERR_INVALID_ARG, "mean and std must both be given or both be NULL");
-    if (n != kZdim) return fail(WAN_ERR_SHAPE, "%d latent statistics given, %d expected", n, kZdim);
-    float h[2 * kZdim];
-    for (int c = 0; c < kZdim; ++c) {
+    const int zd = model->zdim;
+    if (n != zd) return fail(WAN_ERR_SHAPE, "%d latent statistics given, %d expected", n, zd);
+    float h[2 * kZdimMax];
+    for (int c = 0; c < zd; ++c) {
       h[c] = mean[c];
-      h[kZdim + c] = std_dev[c];
-      if (!std::isfinite(h[c]) || !std::isfinite(h[kZdim + c]))
+      h[zd + c] = std_dev[c];
+      if (!std::isfinite(h[c]) || !std::isfinite(h[zd + c]))
         return fail(WAN_ERR_INVALID_ARG, "latent statistic of channel %d is not finite", c);
     }
     if (!model->zstat) {
@@ -1381,7 +1416,7 @@ wan_status wan_vae_model_set_latent_stats(wan_vae_model* model, const float* mea
       WAN_TRY(model->mem.alloc(&p, sizeof(h)));
       model->zstat = (float*)p;
     }
-    CUDA_TRY(cudaMemcpy(model->zstat, h, sizeof(h), cudaMemcpyHostToDevice));
+    CUDA_TRY(cudaMemcpy(model->zstat, h, 2 * zd * sizeof(float), cudaMemcpyHostToDevice));
     model->zstat_on = true;
     return WAN_OK;
   })
@@ -1431,7 +1466,7 @@ wan_status wan_vae_stream_sync_status(wan_vae_stream* st, wan_cuda_stream stream
 // ---- causal-cache checkpoint: header + the two history slots of every ring
 struct StateHeader {
   uint64_t magic;
-  int32_t base, split, B, h, w, first, n_rings;
+  int32_t base, split, B, h, w, first, n_rings;  // split: bit 0 fp32 split format, bit 1 Wan2.1
   int64_t payload;
 };
 static const uint64_t kStateMagic = 0x57414e5641453031ULL;  // "WANVAE01"
@@ -1453,7 +1488,7 @@ wan_status wan_vae_stream_save(wan_vae_stream* st, void* dst, int64_t bytes, wan
       return fail(WAN_ERR_INVALID_ARG, "state buffer of %lld bytes, %lld needed", (long long)bytes,
                   (long long)wan_vae_stream_state_bytes(st));
     cudaStream_t s = (cudaStream_t)stream;
-    StateHeader hd{kStateMagic, st->m->base, st->m->split ? 1 : 0, st->B, st->h, st->w, st->first ? 1 : 0,
+    StateHeader hd{kStateMagic, st->m->base, (st->m->split ? 1 : 0) | (st->m->wan21 ? 2 : 0), st->B, st->h, st->w, st->first ? 1 : 0,
                    (int32_t)st->rings.size(), state_payload(st)};
     CUDA_TRY(cudaMemcpyAsync(dst, &hd, sizeof(hd), cudaMemcpyDefault, s));
     char* o = static_cast<char*>(dst) + rup(sizeof(StateHeader), 256);
@@ -1476,7 +1511,7 @@ wan_status wan_vae_stream_load(wan_vae_stream* st, const void* src, int64_t byte
     CUDA_TRY(cudaMemcpyAsync(&hd, src, sizeof(hd), cudaMemcpyDefault, s));
     CUDA_TRY(cudaStreamSynchronize(s));
     if (hd.magic != kStateMagic) return fail(WAN_ERR_INVALID_ARG, "not a decode state");
-    if (hd.base != st->m->base || hd.split != (st->m->split ? 1 : 0) || hd.B != st->B || hd.h != st->h ||
+    if (hd.base != st->m->base || hd.split != ((st->m->split ? 1 : 0) | (st->m->wan21 ? 2 : 0)) || hd.B != st->B || hd.h != st->h ||
         hd.w != st->w || hd.n_rings != (int32_t)st->rings.size() || hd.payload != state_payload(st))
       return fail(WAN_ERR_STATE, "state of a different model, dtype or shape");
     if (bytes < wan_vae_stream_state_bytes(st)) return fail(WAN_ERR_INVALID_ARG, "state buffer truncated");
@@ -1558,11 +1593,12 @@ wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int3
     if (T < 1) return fail(WAN_ERR_INVALID_ARG, "T = %d", T);
     cudaStream_t s = (cudaStream_t)stream;
     const size_t zes = z_dtype == WAN_F32 ? 4 : 2, oes = out_dtype == WAN_F32 ? 4 : 2;
-    const long long P = (long long)st->h * st->w, HW = 256LL * P;
+    const int zd = st->m->zdim, ppl = 8 * st->m->patch;  // latent channels, pixels per latent
+    const long long P = (long long)st->h * st->w, HW = (long long)ppl * ppl * P;
     const int n = st->nmax;
     const long long nfmax = 4LL * n;
     // staging: two latent chunks and two video chunks, kept by the stream
-    const size_t zneed = (size_t)st->B * kZdim * n * P * 4, vneed = (size_t)st->B * 3 * nfmax * HW * 4;
+    const size_t zneed = (size_t)st->B * zd * n * P * 4, vneed = (size_t)st->B * 3 * nfmax * HW * 4;
     if (st->zb_bytes < zneed || st->vb_bytes < vneed) {
       for (int k = 0; k < 2; ++k) {
         WAN_TRY(st->mem.alloc(&st->zb[k], zneed));
@@ -1594,7 +1630,7 @@ wan_status wan_vae_decode_clip_host(wan_vae_stream* st, const void* z_host, int3
       }
       // latents of this chunk: rows (b, c) of nn*P values
       if (cudaMemcpy2DAsync(st->zb[k], nn * P * zes, (const char*)z_host + t0 * P * zes, (size_t)T * P * zes,
-                            nn * P * zes, (size_t)st->B * kZdim, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+                            nn * P * zes, (size_t)st->B * zd, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         result = fail(WAN_ERR_CUDA, "latent upload failed");
         break;
       }
@@ -1665,7 +1701,7 @@ wan_status wan_vae_decode_tiled(const wan_vae_model* model, const void* z, int32
     if ((uintptr_t)out % 16) return fail(WAN_ERR_INVALID_ARG, "output not 16-byte aligned");
     if (B < 1 || B > 64 || T < 1 || h < 1 || w < 1 || max_chunk > 64)
       return fail(WAN_ERR_INVALID_ARG, "B=%d (1..64) T=%d h=%d w=%d max_chunk=%d (<= 64)", B, T, h, w, max_chunk);
-    if ((long long)16 * h > 65535 || (long long)16 * w > 65535)
+    if ((long long)8 * model->patch * h > 65535 || (long long)8 * model->patch * w > 65535)
       return fail(WAN_ERR_UNSUPPORTED, "frame of %dx%d latents too large", h, w);
     return tiled_impl(model, z, z_dtype, B, T, h, w, tile_h, tile_w, stride_h, stride_w, tile_batch, max_chunk, out,
                       out_dtype, (cudaStream_t)stream);
