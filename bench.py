@@ -300,6 +300,8 @@ def main():
     ap.add_argument("--workload", choices=("decode", "attention", "tiled"), default="decode",
                     help="attention: the isolated mid-block attention (x [8, 1024, 44, 80]) instead of the decode; "
                          "tiled: the 720p clip decoded as overlapping spatial tiles")
+    ap.add_argument("--model", choices=("ti2v", "wan21"), default="ti2v",
+                    help="wan21: the Wan2.1 VAE decode at 720p (latents [1,16,21,90,160]) instead of TI2V-5B's")
     ap.add_argument("--tile", default="256,256", help="tiled workload: tile height,width in pixels")
     ap.add_argument("--stride", default="192,192", help="tiled workload: tile stride height,width in pixels")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -313,12 +315,20 @@ def main():
         return run_attention(args)
     if args.workload == "tiled":
         return run_tiled(args)
-    global B, T, H_LAT, W_LAT, FRAMES, H_OUT, W_OUT, METRIC
+    global B, Z, T, H_LAT, W_LAT, FRAMES, H_OUT, W_OUT, METRIC, WORKLOAD
+    wan21 = args.model == "wan21"
+    if wan21:
+        # the Wan2.1 VAE at 720p: latents [1, 16, 21, 90, 160] -> [1, 3, 81, 720, 1280]
+        WORKLOAD = wan_synth.CONFIGS["wan21_720p"]
+        B, Z, T, H_LAT, W_LAT = WORKLOAD["latents"]
+        FRAMES, H_OUT, W_OUT = 4 * T - 3, 8 * H_LAT, 8 * W_LAT
+        METRIC = f"decoded frames/s ({H_OUT}x{W_OUT}, bf16, Wan2.1 VAE)"
     custom = args.latents is not None
     if custom:
         B, T, H_LAT, W_LAT = (int(v) for v in args.latents.split(","))
-        FRAMES, H_OUT, W_OUT = 4 * T - 3, 16 * H_LAT, 16 * W_LAT
-        METRIC = f"decoded frames/s ({H_OUT}x{W_OUT}, bf16)"
+        k = 8 if wan21 else 16
+        FRAMES, H_OUT, W_OUT = 4 * T - 3, k * H_LAT, k * W_LAT
+        METRIC = f"decoded frames/s ({H_OUT}x{W_OUT}, bf16{', Wan2.1 VAE' if wan21 else ''})"
 
     import torch
     ws, rank, local = _dist()
@@ -337,7 +347,8 @@ def main():
     import video_vae_decoding_gb300 as wv
 
     stream = torch.cuda.current_stream()
-    w = wan_synth.make_weights(base=WORKLOAD["base"], seed=WORKLOAD["weight_seed"])
+    w = wan_synth.make_weights(base=WORKLOAD["base"], seed=WORKLOAD["weight_seed"],
+                               variant=WORKLOAD.get("variant", "ti2v"))
     wdev = {k: torch.from_numpy(np.array(v)).to(dev) for k, v in w.items()}
     model = wv.Model(wdev, dtype=torch.bfloat16)
     torch.cuda.synchronize()
@@ -399,7 +410,7 @@ def main():
                "d2h_bytes_per_step": v_host.numel() * v_host.element_size()}
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not custom:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not custom and not wan21:
         dt, fe, desc = cpu_oracle_sample(z_np)
         cpu = {"value": fe / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": desc}
 
@@ -417,9 +428,11 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic: seeded random-init TI2V-5B decoder weights, N(0,1) latents",
+            "data": (f"synthetic: seeded random-init {'Wan2.1' if wan21 else 'TI2V-5B'} decoder weights, "
+                     "N(0,1) latents"),
             "config": {"workload": (f"latents [{B},48,{T},{H_LAT},{W_LAT}] -> video [{B},3,{FRAMES},{H_OUT},{W_OUT}] bf16"
-                                    if custom else "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280] bf16"),
+                                    if custom or wan21 else
+                                    "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280] bf16"),
                        "chunk_latent_frames": args.chunk, "batch_per_gpu": B,
                        "l2": "working set larger than L2 (1.1 GB packed weights; GB-scale activations per chunk)"},
             "mpix_per_s": value * H_OUT * W_OUT / 1e6,
@@ -435,7 +448,8 @@ def main():
                          "flop_per_step": dom["flops"] / args.steps,
                          # DRAM bytes of one level-D 256->256 launch of 4 output frames from the
                          # ncu capture in profiles/ (algorithmic bytes of that launch: 1.156e9)
-                         "traffic": 1.826e9, "traffic_case": "level-D 256->256 causal conv, 4 frames"},
+                         "traffic": None if wan21 else 1.826e9,
+                         "traffic_case": None if wan21 else "level-D 256->256 causal conv, 4 frames"},
             "tensor_core_tflops": prof["tc_flops"] / (prof["tc_ms"] / 1000.0) / 1e12 if prof["tc_ms"] > 0 else None,
             "tensor_core_ms_per_step": prof["tc_ms"] / args.steps,
             "by_kind": kinds,

@@ -36,6 +36,10 @@ CONV_CASES = [
     (1, 0, 1, 11, 24, 1024, 256, (3, 3, 3)),
     (1, 1, 1, 4, 4, 16, 32, (3, 3, 3)),
     (1, 0, 2, 19, 21, 512, 512, (1, 3, 3)),
+    # the Wan2.1 widths: N tiles of 96 and 192, K padded from 96 to 128
+    (1, 2, 2, 13, 22, 96, 96, (3, 3, 3)),
+    (1, 1, 2, 10, 18, 192, 192, (3, 3, 3)),
+    (2, 0, 1, 9, 14, 192, 384, (3, 3, 3)),
 ]
 
 

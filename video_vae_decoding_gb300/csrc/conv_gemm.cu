@@ -27,13 +27,20 @@ constexpr int kEpiThreads = 256;
 // stage holds three 16 x 10 A boxes (x offsets -1, 0, +1; rows y0-1 .. y0+8)
 // and the nine taps' B blocks; tap (dy, dx) reads box dx from row 16*dy on.
 constexpr int kHaloABox = 16 * kHaloBoxRows * 128;  // 20 KB
+// Row mode: 130 pixels x 128 B, rounded up to whole 1 KB swizzle atoms.
+constexpr int kRowABox = 17 * 1024;
 
-template <int BN, bool HALO = false>
+template <int BN, bool HALO = false, bool ROW = false>
 struct ConvCfg {
-  static constexpr int kStages = HALO ? 2 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
-  static constexpr int kABytes = HALO ? 3 * kHaloABox : kTileM * kBlockK * 2;  // 60 KB : 16 KB
-  static constexpr int kBBytes = (HALO ? 9 : 1) * BN * kBlockK * 2;
-  static constexpr int kAccCols = BN < 32 ? 32 : BN;  // one accumulator buffer; two are allocated
+  // as many stages as fit in 227 KB: 16 KB of A plus BN x 128 B of B each;
+  // row mode: a 130-row A box (17 KB) and three taps of B
+  static constexpr int kStages =
+      HALO ? 2 : ROW ? (BN <= 96 ? 4 : (BN <= 128 ? 3 : 2)) : (BN >= 256 ? 4 : (BN > 128 ? 5 : (BN == 128 ? 6 : (BN > 64 ? 7 : 8))));
+  static constexpr int kABytes = HALO ? 3 * kHaloABox : ROW ? kRowABox : kTileM * kBlockK * 2;  // 60 / 17 / 16 KB
+  static constexpr int kBBytes = (HALO ? 9 : ROW ? 3 : 1) * BN * kBlockK * 2;
+  // one accumulator buffer of BN columns; two are allocated, kAccCols apart
+  // (a power of two, so the allocation is one too)
+  static constexpr int kAccCols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
   static constexpr size_t kSmem =
       1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 7) + 16 + 4 * 2 * 2 * 128;
 };
@@ -124,6 +131,9 @@ struct TileCoord {
 // the same N tile; CTA `rank` of the cluster takes x tile unit.x * CL + rank
 // (past the frame's right edge when tiles_x is not a multiple of CL: an
 // all-out-of-range tile whose loads read zeros and whose stores are masked).
+// Unit order: N tile, sub-pixel phase, frame, then x, y, batch.  Frames come
+// before space so that the output frames of one spatial tile run side by
+// side: each input frame serves three time taps while it is still in L2.
 __device__ __forceinline__ int tiles_x_units(const ConvArgs& a, int CL) { return (a.tiles_x + CL - 1) / CL; }
 __device__ __forceinline__ TileCoord tile_coord(const ConvArgs& a, int t, int CL = 1, int rank = 0) {
   TileCoord c;
@@ -134,14 +144,28 @@ __device__ __forceinline__ TileCoord tile_coord(const ConvArgs& a, int t, int CL
     c.phase = t & 3;
     t >>= 2;
   }
+  c.f = t % a.frames;
+  t /= a.frames;
+  if (a.row) {  // cluster pairs are adjacent rows
+    c.tx = t % a.tiles_x;
+    t /= a.tiles_x;
+    const int ny = (a.tiles_y + CL - 1) / CL;
+    c.ty = (t % ny) * CL + rank;
+    c.b = t / ny;
+    return c;
+  }
   const int nx = tiles_x_units(a, CL);
   c.tx = (t % nx) * CL + rank;
   t /= nx;
   c.ty = t % a.tiles_y;
-  t /= a.tiles_y;
-  c.f = t % a.frames;
-  c.b = t / a.frames;
+  c.b = t / a.tiles_y;
   return c;
+}
+// Work units of a launch: N tiles x phases x frames x spatial units x batches.
+__host__ __device__ __forceinline__ long long conv_units(const ConvArgs& a, int CL) {
+  const long long sp = a.row ? (long long)a.tiles_x * ((a.tiles_y + CL - 1) / CL)
+                             : (long long)((a.tiles_x + CL - 1) / CL) * a.tiles_y;
+  return (long long)a.tiles_n * (a.subpix ? 4 : 1) * sp * a.frames * a.batches;
 }
 
 // Epilogue of a tile that holds all N output channels, with the RMS norm of
@@ -341,11 +365,11 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
 // x tiles of the same N tile: each loads half of the B block and multicasts
 // it to both, and each MMA issuer frees a shared-memory stage in both CTAs
 // (the stage's "empty" barrier counts both), so L2 delivers B once per pair.
-template <int BN, int EPI, int CL, bool HALO>
+template <int BN, int EPI, int CL, bool HALO, bool ROW>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                      const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
-  using Cfg = ConvCfg<BN, HALO>;
+  using Cfg = ConvCfg<BN, HALO, ROW>;
   constexpr int S = Cfg::kStages;
   constexpr uint32_t kAccCols = Cfg::kAccCols;
   extern __shared__ uint8_t smem_raw[];
@@ -365,8 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long lim = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
-  const int num_units =
-      args.tiles_n * (args.subpix ? 4 : 1) * tiles_x_units(args, CL) * args.tiles_y * args.frames * args.batches;
+  const int num_units = (int)conv_units(args, CL);
   const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
   const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
   constexpr uint16_t kPairMask = (1u << CL) - 1;
@@ -434,6 +457,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      if constexpr (ROW) {
+        // per tap (dt, dy) and 64-channel block: one 130-pixel A box (x from
+        // tile start - 1) and the B blocks of its three dx taps
+        for (int ti = 0; ti < args.n_taps && ok; ++ti) {
+          const ConvTap tp = args.taps[ti];
+          const int fr = args.src_f0[0] + tc.f + tp.dt;
+          const int x0 = tc.tx * kTileM - 1, y0 = tc.ty + tp.dy;
+          for (int kb = 0; kb < tp.nkb; ++kb, ++it) {
+            const int s = it % S;
+            const int r = it / S;
+            if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty, lim)) {
+              ok = false;
+              *abort_flag = 1;
+              break;
+            }
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
+            const uint32_t fb = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(fb, (kTileM + 2) * kBlockK * 2 + Cfg::kBBytes);
+            tma_load_5d(smem_u32(sA + s * Cfg::kABytes), &mapA0, fb, tp.a_c0 + kb * kBlockK, x0, y0, fr, tc.b);
+            for (int j = 0; j < 3; ++j) {
+              const uint32_t dst = smem_u32(sB + s * Cfg::kBBytes + j * (BN * kBlockK * 2) +
+                                            rank * (BN / CL) * kBlockK * 2);
+              const int k = tp.b_k0 + j * args.row_bdk + kb * kBlockK;
+              if constexpr (CL > 1)
+                tma_load_3d_multicast(dst, &mapB, fb, k, tc.tn * BN + rank * (BN / CL), 0, kPairMask);
+              else
+                tma_load_3d(dst, &mapB, fb, k, tc.tn * BN, 0);
+            }
+          }
+        }
+        continue;
+      }
       const int gB = args.b_per_frame ? (tc.b * args.b_gstride + tc.f) : tc.phase;
       const int sy = args.subpix ? (tc.phase >> 1) - 1 : 0, sx = args.subpix ? (tc.phase & 1) - 1 : 0;
       for (int ti = 0; ti < args.n_taps && ok; ++ti) {
@@ -490,7 +549,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        if constexpr (HALO) {
+        if constexpr (ROW) {
+          // dx tap j reads the A box from row j, 128 B further on: the 128-byte
+          // swizzle is undone from the shared-memory address bits, as the TMA
+          // applied it, so a start one row into an atom needs nothing else
+          // (the descriptor's base-offset field stays 0); and its own B block
+          const uint64_t a0 = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
+          const uint64_t b0 = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const uint64_t ad = a0 + (uint64_t)((j * 128) >> 4);
+            const uint64_t bd = b0 + (uint64_t)((j * BN * kBlockK * 2) >> 4);
+#pragma unroll
+            for (int k = 0; k < kBlockK / 16; ++k)
+              umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || j > 0 || k > 0) ? 1u : 0u);
+          }
+        } else if constexpr (HALO) {
           // descriptors of the stage's first box and first B block; the taps
           // add constant byte offsets (>> 4) to the start-address field
           const uint64_t a0 = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
@@ -549,15 +623,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int EPI, int CL, bool HALO = false>
+template <int BN, int EPI, int CL, bool HALO = false, bool ROW = false>
 static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
-  using Cfg = ConvCfg<BN, HALO>;
-  auto kern = conv_gemm_kernel<BN, EPI, CL, HALO>;
+  using Cfg = ConvCfg<BN, HALO, ROW>;
+  auto kern = conv_gemm_kernel<BN, EPI, CL, HALO, ROW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
   if (e != cudaSuccess) return e;
   const ConvArgs& a = L.args;
-  const long long units = (long long)a.tiles_n * (a.subpix ? 4 : 1) * ((a.tiles_x + CL - 1) / CL) * a.tiles_y *
-                          a.frames * a.batches;
+  const long long units = conv_units(a, CL);
   if (units <= 0) return cudaSuccess;
   if (units > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -589,11 +662,20 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Clusters of two CTAs share the B block when it is large (BN = 256); the
-// B tensor map's box must then hold BN / 2 rows (conv_b_box_rows).
-int conv_b_box_rows(int bn) { return bn >= 256 ? bn / 2 : bn; }
+// Clusters of two CTAs share the B block (each loads half and multicasts it)
+// for BN = 96, 192 and 256, where the stage's bytes, not the MMAs, would
+// otherwise set the pace; the B tensor map's box then holds BN / 2 rows.
+static bool conv_clustered(int bn) { return bn == 96 || bn == 192 || bn == 256; }
+int conv_b_box_rows(int bn) { return conv_clustered(bn) ? bn / 2 : bn; }
 
 cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
+  if (L.args.row) {
+    if (L.epi != kEpiStore || L.args.halo || L.args.subpix) return cudaErrorInvalidValue;
+    if (L.bn == 96) return launch_t<96, kEpiStore, 2, false, true>(L, stream);
+    if (L.bn == 128) return launch_t<128, kEpiStore, 2, false, true>(L, stream);
+    if (L.bn == 192) return launch_t<192, kEpiStore, 2, false, true>(L, stream);
+    return cudaErrorInvalidValue;
+  }
   if (L.epi == kEpiVideo) {
     if (L.bn != 16) return cudaErrorInvalidValue;
     return L.args.halo ? launch_t<16, kEpiVideo, 1, true>(L, stream) : launch_t<16, kEpiVideo, 1>(L, stream);
@@ -612,7 +694,9 @@ cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
     case 16: return launch_t<16, kEpiStore, 1>(L, stream);
     case 32: return launch_t<32, kEpiStore, 1>(L, stream);
     case 64: return launch_t<64, kEpiStore, 1>(L, stream);
+    case 96: return launch_t<96, kEpiStore, 2>(L, stream);
     case 128: return launch_t<128, kEpiStore, 1>(L, stream);
+    case 192: return launch_t<192, kEpiStore, 2>(L, stream);
     case 256: return launch_t<256, kEpiStore, 2>(L, stream);
   }
   return cudaErrorInvalidValue;

@@ -56,6 +56,13 @@ struct ConvArgs {
   // 64 x 16 x 10 and the B map is 3-D (K, N, 9 spatial taps with stride
   // ci_pad); K iterates time taps then 64-channel blocks (taps[0].nkb of them).
   int halo;
+  // Row mode (3x3 spatial taps without a shortcut, N tile 96, 128 or 192): a tile
+  // is 128 consecutive pixels of one row (box_w 128, box_h 1); every tap
+  // (dt, dy) loads one 130-pixel A box (x from -1) that serves its three dx
+  // taps at row offsets 0, 1, 2, and the three taps' B blocks, which lie
+  // row_bdk K columns apart.  Cluster pairs are adjacent rows (ty).
+  int row;
+  int row_bdk;
   int N;                 // valid output channels
   const float* bias;     // fp32, zero-padded to a multiple of 16 values past N, or null
   // output element (b, frame, y, x, n) at
@@ -109,7 +116,7 @@ struct ConvArgs {
 struct ConvLaunch {
   CUtensorMap a0, a1, b;
   ConvArgs args;
-  int bn;      // 16, 32, 64, 128 or 256
+  int bn;      // 16, 32, 64, 96, 128, 192 or 256 (96 and 192: plain store epilogue only)
   int epi;     // EpiMode
 };
 

@@ -201,8 +201,12 @@ struct ConvW {
   int subpix = 0;                // 4 phases of 2x2 taps (nearest-x2 + 3x3 conv)
 };
 
+// N tile of a conv with co output channels: 256, or 192 where that divides
+// co and 256 does not (384, 1152: the Wan2.1 widths); up to 256 channels one
+// tile holding them all (96 and 192 exactly, else the next power of two).
 static int choose_bn(int co) {
-  if (co >= 256) return 256;
+  if (co > 256) return (co % 256 != 0 && co % 192 == 0) ? 192 : 256;
+  if (co == 96 || co == 192) return co;
   int b = 16;
   while (b < co) b *= 2;
   return b;
@@ -698,12 +702,25 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   ConvArgs& A = L.args;
   if (a0.ldc < cw.ci_pad || (a1 && a1->ldc < cw.sc_ci_pad))
     return fail(WAN_ERR_INTERNAL, "conv source narrower than its packed channels");
-  WAN_TRY(act_map(&L.a0, a0));
-  if (a1)
-    WAN_TRY(act_map(&L.a1, *a1));
-  else
+  // row mode (narrow N, 3x3 spatial taps, one source): 128-pixel row tiles,
+  // one 130-pixel A box per (dt, dy) serving its three dx taps
+  const bool row = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
+                   (cw.bn == 96 || cw.bn == 128 || cw.bn == 192);
+  if (row) {
+    WAN_TRY(act_map(&L.a0, a0.p, a0.ldc, a0.ldc, a0.W, a0.H, a0.F, a0.B, a0.fs(), a0.bs(), 130, 1));
     L.a1 = L.a0;
-  WAN_TRY(b_map(&L.b, cw.w, cw.ktot, cw.co_pad, cw.subpix ? 4 : 1, cw.ktot, (long long)cw.ktot * cw.co_pad, cw.bn));
+    const uint64_t dims[3] = {(uint64_t)cw.ktot, (uint64_t)cw.co_pad, 1};
+    const uint64_t strides[2] = {(uint64_t)cw.ktot * 2, (uint64_t)cw.ktot * cw.co_pad * 2};
+    const uint32_t box[3] = {64, (uint32_t)(cw.bn / 2), 1};  // each CTA of a pair loads half
+    WAN_TRY(encode(&L.b, 3, cw.w, dims, strides, box));
+  } else {
+    WAN_TRY(act_map(&L.a0, a0));
+    if (a1)
+      WAN_TRY(act_map(&L.a1, *a1));
+    else
+      L.a1 = L.a0;
+    WAN_TRY(b_map(&L.b, cw.w, cw.ktot, cw.co_pad, cw.subpix ? 4 : 1, cw.ktot, (long long)cw.ktot * cw.co_pad, cw.bn));
+  }
   if (cw.split && (!a0.lo || (a1 && !a1->lo))) return fail(WAN_ERR_INTERNAL, "split conv on a plain tensor");
   A.subpix = cw.subpix;
   int nt = 0, k = 0;
@@ -712,7 +729,7 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
       for (int dx = 0; dx < cw.kw; ++dx) {
         // sub-pixel taps carry source offsets 0/1; the kernel adds the phase's (i - 1, j - 1)
         const int oy = cw.subpix ? dy : dy - cw.kh / 2, ox = cw.subpix ? dx : dx - cw.kw / 2;
-        WAN_TRY(add_tap(A, nt, 0, dt, oy, ox, cw.ci_pad, a0.lo, k, cw.split));
+        if (!row || dx == 0) WAN_TRY(add_tap(A, nt, 0, dt, oy, ox, cw.ci_pad, a0.lo, k, cw.split));
         k += (cw.split ? 2 : 1) * cw.ci_pad;
       }
   if (cw.sc_ci_pad) {
@@ -721,12 +738,14 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
     k += (cw.split ? 2 : 1) * cw.sc_ci_pad;
   }
   A.n_taps = nt;
-  A.box_w = 16;
-  A.box_h = 8;
+  A.row = row ? 1 : 0;
+  A.row_bdk = row ? cw.ci_pad : 0;
+  A.box_w = row ? 128 : 16;
+  A.box_h = row ? 1 : 8;
   A.H = a0.H;
   A.W = a0.W;
-  A.tiles_x = (int)cdiv(a0.W, 16);
-  A.tiles_y = (int)cdiv(a0.H, 8);
+  A.tiles_x = (int)cdiv(a0.W, A.box_w);
+  A.tiles_y = (int)cdiv(a0.H, A.box_h);
   A.tiles_n = cw.co_pad / cw.bn;
   A.frames = F;
   A.batches = a0.B;
