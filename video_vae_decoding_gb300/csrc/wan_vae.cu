@@ -107,8 +107,11 @@ static wan_status act_map(CUtensorMap* m, const bf16* base, int C, int ldc, int 
   const uint32_t box[5] = {64, (uint32_t)bw, (uint32_t)bh, 1, 1};
   return encode(m, 5, base, dims, strides, box);
 }
+// The channel extent is the tensor's own channel count (the split format's
+// whole row): a 64-channel block reaching into the padding up to ldc reads
+// TMA zero fill there instead of fetching the zeros from memory.
 static wan_status act_map(CUtensorMap* m, const Act& a, int bw = 16, int bh = 8) {
-  return act_map(m, a.p, a.ldc, a.ldc, a.W, a.H, a.F, a.B, a.fs(), a.bs(), bw, bh);
+  return act_map(m, a.p, a.chans(), a.ldc, a.W, a.H, a.F, a.B, a.fs(), a.bs(), bw, bh);
 }
 // B-operand map for an N tile of bn: dims (K, N, G), box (64, rows, 1) with
 // rows = bn, or bn / 2 when two CTAs of a cluster each load half of the tile.
@@ -707,7 +710,7 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   const bool row = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
                    (cw.bn == 96 || cw.bn == 128 || cw.bn == 192);
   if (row) {
-    WAN_TRY(act_map(&L.a0, a0.p, a0.ldc, a0.ldc, a0.W, a0.H, a0.F, a0.B, a0.fs(), a0.bs(), 130, 1));
+    WAN_TRY(act_map(&L.a0, a0, 130, 1));
     L.a1 = L.a0;
     const uint64_t dims[3] = {(uint64_t)cw.ktot, (uint64_t)cw.co_pad, 1};
     const uint64_t strides[2] = {(uint64_t)cw.ktot * 2, (uint64_t)cw.ktot * cw.co_pad * 2};
@@ -1105,7 +1108,7 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
     if (!co.split && co.bn == 16 && co.kt == 3 && co.kh == 3 && co.kw == 3) {
       // halo mode: three 16 x 10 boxes per time tap and channel block serve all nine spatial taps
       const Act& a = st->ringOut;
-      WAN_TRY(act_map(&L.a0, a.p, a.ldc, a.ldc, a.W, a.H, a.F, a.B, a.fs(), a.bs(), 16, kHaloBoxRows));
+      WAN_TRY(act_map(&L.a0, a, 16, kHaloBoxRows));
       L.a1 = L.a0;
       const uint64_t dims[3] = {(uint64_t)co.ktot, (uint64_t)co.co_pad, 9};
       const uint64_t strides[2] = {(uint64_t)co.ktot * 2, (uint64_t)co.ci_pad * 2};
