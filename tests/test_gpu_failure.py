@@ -16,7 +16,7 @@ from tests.gpu_util import lib_ready, to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cout", [64, 256], ids=["one_cta", "cluster_of_two"])
+@pytest.mark.parametrize("cout", [64, 256, 96], ids=["one_cta", "cluster_of_two", "row_tiles_pair"])
 def test_bounded_wait_expires_and_is_reported(cout):
     wv = lib_ready()
     lib = wv.load()

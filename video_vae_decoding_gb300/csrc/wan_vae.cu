@@ -1887,7 +1887,8 @@ wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F
 extern "C" wan_status wan_selftest_wait_timeout(int32_t cout, int32_t* device_code, wan_cuda_stream stream) {
   API_GUARD({
     if (device_code) *device_code = 0;
-    if (cout != 64 && cout != 256) return fail(WAN_ERR_INVALID_ARG, "cout must be 64 or 256, not %d", cout);
+    if (cout != 64 && cout != 96 && cout != 256)
+      return fail(WAN_ERR_INVALID_ARG, "cout must be 64, 96 or 256, not %d", cout);
     cudaStream_t s = (cudaStream_t)stream;
     DevMem mem;
     mem.use_async = true;
