@@ -30,19 +30,25 @@ constexpr int kHaloABox = 16 * kHaloBoxRows * 128;  // 20 KB
 // Row mode: 130 pixels x 128 B, rounded up to whole 1 KB swizzle atoms.
 constexpr int kRowABox = 17 * 1024;
 
-template <int BN, bool HALO = false, bool ROW = false>
+template <int BN, bool HALO = false, bool ROW = false, bool BAND = false>
 struct ConvCfg {
   // as many stages as fit in 227 KB: 16 KB of A plus BN x 128 B of B each;
-  // row mode: a 130-row A box (17 KB) and three taps of B
+  // row mode: a 130-row A box (17 KB) and three taps of B; band mode: A
+  // boxes (16 x 10 pixels, 20 KB) and one-tap B blocks in separate rings
   static constexpr int kStages =
-      HALO ? 2 : ROW ? (BN <= 96 ? 4 : (BN <= 128 ? 3 : 2)) : (BN >= 256 ? 4 : (BN > 128 ? 5 : (BN == 128 ? 6 : (BN > 64 ? 7 : 8))));
-  static constexpr int kABytes = HALO ? 3 * kHaloABox : ROW ? kRowABox : kTileM * kBlockK * 2;  // 60 / 17 / 16 KB
+      HALO ? 2
+           : BAND ? 5
+                  : ROW ? (BN <= 96 ? 4 : (BN <= 128 ? 3 : 2))
+                        : (BN >= 256 ? 4 : (BN > 128 ? 5 : (BN == 128 ? 6 : (BN > 64 ? 7 : 8))));
+  static constexpr int kAStages = BAND ? 3 : kStages;  // A slots (the B ring has kStages)
+  static constexpr int kABytes =
+      HALO ? 3 * kHaloABox : ROW ? kRowABox : BAND ? kHaloABox : kTileM * kBlockK * 2;  // 60 / 17 / 20 / 16 KB
   static constexpr int kBBytes = (HALO ? 9 : ROW ? 3 : 1) * BN * kBlockK * 2;
   // one accumulator buffer of BN columns; two are allocated, kAccCols apart
   // (a power of two, so the allocation is one too)
   static constexpr int kAccCols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
-  static constexpr size_t kSmem =
-      1024 + (size_t)kStages * (kABytes + kBBytes) + 8 * (2 * kStages + 7) + 16 + 4 * 2 * 2 * 128;
+  static constexpr size_t kSmem = 1024 + (size_t)kAStages * kABytes + (size_t)kStages * kBBytes +
+                                   8 * (2 * kStages + 2 * kAStages + 7) + 16 + 4 * 2 * 2 * 128;
 };
 
 __device__ __forceinline__ void store16(void* dst, int f32, const float (&v)[16], int lo = 0) {
@@ -365,20 +371,24 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
 // x tiles of the same N tile: each loads half of the B block and multicasts
 // it to both, and each MMA issuer frees a shared-memory stage in both CTAs
 // (the stage's "empty" barrier counts both), so L2 delivers B once per pair.
-template <int BN, int EPI, int CL, bool HALO, bool ROW>
+template <int BN, int EPI, int CL, bool HALO, bool ROW, bool BAND>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                      const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
-  using Cfg = ConvCfg<BN, HALO, ROW>;
+  using Cfg = ConvCfg<BN, HALO, ROW, BAND>;
+  static_assert(!BAND || CL == 2, "band mode shares B across a pair of CTAs");
   constexpr int S = Cfg::kStages;
+  constexpr int SA = Cfg::kAStages;
   constexpr uint32_t kAccCols = Cfg::kAccCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + S * Cfg::kABytes;
+  uint8_t* sB = smem + SA * Cfg::kABytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * Cfg::kBBytes);
   uint64_t* empty = full + S;
-  uint64_t* tfull = empty + S;   // [2] accumulator ready (MMA -> epilogue)
+  uint64_t* fullA = empty + S;    // [SA] band mode: A box landed (unused otherwise)
+  uint64_t* emptyA = fullA + SA;  // [SA] band mode: A box consumed
+  uint64_t* tfull = emptyA + SA;  // [2] accumulator ready (MMA -> epilogue)
   uint64_t* tempty = tfull + 2;  // [2] accumulator drained (epilogue -> MMA)
   uint64_t* done = tempty + 2;   // all MMAs of this CTA complete
   uint64_t* ssbar = done + 1;    // [2] fused norm: both column halves' partial sums written
@@ -398,6 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), CL);  // one MMA commit per CTA of the cluster
+    }
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(smem_u32(&fullA[s]), 1);
+      mbar_init(smem_u32(&emptyA[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
@@ -423,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    int it = 0;
+    int it = 0, ia = 0;  // B (or shared) stages and, in band mode, A boxes issued
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
       const TileCoord tc = tile_coord(args, unit, CL, rank);
@@ -457,7 +471,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if constexpr (ROW) {
+      if constexpr (BAND) {
+        // per tap (dt, dx) and 64-channel block: one 16 x 10 A box (rows from
+        // tile start - 1) into the A ring, then its three dy taps' B blocks,
+        // one per B slot
+        for (int ti = 0; ti < args.n_taps && ok; ++ti) {
+          const ConvTap tp = args.taps[ti];
+          const int fr = args.src_f0[0] + tc.f + tp.dt;
+          const int x0 = tc.tx * args.box_w + tp.dx, y0 = tc.ty * args.box_h - 1;
+          for (int kb = 0; kb < tp.nkb && ok; ++kb) {
+            const int sa = ia % SA;
+            const int ra = ia / SA;
+            if (ra > 0 && !mbar_wait_bounded(smem_u32(&emptyA[sa]), (ra - 1) & 1, args.err, kDevTimeoutEmpty, lim)) {
+              ok = false;
+              *abort_flag = 1;
+              break;
+            }
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            const uint32_t fa = smem_u32(&fullA[sa]);
+            mbar_arrive_expect_tx(fa, Cfg::kABytes);
+            tma_load_5d(smem_u32(sA + sa * Cfg::kABytes), &mapA0, fa, tp.a_c0 + kb * kBlockK, x0, y0, fr, tc.b);
+            ++ia;
+            for (int j = 0; j < 3; ++j, ++it) {
+              const int s = it % S;
+              const int r = it / S;
+              if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty, lim)) {
+                ok = false;
+                *abort_flag = 1;
+                break;
+              }
+              if (*abort_flag) {
+                ok = false;
+                break;
+              }
+              if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
+              const uint32_t fb = smem_u32(&full[s]);
+              mbar_arrive_expect_tx(fb, Cfg::kBBytes);
+              tma_load_3d_multicast(smem_u32(sB + s * Cfg::kBBytes + rank * (BN / CL) * kBlockK * 2), &mapB, fb,
+                                    tp.b_k0 + j * args.row_bdk + kb * kBlockK, tc.tn * BN + rank * (BN / CL), 0,
+                                    kPairMask);
+            }
+          }
+        }
+        continue;
+      } else if constexpr (ROW) {
         // per tap (dt, dy) and 64-channel block: one 130-pixel A box (x from
         // tile start - 1) and the B blocks of its three dx taps
         for (int ti = 0; ti < args.n_taps && ok; ++ti) {
@@ -528,10 +588,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Do not leave while copies into this CTA's shared memory are in flight.
     for (int j = (it > S ? it - S : 0); j < it; ++j)
       mbar_wait_bounded(smem_u32(&full[j % S]), (j / S) & 1, args.err, kDevTimeoutFull, lim);
+    if constexpr (BAND)
+      for (int j = (ia > SA ? ia - SA : 0); j < ia; ++j)
+        mbar_wait_bounded(smem_u32(&fullA[j % SA]), (j / SA) & 1, args.err, kDevTimeoutFull, lim);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
-    int it = 0, lt = 0;
+    int it = 0, ia = 0, lt = 0;
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
@@ -541,6 +604,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t d = tmem + buf * kAccCols;
+      if constexpr (BAND) {
+        // per A box: its three dy taps from three consecutive B slots; tap dy
+        // reads the box from image row dy on (16 pixels = 2 KB = two whole
+        // swizzle atoms further); B slots are freed in both CTAs of the pair,
+        // the A slot in this CTA only
+        for (int kk = 0; kk < args.total_kb && ok; ++kk, ++ia) {
+          const int sa = ia % SA;
+          if (*abort_flag || !mbar_wait_bounded(smem_u32(&fullA[sa]), (ia / SA) & 1, args.err, kDevTimeoutFull, lim)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a0 = sdesc_k128(smem_u32(sA + sa * Cfg::kABytes));
+          for (int j = 0; j < 3; ++j, ++it) {
+            const int s = it % S;
+            if (*abort_flag || !mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull, lim)) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = a0 + (uint64_t)((j * 16 * 128) >> 4);
+            const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+#pragma unroll
+            for (int k = 0; k < kBlockK / 16; ++k)
+              umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || j > 0 || k > 0) ? 1u : 0u);
+            umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&emptyA[sa]));
+        }
+        umma_commit(smem_u32(&tfull[buf]));
+        continue;
+      }
       for (int kk = 0; kk < args.total_kb; ++kk, ++it) {
         const int s = it % S;
         if (*abort_flag || !mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull, lim)) {
@@ -623,10 +721,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int EPI, int CL, bool HALO = false, bool ROW = false>
+template <int BN, int EPI, int CL, bool HALO = false, bool ROW = false, bool BAND = false>
 static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
-  using Cfg = ConvCfg<BN, HALO, ROW>;
-  auto kern = conv_gemm_kernel<BN, EPI, CL, HALO, ROW>;
+  using Cfg = ConvCfg<BN, HALO, ROW, BAND>;
+  auto kern = conv_gemm_kernel<BN, EPI, CL, HALO, ROW, BAND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
   if (e != cudaSuccess) return e;
   const ConvArgs& a = L.args;
@@ -669,6 +767,10 @@ static bool conv_clustered(int bn) { return bn == 96 || bn == 192 || bn == 256; 
 int conv_b_box_rows(int bn) { return conv_clustered(bn) ? bn / 2 : bn; }
 
 cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
+  if (L.args.band) {
+    if (L.epi != kEpiStore || L.args.halo || L.args.subpix || L.args.row || L.bn != 256) return cudaErrorInvalidValue;
+    return launch_t<256, kEpiStore, 2, false, false, true>(L, stream);
+  }
   if (L.args.row) {
     if (L.epi != kEpiStore || L.args.halo || L.args.subpix) return cudaErrorInvalidValue;
     if (L.bn == 96) return launch_t<96, kEpiStore, 2, false, true>(L, stream);

@@ -62,7 +62,12 @@ struct ConvArgs {
   // taps at row offsets 0, 1, 2, and the three taps' B blocks, which lie
   // row_bdk K columns apart.  Cluster pairs are adjacent rows (ty).
   int row;
-  int row_bdk;
+  int row_bdk;  // row mode: K stride between dx taps; band mode: between dy taps
+  // Band mode (bf16 3x3 spatial taps without a shortcut, N tile 256, 16 x 8
+  // tiles): every tap (dt, dx) loads one 16 x 10 A box (rows from -1) into an
+  // A ring that serves its three dy taps at 2 KB offsets; the taps' one-tap
+  // B blocks go through a separate ring.
+  int band;
   int N;                 // valid output channels
   const float* bias;     // fp32, zero-padded to a multiple of 16 values past N, or null
   // output element (b, frame, y, x, n) at

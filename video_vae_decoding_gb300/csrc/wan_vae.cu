@@ -709,7 +709,17 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   // one 130-pixel A box per (dt, dy) serving its three dx taps
   const bool row = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
                    (cw.bn == 96 || cw.bn == 128 || cw.bn == 192);
-  if (row) {
+  // band mode (256-wide 3x3 convs, one source): a 16 x 10 A box per (dt, dx)
+  // serving its three dy taps
+  const bool band = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 && cw.bn == 256;
+  if (band) {
+    WAN_TRY(act_map(&L.a0, a0, 16, kHaloBoxRows));
+    L.a1 = L.a0;
+    const uint64_t dims[3] = {(uint64_t)cw.ktot, (uint64_t)cw.co_pad, 1};
+    const uint64_t strides[2] = {(uint64_t)cw.ktot * 2, (uint64_t)cw.ktot * cw.co_pad * 2};
+    const uint32_t box[3] = {64, (uint32_t)(cw.bn / 2), 1};  // each CTA of a pair loads half
+    WAN_TRY(encode(&L.b, 3, cw.w, dims, strides, box));
+  } else if (row) {
     WAN_TRY(act_map(&L.a0, a0, 130, 1));
     L.a1 = L.a0;
     const uint64_t dims[3] = {(uint64_t)cw.ktot, (uint64_t)cw.co_pad, 1};
@@ -732,7 +742,15 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
       for (int dx = 0; dx < cw.kw; ++dx) {
         // sub-pixel taps carry source offsets 0/1; the kernel adds the phase's (i - 1, j - 1)
         const int oy = cw.subpix ? dy : dy - cw.kh / 2, ox = cw.subpix ? dx : dx - cw.kw / 2;
-        if (!row || dx == 0) WAN_TRY(add_tap(A, nt, 0, dt, oy, ox, cw.ci_pad, a0.lo, k, cw.split));
+        if (band) {
+          // taps (dt, dx) in that order, each standing for its three dy taps
+          if (dy == 0) {
+            const int kd = ((dt * cw.kh + 0) * cw.kw + dx) * cw.ci_pad;
+            WAN_TRY(add_tap(A, nt, 0, dt, -1, ox, cw.ci_pad, a0.lo, kd, 0));
+          }
+        } else if (!row || dx == 0) {
+          WAN_TRY(add_tap(A, nt, 0, dt, oy, ox, cw.ci_pad, a0.lo, k, cw.split));
+        }
         k += (cw.split ? 2 : 1) * cw.ci_pad;
       }
   if (cw.sc_ci_pad) {
@@ -742,7 +760,8 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   }
   A.n_taps = nt;
   A.row = row ? 1 : 0;
-  A.row_bdk = row ? cw.ci_pad : 0;
+  A.band = band ? 1 : 0;
+  A.row_bdk = row ? cw.ci_pad : band ? cw.kw * cw.ci_pad : 0;
   A.box_w = row ? 128 : 16;
   A.box_h = row ? 1 : 8;
   A.H = a0.H;
