@@ -594,7 +594,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
-    int it = 0, ia = 0, lt = 0;
+    int lt = 0;
+    // The issuing thread is on the critical path: ring slots and phases are
+    // tracked incrementally, and the abort flag is read once per tile (every
+    // wait is bounded and raises the flag when it runs out).
+    int it_slot = 0, it_phase = 0;  // stage ring (the B ring in band mode)
+    int ia_slot = 0, ia_phase = 0;  // band mode: A ring
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
@@ -609,21 +614,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // reads the box from image row dy on (16 pixels = 2 KB = two whole
         // swizzle atoms further); B slots are freed in both CTAs of the pair,
         // the A slot in this CTA only
-        for (int kk = 0; kk < args.total_kb && ok; ++kk, ++ia) {
-          const int sa = ia % SA;
-          if (*abort_flag || !mbar_wait_bounded(smem_u32(&fullA[sa]), (ia / SA) & 1, args.err, kDevTimeoutFull, lim)) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        for (int kk = 0; kk < args.total_kb; ++kk) {
+          const int sa = ia_slot;
+          if (!mbar_wait_bounded(smem_u32(&fullA[sa]), ia_phase, args.err, kDevTimeoutFull, lim)) {
             *abort_flag = 1;
             ok = false;
             break;
           }
+          if (++ia_slot == SA) {
+            ia_slot = 0;
+            ia_phase ^= 1;
+          }
           tc_fence_after();
           const uint64_t a0 = sdesc_k128(smem_u32(sA + sa * Cfg::kABytes));
-          for (int j = 0; j < 3; ++j, ++it) {
-            const int s = it % S;
-            if (*abort_flag || !mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull, lim)) {
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const int s = it_slot;
+            if (!mbar_wait_bounded(smem_u32(&full[s]), it_phase, args.err, kDevTimeoutFull, lim)) {
               *abort_flag = 1;
               ok = false;
               break;
+            }
+            if (++it_slot == S) {
+              it_slot = 0;
+              it_phase ^= 1;
             }
             tc_fence_after();
             const uint64_t ad = a0 + (uint64_t)((j * 16 * 128) >> 4);
@@ -639,12 +657,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(smem_u32(&tfull[buf]));
         continue;
       }
-      for (int kk = 0; kk < args.total_kb; ++kk, ++it) {
-        const int s = it % S;
-        if (*abort_flag || !mbar_wait_bounded(smem_u32(&full[s]), (it / S) & 1, args.err, kDevTimeoutFull, lim)) {
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      for (int kk = 0; kk < args.total_kb; ++kk) {
+        const int s = it_slot;
+        if (!mbar_wait_bounded(smem_u32(&full[s]), it_phase, args.err, kDevTimeoutFull, lim)) {
           *abort_flag = 1;
           ok = false;
           break;
+        }
+        if (++it_slot == S) {
+          it_slot = 0;
+          it_phase ^= 1;
         }
         tc_fence_after();
         if constexpr (ROW) {
