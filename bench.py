@@ -448,7 +448,7 @@ def main():
                          "flop_per_step": dom["flops"] / args.steps,
                          # DRAM bytes of one level-D 256->256 launch of 4 output frames from the
                          # ncu capture in profiles/ (algorithmic bytes of that launch: 1.156e9)
-                         "traffic": None if wan21 else 1.125e9,
+                         "traffic": None if wan21 else 1.124e9,
                          "traffic_case": None if wan21 else "level-D 256->256 causal conv, 4 frames"},
             "tensor_core_tflops": prof["tc_flops"] / (prof["tc_ms"] / 1000.0) / 1e12 if prof["tc_ms"] > 0 else None,
             "tensor_core_ms_per_step": prof["tc_ms"] / args.steps,
