@@ -1,17 +1,19 @@
 // Implicit-GEMM convolution / batched GEMM on the sm_103a tensor cores.
 //
 // One CTA computes a 128 x BN output tile: 128 positions of one output frame
-// (a box_w x box_h rectangle) by BN output channels, accumulated in fp32 in
-// tensor memory.  Warp roles (256 threads):
+// (a box_w x box_h rectangle: 16 x 8, or 128 x 1 in row mode) by BN output
+// channels, accumulated in fp32 in tensor memory.  Warp roles (384 threads):
 //   warp 0, lane 0   TMA producer: per K block, one 5-D tile load of the A
-//                    activation box (64 channels x box_w x box_h, zero-filled
-//                    outside the frame) and one 3-D load of the B weight block
-//   warp 1, lane 0   MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per block
+//                    activation box (64 channels x pixels, zero-filled
+//                    outside the frame) and 3-D loads of the B weight blocks
+//   warp 1, lane 0   MMA issuer: tcgen05.mma (M=128, N=BN, K=16), 4 per K
+//                    block and tap, then a tcgen05.commit freeing the stage
 //   warp 2           TMEM allocation / release
-//   warps 4-7        epilogue: tcgen05.ld of the accumulator, bias, residual /
-//                    DupUp3D / unpatchify, stores
-// A STAGES-deep shared-memory ring, with one "full" and one "empty" mbarrier
-// per stage, overlaps the loads with the MMAs.  All waits are bounded.
+//   warps 4-11       epilogue: tcgen05.ld of the accumulator, bias, residual /
+//                    fused RMS norm / DupUp3D / unpatchify, stores
+// Shared-memory rings with "full" and "empty" mbarriers per slot overlap the
+// loads with the MMAs (plain, halo and row modes: one ring of A + B stages;
+// band mode: an A ring and a B ring).  All waits are bounded.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -368,9 +370,10 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
 // blockIdx.x / CL, + gridDim.x / CL, ...  The accumulator is double-buffered
 // in TMEM (2 x BN columns), so the epilogue warps drain tile i while the MMA
 // issuer accumulates tile i + 1.  With CL = 2 the two CTAs compute adjacent
-// x tiles of the same N tile: each loads half of the B block and multicasts
-// it to both, and each MMA issuer frees a shared-memory stage in both CTAs
-// (the stage's "empty" barrier counts both), so L2 delivers B once per pair.
+// tiles (x tiles, or rows in row mode) of the same N tile: each loads half of
+// the B block and multicasts it to both, and each MMA issuer frees a B slot
+// in both CTAs (the slot's "empty" barrier counts both), so L2 delivers B
+// once per pair.
 template <int BN, int EPI, int CL, bool HALO, bool ROW, bool BAND>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
