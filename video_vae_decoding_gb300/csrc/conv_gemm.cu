@@ -602,6 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tracked incrementally, and the abort flag is read once per tile (every
     // wait is bounded and raises the flag when it runs out).
     int it_slot = 0, it_phase = 0;  // stage ring (the B ring in band mode)
+    int kbc = 0;                    // row and halo modes: channel block within the tap
+    const int last_kb = args.taps[0].nkb - 1;
     int ia_slot = 0, ia_phase = 0;  // band mode: A ring
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step, ++lt) {
@@ -683,28 +685,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           // (the descriptor's base-offset field stays 0); and its own B block
           const uint64_t a0 = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
           const uint64_t b0 = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+          // a tap's last channel block may hold only tail_k16 x 16 channels
+          // (the rest is TMA zero fill): issue just those K steps
+          const bool tail = args.tail_k16 && kbc == last_kb;
+          if (++kbc > last_kb) kbc = 0;
+          if (tail && args.tail_k16 == 2) {
 #pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            const uint64_t ad = a0 + (uint64_t)((j * 128) >> 4);
-            const uint64_t bd = b0 + (uint64_t)((j * BN * kBlockK * 2) >> 4);
+            for (int j = 0; j < 3; ++j) {
+              const uint64_t ad = a0 + (uint64_t)((j * 128) >> 4);
+              const uint64_t bd = b0 + (uint64_t)((j * BN * kBlockK * 2) >> 4);
 #pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k)
-              umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || j > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 2; ++k)
+                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || j > 0 || k > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+              const uint64_t ad = a0 + (uint64_t)((j * 128) >> 4);
+              const uint64_t bd = b0 + (uint64_t)((j * BN * kBlockK * 2) >> 4);
+#pragma unroll
+              for (int k = 0; k < kBlockK / 16; ++k)
+                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || j > 0 || k > 0) ? 1u : 0u);
+            }
           }
         } else if constexpr (HALO) {
           // descriptors of the stage's first box and first B block; the taps
           // add constant byte offsets (>> 4) to the start-address field
           const uint64_t a0 = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
           const uint64_t b0 = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
+          // a time tap's last channel block may hold only tail_k16 x 16 channels
+          const bool tail = args.tail_k16 && kbc == last_kb;
+          if (++kbc > last_kb) kbc = 0;
+          if (tail && args.tail_k16 == 2) {
 #pragma unroll
-          for (int t9 = 0; t9 < 9; ++t9) {
-            const int dy = t9 / 3, dx = t9 % 3;
-            // rows of tap (dy, dx): box dx from image row dy on (16 rows per image row, 2 KB)
-            const uint64_t ad = a0 + (uint64_t)((dx * kHaloABox + dy * 16 * 128) >> 4);
-            const uint64_t bd = b0 + (uint64_t)((t9 * BN * 128) >> 4);
+            for (int t9 = 0; t9 < 9; ++t9) {
+              const int dy = t9 / 3, dx = t9 % 3;
+              const uint64_t ad = a0 + (uint64_t)((dx * kHaloABox + dy * 16 * 128) >> 4);
+              const uint64_t bd = b0 + (uint64_t)((t9 * BN * 128) >> 4);
 #pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k)
-              umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || t9 > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 2; ++k)
+                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || t9 > 0 || k > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+              const int dy = t9 / 3, dx = t9 % 3;
+              // rows of tap (dy, dx): box dx from image row dy on (16 rows per image row, 2 KB)
+              const uint64_t ad = a0 + (uint64_t)((dx * kHaloABox + dy * 16 * 128) >> 4);
+              const uint64_t bd = b0 + (uint64_t)((t9 * BN * 128) >> 4);
+#pragma unroll
+              for (int k = 0; k < kBlockK / 16; ++k)
+                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || t9 > 0 || k > 0) ? 1u : 0u);
+            }
           }
         } else {
           const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));

@@ -62,6 +62,7 @@ struct ConvArgs {
   // taps at row offsets 0, 1, 2, and the three taps' B blocks, which lie
   // row_bdk K columns apart.  Cluster pairs are adjacent rows (ty).
   int row;
+  int tail_k16;  // row / halo modes: K16 steps holding channels in each tap's last block (0: all 4)
   int row_bdk;  // row mode: K stride between dx taps; band mode: between dy taps
   // Band mode (bf16 3x3 spatial taps without a shortcut, N tile 256, 16 x 8
   // tiles): every tap (dt, dx) loads one 16 x 10 A box (rows from -1) into an

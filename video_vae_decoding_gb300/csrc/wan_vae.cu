@@ -760,6 +760,10 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   }
   A.n_taps = nt;
   A.row = row ? 1 : 0;
+  // the last 64-channel block of a tap with 96 (160, ...) input channels holds
+  // 32 of them: two K16 steps (the source's channel extent ends there, so the
+  // TMA fills the rest with zeros and those MMAs would add nothing)
+  A.tail_k16 = (row && !a0.lo && cw.Ci % 64 == 32 && a0.chans() == cw.Ci) ? 2 : 0;
   A.band = band ? 1 : 0;
   A.row_bdk = row ? cw.ci_pad : band ? cw.kw * cw.ci_pad : 0;
   A.box_w = row ? 128 : 16;
@@ -1135,6 +1139,7 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
       WAN_TRY(encode(&L.b, 3, co.w, dims, strides, box));
       L.args.halo = 1;
       L.args.total_kb = 3 * (co.ci_pad / 64);
+      L.args.tail_k16 = (co.Ci % 64 == 32) ? 2 : 0;  // e.g. 96 channels: the last block holds 32
     }
     L.epi = kEpiVideo;
     L.args.out = out;
