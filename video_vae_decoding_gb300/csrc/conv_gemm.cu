@@ -39,7 +39,7 @@ struct ConvCfg {
   // boxes (16 x 10 pixels, 20 KB) and one-tap B blocks in separate rings
   static constexpr int kStages =
       HALO ? 2
-           : BAND ? 5
+           : BAND ? (BN >= 256 ? 5 : 6)
                   : ROW ? (BN <= 96 ? 4 : (BN <= 128 ? 3 : 2))
                         : (BN >= 256 ? 4 : (BN > 128 ? 5 : (BN == 128 ? 6 : (BN > 64 ? 7 : 8))));
   static constexpr int kAStages = BAND ? 3 : kStages;  // A slots (the B ring has kStages)
@@ -829,8 +829,10 @@ int conv_b_box_rows(int bn) { return conv_clustered(bn) ? bn / 2 : bn; }
 
 cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
   if (L.args.band) {
-    if (L.epi != kEpiStore || L.args.halo || L.args.subpix || L.args.row || L.bn != 256) return cudaErrorInvalidValue;
-    return launch_t<256, kEpiStore, 2, false, false, true>(L, stream);
+    if (L.epi != kEpiStore || L.args.halo || L.args.subpix || L.args.row) return cudaErrorInvalidValue;
+    if (L.bn == 256) return launch_t<256, kEpiStore, 2, false, false, true>(L, stream);
+    if (L.bn == 192) return launch_t<192, kEpiStore, 2, false, false, true>(L, stream);
+    return cudaErrorInvalidValue;
   }
   if (L.args.row) {
     if (L.epi != kEpiStore || L.args.halo || L.args.subpix) return cudaErrorInvalidValue;

@@ -708,10 +708,11 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   // row mode (narrow N, 3x3 spatial taps, one source): 128-pixel row tiles,
   // one 130-pixel A box per (dt, dy) serving its three dx taps
   const bool row = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
-                   (cw.bn == 96 || cw.bn == 128 || cw.bn == 192);
+                   (cw.bn == 96 || cw.bn == 128);
   // band mode (256-wide 3x3 convs, one source): a 16 x 10 A box per (dt, dx)
   // serving its three dy taps
-  const bool band = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 && cw.bn == 256;
+  const bool band = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
+                    (cw.bn == 192 || cw.bn == 256);
   if (band) {
     WAN_TRY(act_map(&L.a0, a0, 16, kHaloBoxRows));
     L.a1 = L.a0;
