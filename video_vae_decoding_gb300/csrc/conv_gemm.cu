@@ -229,7 +229,6 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
           store16(op, args.out_f32, v, args.out_lo);
         }
       } else {
-#pragma unroll
         float g[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {

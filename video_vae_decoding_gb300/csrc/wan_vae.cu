@@ -186,11 +186,12 @@ struct Prof {
 // A memory-bound launch, timed when profiling, with its algorithmic bytes.
 #define ELT(prof, kind, bytes, expr)                                   \
   do {                                                                 \
+    Prof* p_ = (prof);                                                 \
     cudaEvent_t e1_ = nullptr;                                         \
-    if (prof) WAN_TRY((prof)->begin((kind), (double)(bytes), s, &e1_)); \
+    if (p_) WAN_TRY(p_->begin((kind), (double)(bytes), s, &e1_));      \
     CUDA_TRY(expr);                                                    \
     if (e1_) CUDA_TRY(cudaEventRecord(e1_, s));                        \
-    if (prof) (prof)->launches++;                                      \
+    if (p_) p_->launches++;                                            \
   } while (0)
 
 // ------------------------------------------------------------ packed convs
@@ -572,7 +573,7 @@ static wan_status make_act(wan_vae_stream* st, Act& a, int F, int H, int W, int 
     st->ws_used = rup(st->ws_used, 256) + a.bytes();
     return WAN_OK;
   }
-  void* p;
+  void* p = nullptr;
   WAN_TRY(ws_take(st, a.bytes(), &p));
   a.p = (bf16*)p;
   return WAN_OK;
