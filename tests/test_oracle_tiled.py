@@ -138,3 +138,17 @@ def test_tile_arguments_are_checked(tiny):
     for tile, stride in [((40, 32), (16, 16)), ((32, 32), (48, 16)), ((32, 32), (0, 16))]:
         with pytest.raises(ValueError):
             oracle.decode_tiled(z, tiny, tile=tile, stride=stride)
+
+
+def test_wan21_tiles_use_eight_pixels_per_latent():
+    # Wan2.1 decodes 8 pixels per latent: 16-pixel tiles are 2 latents; one
+    # covering tile is the untiled decode, non-overlapping tiles are
+    # independent block decodes
+    w = wan_synth.make_weights(base=16, seed=0, variant="wan21")
+    z = wan_synth.make_latents((1, 16, 2, 4, 4), seed=3)
+    ref = oracle.decode(z, w)
+    assert ref.shape[-2:] == (32, 32)
+    np.testing.assert_array_equal(oracle.decode_tiled(z, w, tile=(32, 32), stride=(32, 32)), ref)
+    out = oracle.decode_tiled(z, w, tile=(16, 32), stride=(16, 32))
+    for r0 in (0, 2):
+        np.testing.assert_array_equal(out[..., 8 * r0:8 * r0 + 16, :], oracle.decode(z[..., r0:r0 + 2, :], w))
