@@ -1,9 +1,21 @@
-"""GB300 (sm_103a) Wan2.2-TI2V-5B VAE decode.
+"""GB300 (sm_103a) Wan VAE decode: the Wan2.2-TI2V-5B decoder, and the Wan2.1
+decoder when given its weights.
 
 A thin Python binding over the C ABI of ``include/wan_vae.h``: it only
 marshals torch CUDA tensors (device memory, streams) into the library's
 calls.  Every step of the decode runs in the library's CUDA kernels; if the
 library is not built, calls raise instead of falling back to anything else.
+
+Typical use::
+
+    model = Model(weights, dtype=torch.bfloat16)   # packs the decoder once
+    stream = DecodeStream(model, B, h, w)           # causal caches + workspace
+    video = stream.decode_clip(z)                   # [B, 3, 4T-3, 16h, 16w]
+    stream.decode_chunk(z, t0, n, out, out_f0)      # or chunk by chunk
+    tiled = model.decode_tiled(z, tile=(256, 256), stride=(192, 192))
+    model.set_latent_stats(mean, std)               # de-normalise latents first
+
+``decode(z, weights, dtype)`` is the one-shot form.
 """
 
 from __future__ import annotations
