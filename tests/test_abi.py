@@ -33,6 +33,14 @@ def test_header_symbols_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_binding_declares_every_header_function():
+    # the ctypes table gives every declared entry point its argument and
+    # return types (an entry point without one would be called untyped)
+    from video_vae_decoding_gb300._lib import SIGNATURES
+    missing = [n for n in _declared() if n not in SIGNATURES]
+    assert not missing, missing
+
+
 def test_out_frames(lib):
     assert [lib.wan_vae_out_frames(t) for t in (0, 1, 2, 31, 21)] == [0, 1, 5, 121, 81]
 
