@@ -7,11 +7,13 @@ through the library's stream API (causal chunks of --chunk latent frames).
 Weights are seeded random init of the full-width TI2V-5B decoder, latents
 ~ N(0, 1); weight packing happens before the timed region.
 
-Prints one JSON line (rank 0).  With --gpus N under torchrun every rank
-decodes its own clip (independent samples; no collective on the data path:
-weak scaling); the timing barrier and the max over ranks use the process
-group.  `--impl reference` times the CPU oracle instead, on a bounded crop of
-the same workload, on this machine's host cores.
+Prints one JSON line.  The decode runs on one GPU: its conv kernels share
+weight tiles between the two CTAs of a cluster with multicast TMA loads,
+which this library issues only in one-GPU processes, so `--gpus N` with
+N > 1 (or a torchrun launch with WORLD_SIZE > 1) stops with an error before
+any GPU work.  `--impl reference` times the CPU oracle instead, on a bounded
+crop of the same workload, on this machine's host cores; under torchrun only
+rank 0 runs it.
 """
 
 from __future__ import annotations
@@ -54,20 +56,23 @@ def _peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def max_over_ranks(x: float, pg=None, device="cpu") -> float:
-    """The largest x over all ranks (the slowest rank's time); x itself on one rank."""
-    if pg is None:
-        return x
-    import torch
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    pg.all_reduce(t, op=pg.ReduceOp.MAX)
-    return float(t.item())
+def _sustained_peak_mhz():
+    """Median SM clock under load while the sustained bf16 peak was measured."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["clocks_under_load"]["sm_mhz_median"])
+    except Exception:
+        return None
 
 
-def weak_scaling_value(ms_per_step_max: float, world: int, frames_per_rank: int) -> float:
-    """Whole-job frames/s: every rank decodes its own clip each step; the
-    step takes as long as the slowest rank."""
-    return world * frames_per_rank / (ms_per_step_max / 1000.0)
+def clock_note(clocks):
+    """The sustained peak's clock next to this run's: a fraction above 1 of a
+    peak measured at a lower clock is a clock effect, not more work per cycle."""
+    ref = _sustained_peak_mhz()
+    run = clocks.get("sm_mhz") if clocks else None
+    if not ref or not run:
+        return None
+    return {"sustained_peak_sm_mhz": ref, "this_run_sm_mhz": run, "ratio": run / ref}
 
 
 def _dist():
@@ -75,6 +80,16 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+ONE_GPU_ONLY = ("the decode runs on one GPU: its conv kernels use cluster-multicast TMA loads, which this "
+                "library issues only in one-GPU processes")
+
+
+def check_one_gpu(gpus: int, world: int) -> None:
+    """Stops (before any CUDA call) unless this is a one-GPU, one-process run."""
+    if gpus != 1 or world != 1:
+        raise SystemExit(f"bench.py --gpus {gpus} (WORLD_SIZE {world}): {ONE_GPU_ONLY}")
 
 
 class ClockSampler:
@@ -310,6 +325,7 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    check_one_gpu(args.gpus, _dist()[0])
     if args.workload == "attention":
         return run_attention(args)
     if args.workload == "tiled":
@@ -330,16 +346,8 @@ def main():
         METRIC = f"decoded frames/s ({H_OUT}x{W_OUT}, bf16{', Wan2.1 VAE' if wan21 else ''})"
 
     import torch
-    ws, rank, local = _dist()
-    if ws != args.gpus:
-        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {ws}")
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    pg = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
 
     from video_vae_decoding_gb300 import build as _build
     _build.build()
@@ -352,7 +360,7 @@ def main():
     model = wv.Model(wdev, dtype=torch.bfloat16)
     torch.cuda.synchronize()
     del wdev
-    z_np = wan_synth.make_latents((B, Z, T, H_LAT, W_LAT), WORKLOAD["latent_seed"] + rank)
+    z_np = wan_synth.make_latents((B, Z, T, H_LAT, W_LAT), WORKLOAD["latent_seed"])
     z = torch.from_numpy(z_np).to(dev)
     st = wv.DecodeStream(model, B, H_LAT, W_LAT, max_chunk=args.chunk)
     out = torch.empty((B, 3, FRAMES, H_OUT, W_OUT), device=dev, dtype=torch.bfloat16)
@@ -364,8 +372,6 @@ def main():
     sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
 
     # ---- timed region: K clips, device-resident inputs
-    if pg:
-        pg.barrier()
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
@@ -379,11 +385,9 @@ def main():
     torch.cuda.synchronize()
     prof = st.profile_end()
     clocks = sampler.stop()
-    if pg:
-        pg.barrier()
     st.sync_status()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, dev)
-    value = weak_scaling_value(ms, ws, B * FRAMES)
+    ms = e0.elapsed_time(e1) / args.steps
+    value = B * FRAMES / (ms / 1000.0)
     burst, sustained, hbm, peak_src = _peaks()
     flops_step = prof["tc_flops"] / args.steps
     # dominant kernel: conv_gemm_kernel on the causal 3x3x3 convs (conv_in and
@@ -397,70 +401,72 @@ def main():
         z_host = torch.from_numpy(z_np).pin_memory()
         v_host = torch.empty((B, 3, FRAMES, H_OUT, W_OUT), dtype=torch.bfloat16).pin_memory()
         st.decode_clip_host(z_host, v_host)
-        if pg:
-            pg.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             st.decode_clip_host(z_host, v_host)
-        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, pg, dev)
-        e2e = {"value": weak_scaling_value(1000.0 * e2e_s, ws, B * FRAMES), "unit": UNIT,
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        e2e = {"value": B * FRAMES / e2e_s, "unit": UNIT,
                "h2d_bytes_per_step": z_host.numel() * z_host.element_size(),
                "d2h_bytes_per_step": v_host.numel() * v_host.element_size()}
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not custom and not wan21:
+    if not args.no_cpu_baseline and not custom and not wan21:
         dt, fe, desc = cpu_oracle_sample(z_np)
         cpu = {"value": fe / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": desc}
 
-    if rank == 0:
-        kinds = {}
-        for k, v in prof["kinds"].items():
-            row = {"ms_per_step": v["ms"] / args.steps, "launches_per_step": v["launches"] / args.steps}
-            if "flops" in v:
-                row["tflops"] = v["flops"] / (v["ms"] / 1000.0) / 1e12 if v["ms"] > 0 else None
-            else:
-                row["gbs"] = v["bytes"] / (v["ms"] / 1000.0) / 1e9 if v["ms"] > 0 else None
-                row["frac_of_hbm"] = row["gbs"] / hbm if row["gbs"] else None
-            kinds[k] = row
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16",
-            "data": (f"synthetic: seeded random-init {'Wan2.1' if wan21 else 'TI2V-5B'} decoder weights, "
-                     "N(0,1) latents"),
-            "config": {"workload": (f"latents [{B},48,{T},{H_LAT},{W_LAT}] -> video [{B},3,{FRAMES},{H_OUT},{W_OUT}] bf16"
-                                    if custom or wan21 else
-                                    "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280] bf16"),
-                       "chunk_latent_frames": args.chunk, "batch_per_gpu": B,
-                       "l2": "working set larger than L2 (1.1 GB packed weights; GB-scale activations per chunk)"},
-            "mpix_per_s": value * H_OUT * W_OUT / 1e6,
-            "nominal_tflop_per_step": flops_step / 1e12,
-            "tflops_nominal": flops_step / (ms / 1000.0) / 1e12,
-            "frac_of_bf16_peak": {"burst": flops_step / (ms / 1000.0) / 1e12 / burst,
-                                  "sustained": flops_step / (ms / 1000.0) / 1e12 / sustained, "source": peak_src},
-            "roofline": {"bound": "tensor",
-                         "kernel": "conv_gemm_kernel<256, store, pairs, band>: causal 3x3x3 convs (implicit GEMM, tcgen05)",
-                         "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
-                         "frac": achieved / sustained, "peak_kind": f"bf16 sustained ({peak_src})",
-                         "launches_per_step": dom["launches"] / args.steps,
-                         "flop_per_step": dom["flops"] / args.steps,
-                         # DRAM bytes of one level-D 256->256 launch of 4 output frames from the
-                         # ncu capture in profiles/ (algorithmic bytes of that launch: 1.156e9)
-                         "traffic": None if wan21 else 1.124e9,
-                         "traffic_case": None if wan21 else "level-D 256->256 causal conv, 4 frames"},
-            "tensor_core_tflops": prof["tc_flops"] / (prof["tc_ms"] / 1000.0) / 1e12 if prof["tc_ms"] > 0 else None,
-            "tensor_core_ms_per_step": prof["tc_ms"] / args.steps,
-            "by_kind": kinds,
-            "gpu_launches": prof["launches"],
-            "workspace_gb": st.workspace_bytes / 1e9,
-            "clocks": clocks,
-            "e2e": e2e,
-            "cpu_baseline": cpu,
-        }
-        print(json.dumps(line))
-    if pg:
-        pg.destroy_process_group()
+    kinds = {}
+    for k, v in prof["kinds"].items():
+        row = {"ms_per_step": v["ms"] / args.steps, "launches_per_step": v["launches"] / args.steps}
+        if "flops" in v:
+            row["tflops"] = v["flops"] / (v["ms"] / 1000.0) / 1e12 if v["ms"] > 0 else None
+            # executed: the sub-pixel upsample runs 4/9 of its nominal FLOPs
+            row["tflops_executed"] = v["exec_flops"] / (v["ms"] / 1000.0) / 1e12 if v["ms"] > 0 else None
+            row["frac_of_sustained_executed"] = (row["tflops_executed"] / sustained
+                                                 if row["tflops_executed"] else None)
+        else:
+            row["gbs"] = v["bytes"] / (v["ms"] / 1000.0) / 1e9 if v["ms"] > 0 else None
+            row["frac_of_hbm"] = row["gbs"] / hbm if row["gbs"] else None
+        kinds[k] = row
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": (f"synthetic: seeded random-init {'Wan2.1' if wan21 else 'TI2V-5B'} decoder weights, "
+                 "N(0,1) latents"),
+        "config": {"workload": (f"latents [{B},48,{T},{H_LAT},{W_LAT}] -> video [{B},3,{FRAMES},{H_OUT},{W_OUT}] bf16"
+                                if custom or wan21 else
+                                "720p: latents [1,48,31,44,80] -> video [1,3,121,704,1280] bf16"),
+                   "chunk_latent_frames": args.chunk, "batch_per_gpu": B,
+                   "l2": "working set larger than L2 (1.1 GB packed weights; GB-scale activations per chunk)"},
+        "mpix_per_s": value * H_OUT * W_OUT / 1e6,
+        "nominal_tflop_per_step": flops_step / 1e12,
+        "executed_tflop_per_step": prof["tc_exec_flops"] / args.steps / 1e12,
+        "tflops_nominal": flops_step / (ms / 1000.0) / 1e12,
+        "frac_of_bf16_peak": {"burst": flops_step / (ms / 1000.0) / 1e12 / burst,
+                              "sustained": flops_step / (ms / 1000.0) / 1e12 / sustained, "source": peak_src},
+        "roofline": {"bound": "tensor",
+                     "kernel": "conv_gemm_kernel<256, store, pairs, band>: causal 3x3x3 convs (implicit GEMM, tcgen05)",
+                     "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
+                     "frac": achieved / sustained, "peak_kind": f"bf16 sustained ({peak_src})",
+                     "frac_of_burst": achieved / burst,
+                     "clock_note": clock_note(clocks),
+                     "launches_per_step": dom["launches"] / args.steps,
+                     "flop_per_step": dom["flops"] / args.steps,
+                     # DRAM bytes of one level-D 256->256 launch of 4 output frames from the
+                     # ncu capture in profiles/ (algorithmic bytes of that launch: 1.156e9)
+                     "traffic": None if wan21 else 1.124e9,
+                     "traffic_case": None if wan21 else "level-D 256->256 causal conv, 4 frames"},
+        "tensor_core_tflops": prof["tc_flops"] / (prof["tc_ms"] / 1000.0) / 1e12 if prof["tc_ms"] > 0 else None,
+        "tensor_core_ms_per_step": prof["tc_ms"] / args.steps,
+        "by_kind": kinds,
+        "gpu_launches": prof["launches"],
+        "workspace_gb": st.workspace_bytes / 1e9,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
     return 0
 
 

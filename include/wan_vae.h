@@ -178,15 +178,20 @@ wan_status wan_vae_stream_load(wan_vae_stream* st, const void* src, int64_t byte
  * kind index: 0 causal 3x3x3 convs (conv_in, residual blocks), 1 time convs,
  * 2 upsample2d convs (+DupUp3D), 3 attention GEMMs, 4 conv_out,
  * 5 RMS norm (+SiLU), 6 other memory-bound kernels (post_quant_conv, softmax,
- * transposes, frame copies, the cache ring shift). */
+ * transposes, frame copies, the cache ring shift).  Executed FLOPs count
+ * the arithmetic the kernels run: equal to nominal except for the upsample2d
+ * convs, which run in sub-pixel form (four 2x2 phase convs at the low
+ * resolution: 4/9 of the nominal 3x3 conv at the high resolution). */
 typedef struct {
   int64_t launches;          /* all kernel launches enqueued */
   int64_t tc_launches;       /* tensor-core launches among them */
   double tc_ms;              /* their summed device time */
   double tc_flops;           /* their nominal FLOPs */
   double kind_ms[7];
-  double kind_work[7];       /* FLOPs (kinds 0-4) or bytes (kinds 5-6) */
+  double kind_work[7];       /* nominal FLOPs (kinds 0-4) or bytes (kinds 5-6) */
   int64_t kind_launches[7];
+  double tc_exec_flops;      /* executed FLOPs of the tensor-core launches */
+  double kind_exec[7];       /* executed FLOPs (kinds 0-4; equal to kind_work for 5-6) */
 } wan_vae_profile;
 wan_status wan_vae_stream_profile_begin(wan_vae_stream* st);
 wan_status wan_vae_stream_profile_end(wan_vae_stream* st, wan_cuda_stream stream, wan_vae_profile* out);
@@ -302,12 +307,14 @@ wan_status wan_selftest_wait_timeout(int32_t cout, int32_t* device_code, wan_cud
  * slots, an error word) lives in one fixed 32 MiB device array inside the
  * library, which every GPU that loads the library holds until the process
  * exits; a conv whose scratch exceeds 32 MiB is rejected with
- * WAN_ERR_UNSUPPORTED before any work is enqueued.  The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress, with
- * that device current); make that first call before any stream capture.
- * All calls share the array: each call clears the parts that must start at
- * zero, and calls whose work overlaps on the GPU (different streams, or
- * devices sharing one context) race on it -- serialise them. */
+ * WAN_ERR_UNSUPPORTED before any work is enqueued.  The first call in a
+ * CUDA context (per device, and again after a cudaDeviceReset) looks up the
+ * array's device address with cudaGetSymbolAddress while that context is
+ * current; make that first call before any stream capture.  All calls in one
+ * context share that device's array: each call clears the parts that must
+ * start at zero, and calls whose work overlaps on the same device (different
+ * streams, or different host threads) race on it -- serialise them.  Calls on
+ * different devices use different copies of the array and do not race. */
 wan_status wan_causal_conv3d_noalloc(const void* x, int32_t B, int32_t n_hist, int32_t F, int32_t H, int32_t W,
                                      int32_t Cin, const void* weight, const void* bias, int32_t w_dtype,
                                      int32_t Cout, int32_t kt, int32_t kh, int32_t kw, void* out,

@@ -17,3 +17,16 @@ def pytest_configure(config):
 def tiny_weights():
     import wan_synth
     return wan_synth.make_weights(base=16, seed=0)
+
+
+def pytest_collection_finish(session):
+    """Starts the background oracle runs of the full-size parity tests as soon
+    as one of them is selected, so they overlap the other GPU tests."""
+    if any("test_gpu_fullsize.py" in item.nodeid for item in session.items):
+        from tests import oracle_jobs
+        oracle_jobs.start()
+
+
+def pytest_sessionfinish(session, exitstatus):
+    from tests import oracle_jobs
+    oracle_jobs.shutdown()

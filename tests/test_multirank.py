@@ -1,15 +1,17 @@
-"""The benchmark's multi-rank logic on CPU: two gloo ranks on 127.0.0.1.
+"""The benchmark's process handling on CPU.
 
-Each rank decodes its own clip (no exchange on the data path); the step time
-is the slowest rank's and the value is the whole job's frames/s.  The
-reference arm runs on rank 0 only.
+The decode runs on one GPU only (its conv kernels share weight tiles inside a
+CTA cluster with multicast TMA loads, issued only in one-GPU processes), so a
+multi-GPU launch of the decode stops before any CUDA call; the reference arm
+(the CPU oracle) runs on rank 0 alone when launched under torchrun, which is
+checked here with two gloo ranks on 127.0.0.1.
 """
 
 import os
 import socket
+import sys
 
 import pytest
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
@@ -25,28 +27,39 @@ def _rank_main(rank, world, port, out):
     import bench
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        ms = bench.max_over_ranks(100.0 + 50.0 * rank, dist, "cpu")
-        value = bench.weak_scaling_value(ms, world, 121)
-        out[rank] = (ms, value)
+        # the decode arm refuses a multi-process launch on every rank
+        try:
+            bench.check_one_gpu(world, world)
+            out[f"refused{rank}"] = False
+        except SystemExit as e:
+            out[f"refused{rank}"] = "one GPU" in str(e)
         dist.barrier()
     finally:
         dist.destroy_process_group()
 
 
-def test_two_ranks_max_time_and_weak_scaling():
+def test_two_ranks_both_refuse_the_decode():
     world = 2
     out = mp.Manager().dict()
     mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
-    for r in range(world):
-        ms, value = out[r]
-        assert ms == 150.0
-        assert value == pytest.approx(2 * 121 / 0.150)
+    assert out["refused0"] is True and out["refused1"] is True
 
 
-def test_single_rank_is_identity():
+def test_one_gpu_check():
     import bench
-    assert bench.max_over_ranks(12.5) == 12.5
-    assert bench.weak_scaling_value(1000.0, 1, 121) == pytest.approx(121.0)
+    bench.check_one_gpu(1, 1)
+    for gpus, world in ((2, 1), (1, 2), (8, 8)):
+        with pytest.raises(SystemExit):
+            bench.check_one_gpu(gpus, world)
+
+
+def test_bench_main_refuses_before_cuda(monkeypatch):
+    import bench
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "2"])
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert "one GPU" in str(e.value)
 
 
 def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):

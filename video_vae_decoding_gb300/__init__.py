@@ -187,12 +187,16 @@ class DecodeStream:
         time and nominal FLOPs of the tensor-core launches since profile_begin."""
         p = WanProfile()
         check(load().wan_vae_stream_profile_end(self._s, _stream(stream), ctypes.byref(p)))
-        return {
-            "launches": p.launches, "tc_launches": p.tc_launches, "tc_ms": p.tc_ms, "tc_flops": p.tc_flops,
-            "kinds": {k: {"ms": p.kind_ms[i], ("flops" if i < 5 else "bytes"): p.kind_work[i],
-                          "launches": p.kind_launches[i]}
-                      for i, k in enumerate(PROFILE_KINDS)},
-        }
+        kinds = {}
+        for i, k in enumerate(PROFILE_KINDS):
+            row = {"ms": p.kind_ms[i], "launches": p.kind_launches[i]}
+            if i < 5:
+                row["flops"], row["exec_flops"] = p.kind_work[i], p.kind_exec[i]
+            else:
+                row["bytes"] = p.kind_work[i]
+            kinds[k] = row
+        return {"launches": p.launches, "tc_launches": p.tc_launches, "tc_ms": p.tc_ms, "tc_flops": p.tc_flops,
+                "tc_exec_flops": p.tc_exec_flops, "kinds": kinds}
 
     def decode_chunk(self, z, t0, n, out, out_f0, preclamp=None, stream=None):
         p = 0 if preclamp is None else _dev(preclamp, "preclamp")

@@ -36,6 +36,8 @@ class WanProfile(ctypes.Structure):
         ("kind_ms", ctypes.c_double * 7),
         ("kind_work", ctypes.c_double * 7),
         ("kind_launches", ctypes.c_int64 * 7),
+        ("tc_exec_flops", ctypes.c_double),
+        ("kind_exec", ctypes.c_double * 7),
     ]
 
 

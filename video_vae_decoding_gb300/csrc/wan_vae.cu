@@ -159,16 +159,22 @@ enum LaunchKind {
   kKindMisc = 6,
   kNumKinds = 7
 };
+struct ProfRec {
+  int kind;
+  double work;  // nominal FLOPs (tensor-core kinds) or algorithmic bytes
+  double exec;  // FLOPs of the arithmetic the kernels actually run (sub-pixel form: 4/9 of nominal)
+};
 struct Prof {
   bool on = false;
-  long long launches = 0;                  // every kernel launch enqueued
-  std::vector<cudaEvent_t> ev;             // start/end pairs of timed launches
-  std::vector<std::pair<int, double>> rec; // (kind, nominal FLOPs or bytes) per timed launch
+  long long launches = 0;     // every kernel launch enqueued
+  std::vector<cudaEvent_t> ev;  // start/end pairs of timed launches
+  std::vector<ProfRec> rec;     // one per timed launch
   ~Prof() {
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
   }
-  // Events of the next timed launch (null when not profiling).
-  wan_status begin(int kind, double work, cudaStream_t s, cudaEvent_t* e1) {
+  // Events of the next timed launch (null when not profiling); exec < 0
+  // means "as nominal".
+  wan_status begin(int kind, double work, cudaStream_t s, cudaEvent_t* e1, double exec = -1.0) {
     *e1 = nullptr;
     if (!on) return WAN_OK;
     const size_t i = rec.size();
@@ -177,7 +183,7 @@ struct Prof {
       CUDA_TRY(cudaEventCreate(&e));
       ev.push_back(e);
     }
-    rec.push_back({kind, work});
+    rec.push_back({kind, work, exec < 0 ? work : exec});
     *e1 = ev[2 * i + 1];
     CUDA_TRY(cudaEventRecord(ev[2 * i], s));
     return WAN_OK;
@@ -801,11 +807,12 @@ static void set_out(ConvArgs& A, const OutSpec& o) {
 // Enqueues a tensor-core launch; when profiling, brackets it with CUDA events
 // on the same stream and records its nominal FLOPs (2 * M * N * K with the
 // zero-padded taps included).
-static wan_status run(ConvLaunch& L, Prof* prof, int kind, double flops, int* err, cudaStream_t s) {
+static wan_status run(ConvLaunch& L, Prof* prof, int kind, double flops, int* err, cudaStream_t s,
+                      double exec_flops = -1.0) {
   L.args.err = err;
   if (L.args.N % 16 && L.epi != kEpiVideo) return fail(WAN_ERR_INTERNAL, "conv output channels not a multiple of 16");
   cudaEvent_t e1 = nullptr;
-  if (prof) WAN_TRY(prof->begin(kind, flops, s, &e1));
+  if (prof) WAN_TRY(prof->begin(kind, flops, s, &e1, exec_flops));
   CUDA_TRY(launch_conv(L, s));
   if (e1) CUDA_TRY(cudaEventRecord(e1, s));
   if (prof) prof->launches++;
@@ -1037,9 +1044,11 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
   if (!cw.subpix || y.H != 2 * x.H || y.W != 2 * x.W) return fail(WAN_ERR_INTERNAL, "resample shapes");
   WAN_TRY(conv_setup(cw, x, 0, nullptr, 0, F, L));
   set_out(L.args, out_of(y));
-  // nominal FLOPs: the 3x3 conv at the upsampled resolution (4/9 of it is executed)
+  // nominal FLOPs: the 3x3 conv at the upsampled resolution; executed: the
+  // four phases' 2x2 convs at the low resolution (4/9 of nominal)
   const double nominal = 2.0 * x.B * F * 4.0 * x.H * x.W * cw.Co * 9.0 * cw.Ci;
-  if (st->m->wan21) return run(L, &st->prof, kKindResample, nominal, st->err_dev, s);
+  const double executed = 2.0 * x.B * F * 4.0 * x.H * x.W * cw.Co * 4.0 * cw.Ci;
+  if (st->m->wan21) return run(L, &st->prof, kKindResample, nominal, st->err_dev, s, executed);
   L.epi = kEpiDup;
   L.args.dup = blk.p;
   L.args.dup_bs = blk.bs();
@@ -1058,7 +1067,7 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
     L.args.dup_pairs = 1;
   else
     return fail(WAN_ERR_UNSUPPORTED, "DupUp3D with %d -> %d channels, ft %d", blk.C, cw.Co, ft);
-  return run(L, &st->prof, kKindResample, nominal, st->err_dev, s);
+  return run(L, &st->prof, kKindResample, nominal, st->err_dev, s, executed);
 }
 
 // The three residual blocks of an up block: R[0] -> R[1] -> R[2] -> R[1]
@@ -1598,15 +1607,17 @@ wan_status wan_vae_stream_profile_end(wan_vae_stream* st, wan_cuda_stream stream
       for (size_t i = 0; i < p.rec.size(); ++i) {
         float ms = 0.f;
         CUDA_TRY(cudaEventElapsedTime(&ms, p.ev[2 * i], p.ev[2 * i + 1]));
-        const int k = p.rec[i].first;
+        const int k = p.rec[i].kind;
         if (k < kKindNorm) {
           r.tc_ms += ms;
-          r.tc_flops += p.rec[i].second;
+          r.tc_flops += p.rec[i].work;
+          r.tc_exec_flops += p.rec[i].exec;
           r.tc_launches += 1;
         }
         if (k >= 0 && k < kNumKinds) {
           r.kind_ms[k] += ms;
-          r.kind_work[k] += p.rec[i].second;
+          r.kind_work[k] += p.rec[i].work;
+          r.kind_exec[k] += p.rec[i].exec;
           r.kind_launches[k] += 1;
         }
       }
@@ -1990,26 +2001,58 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kNoAllocMaxDevices = 64;
+// Device address of the scratch array, cached per CUDA context.  In host
+// code the array's name is only a stand-in: the address is looked up with
+// cudaGetSymbolAddress while the calling thread's context is current, once
+// per context.  Contexts are told apart by cuCtxGetId, whose ids are never
+// reused within a process, so a context created after a cudaDeviceReset (or
+// another context made current on the same device) gets its own lookup.
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+constexpr size_t kNoAllocMaxContexts = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+std::vector<std::pair<unsigned long long, void*>> g_noalloc_addr;  // (context id, address)
 
-// Device address of the scratch array on the current device.  The array's
-// name is only a host-side stand-in, so the address is looked up once per
-// device, with that device current.
+bool current_context_id(unsigned long long* id) {
+  static PfnCtxGetCurrent get_current = nullptr;
+  static PfnCtxGetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = (PfnCtxGetCurrent)fn;
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = (PfnCtxGetId)fn;
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 wan_status noalloc_scratch(char** out) {
   int dev = -1;
   CUDA_TRY(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(WAN_ERR_UNSUPPORTED, "device index %d", dev);
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p)
-      return fail(WAN_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s", cudaGetErrorString(e));
-    g_noalloc_addr[dev] = p;
-  }
-  *out = static_cast<char*>(g_noalloc_addr[dev]);
+  unsigned long long id = 0;
+  if (current_context_id(&id))
+    for (const auto& e : g_noalloc_addr)
+      if (e.first == id) {
+        *out = static_cast<char*>(e.second);
+        return WAN_OK;
+      }
+  // set-up for this context (it also makes the device's primary context
+  // current if the thread had none)
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p)
+    return fail(WAN_ERR_CUDA, "cudaGetSymbolAddress of the scratch array on device %d failed: %s", dev,
+                cudaGetErrorString(e));
+  if (current_context_id(&id) && g_noalloc_addr.size() < kNoAllocMaxContexts) g_noalloc_addr.push_back({id, p});
+  *out = static_cast<char*>(p);
   return WAN_OK;
 }
 
@@ -2028,6 +2071,7 @@ extern "C" wan_status wan_causal_conv3d_noalloc(const void* x, int32_t B, int32_
       return fail(WAN_ERR_UNSUPPORTED, "Cin %% 8 and Cout %% 16 must be 0 (Cin=%d Cout=%d)", Cin, Cout);
     for (int k : {kt, kh, kw})
       if (k != 1 && k != 3) return fail(WAN_ERR_UNSUPPORTED, "kernel extents must be 1 or 3");
+    if (kt * kh * kw > kMaxTaps) return fail(WAN_ERR_UNSUPPORTED, "too many taps");
     cudaStream_t s = (cudaStream_t)stream;
     // scratch plan: packed weights | bias | input with history slots | error word
     ConvW cw;
