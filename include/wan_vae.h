@@ -285,6 +285,23 @@ wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F
                              const void* weight, const void* bias, int32_t w_dtype, int32_t Cout, int32_t kt,
                              int32_t kh, int32_t kw, void* out, wan_cuda_stream stream);
 
+/* The decoder's conv_out and what follows it (page section "What is
+ * computed", item 2: norm_out, SiLU, then a causal 3x3x3 conv to 3 colours x
+ * 2 x 2 patch channels; items 3-4: unpatchify and clamp), as the bf16 decode
+ * runs it: the kernel that folds the nine spatial taps into the GEMM's N.
+ * x [B][n_hist + F][H][W][Cin] bf16 channels-last (device), the conv's input
+ * (already normalised), its first n_hist (0..2) frames being history; zero
+ * padding 1 in space and zeros for the missing history frames.  weight
+ * [Cout, Cin, 3, 3, 3], bias [Cout] (w_dtype, rounded to bf16).  Cout 12:
+ * out [B][3][F][2H][2W], channel 4k + 2j + i -> colour k, row 2y + i, column
+ * 2x + j; Cout 3: out [B][3][F][H][W].  Values clamped to [-1, 1] in
+ * out_dtype; preclamp (optional, fp32, same shape) receives them before the
+ * clamp.  Cin: a multiple of 8 up to 1024.  Temporaries come from the
+ * stream-ordered allocator. */
+wan_status wan_conv_out_video(const void* x, int32_t B, int32_t n_hist, int32_t F, int32_t H, int32_t W, int32_t Cin,
+                              const void* weight, const void* bias, int32_t w_dtype, int32_t Cout, void* out,
+                              int32_t out_dtype, float* preclamp, wan_cuda_stream stream);
+
 /* Failure-detection self test (the pages have no counterpart: it exercises
  * this library's own bounded waits).  Runs one small causal conv (64 -> cout
  * channels: cout 64 for the one-CTA kernel, 256 for the two-CTA cluster

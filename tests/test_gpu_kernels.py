@@ -95,3 +95,43 @@ def test_attention_full_width_720p_frames(wv):
     """The isolated attention block at its full size: 8 frames of 44x80
     positions, C = 1024; frames 0 and 7 checked against the oracle."""
     _attention_check(wv, N=8, C=1024, H=44, W=80, frames=(0, 7), seed=2)
+
+
+# conv_out as the bf16 decode runs it (spatial taps folded into N, 16 x 16
+# input boxes with 14 x 14 outputs each): (B, n_hist, F, H, W, Cin, Cout).
+# 256 -> 12 with the 2 x 2 unpatchify (TI2V-5B) and 96 -> 3 (Wan2.1, a 64-channel
+# block holding 32); ragged boxes at both edges, history 0/1/2, a frame
+# smaller than one box, exactly one box, and 16 input channels (one block of
+# which 48 channels are TMA zero fill).
+VIDEO_CASES = [
+    (1, 2, 2, 17, 33, 256, 12),
+    (2, 0, 1, 30, 29, 256, 12),
+    (1, 1, 3, 8, 16, 256, 12),
+    (1, 2, 2, 1, 5, 256, 12),
+    (1, 2, 2, 45, 20, 96, 3),
+    (1, 0, 1, 14, 14, 16, 12),
+]
+
+
+@pytest.mark.parametrize("case", VIDEO_CASES, ids=lambda c: "B{}h{}F{}_{}x{}_{}to{}".format(*c))
+def test_conv_out_video_vs_oracle(wv, case):
+    B, nh, F, H, W, Cin, Cout = case
+    x = _bf(RNG.standard_normal((B, nh + F, H, W, Cin)))
+    w = _bf(RNG.uniform(-1, 1, (Cout, Cin, 3, 3, 3)) / math.sqrt(Cin * 27) * 4.0)
+    b = _bf(RNG.uniform(-0.1, 0.1, Cout))
+    got, pre = wv.conv_out_video(to_dev(x, torch.bfloat16), nh, to_dev(w), to_dev(b), preclamp=True)
+    torch.cuda.synchronize()
+    got, pre = got.float().cpu().numpy(), pre.cpu().numpy()
+    xn = x.transpose(0, 4, 1, 2, 3)                      # NCDHW
+    conv = oracle.causal_conv(xn[:, :, nh:], w, b, xn[:, :, :nh] if nh else None)
+    ref_pre = oracle.unpatchify(conv) if Cout == 12 else conv
+    ref = np.clip(ref_pre, -1.0, 1.0)
+    assert pre.shape == ref_pre.shape and got.shape == ref.shape
+    # fp32 accumulation of exact bf16 products, in another order than the oracle's
+    err_pre = np.abs(pre - ref_pre)
+    assert err_pre.max() <= 1e-4 * np.abs(ref_pre).max(), float(err_pre.max())
+    # the clamped video is rounded to bf16
+    err = np.abs(got - ref)
+    assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-6), float(err.max())
+    record(f"conv_out video {H}x{W} {Cin}->{Cout} (bf16 in)", float(err.max()), None,
+           preclamp_max_abs=float(err_pre.max()))

@@ -258,6 +258,25 @@ def attention_block(x: torch.Tensor, weights: "dict[str, torch.Tensor]", H: int,
     return out
 
 
+def conv_out_video(x: torch.Tensor, n_hist: int, weight: torch.Tensor, bias: torch.Tensor, out_dtype=torch.bfloat16,
+                   preclamp: bool = False, stream=None):
+    """x [B, n_hist + F, H, W, Cin] bf16 channels-last -> the clamped video
+    [B, 3, F, 2H, 2W] (weight [12, Cin, 3, 3, 3]) or [B, 3, F, H, W] (weight
+    [3, Cin, 3, 3, 3]); with preclamp, also the fp32 values before the clamp."""
+    B, Ft, H, W, Cin = x.shape
+    Cout = weight.shape[0]
+    F = Ft - n_hist
+    p = 2 if Cout == 12 else 1
+    out = torch.empty((B, 3, F, p * H, p * W), device=x.device, dtype=out_dtype)
+    pre = torch.empty(out.shape, device=x.device, dtype=torch.float32) if preclamp else None
+    if weight.dtype != bias.dtype:
+        raise ValueError("weight and bias must share a dtype")
+    check(load().wan_conv_out_video(_dev(x, "x"), B, n_hist, F, H, W, Cin, _dev(weight, "weight"), _dev(bias, "bias"),
+                                    _code(weight.dtype), Cout, _dev(out, "out"), _code(out_dtype),
+                                    _dev(pre, "preclamp") if pre is not None else None, _stream(stream)))
+    return (out, pre) if preclamp else out
+
+
 def causal_conv3d(x: torch.Tensor, n_hist: int, weight: torch.Tensor, bias: torch.Tensor, stream=None):
     """x [B, n_hist + F, H, W, Cin] bf16 channels-last -> [B, F, H, W, Cout] bf16."""
     B, Ft, H, W, Cin = x.shape

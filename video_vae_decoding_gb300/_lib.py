@@ -76,6 +76,8 @@ SIGNATURES = {
     "wan_attention_block": (_i32, [_vp, _i32, _i32, _i32, _i32, ctypes.POINTER(WanTensor), _i32, _vp, _vp]),
     "wan_causal_conv3d": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                  _vp, _vp]),
+    "wan_conv_out_video": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _i32, _vp,
+                                  _vp]),
     "wan_selftest_wait_timeout": (_i32, [_i32, ctypes.POINTER(_i32), _vp]),
     "wan_causal_conv3d_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                          _i32, _vp, _vp]),

@@ -132,6 +132,42 @@ cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream);
 int conv_b_box_rows(int bn);
 
 // ---------------------------------------------------------------------------
+// conv_out with the spatial taps folded into N (conv_out.cu): a causal
+// 3x3x3 conv of a ring [B][F slots][H][W][ldc] (bf16) to COUT = 12 channels
+// (unpatchified 2 x 2, vid_patch 2) or 3 colours (vid_patch 1), clamped into
+// the NCDHW video.  One tile = a 16 x 16 box of input positions whose 14 x 14
+// interior it outputs.  B = tap-folded weights [N = video_conv_n(cout)][K =
+// 3 * ci_pad], row (3 dy + dx) * cout + co, column dt * ci_pad + ci.
+// ---------------------------------------------------------------------------
+struct VideoConvArgs {
+  int H, W;                       // frame size
+  int frames, batches;            // output frames, batch
+  int tiles_x, tiles_y;           // ceil(W / 14), ceil(H / 14)
+  int src_f0;                     // ring slot read by output frame 0 at time tap 0
+  int ci_pad, nkb;                // channels per time tap (64 nkb)
+  int tail_k16;                   // K16 steps holding channels in the last block (0: all 4)
+  int cout;                       // 12 or 3
+  const float* bias;              // fp32, cout values
+  void* out;                      // video [B][3][F][vid_patch H][vid_patch W]
+  int out_f32, out_f0, vid_patch;
+  long long vid_bs, vid_cs;       // batch and colour strides (elements)
+  float* preclamp;                // optional fp32 copy before the clamp
+  int* err;                       // device error word (kDev* codes)
+  long long wait_limit;           // bounded waits: SM clocks (0: about 2 s)
+  int stall_at1;                  // failure injection (0: none)
+};
+struct VideoConvLaunch {
+  CUtensorMap a, b;  // A box 64 x 16 x 16 x 1 x 1; B box 64 x N x 1
+  VideoConvArgs args;
+};
+int video_conv_n(int cout);
+cudaError_t launch_video_conv(const VideoConvLaunch& L, cudaStream_t stream);
+// src [Co][Ci][3][3][3] (fp32 or bf16) -> dst[(3 dy + dx) * Co + co][dt * ci_pad + ci] bf16
+// (rows past 9 Co and channels past Ci are left as they are).
+cudaError_t launch_pack_tapfold(const void* src, int src_f32, int Co, int Ci, int ci_pad, __nv_bfloat16* dst,
+                                cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // Memory-bound kernels (channels-last bf16 unless stated).
 // A "frame view" addresses element (b, f, p, c) of a tensor as
 //   base + b*bs + (f0 + f)*fs + p*ldc + c.

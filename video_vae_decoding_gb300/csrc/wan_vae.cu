@@ -372,6 +372,61 @@ static wan_status pack_subpix_conv(const WeightTable& wt, const std::string& nam
   return WAN_OK;
 }
 
+// conv_out packed for the tap-folded kernel: [n][3 * ci_pad] bf16, row
+// (3 dy + dx) * Co + co, column dt * ci_pad + ci (zero elsewhere).
+struct TapFoldW {
+  bf16* w = nullptr;
+  int n = 0, ci_pad = 0, Co = 0, Ci = 0;
+};
+static wan_status pack_tapfold(const WeightTable& wt, const std::string& name, int Co, int Ci, TapFoldW& tf,
+                               DevMem& mem, cudaStream_t s) {
+  const wan_tensor* W;
+  WAN_TRY(get_tensor(wt, name + ".weight", &W));
+  WAN_TRY(check_shape(W, {Co, Ci, 3, 3, 3}));
+  if (mem.dry) return WAN_OK;
+  tf.Co = Co;
+  tf.Ci = Ci;
+  tf.ci_pad = (int)rup(Ci, 64);
+  tf.n = video_conv_n(Co);
+  const size_t bytes = (size_t)tf.n * 3 * tf.ci_pad * sizeof(bf16);
+  void* p;
+  WAN_TRY(mem.alloc(&p, bytes));
+  tf.w = (bf16*)p;
+  CUDA_TRY(cudaMemsetAsync(tf.w, 0, bytes, s));
+  CUDA_TRY(launch_pack_tapfold(W->data, W->dtype == WAN_F32, Co, Ci, tf.ci_pad, tf.w, s));
+  return WAN_OK;
+}
+
+// The tap-folded conv_out over F frames of `ring` (output frame f reads
+// slots f, f + 1, f + 2) into the video: 16 x 16 input boxes, 14 x 14
+// outputs each.
+static wan_status video_conv_setup(const TapFoldW& tf, const float* bias, const Act& ring, int F, int patch,
+                                   VideoConvLaunch& V) {
+  memset(&V, 0, sizeof(V));
+  if (ring.lo || ring.ldc < tf.ci_pad) return fail(WAN_ERR_INTERNAL, "tap-folded conv_out on a split or narrow ring");
+  WAN_TRY(act_map(&V.a, ring, 16, 16));
+  const uint64_t dims[3] = {(uint64_t)3 * tf.ci_pad, (uint64_t)tf.n, 1};
+  const uint64_t strides[2] = {(uint64_t)3 * tf.ci_pad * 2, (uint64_t)3 * tf.ci_pad * tf.n * 2};
+  const uint32_t box[3] = {64, (uint32_t)tf.n, 1};
+  WAN_TRY(encode(&V.b, 3, tf.w, dims, strides, box));
+  VideoConvArgs& a = V.args;
+  a.H = ring.H;
+  a.W = ring.W;
+  a.frames = F;
+  a.batches = ring.B;
+  a.tiles_x = (int)cdiv(ring.W, 14);
+  a.tiles_y = (int)cdiv(ring.H, 14);
+  a.src_f0 = 0;
+  a.ci_pad = tf.ci_pad;
+  a.nkb = tf.ci_pad / 64;
+  // the last 64-channel block of 96 (160, ...) channels holds 32 of them
+  a.tail_k16 = (tf.Ci % 64 == 32 && ring.chans() == tf.Ci) ? 2 : 0;
+  a.cout = tf.Co;
+  a.bias = bias;
+  a.vid_patch = patch;
+  return WAN_OK;
+}
+
 }  // namespace wan
 
 using namespace wan;
@@ -402,6 +457,7 @@ struct wan_vae_model {
   ConvW resample[3];
   float* out_g = nullptr;
   ConvW conv_out;
+  TapFoldW out_tf;  // conv_out with its spatial taps folded into N (bf16 decode)
   // latent de-normalisation in front of post_quant_conv: mean[48], std[48]
   float* zstat = nullptr;
   bool zstat_on = false;
@@ -492,6 +548,7 @@ static wan_status model_build(const wan_tensor* weights, int n, int dtype, cudaS
   WAN_TRY(pack_gamma(wt, "decoder.norm_out.gamma", b, &m->out_g, mem, s, sp));
   WAN_TRY(pack_conv(wt, "decoder.conv_out", 3 * m->patch * m->patch, b, 3, 3, 3, false, "", 0, m->conv_out, mem, s,
                     sp));
+  if (!sp) WAN_TRY(pack_tapfold(wt, "decoder.conv_out", 3 * m->patch * m->patch, b, m->out_tf, mem, s));
   if (!mem.dry) CUDA_TRY(cudaGetLastError());
   return WAN_OK;
 }
@@ -1135,7 +1192,24 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
         launch_rms_norm(st->RD[1].view(0), st->ringOut.view(2), m->out_g, m->base, st->B, FC,
                         st->RD[1].H * st->RD[1].W, true, s, st->RD[1].lo, st->ringOut.lo));
   }
-  {
+  if (m->out_tf.w) {
+    VideoConvLaunch V;
+    WAN_TRY(video_conv_setup(m->out_tf, m->conv_out.bias, st->ringOut, FC, m->patch, V));
+    VideoConvArgs& a = V.args;
+    a.out = out;
+    a.out_f32 = out_f32;
+    a.out_f0 = (int)out_f0;
+    a.preclamp = pre;
+    a.vid_cs = out_frames * (long long)(m->patch * m->patch) * st->ringOut.H * st->ringOut.W;
+    a.vid_bs = 3 * a.vid_cs;
+    a.err = st->err_dev;
+    cudaEvent_t e1 = nullptr;
+    WAN_TRY(st->prof.begin(kKindConvOut, conv_flops(m->conv_out, st->ringOut, FC), s, &e1));
+    CUDA_TRY(launch_video_conv(V, s));
+    if (e1) CUDA_TRY(cudaEventRecord(e1, s));
+    st->prof.launches++;
+    st->shifts.push_back(RingShift{st->ringOut.p, st->ringOut.fs(), st->ringOut.bs(), FC, st->B});
+  } else {
     ConvLaunch L;
     const ConvW& co = m->conv_out;
     WAN_TRY(conv_setup(co, st->ringOut, 0, nullptr, 0, FC, L));
@@ -1910,6 +1984,76 @@ wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F
       o.ldc = Cout;
       set_out(L.args, o);
       r = run(L, nullptr, 0, 0.0, err, s);
+    } while (false);
+    mem.release();
+    return r;
+  })
+}
+
+wan_status wan_conv_out_video(const void* x, int32_t B, int32_t n_hist, int32_t F, int32_t H, int32_t W, int32_t Cin,
+                              const void* weight, const void* bias, int32_t w_dtype, int32_t Cout, void* out,
+                              int32_t out_dtype, float* preclamp, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!x || !weight || !bias || !out) return fail(WAN_ERR_INVALID_ARG, "null argument");
+    WAN_TRY(dtype_ok(w_dtype, "weights"));
+    WAN_TRY(dtype_ok(out_dtype, "output"));
+    if (B < 1 || F < 1 || H < 1 || W < 1 || Cin < 8 || n_hist < 0 || n_hist > 2)
+      return fail(WAN_ERR_INVALID_ARG, "B=%d F=%d H=%d W=%d Cin=%d n_hist=%d", B, F, H, W, Cin, n_hist);
+    if (Cout != 12 && Cout != 3) return fail(WAN_ERR_UNSUPPORTED, "Cout must be 12 (2 x 2 patch) or 3, not %d", Cout);
+    if (Cin % 8 || Cin > 1024) return fail(WAN_ERR_UNSUPPORTED, "Cin must be a multiple of 8 up to 1024, not %d", Cin);
+    const int patch = Cout == 12 ? 2 : 1;
+    cudaStream_t s = (cudaStream_t)stream;
+    wan_tensor t[2] = {{"c.weight", weight, w_dtype, 5, {Cout, Cin, 3, 3, 3}}, {"c.bias", bias, w_dtype, 1, {Cout}}};
+    WeightTable wt{t, 2};
+    DevMem mem;
+    mem.use_async = true;
+    mem.async = s;
+    wan_status r = WAN_OK;
+    do {
+      TapFoldW tf;
+      if ((r = pack_tapfold(wt, "c", Cout, Cin, tf, mem, s)) != WAN_OK) break;
+      float* bf;
+      if ((r = mem.alloc((void**)&bf, 16 * sizeof(float))) != WAN_OK) break;
+      if (cudaMemsetAsync(bf, 0, 16 * sizeof(float), s) != cudaSuccess ||
+          launch_to_f32(bias, w_dtype == WAN_F32, nullptr, 0, bf, Cout, 1.0f, 1, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "bias conversion failed");
+        break;
+      }
+      // the input with two history slots in front, channels padded to 64
+      Act xr;
+      xr.B = B;
+      xr.F = 2 + F;
+      xr.H = H;
+      xr.W = W;
+      xr.C = Cin;
+      xr.ldc = (int)rup(Cin, 64);
+      void* p;
+      if ((r = mem.alloc(&p, xr.bytes())) != WAN_OK) break;
+      xr.p = (bf16*)p;
+      int* err;
+      if ((r = mem.alloc((void**)&err, 256)) != WAN_OK) break;
+      if (cudaMemsetAsync(xr.p, 0, xr.bytes(), s) != cudaSuccess || cudaMemsetAsync(err, 0, 256, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "memset failed");
+        break;
+      }
+      const long long fs_in = (long long)H * W * Cin;
+      FrameView vin{const_cast<void*>(x), (long long)(n_hist + F) * fs_in, fs_in, Cin, 0};
+      if (launch_copy_frames(vin, xr.view(2 - n_hist), Cin, B, n_hist + F, H * W, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "copy failed");
+        break;
+      }
+      VideoConvLaunch V;
+      if ((r = video_conv_setup(tf, bf, xr, F, patch, V)) != WAN_OK) break;
+      V.args.out = out;
+      V.args.out_f32 = out_dtype == WAN_F32;
+      V.args.preclamp = preclamp;
+      V.args.vid_cs = (long long)F * patch * patch * H * W;
+      V.args.vid_bs = 3 * V.args.vid_cs;
+      V.args.err = err;
+      if (launch_video_conv(V, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "conv_out launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+        break;
+      }
     } while (false);
     mem.release();
     return r;
