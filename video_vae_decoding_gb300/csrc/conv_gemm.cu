@@ -244,8 +244,9 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
           if (args.norm_silu) y = __fdividef(y, 1.0f + __expf(-y));
           v[i] = y;
         }
-        const long long oo =
-            (long long)b * args.out2_bs + (long long)(args.out2_f0 + f) * args.out2_fs + pos * args.out2_ldc + n0;
+        const long long oo = (long long)b * args.out2_bs +
+                             (long long)ring_slot(args.out2_f0 + f, args.out2_fmod) * args.out2_fs +
+                             pos * args.out2_ldc + n0;
         store16(static_cast<__nv_bfloat16*>(args.out2) + oo, 0, v, args.out2_lo);
       }
     }
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
             const uint32_t fb = smem_u32(&full[s]);
             mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
-            const int fr = args.src_f0[0] + tc.f + dt;
+            const int fr = ring_slot(args.src_f0[0] + tc.f + dt, args.src_fmod);
             for (int dx = 0; dx < 3; ++dx)
               tma_load_5d(smem_u32(sA + s * Cfg::kABytes + dx * kHaloABox), &mapA0, fb, kb * kBlockK,
                           tc.tx * args.box_w + dx - 1, tc.ty * args.box_h - 1, fr, tc.b);
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one per B slot
         for (int ti = 0; ti < args.n_taps && ok; ++ti) {
           const ConvTap tp = args.taps[ti];
-          const int fr = args.src_f0[0] + tc.f + tp.dt;
+          const int fr = ring_slot(args.src_f0[0] + tc.f + tp.dt, args.src_fmod);
           const int x0 = tc.tx * args.box_w + tp.dx, y0 = tc.ty * args.box_h - 1;
           for (int kb = 0; kb < tp.nkb && ok; ++kb) {
             const int sa = ia % SA;
@@ -524,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile start - 1) and the B blocks of its three dx taps
         for (int ti = 0; ti < args.n_taps && ok; ++ti) {
           const ConvTap tp = args.taps[ti];
-          const int fr = args.src_f0[0] + tc.f + tp.dt;
+          const int fr = ring_slot(args.src_f0[0] + tc.f + tp.dt, args.src_fmod);
           const int x0 = tc.tx * kTileM - 1, y0 = tc.ty + tp.dy;
           for (int kb = 0; kb < tp.nkb; ++kb, ++it) {
             const int s = it % S;
@@ -560,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ti = 0; ti < args.n_taps && ok; ++ti) {
         const ConvTap tp = args.taps[ti];
         const CUtensorMap* am = tp.src ? &mapA1 : &mapA0;
-        const int fr = args.src_f0[tp.src] + tc.f + tp.dt;
+        const int fr = tp.src ? args.src_f0[1] + tc.f + tp.dt : ring_slot(args.src_f0[0] + tc.f + tp.dt, args.src_fmod);
         const int x0 = tc.tx * args.box_w + tp.dx + sx;
         const int y0 = tc.ty * args.box_h + tp.dy + sy;
         for (int kb = 0; kb < tp.nkb; ++kb, ++it) {

@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(kVThreads, 1)
         if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, kVABytes + Cfg::kBBytes);
-        tma_load_5d(smem_u32(sA + s * kVABytes), &mapA, fb, kb * kBlockK, x0, y0, args.src_f0 + t.f + dt, t.b);
+        tma_load_5d(smem_u32(sA + s * kVABytes), &mapA, fb, kb * kBlockK, x0, y0,
+                    ring_slot(args.src_f0 + t.f + dt, args.src_fmod), t.b);
         tma_load_3d(smem_u32(sB + s * Cfg::kBBytes), &mapB, fb, dt * args.ci_pad + kb * kBlockK, 0, 0);
       }
     }

@@ -1,7 +1,8 @@
-// Memory-bound kernels of the decode: RMS norm (+SiLU), nearest x2 upsample,
-// frame copies, post_quant_conv, attention softmax and V transpose, the causal
-// cache ring shift, and weight packing.  All activations are channels-last
-// bf16; every access is a 16-byte vector of 8 channels where the layout allows.
+// Memory-bound kernels of the decode: RMS norm (+SiLU), frame copies,
+// post_quant_conv, attention softmax and V transpose, and weight packing.
+// All activations are channels-last bf16; every access is a 16-byte vector of
+// 8 channels where the layout allows.  Frame views may address circular
+// causal-cache rings (FrameView::fmod).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -10,10 +11,11 @@ namespace wan {
 namespace {
 
 __device__ __forceinline__ const __nv_bfloat16* at(const FrameView& v, int b, int f, long long p) {
-  return static_cast<const __nv_bfloat16*>(v.base) + b * v.bs + (long long)(v.f0 + f) * v.fs + p * v.ldc;
+  return static_cast<const __nv_bfloat16*>(v.base) + b * v.bs + (long long)ring_slot(v.f0 + f, v.fmod) * v.fs +
+         p * v.ldc;
 }
 __device__ __forceinline__ __nv_bfloat16* at_mut(const FrameView& v, int b, int f, long long p) {
-  return static_cast<__nv_bfloat16*>(v.base) + b * v.bs + (long long)(v.f0 + f) * v.fs + p * v.ldc;
+  return static_cast<__nv_bfloat16*>(v.base) + b * v.bs + (long long)ring_slot(v.f0 + f, v.fmod) * v.fs + p * v.ldc;
 }
 
 inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + per_block - 1) / per_block); }
@@ -234,27 +236,6 @@ __global__ void transpose_kernel(const __nv_bfloat16* __restrict__ src, long lon
   }
 }
 
-struct RingTable {
-  RingShift r[kMaxRings];
-};
-
-// slots (0, 1) <- slots (F, F + 1).  One thread owns one 8-channel vector at
-// the same offset in all four slots, so the overlapping F == 1 case (slot 1
-// is read and written) is race-free.
-__global__ void ring_shift_kernel(const __grid_constant__ RingTable t) {
-  const RingShift& R = t.r[blockIdx.y];
-  const long long n8 = R.frame_elems / 8;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8 * R.batches;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long b = i / n8, e = (i % n8) * 8;
-    __nv_bfloat16* base = R.base + b * R.batch_stride + e;
-    const uint4 a = *reinterpret_cast<const uint4*>(base + (long long)R.F * R.frame_elems);
-    const uint4 c = *reinterpret_cast<const uint4*>(base + (long long)(R.F + 1) * R.frame_elems);
-    *reinterpret_cast<uint4*>(base) = a;
-    *reinterpret_cast<uint4*>(base + R.frame_elems) = c;
-  }
-}
-
 __global__ void pack_weight_kernel(const void* __restrict__ src, int src_f32, int Co, int Ci, int taps,
                                    __nv_bfloat16* __restrict__ dst, int ld, int k0, int ci_pad, long long n, int lo) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -382,22 +363,6 @@ cudaError_t launch_transpose(const __nv_bfloat16* src, long long src_gs, int ld_
   dim3 grid((P + 31) / 32, (C + 31) / 32, G), block(32, 8);
   transpose_kernel<<<grid, block, 0, s>>>(src, src_gs, ld_src, dst, dst_gs, ld_dst, P, C);
   return cudaGetLastError();
-}
-
-cudaError_t launch_ring_shift(const RingShift* rings, int n, cudaStream_t s) {
-  for (int i0 = 0; i0 < n; i0 += kMaxRings) {
-    RingTable t{};
-    const int m = (n - i0) < kMaxRings ? (n - i0) : kMaxRings;
-    for (int i = 0; i < m; ++i) {
-      t.r[i] = rings[i0 + i];
-      if (t.r[i].frame_elems % 8) return cudaErrorInvalidValue;
-    }
-    dim3 grid(296, m);
-    ring_shift_kernel<<<grid, 256, 0, s>>>(t);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
 }
 
 cudaError_t launch_pack_weight(const void* src, int src_f32, int Co, int Ci, int taps, __nv_bfloat16* dst, int ld,

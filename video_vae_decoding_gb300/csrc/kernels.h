@@ -45,6 +45,7 @@ struct ConvArgs {
   int box_w, box_h;      // spatial tile, box_w * box_h == 128
   int H, W;              // output spatial size (equal to the A sources')
   int src_f0[2];         // frame coordinate of output frame 0 in each A source
+  int src_fmod;          // > 0: source 0 is a circular ring of src_fmod frame slots (ring_slot)
   int b_per_frame;       // 1: B's third coordinate is b * b_gstride + output frame (batched GEMMs)
   int b_gstride;
   // Sub-pixel form of nearest-x2 + 3x3 conv: the grid carries a phase
@@ -110,6 +111,7 @@ struct ConvArgs {
   void* out2;
   long long out2_bs, out2_fs;
   int out2_ldc, out2_f0, out2_lo;
+  int out2_fmod;         // > 0: out2 is a circular ring of out2_fmod frame slots
   int* err;              // device error word (kDev* codes)
   // Failure-detection self test: a bounded wait gives up after wait_limit
   // SM clocks (0: the default of about 2 s), and the TMA producer withholds
@@ -144,6 +146,7 @@ struct VideoConvArgs {
   int frames, batches;            // output frames, batch
   int tiles_x, tiles_y;           // ceil(W / 14), ceil(H / 14)
   int src_f0;                     // ring slot read by output frame 0 at time tap 0
+  int src_fmod;                   // ring slots (circular ring; 0: a plain tensor)
   int ci_pad, nkb;                // channels per time tap (64 nkb)
   int tail_k16;                   // K16 steps holding channels in the last block (0: all 4)
   int cout;                       // 12 or 3
@@ -172,11 +175,15 @@ cudaError_t launch_pack_tapfold(const void* src, int src_f32, int Co, int Ci, in
 // A "frame view" addresses element (b, f, p, c) of a tensor as
 //   base + b*bs + (f0 + f)*fs + p*ldc + c.
 // ---------------------------------------------------------------------------
+// With fmod > 0 the tensor is a circular ring of fmod frame slots: frame
+// f0 + f lives in slot (f0 + f) mod fmod (f0 < fmod, f < fmod).
 struct FrameView {
   void* base;
   long long bs, fs;
   int ldc, f0;
+  int fmod;
 };
+__host__ __device__ __forceinline__ int ring_slot(int f, int fmod) { return (fmod > 0 && f >= fmod) ? f - fmod : f; }
 
 // y = x / max(||x||, 1e-12) * gs (gs = sqrt(C)*gamma, fp32), then SiLU if silu.
 // in_lo / out_lo: split-format offsets of the low halves (0 = plain bf16).
@@ -199,16 +206,6 @@ cudaError_t launch_softmax_rows(const float* S, long long ld_s, __nv_bfloat16* P
 // Vt[g][c][p] = src[g][p][c] (bf16), p < P, c < C; src row stride ld_src.
 cudaError_t launch_transpose(const __nv_bfloat16* src, long long src_gs, int ld_src, __nv_bfloat16* dst,
                              long long dst_gs, int ld_dst, int G, int P, int C, cudaStream_t s);
-// Causal-cache shift: for each ring, slots (0, 1) <- slots (F, F + 1).
-struct RingShift {
-  __nv_bfloat16* base;
-  long long frame_elems;   // elements per frame slot
-  long long batch_stride;  // elements per batch item
-  int F;                   // current frames (slots 2 .. F+1)
-  int batches;
-};
-constexpr int kMaxRings = 48;
-cudaError_t launch_ring_shift(const RingShift* rings, int n, cudaStream_t s);
 // Weight packing: src [Co][Ci][taps] (fp32 or bf16, taps = kt*kh*kw) ->
 // dst[co][k0 + tap*ci_pad + ci] bf16 for co < Co, ci < Ci; dst has ld columns.
 // lo = 1 packs the low half bf16(w - bf16(w)) of the split format instead.

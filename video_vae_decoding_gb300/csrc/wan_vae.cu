@@ -87,15 +87,21 @@ static wan_status encode(CUtensorMap* m, int rank, const void* base, const uint6
 
 // Channels-last bf16 activation tensor [B][F][H][W][ldc]; channels C..ldc-1
 // hold zeros.  ldc is a multiple of 64 for tensors that feed the tensor cores.
+// A causal conv's ring is circular (fmod = F slots): its logical frame f
+// (0, 1 the history, 2.. the chunk's frames) lives in slot (base + f) mod F,
+// and after a chunk of n frames base advances by n, so the chunk's last two
+// frames become the next chunk's history without being copied.
 struct Act {
   bf16* p = nullptr;
   int B = 0, F = 0, H = 0, W = 0, C = 0, ldc = 0;
   int lo = 0;  // split format: low halves at channel offset lo (0: plain bf16)
+  int fmod = 0, base = 0;  // circular ring: F slots, logical frame 0 at slot `base`
   int chans() const { return lo ? ldc : C; }  // channels a copy must move
   long long fs() const { return (long long)H * W * ldc; }
   long long bs() const { return (long long)F * fs(); }
   size_t bytes() const { return (size_t)B * bs() * sizeof(bf16); }
-  FrameView view(int f0 = 0) const { return FrameView{p, bs(), fs(), ldc, f0}; }
+  int slot(int f) const { return fmod ? (base + f) % fmod : f; }  // physical slot of logical frame f
+  FrameView view(int f0 = 0) const { return FrameView{p, bs(), fs(), ldc, slot(f0), fmod}; }
 };
 
 // A-operand map over an activation tensor: dims (C, W, H, F, B), box
@@ -416,7 +422,8 @@ static wan_status video_conv_setup(const TapFoldW& tf, const float* bias, const 
   a.batches = ring.B;
   a.tiles_x = (int)cdiv(ring.W, 14);
   a.tiles_y = (int)cdiv(ring.H, 14);
-  a.src_f0 = 0;
+  a.src_f0 = ring.slot(0);
+  a.src_fmod = ring.fmod;
   a.ci_pad = tf.ci_pad;
   a.nkb = tf.ci_pad / 64;
   // the last 64-channel block of 96 (160, ...) channels holds 32 of them
@@ -601,7 +608,7 @@ struct wan_vae_stream {
   // level D (8h x 8w)
   Act RD[3], HD, ringD[6], ringOut;
   std::vector<Act*> rings;
-  std::vector<RingShift> shifts;
+  std::vector<std::pair<Act*, int>> advance;  // rings a chunk consumed, and its frames
   // decode_clip_host: double-buffered latent / video staging, a copy stream
   // and its events, created on first use and kept until destroy
   void* zb[2] = {nullptr, nullptr};
@@ -656,6 +663,8 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   st->rings.clear();
   auto ring = [&](Act& a, int F, int H, int W, int C) -> wan_status {
     WAN_TRY(make_act(st, a, 2 + F, H, W, C));
+    a.fmod = a.F;
+    a.base = 0;
     st->rings.push_back(&a);
     return WAN_OK;
   };
@@ -840,7 +849,8 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   A.tiles_n = cw.co_pad / cw.bn;
   A.frames = F;
   A.batches = a0.B;
-  A.src_f0[0] = a0_f0;
+  A.src_f0[0] = a0.slot(a0_f0);
+  A.src_fmod = a0.fmod;
   A.src_f0[1] = a1_f0;
   A.N = cw.Co;
   A.bias = cw.bias;
@@ -905,7 +915,8 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
     L.args.out2_bs = nrm->ring->bs();
     L.args.out2_fs = nrm->ring->fs();
     L.args.out2_ldc = nrm->ring->ldc;
-    L.args.out2_f0 = 2;
+    L.args.out2_f0 = nrm->ring->slot(2);
+    L.args.out2_fmod = nrm->ring->fmod;
     L.args.out2_lo = nrm->ring->lo;
   }
   if (res) {
@@ -916,7 +927,7 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
     L.args.res_lo = res->lo;
   }
   WAN_TRY(run(L, &st->prof, kind, conv_flops(cw, in, F), st->err_dev, s));
-  st->shifts.push_back(RingShift{in.p, in.fs(), in.bs(), F, in.B});
+  st->advance.push_back({&in, F});
   return WAN_OK;
 }
 
@@ -1159,7 +1170,7 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
   const bool first = st->first;
   const int FA = n, FB = first ? 2 * n - 1 : 2 * n, FC = first ? 4 * n - 3 : 4 * n;
   const int P = st->h * st->w;
-  st->shifts.clear();
+  st->advance.clear();
   // 1. post_quant_conv into conv_in's ring
   ELT(&st->prof, kKindMisc, (double)st->B * FA * P * (m->zdim * (z_f32 ? 4 : 2) + 2 * st->ringIn.ldc),
       launch_post_quant(z, z_f32, m->zdim, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b,
@@ -1208,7 +1219,7 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
     CUDA_TRY(launch_video_conv(V, s));
     if (e1) CUDA_TRY(cudaEventRecord(e1, s));
     st->prof.launches++;
-    st->shifts.push_back(RingShift{st->ringOut.p, st->ringOut.fs(), st->ringOut.bs(), FC, st->B});
+    st->advance.push_back({&st->ringOut, FC});
   } else {
     ConvLaunch L;
     const ConvW& co = m->conv_out;
@@ -1235,12 +1246,10 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
     L.args.vid_cs = out_frames * (long long)(m->patch * m->patch) * st->ringOut.H * st->ringOut.W;
     L.args.vid_bs = 3 * L.args.vid_cs;
     WAN_TRY(run(L, &st->prof, kKindConvOut, conv_flops(m->conv_out, st->ringOut, FC), st->err_dev, s));
-    st->shifts.push_back(RingShift{st->ringOut.p, st->ringOut.fs(), st->ringOut.bs(), FC, st->B});
+    st->advance.push_back({&st->ringOut, FC});
   }
-  // 3. the causal caches: each ring keeps the last two frames it convolved
-  double shift_bytes = 0;
-  for (const RingShift& r : st->shifts) shift_bytes += 8.0 * r.frame_elems * r.batches;  // 2 slots, read + write
-  ELT(&st->prof, kKindMisc, shift_bytes, launch_ring_shift(st->shifts.data(), (int)st->shifts.size(), s));
+  // 3. the causal caches: each ring's last two frames become its history
+  for (auto& r : st->advance) r.first->base = r.first->slot(r.second);
   st->first = false;
   if (st->err_host) {
     CUDA_TRY(cudaMemcpyAsync(st->err_host, st->err_dev, sizeof(int), cudaMemcpyDeviceToHost, s));
@@ -1337,8 +1346,10 @@ static wan_status decode_chunk_impl(wan_vae_stream* st, const void* z, int z_dty
 }
 
 static wan_status reset_impl(wan_vae_stream* st, cudaStream_t s) {
-  for (Act* r : st->rings)
+  for (Act* r : st->rings) {
+    r->base = 0;
     for (int b = 0; b < r->B; ++b) CUDA_TRY(cudaMemsetAsync(r->p + b * r->bs(), 0, 2 * r->fs() * sizeof(bf16), s));
+  }
   st->first = true;
   return WAN_OK;
 }
@@ -1623,12 +1634,15 @@ wan_status wan_vae_stream_save(wan_vae_stream* st, void* dst, int64_t bytes, wan
                    (int32_t)st->rings.size(), state_payload(st)};
     CUDA_TRY(cudaMemcpyAsync(dst, &hd, sizeof(hd), cudaMemcpyDefault, s));
     char* o = static_cast<char*>(dst) + rup(sizeof(StateHeader), 256);
+    // each ring's two history frames (logical frames 0 and 1, which may sit
+    // at the ring's last and first slots)
     for (const Act* r : st->rings)
-      for (int b = 0; b < r->B; ++b) {
-        const size_t n = 2 * r->fs() * sizeof(bf16);
-        CUDA_TRY(cudaMemcpyAsync(o, r->p + b * r->bs(), n, cudaMemcpyDefault, s));
-        o += n;
-      }
+      for (int b = 0; b < r->B; ++b)
+        for (int f = 0; f < 2; ++f) {
+          const size_t n = r->fs() * sizeof(bf16);
+          CUDA_TRY(cudaMemcpyAsync(o, r->p + b * r->bs() + r->slot(f) * r->fs(), n, cudaMemcpyDefault, s));
+          o += n;
+        }
     return WAN_OK;
   })
 }
@@ -1647,12 +1661,14 @@ wan_status wan_vae_stream_load(wan_vae_stream* st, const void* src, int64_t byte
       return fail(WAN_ERR_STATE, "state of a different model, dtype or shape");
     if (bytes < wan_vae_stream_state_bytes(st)) return fail(WAN_ERR_INVALID_ARG, "state buffer truncated");
     const char* o = static_cast<const char*>(src) + rup(sizeof(StateHeader), 256);
-    for (Act* r : st->rings)
+    for (Act* r : st->rings) {
+      r->base = 0;  // the history goes to slots 0 and 1
       for (int b = 0; b < r->B; ++b) {
         const size_t n = 2 * r->fs() * sizeof(bf16);
         CUDA_TRY(cudaMemcpyAsync(r->p + b * r->bs(), o, n, cudaMemcpyDefault, s));
         o += n;
       }
+    }
     st->first = hd.first != 0;
     return WAN_OK;
   })
