@@ -183,39 +183,55 @@ def run_reference(args):
 
 
 def run_attention(args):
-    """The isolated attention block: RMS norm, qkv 1x1 conv, softmax(q k^T / 32) v over
-    3520 positions per frame (one head, d = 1024), proj, + x; 8 frames, bf16."""
+    """The isolated attention block: RMS norm, qkv 1x1 conv, softmax(q k^T / sqrt(C)) v over
+    the frame's positions (one head, d = C), proj, + x; bf16.  Default: 8 frames of 44x80 at
+    C = 1024 (the TI2V-5B mid block at 720p); --attn-shape N,C,H,W for others (e.g.
+    4,384,90,160: the Wan2.1 mid block at 720p, which runs the flash kernel).  Weights are
+    packed once, before the timed region (wan_attention_create)."""
     import torch
     from video_vae_decoding_gb300 import build as _build
     _build.build()
     import video_vae_decoding_gb300 as wv
     cfg = wan_synth.CONFIGS["attention"]
-    N, C, H, W = cfg["x"]
+    N, C, H, W = (int(v) for v in args.attn_shape.split(",")) if args.attn_shape else cfg["x"]
     HW = H * W
-    w = wan_synth.make_weights(base=cfg["base"], seed=cfg["weight_seed"])
-    name = "decoder.mid_block.attentions.0"
-    wd = {k: torch.from_numpy(np.array(v)).cuda() for k, v in w.items() if k.startswith(name)}
+    r = np.random.default_rng(cfg["weight_seed"])
+    bound = np.float32(1.0 / np.sqrt(C))
+    name = "a"
+    wnp = {f"{name}.norm.gamma": 1 + 0.1 * r.standard_normal(C, dtype=np.float32),
+           f"{name}.to_qkv.weight": (r.random((3 * C, C, 1, 1), dtype=np.float32) * 2 - 1) * bound,
+           f"{name}.to_qkv.bias": (r.random(3 * C, dtype=np.float32) * 2 - 1) * bound,
+           f"{name}.proj.weight": (r.random((C, C, 1, 1), dtype=np.float32) * 2 - 1) * bound,
+           f"{name}.proj.bias": (r.random(C, dtype=np.float32) * 2 - 1) * bound}
+    wd = {k: torch.from_numpy(v).cuda() for k, v in wnp.items()}
     x = torch.from_numpy(wan_synth.make_normal((N, C, H, W), cfg["x_seed"])).cuda()
     x = x.permute(0, 2, 3, 1).reshape(N, HW, C).contiguous().to(torch.bfloat16)
+    block = wv.AttentionBlock(wd, N, H, W, C)
+    out = torch.empty_like(x)
     for _ in range(args.warmup):
-        wv.attention_block(x, wd, H, W)
+        block(x, out)
     torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e0.record(stream)
     for _ in range(args.steps):
-        wv.attention_block(x, wd, H, W)
-    e1.record()
+        block(x, out)
+    e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     flops = 2.0 * N * HW * (3 * C * C + 2 * HW * C + C * C)
     burst, sustained, _, src = _peaks()
     tf = flops / (ms / 1000.0) / 1e12
     print(json.dumps({
-        "metric": "attention block TFLOP/s (x [8,1024,44,80], bf16)", "value": tf, "unit": "TFLOP/s",
+        "metric": f"attention block TFLOP/s (x [{N},{C},{H},{W}], bf16)", "value": tf, "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "dtype": "bf16", "data": "synthetic", "config": {"workload": "isolated mid-block attention, 8 frames of 44x80, C 1024"},
+        "dtype": "bf16", "data": "synthetic", "config": {
+            "workload": f"isolated mid-block attention, {N} frames of {H}x{W}, C {C}",
+            "kernel": "flash" if C <= 384 else "score GEMM + row softmax + P V GEMM",
+            "weights": "packed before the timed region"},
         "nominal_gflop_per_step": flops / 1e9, "frac_of_bf16_peak": {"burst": tf / burst, "sustained": tf / sustained,
                                                                     "source": src}}))
+    block.close()
     return 0
 
 
@@ -316,6 +332,8 @@ def main():
                          "tiled: the 720p clip decoded as overlapping spatial tiles")
     ap.add_argument("--model", choices=("ti2v", "wan21"), default="ti2v",
                     help="wan21: the Wan2.1 VAE decode at 720p (latents [1,16,21,90,160]) instead of TI2V-5B's")
+    ap.add_argument("--attn-shape", default=None,
+                    help="attention workload: N,C,H,W (default 8,1024,44,80; 4,384,90,160 is Wan2.1's at 720p)")
     ap.add_argument("--tile", default="256,256", help="tiled workload: tile height,width in pixels")
     ap.add_argument("--stride", default="192,192", help="tiled workload: tile stride height,width in pixels")
     ap.add_argument("--no-cpu-baseline", action="store_true")

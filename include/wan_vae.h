@@ -274,6 +274,21 @@ wan_status wan_vae_decode(const void* z, int32_t z_dtype, int32_t B, int32_t T, 
 wan_status wan_attention_block(const void* x, int32_t N, int32_t H, int32_t W, int32_t C, const wan_tensor* weights,
                                int32_t n_weights, void* out, wan_cuda_stream stream);
 
+/* The same attention block with its weights packed once: create packs the
+ * five tensors (as wan_attention_block names them) and sizes a workspace
+ * for N frames of H x W positions at C channels (device memory owned by the
+ * handle until destroy; blocks until the packing is done); run computes out =
+ * block(x) for x, out [N][H*W][C] bf16 channels-last (device), stream-ordered,
+ * no allocation; destroy waits for the device and frees.  Head dims up to 384
+ * run the flash kernel (the HW x HW scores never leave the SM); wider heads
+ * (1024) run a score GEMM, a row softmax and a P V GEMM over an fp32 score
+ * workspace of N*HW*HW values.  Errors as wan_attention_block. */
+typedef struct wan_attention wan_attention;
+wan_status wan_attention_create(const wan_tensor* weights, int32_t n_weights, int32_t N, int32_t H, int32_t W,
+                                int32_t C, wan_cuda_stream stream, wan_attention** out);
+wan_status wan_attention_run(wan_attention* block, const void* x, void* out, wan_cuda_stream stream);
+void wan_attention_destroy(wan_attention* block);
+
 /* One causal conv (page "The parts", first bullet, WanCausalConv3d): x
  * [B][n_hist + F][H][W][Cin] bf16 channels-last (device), its first n_hist
  * (0..2) frames being the conv's history; zero padding kh//2, kw//2 in space

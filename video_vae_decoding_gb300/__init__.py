@@ -258,6 +258,33 @@ def attention_block(x: torch.Tensor, weights: "dict[str, torch.Tensor]", H: int,
     return out
 
 
+class AttentionBlock:
+    """The mid-block attention with its weights packed once
+    (wan_attention_create / _run / _destroy) for N frames of H x W positions."""
+
+    def __init__(self, weights: "dict[str, torch.Tensor]", N: int, H: int, W: int, C: int, stream=None):
+        arr, keep = weight_table(weights)
+        h = ctypes.c_void_p()
+        check(load().wan_attention_create(arr, len(keep) // 2, N, H, W, C, _stream(stream), ctypes.byref(h)))
+        self._h = h
+        self.N, self.H, self.W, self.C = N, H, W, C
+
+    def __call__(self, x: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+        if tuple(x.shape) != (self.N, self.H * self.W, self.C) or x.dtype != torch.bfloat16:
+            raise ValueError(f"x must be bf16 [{self.N}, {self.H * self.W}, {self.C}]")
+        out = torch.empty_like(x) if out is None else out
+        check(load().wan_attention_run(self._h, _dev(x, "x"), _dev(out, "out"), _stream(stream)))
+        return out
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().wan_attention_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+
 def conv_out_video(x: torch.Tensor, n_hist: int, weight: torch.Tensor, bias: torch.Tensor, out_dtype=torch.bfloat16,
                    preclamp: bool = False, stream=None):
     """x [B, n_hist + F, H, W, Cin] bf16 channels-last -> the clamped video

@@ -1,0 +1,349 @@
+// Flash-style mid-block attention core (page "wan22_vae_decode/reference.py",
+// "The parts", fourth bullet; the single-head attention of the page "Fix the
+// Wan VAE attention block"): per frame, O = softmax(q k^T / sqrt(C)) v over
+// the frame's HW positions, without the HW x HW score matrix ever leaving the
+// SM.
+//
+// One CTA takes 128 queries of one frame.  The score block S = Q K_j^T of 128
+// keys and the output accumulator O (128 x C fp32) both live in tensor memory
+// (128 + C <= 512 columns, so C <= 384); Q stays in shared memory for the
+// whole key loop.  Per key block j:
+//   MMA issuer   S_j = Q K_j^T (M=128, N=128, K=C), then O += P_{j-1} V_{j-1}
+//   softmax      row max and exp2 of the scaled scores (online softmax: the
+//                running max m only moves when a block's max exceeds it by more
+//                than 8 in log2 units, so P <= 256 and O is rescaled rarely),
+//                P_j as bf16 into shared memory in the MMA's operand layout
+// and at the end O / l is written as bf16.  Keys past HW are masked to -inf;
+// queries past HW are computed on zero rows and not stored.
+//
+// Warp roles (256 threads): warp 0 lane 0 TMA producer (Q once; per key block
+// C/64 boxes of 128 keys x 64 channels of K and the V^T boxes of VR rows x 64
+// keys, through one 16 KB-slot ring in the order the MMA consumes them), warp
+// 1 lane 0 MMA issuer, warp 2 TMEM allocation, warps 4-7 softmax and output
+// (thread = query row = TMEM lane).  Every wait is bounded.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace wan {
+
+namespace {
+
+constexpr int kFThreads = 256;
+constexpr int kFStages = 6;
+constexpr int kFUnit = 16384;  // one ring slot: 128 x 64 bf16
+
+template <int NQ>  // C = 64 * NQ
+struct FCfg {
+  static constexpr int C = 64 * NQ;
+  static constexpr int VR = (C % 128 == 0) ? 128 : 64;  // V^T rows per box (an MMA's N)
+  static constexpr int NV = C / VR;                     // V^T row groups
+  static constexpr int kVBytes = VR * 128;              // one V^T box: VR rows x 64 keys
+  static constexpr int kTmemCols = (128 + C) <= 256 ? 256 : 512;
+  static constexpr size_t kSmem = 1024 + (size_t)NQ * kFUnit + 2 * kFUnit + (size_t)kFStages * kFUnit + 8 * 32;
+};
+
+template <int NQ>
+__global__ void __launch_bounds__(kFThreads, 1)
+    flash_attn_kernel(const __grid_constant__ CUtensorMap mapQK, const __grid_constant__ CUtensorMap mapV,
+                      const __grid_constant__ FlashArgs args) {
+  using Cfg = FCfg<NQ>;
+  constexpr int S = kFStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                    // NQ boxes of 128 queries x 64 channels
+  uint8_t* sP = sQ + NQ * kFUnit;        // 2 boxes of 128 queries x 64 keys
+  uint8_t* sR = sP + 2 * kFUnit;         // ring
+  uint64_t* full = reinterpret_cast<uint64_t*>(sR + S * kFUnit);
+  uint64_t* empty = full + S;
+  uint64_t* q_full = empty + S;
+  uint64_t* s_full = q_full + 1;   // S_j in TMEM
+  uint64_t* s_free = s_full + 1;   // S_j read by the softmax threads
+  uint64_t* p_full = s_free + 1;   // P_j in shared memory (and O rescaled)
+  uint64_t* pv_done = p_full + 1;  // O += P_j V_j complete
+  uint64_t* done = pv_done + 1;    // all MMAs of this CTA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qb = blockIdx.x, f = blockIdx.y, b = blockIdx.z;
+  const int nkb = args.nkb;
+  const long long lim = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(q_full), 1);
+    mbar_init(smem_u32(s_full), 1);
+    mbar_init(smem_u32(s_free), 128);
+    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(pv_done), 1);
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&mapQK);
+    tma_prefetch_map(&mapV);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 128;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    mbar_arrive_expect_tx(smem_u32(q_full), NQ * kFUnit);
+    for (int u = 0; u < NQ; ++u)
+      tma_load_4d(smem_u32(sQ + u * kFUnit), &mapQK, smem_u32(q_full), args.q_c0 + 64 * u, 128 * qb, f, b);
+    int it = 0;
+    bool ok = true;
+    // order of consumption: K_0, then (K_j, V_{j-1}) for j = 1 .. nkb - 1, then V_{nkb-1}
+    for (int j = 0; j <= nkb && ok; ++j) {
+      const int nk = j < nkb ? NQ : 0, nv = j >= 1 ? 2 * Cfg::NV : 0;
+      for (int i = 0; i < nk + nv; ++i, ++it) {
+        const int s = it % S, r = it / S;
+        if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty, lim)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[s]);
+        if (i < nk) {
+          mbar_arrive_expect_tx(fb, kFUnit);
+          tma_load_4d(smem_u32(sR + s * kFUnit), &mapQK, fb, args.k_c0 + 64 * i, 128 * j, f, b);
+        } else {
+          const int v = i - nk, rg = v >> 1, h = v & 1;  // V^T row group, key half
+          mbar_arrive_expect_tx(fb, Cfg::kVBytes);
+          tma_load_4d(smem_u32(sR + s * kFUnit), &mapV, fb, 128 * (j - 1) + 64 * h, Cfg::VR * rg, f, b);
+        }
+      }
+    }
+    for (int jj = (it > S ? it - S : 0); jj < it; ++jj)
+      mbar_wait_bounded(smem_u32(&full[jj % S]), (jj / S) & 1, args.err, kDevTimeoutFull, lim);
+    mbar_wait_bounded(smem_u32(q_full), 0, args.err, kDevTimeoutFull, lim);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128);
+    constexpr uint32_t idO = idesc_bf16_f32(128, Cfg::VR);
+    bool ok = mbar_wait_bounded(smem_u32(q_full), 0, args.err, kDevTimeoutFull, lim);
+    if (!ok) *abort_flag = 1;
+    int slot = 0, phase = 0;
+    for (int j = 0; j <= nkb && ok; ++j) {
+      if (j < nkb) {
+        // S_j = Q K_j^T, once the softmax has read S_{j-1}
+        if (j > 0 && !mbar_wait_bounded(smem_u32(s_free), (j - 1) & 1, args.err, kDevTimeoutAccum, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int u = 0; u < NQ && ok; ++u) {
+          if (!mbar_wait_bounded(smem_u32(&full[slot]), phase, args.err, kDevTimeoutFull, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k128(smem_u32(sQ + u * kFUnit));
+          const uint64_t bd = sdesc_k128(smem_u32(sR + slot * kFUnit));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) umma_bf16(tS, ad + 2 * k, bd + 2 * k, idS, (u > 0 || k > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&empty[slot]));
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(s_full));
+      }
+      if (j >= 1) {
+        // O += P_{j-1} V_{j-1}, once P_{j-1} is written (and O rescaled)
+        const int jv = j - 1;
+        if (!mbar_wait_bounded(smem_u32(p_full), jv & 1, args.err, kDevTimeoutAccum, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int v = 0; v < 2 * Cfg::NV && ok; ++v) {
+          const int rg = v >> 1, h = v & 1;
+          if (!mbar_wait_bounded(smem_u32(&full[slot]), phase, args.err, kDevTimeoutFull, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k128(smem_u32(sP + h * kFUnit));
+          const uint64_t bd = sdesc_k128(smem_u32(sR + slot * kFUnit));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tO + Cfg::VR * rg, ad + 2 * k, bd + 2 * k, idO, (jv > 0 || h > 0 || k > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&empty[slot]));
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(pv_done));
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    // every MMA of this CTA completes before the TMEM is released
+    umma_commit(smem_u32(done));
+    mbar_wait_bounded(smem_u32(done), 0, args.err, kDevTimeoutAccum, lim);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ softmax, output
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkb; ++j) {
+      ok = __all_sync(0xffffffffu, !*abort_flag &&
+                                       mbar_wait_bounded(smem_u32(s_full), j & 1, args.err, kDevTimeoutAccum, lim));
+      if (!ok) break;
+      tc_fence_after();
+      float t[128];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tS + lane_off + 16 * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t[16 * c + i] = __uint_as_float(r[i]) * args.scale_log2;
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(s_free));
+      // keys past the frame's positions
+      const int kv = args.HW - 128 * j;
+      if (kv < 128) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= kv) t[i] = -INFINITY;
+      }
+      float mb = t[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mb = fmaxf(mb, t[i]);
+      float alpha = 1.f;
+      if (mb > m + 8.f) {  // move the reference max (and rescale O and l by alpha)
+        alpha = exp2f(m - mb);
+        m = mb;
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        t[i] = exp2f(t[i] - m);
+        rs += t[i];
+      }
+      l = l * alpha + rs;
+      // P buffer free and O stable once O += P_{j-1} V_{j-1} has completed
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(pv_done), (j - 1) & 1, args.err, kDevTimeoutAccum, lim));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < Cfg::C / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(tO + lane_off + 16 * c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st16(tO + lane_off + 16 * c, r);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P_j (bf16) in the 128-byte-swizzled K-major layout: row `row`, key
+      // chunk c of 8 keys at 16-byte slot c ^ (row & 7) of its 128-byte line
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint8_t* line = sP + h * kFUnit + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float* v = t + 64 * h + 8 * c;
+          const uint4 w = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                     pack_bf16x2(v[6], v[7]));
+          *reinterpret_cast<uint4*>(line + ((c ^ (row & 7)) << 4)) = w;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(p_full));
+    }
+    if (ok)
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait_bounded(smem_u32(pv_done), (nkb - 1) & 1, args.err, kDevTimeoutAccum, lim));
+    if (!ok) {
+      *abort_flag = 1;
+    } else {
+      tc_fence_after();
+      const int qrow = 128 * qb + row;
+      const float rl = 1.f / l;
+      __nv_bfloat16* dst = args.out + (long long)b * args.out_bs + (long long)f * args.out_fs +
+                           (long long)qrow * args.out_ldc;
+#pragma unroll 1
+      for (int c = 0; c < Cfg::C / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tO + lane_off + 16 * c, r);
+        tmem_ld_wait();
+        if (qrow < args.HW) {
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * rl;
+          uint4* d = reinterpret_cast<uint4*>(dst + 16 * c);
+          d[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                            pack_bf16x2(v[6], v[7]));
+          d[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                            pack_bf16x2(v[14], v[15]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int NQ>
+cudaError_t launch_f(const FlashLaunch& L, cudaStream_t stream) {
+  using Cfg = FCfg<NQ>;
+  auto kern = flash_attn_kernel<NQ>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  const FlashArgs& a = L.args;
+  if (a.HW <= 0 || a.frames <= 0 || a.batches <= 0) return cudaSuccess;
+  dim3 grid((unsigned)((a.HW + 127) / 128), (unsigned)a.frames, (unsigned)a.batches);
+  kern<<<grid, kFThreads, Cfg::kSmem, stream>>>(L.qk, L.v, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int flash_attn_max_c() { return 384; }
+
+cudaError_t launch_flash_attn(const FlashLaunch& L, cudaStream_t stream) {
+  const FlashArgs& a = L.args;
+  if (a.C % 64 || a.C < 64 || a.C > 384 || a.nkb != (a.HW + 127) / 128) return cudaErrorInvalidValue;
+  switch (a.C / 64) {
+    case 1: return launch_f<1>(L, stream);
+    case 2: return launch_f<2>(L, stream);
+    case 3: return launch_f<3>(L, stream);
+    case 4: return launch_f<4>(L, stream);
+    case 5: return launch_f<5>(L, stream);
+    case 6: return launch_f<6>(L, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace wan

@@ -12,7 +12,7 @@
 //   warps 4-11       epilogue: tcgen05.ld of the accumulator, bias, residual /
 //                    fused RMS norm / DupUp3D / unpatchify, stores
 // Shared-memory rings with "full" and "empty" mbarriers per slot overlap the
-// loads with the MMAs (plain, halo and row modes: one ring of A + B stages;
+// loads with the MMAs (plain and row modes: one ring of A + B stages;
 // band mode: an A ring and a B ring).  All waits are bounded.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -25,27 +25,23 @@ namespace wan {
 constexpr int kThreads = 384;
 constexpr int kEpiThreads = 256;
 
-// Halo mode (3x3 spatial taps, small N): per (time tap, 64-channel block) a
-// stage holds three 16 x 10 A boxes (x offsets -1, 0, +1; rows y0-1 .. y0+8)
-// and the nine taps' B blocks; tap (dy, dx) reads box dx from row 16*dy on.
-constexpr int kHaloABox = 16 * kHaloBoxRows * 128;  // 20 KB
+// Band mode: A boxes of 16 x 10 positions (a tile's 8 rows and one halo row
+// above and below), 20 KB.
+constexpr int kBandABox = 16 * kBandBoxRows * 128;
 // Row mode: 130 pixels x 128 B, rounded up to whole 1 KB swizzle atoms.
 constexpr int kRowABox = 17 * 1024;
 
-template <int BN, bool HALO = false, bool ROW = false, bool BAND = false>
+template <int BN, bool ROW = false, bool BAND = false>
 struct ConvCfg {
   // as many stages as fit in 227 KB: 16 KB of A plus BN x 128 B of B each;
   // row mode: a 130-row A box (17 KB) and three taps of B; band mode: A
   // boxes (16 x 10 pixels, 20 KB) and one-tap B blocks in separate rings
-  static constexpr int kStages =
-      HALO ? 2
-           : BAND ? (BN >= 256 ? 5 : 6)
-                  : ROW ? (BN <= 96 ? 4 : (BN <= 128 ? 3 : 2))
-                        : (BN >= 256 ? 4 : (BN > 128 ? 5 : (BN == 128 ? 6 : (BN > 64 ? 7 : 8))));
+  static constexpr int kStages = BAND ? (BN >= 256 ? 5 : 6)
+                                      : ROW ? (BN <= 96 ? 4 : (BN <= 128 ? 3 : 2))
+                                            : (BN >= 256 ? 4 : (BN > 128 ? 5 : (BN == 128 ? 6 : (BN > 64 ? 7 : 8))));
   static constexpr int kAStages = BAND ? 3 : kStages;  // A slots (the B ring has kStages)
-  static constexpr int kABytes =
-      HALO ? 3 * kHaloABox : ROW ? kRowABox : BAND ? kHaloABox : kTileM * kBlockK * 2;  // 60 / 17 / 20 / 16 KB
-  static constexpr int kBBytes = (HALO ? 9 : ROW ? 3 : 1) * BN * kBlockK * 2;
+  static constexpr int kABytes = ROW ? kRowABox : BAND ? kBandABox : kTileM * kBlockK * 2;  // 17 / 20 / 16 KB
+  static constexpr int kBBytes = (ROW ? 3 : 1) * BN * kBlockK * 2;
   // one accumulator buffer of BN columns; two are allocated, kAccCols apart
   // (a power of two, so the allocation is one too)
   static constexpr int kAccCols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
@@ -374,11 +370,11 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
 // the B block and multicasts it to both, and each MMA issuer frees a B slot
 // in both CTAs (the slot's "empty" barrier counts both), so L2 delivers B
 // once per pair.
-template <int BN, int EPI, int CL, bool HALO, bool ROW, bool BAND>
+template <int BN, int EPI, int CL, bool ROW, bool BAND>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                      const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
-  using Cfg = ConvCfg<BN, HALO, ROW, BAND>;
+  using Cfg = ConvCfg<BN, ROW, BAND>;
   static_assert(!BAND || CL == 2, "band mode shares B across a pair of CTAs");
   constexpr int S = Cfg::kStages;
   constexpr int SA = Cfg::kAStages;
@@ -444,36 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
       const TileCoord tc = tile_coord(args, unit, CL, rank);
-      if constexpr (HALO) {
-        // K order: time tap dt, then 64-channel block kb; 9 spatial taps per stage
-        const int nkb = args.taps[0].nkb;
-        for (int dt = 0; dt < 3 && ok; ++dt) {
-          for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int s = it % S;
-            const int r = it / S;
-            if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty, lim)) {
-              ok = false;
-              *abort_flag = 1;
-              break;
-            }
-            if (*abort_flag) {
-              ok = false;
-              break;
-            }
-            if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
-            const uint32_t fb = smem_u32(&full[s]);
-            mbar_arrive_expect_tx(fb, Cfg::kABytes + Cfg::kBBytes);
-            const int fr = ring_slot(args.src_f0[0] + tc.f + dt, args.src_fmod);
-            for (int dx = 0; dx < 3; ++dx)
-              tma_load_5d(smem_u32(sA + s * Cfg::kABytes + dx * kHaloABox), &mapA0, fb, kb * kBlockK,
-                          tc.tx * args.box_w + dx - 1, tc.ty * args.box_h - 1, fr, tc.b);
-            // B: the 9 spatial taps of time tap dt, block kb (a 3-D box over the packed weights)
-            tma_load_3d(smem_u32(sB + s * Cfg::kBBytes), &mapB, fb, dt * 9 * args.taps[0].nkb * kBlockK + kb * kBlockK,
-                        tc.tn * BN, 0);
-          }
-        }
-        continue;
-      }
       if constexpr (BAND) {
         // per tap (dt, dx) and 64-channel block: one 16 x 10 A box (rows from
         // tile start - 1) into the A ring, then its three dy taps' B blocks,
@@ -602,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tracked incrementally, and the abort flag is read once per tile (every
     // wait is bounded and raises the flag when it runs out).
     int it_slot = 0, it_phase = 0;  // stage ring (the B ring in band mode)
-    int kbc = 0;                    // row and halo modes: channel block within the tap
+    int kbc = 0;                    // row mode: channel block within the tap
     const int last_kb = args.taps[0].nkb - 1;
     int ia_slot = 0, ia_phase = 0;  // band mode: A ring
     bool ok = true;
@@ -708,36 +674,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || j > 0 || k > 0) ? 1u : 0u);
             }
           }
-        } else if constexpr (HALO) {
-          // descriptors of the stage's first box and first B block; the taps
-          // add constant byte offsets (>> 4) to the start-address field
-          const uint64_t a0 = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
-          const uint64_t b0 = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
-          // a time tap's last channel block may hold only tail_k16 x 16 channels
-          const bool tail = args.tail_k16 && kbc == last_kb;
-          if (++kbc > last_kb) kbc = 0;
-          if (tail && args.tail_k16 == 2) {
-#pragma unroll
-            for (int t9 = 0; t9 < 9; ++t9) {
-              const int dy = t9 / 3, dx = t9 % 3;
-              const uint64_t ad = a0 + (uint64_t)((dx * kHaloABox + dy * 16 * 128) >> 4);
-              const uint64_t bd = b0 + (uint64_t)((t9 * BN * 128) >> 4);
-#pragma unroll
-              for (int k = 0; k < 2; ++k)
-                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || t9 > 0 || k > 0) ? 1u : 0u);
-            }
-          } else {
-#pragma unroll
-            for (int t9 = 0; t9 < 9; ++t9) {
-              const int dy = t9 / 3, dx = t9 % 3;
-              // rows of tap (dy, dx): box dx from image row dy on (16 rows per image row, 2 KB)
-              const uint64_t ad = a0 + (uint64_t)((dx * kHaloABox + dy * 16 * 128) >> 4);
-              const uint64_t bd = b0 + (uint64_t)((t9 * BN * 128) >> 4);
-#pragma unroll
-              for (int k = 0; k < kBlockK / 16; ++k)
-                umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > 0 || t9 > 0 || k > 0) ? 1u : 0u);
-            }
-          }
         } else {
           const uint64_t ad = sdesc_k128(smem_u32(sA + s * Cfg::kABytes));
           const uint64_t bd = sdesc_k128(smem_u32(sB + s * Cfg::kBBytes));
@@ -782,10 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int EPI, int CL, bool HALO = false, bool ROW = false, bool BAND = false>
+template <int BN, int EPI, int CL, bool ROW = false, bool BAND = false>
 static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
-  using Cfg = ConvCfg<BN, HALO, ROW, BAND>;
-  auto kern = conv_gemm_kernel<BN, EPI, CL, HALO, ROW, BAND>;
+  using Cfg = ConvCfg<BN, ROW, BAND>;
+  auto kern = conv_gemm_kernel<BN, EPI, CL, ROW, BAND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
   if (e != cudaSuccess) return e;
   const ConvArgs& a = L.args;
@@ -829,21 +765,21 @@ int conv_b_box_rows(int bn) { return conv_clustered(bn) ? bn / 2 : bn; }
 
 cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
   if (L.args.band) {
-    if (L.epi != kEpiStore || L.args.halo || L.args.subpix || L.args.row) return cudaErrorInvalidValue;
-    if (L.bn == 256) return launch_t<256, kEpiStore, 2, false, false, true>(L, stream);
-    if (L.bn == 192) return launch_t<192, kEpiStore, 2, false, false, true>(L, stream);
+    if (L.epi != kEpiStore || L.args.subpix || L.args.row) return cudaErrorInvalidValue;
+    if (L.bn == 256) return launch_t<256, kEpiStore, 2, false, true>(L, stream);
+    if (L.bn == 192) return launch_t<192, kEpiStore, 2, false, true>(L, stream);
     return cudaErrorInvalidValue;
   }
   if (L.args.row) {
-    if (L.epi != kEpiStore || L.args.halo || L.args.subpix) return cudaErrorInvalidValue;
-    if (L.bn == 96) return launch_t<96, kEpiStore, 2, false, true>(L, stream);
-    if (L.bn == 128) return launch_t<128, kEpiStore, 2, false, true>(L, stream);
-    if (L.bn == 192) return launch_t<192, kEpiStore, 2, false, true>(L, stream);
+    if (L.epi != kEpiStore || L.args.subpix) return cudaErrorInvalidValue;
+    if (L.bn == 96) return launch_t<96, kEpiStore, 2, true>(L, stream);
+    if (L.bn == 128) return launch_t<128, kEpiStore, 2, true>(L, stream);
+    if (L.bn == 192) return launch_t<192, kEpiStore, 2, true>(L, stream);
     return cudaErrorInvalidValue;
   }
   if (L.epi == kEpiVideo) {
     if (L.bn != 16) return cudaErrorInvalidValue;
-    return L.args.halo ? launch_t<16, kEpiVideo, 1, true>(L, stream) : launch_t<16, kEpiVideo, 1>(L, stream);
+    return launch_t<16, kEpiVideo, 1>(L, stream);
   }
   if (L.epi == kEpiDup) {
     switch (L.bn) {

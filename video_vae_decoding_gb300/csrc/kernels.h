@@ -21,7 +21,7 @@ namespace wan {
 // history frames in slots 0-1 in front of the current frames.
 // ---------------------------------------------------------------------------
 constexpr int kMaxTaps = 96;
-constexpr int kHaloBoxRows = 10;  // halo mode: A boxes of 16 x 10 positions (8 rows + 2 halo rows)
+constexpr int kBandBoxRows = 10;  // band mode: A boxes of 16 x 10 positions (8 rows + 2 halo rows)
 constexpr int kTileM = 128;
 constexpr int kBlockK = 64;
 
@@ -53,17 +53,13 @@ struct ConvArgs {
   // shifted by (i - 1, j - 1), B's third coordinate is p, and the output of
   // low-resolution position (y, x) goes to (2y + i, 2x + j) of a 2H x 2W frame.
   int subpix;
-  // Halo mode (conv_out: causal 3x3x3, N = 16): the A tensor map's box is
-  // 64 x 16 x 10 and the B map is 3-D (K, N, 9 spatial taps with stride
-  // ci_pad); K iterates time taps then 64-channel blocks (taps[0].nkb of them).
-  int halo;
   // Row mode (3x3 spatial taps without a shortcut, N tile 96, 128 or 192): a tile
   // is 128 consecutive pixels of one row (box_w 128, box_h 1); every tap
   // (dt, dy) loads one 130-pixel A box (x from -1) that serves its three dx
   // taps at row offsets 0, 1, 2, and the three taps' B blocks, which lie
   // row_bdk K columns apart.  Cluster pairs are adjacent rows (ty).
   int row;
-  int tail_k16;  // row / halo modes: K16 steps holding channels in each tap's last block (0: all 4)
+  int tail_k16;  // row mode: K16 steps holding channels in each tap's last block (0: all 4)
   int row_bdk;  // row mode: K stride between dx taps; band mode: between dy taps
   // Band mode (bf16 3x3 spatial taps without a shortcut, N tile 256, 16 x 8
   // tiles): every tap (dt, dx) loads one 16 x 10 A box (rows from -1) into an
@@ -169,6 +165,34 @@ cudaError_t launch_video_conv(const VideoConvLaunch& L, cudaStream_t stream);
 // (rows past 9 Co and channels past Ci are left as they are).
 cudaError_t launch_pack_tapfold(const void* src, int src_f32, int Co, int Ci, int ci_pad, __nv_bfloat16* dst,
                                 cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Flash-style attention core (attention.cu): per frame, O = softmax(q k^T *
+// scale) v over HW positions, head dim C (a multiple of 64, at most
+// flash_attn_max_c(): S and O share the 512 TMEM columns).  q and k are
+// channel ranges of one tensor [B][F][HW][ldc] (map qk: 4-D (channels, HW,
+// F, B), box 64 x 128); v comes transposed, [B][F][C][HWp] with zeros past
+// HW (map v: 4-D (HWp, C, F, B), box 64 x VR, VR = 128 if 128 divides C, else
+// 64).  O is written as bf16 [B][F][HW][out_ldc].
+// ---------------------------------------------------------------------------
+struct FlashArgs {
+  int HW, frames, batches;
+  int nkb;             // key blocks: ceil(HW / 128)
+  int C;               // head dim
+  int q_c0, k_c0;      // first channel of q and of k in the qk tensor
+  float scale_log2;    // log2(e) / sqrt(C)
+  __nv_bfloat16* out;
+  long long out_bs, out_fs;
+  int out_ldc;
+  int* err;
+  long long wait_limit;
+};
+struct FlashLaunch {
+  CUtensorMap qk, v;
+  FlashArgs args;
+};
+int flash_attn_max_c();
+cudaError_t launch_flash_attn(const FlashLaunch& L, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Memory-bound kernels (channels-last bf16 unless stated).

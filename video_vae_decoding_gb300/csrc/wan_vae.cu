@@ -579,12 +579,19 @@ struct AttnBufs {
   bf16* Vt = nullptr;
   int HW = 0, HWs = 0, HWp = 0, Fmax = 0, B = 0, C = 0;
   int sp = 1;  // 2 in split mode: P and V^T rows hold [hi HWp | lo HWp]
+  bool flash = false;  // the flash kernel (no S, no P); else score GEMM + row softmax + P V GEMM
   long long ldp() const { return (long long)sp * HWp; }
   long long s_bs() const { return (long long)Fmax * HW * HWs; }
   long long p_bs() const { return (long long)Fmax * HW * ldp(); }
   long long vt_fs() const { return (long long)C * ldp(); }
   long long vt_bs() const { return (long long)Fmax * vt_fs(); }
 };
+
+// The flash kernel holds a 128-query block's scores and output (C columns)
+// in the 512 TMEM columns: head dims up to 384 (Wan2.1's 384, the narrow test
+// widths).  Wider heads (TI2V-5B's 1024) and the fp32 split format take the
+// score GEMM, row softmax and P V GEMM path.
+static bool attention_is_flash(bool split, int C) { return !split && C % 64 == 0 && C <= flash_attn_max_c(); }
 
 struct wan_vae_stream {
   const wan_vae_model* m = nullptr;
@@ -685,14 +692,17 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   at.B = st->B;
   at.C = c4;
   at.sp = st->m->split ? 2 : 1;
+  at.flash = attention_is_flash(st->m->split, c4);
   WAN_TRY(make_act(st, at.an, n, 1, at.HW, c4));
   WAN_TRY(make_act(st, at.qkv, n, 1, at.HW, 3 * c4));
   WAN_TRY(make_act(st, at.O, n, 1, at.HW, c4));
   void* p;
-  WAN_TRY(make_raw(st, (size_t)st->B * at.s_bs() * sizeof(float), &p));
-  at.S = (float*)p;
-  WAN_TRY(make_raw(st, (size_t)st->B * at.p_bs() * sizeof(bf16), &p));
-  at.P = (bf16*)p;
+  if (!at.flash) {  // the HW x HW scores and probabilities
+    WAN_TRY(make_raw(st, (size_t)st->B * at.s_bs() * sizeof(float), &p));
+    at.S = (float*)p;
+    WAN_TRY(make_raw(st, (size_t)st->B * at.p_bs() * sizeof(bf16), &p));
+    at.P = (bf16*)p;
+  }
   WAN_TRY(make_raw(st, (size_t)st->B * at.vt_bs() * sizeof(bf16), &p));
   at.Vt = (bf16*)p;
   // level B
@@ -787,7 +797,7 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   const bool band = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
                     (cw.bn == 192 || cw.bn == 256);
   if (band) {
-    WAN_TRY(act_map(&L.a0, a0, 16, kHaloBoxRows));
+    WAN_TRY(act_map(&L.a0, a0, 16, kBandBoxRows));
     L.a1 = L.a0;
     const uint64_t dims[3] = {(uint64_t)cw.ktot, (uint64_t)cw.co_pad, 1};
     const uint64_t strides[2] = {(uint64_t)cw.ktot * 2, (uint64_t)cw.ktot * cw.co_pad * 2};
@@ -1016,48 +1026,89 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
   L.args.bias = qkv.bias;
   set_out(L.args, out_of(at.qkv));
   WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * 3 * C * C, err, s));
-  // S = q k^T: q = channels [0, C) of qkv, k = [C, 2C) (low halves 3C further on)
-  // N tile: the largest power of two <= min(HW, 256), at least 16.  With
-  // fewer than 16 positions the key box runs past the frame's rows: TMA reads
-  // zeros there, the extra columns of S are never read by the softmax (n =
-  // HW), and P and V^T keep zeros beyond HW from the workspace clear.
-  int bnS = 16;
-  while (bnS * 2 <= std::min(HW, 256)) bnS *= 2;
-  WAN_TRY(gemm_setup(L, at.qkv.p, at.qkv.ldc, at.qkv.lo, HW, at.qkv.F, B, at.qkv.fs(), at.qkv.bs(), C, C, at.qkv.lo,
-                     sp, (int)cdiv(at.HWs, bnS), bnS, F));
-  WAN_TRY(b_map(&L.b, at.qkv.p, at.qkv.ldc, HW, (long long)B * at.Fmax, at.qkv.ldc, at.qkv.fs(), bnS));
-  L.args.b_per_frame = 1;
-  L.args.b_gstride = at.Fmax;
-  L.args.N = at.HWs;
-  {
-    OutSpec o;
-    o.p = at.S;
-    o.f32 = 1;
-    o.bs = at.s_bs();
-    o.fs = (long long)HW * at.HWs;
-    o.ldc = at.HWs;
-    set_out(L.args, o);
+  if (at.flash) {
+    // V^T per frame, then the flash kernel: O = softmax(q k^T / sqrt(C)) v
+    for (int b = 0; b < B; ++b)
+      ELT(prof, kKindMisc, 4.0 * F * HW * C,
+          launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C, at.qkv.fs(), at.qkv.ldc, at.Vt + b * at.vt_bs(),
+                           at.vt_fs(), (int)at.ldp(), F, HW, C, s));
+    FlashLaunch FL;
+    memset(&FL, 0, sizeof(FL));
+    {
+      const uint64_t dims[4] = {(uint64_t)at.qkv.chans(), (uint64_t)HW, (uint64_t)at.qkv.F, (uint64_t)B};
+      const uint64_t strides[3] = {(uint64_t)at.qkv.ldc * 2, (uint64_t)at.qkv.fs() * 2, (uint64_t)at.qkv.bs() * 2};
+      const uint32_t box[4] = {64, 128, 1, 1};
+      WAN_TRY(encode(&FL.qk, 4, at.qkv.p, dims, strides, box));
+    }
+    {
+      const uint64_t dims[4] = {(uint64_t)at.HWp, (uint64_t)C, (uint64_t)at.Fmax, (uint64_t)B};
+      const uint64_t strides[3] = {(uint64_t)at.ldp() * 2, (uint64_t)at.vt_fs() * 2, (uint64_t)at.vt_bs() * 2};
+      const uint32_t box[4] = {64, (uint32_t)(C % 128 == 0 ? 128 : 64), 1, 1};
+      WAN_TRY(encode(&FL.v, 4, at.Vt, dims, strides, box));
+    }
+    FlashArgs& a = FL.args;
+    a.HW = HW;
+    a.frames = F;
+    a.batches = B;
+    a.nkb = (HW + 127) / 128;
+    a.C = C;
+    a.q_c0 = 0;
+    a.k_c0 = C;
+    a.scale_log2 = 1.4426950408889634f / std::sqrt((float)C);
+    a.out = at.O.p;
+    a.out_bs = at.O.bs();
+    a.out_fs = at.O.fs();
+    a.out_ldc = at.O.ldc;
+    a.err = err;
+    cudaEvent_t e1 = nullptr;
+    if (prof) WAN_TRY(prof->begin(kKindAttention, 4.0 * M * HW * C, s, &e1));
+    CUDA_TRY(launch_flash_attn(FL, s));
+    if (e1) CUDA_TRY(cudaEventRecord(e1, s));
+    if (prof) prof->launches++;
+  } else {
+    // S = q k^T: q = channels [0, C) of qkv, k = [C, 2C) (low halves 3C further on)
+    // N tile: the largest power of two <= min(HW, 256), at least 16.  With
+    // fewer than 16 positions the key box runs past the frame's rows: TMA reads
+    // zeros there, the extra columns of S are never read by the softmax (n =
+    // HW), and P and V^T keep zeros beyond HW from the workspace clear.
+    int bnS = 16;
+    while (bnS * 2 <= std::min(HW, 256)) bnS *= 2;
+    WAN_TRY(gemm_setup(L, at.qkv.p, at.qkv.ldc, at.qkv.lo, HW, at.qkv.F, B, at.qkv.fs(), at.qkv.bs(), C, C, at.qkv.lo,
+                       sp, (int)cdiv(at.HWs, bnS), bnS, F));
+    WAN_TRY(b_map(&L.b, at.qkv.p, at.qkv.ldc, HW, (long long)B * at.Fmax, at.qkv.ldc, at.qkv.fs(), bnS));
+    L.args.b_per_frame = 1;
+    L.args.b_gstride = at.Fmax;
+    L.args.N = at.HWs;
+    {
+      OutSpec o;
+      o.p = at.S;
+      o.f32 = 1;
+      o.bs = at.s_bs();
+      o.fs = (long long)HW * at.HWs;
+      o.ldc = at.HWs;
+      set_out(L.args, o);
+    }
+    WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * HW * C, err, s));
+    // P = softmax(S / sqrt(C)); V^T per frame
+    const float scale = 1.0f / std::sqrt((float)C);
+    for (int b = 0; b < B; ++b) {
+      ELT(prof, kKindMisc, (4.0 * at.HWs + 2.0 * at.ldp()) * F * HW, launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.ldp(), HW, (long long)F * HW,
+                                    scale, s, sp ? at.HWp : 0));
+      for (int part = 0; part <= sp; ++part)
+        ELT(prof, kKindMisc, 4.0 * F * HW * C, launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C + part * at.qkv.lo, at.qkv.fs(), at.qkv.ldc,
+                                   at.Vt + b * at.vt_bs() + part * at.HWp, at.vt_fs(), (int)at.ldp(), F, HW, C, s));
+    }
+    // O = P V
+    const int bnC = choose_bn(C);
+    WAN_TRY(gemm_setup(L, at.P, (int)at.ldp(), sp ? at.HWp : 0, HW, at.Fmax, B, (long long)HW * at.ldp(), at.p_bs(),
+                       at.HWp, 0, at.HWp, sp, (int)cdiv(C, bnC), bnC, F));
+    WAN_TRY(b_map(&L.b, at.Vt, at.ldp(), C, (long long)B * at.Fmax, at.ldp(), at.vt_fs(), bnC));
+    L.args.b_per_frame = 1;
+    L.args.b_gstride = at.Fmax;
+    L.args.N = C;
+    set_out(L.args, out_of(at.O));
+    WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * HW * C, err, s));
   }
-  WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * HW * C, err, s));
-  // P = softmax(S / sqrt(C)); V^T per frame
-  const float scale = 1.0f / std::sqrt((float)C);
-  for (int b = 0; b < B; ++b) {
-    ELT(prof, kKindMisc, (4.0 * at.HWs + 2.0 * at.ldp()) * F * HW, launch_softmax_rows(at.S + b * at.s_bs(), at.HWs, at.P + b * at.p_bs(), at.ldp(), HW, (long long)F * HW,
-                                  scale, s, sp ? at.HWp : 0));
-    for (int part = 0; part <= sp; ++part)
-      ELT(prof, kKindMisc, 4.0 * F * HW * C, launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C + part * at.qkv.lo, at.qkv.fs(), at.qkv.ldc,
-                                 at.Vt + b * at.vt_bs() + part * at.HWp, at.vt_fs(), (int)at.ldp(), F, HW, C, s));
-  }
-  // O = P V
-  const int bnC = choose_bn(C);
-  WAN_TRY(gemm_setup(L, at.P, (int)at.ldp(), sp ? at.HWp : 0, HW, at.Fmax, B, (long long)HW * at.ldp(), at.p_bs(),
-                     at.HWp, 0, at.HWp, sp, (int)cdiv(C, bnC), bnC, F));
-  WAN_TRY(b_map(&L.b, at.Vt, at.ldp(), C, (long long)B * at.Fmax, at.ldp(), at.vt_fs(), bnC));
-  L.args.b_per_frame = 1;
-  L.args.b_gstride = at.Fmax;
-  L.args.N = C;
-  set_out(L.args, out_of(at.O));
-  WAN_TRY(run(L, prof, kKindAttention, 2.0 * M * HW * C, err, s));
   // y = O Wp^T + b + x
   WAN_TRY(gemm_setup(L, at.O.p, at.O.ldc, at.O.lo, HW, at.O.F, B, at.O.fs(), at.O.bs(), proj.ci_pad, 0, proj.ci_pad,
                      sp, proj.co_pad / proj.bn, proj.bn, F));
@@ -1224,19 +1275,6 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
     ConvLaunch L;
     const ConvW& co = m->conv_out;
     WAN_TRY(conv_setup(co, st->ringOut, 0, nullptr, 0, FC, L));
-    if (!co.split && co.bn == 16 && co.kt == 3 && co.kh == 3 && co.kw == 3) {
-      // halo mode: three 16 x 10 boxes per time tap and channel block serve all nine spatial taps
-      const Act& a = st->ringOut;
-      WAN_TRY(act_map(&L.a0, a, 16, kHaloBoxRows));
-      L.a1 = L.a0;
-      const uint64_t dims[3] = {(uint64_t)co.ktot, (uint64_t)co.co_pad, 9};
-      const uint64_t strides[2] = {(uint64_t)co.ktot * 2, (uint64_t)co.ci_pad * 2};
-      const uint32_t box[3] = {64, 16, 9};
-      WAN_TRY(encode(&L.b, 3, co.w, dims, strides, box));
-      L.args.halo = 1;
-      L.args.total_kb = 3 * (co.ci_pad / 64);
-      L.args.tail_k16 = (co.Ci % 64 == 32) ? 2 : 0;  // e.g. 96 channels: the last block holds 32
-    }
     L.epi = kEpiVideo;
     L.args.out = out;
     L.args.out_f32 = out_f32;
@@ -1857,91 +1895,145 @@ wan_status wan_vae_decode_tiled(const wan_vae_model* model, const void* z, int32
   })
 }
 
+}  // extern "C"
+
+// Packed weights and workspace of the isolated attention block for N frames
+// of H x W positions (the layer entry points below).
+struct wan_attention {
+  int N = 0, H = 0, W = 0, C = 0;
+  float* g = nullptr;
+  ConvW qkv, proj;
+  AttnBufs at;
+  int* err = nullptr;
+  DevMem mem;
+};
+
+static wan_status attention_build(const wan_tensor* weights, int32_t n_weights, int32_t N, int32_t H, int32_t W,
+                                  int32_t C, cudaStream_t s, wan_attention* A) {
+  if (!weights) return fail(WAN_ERR_INVALID_ARG, "null weights");
+  if (N < 1 || H < 1 || W < 1) return fail(WAN_ERR_INVALID_ARG, "N=%d H=%d W=%d", N, H, W);
+  if (C % 64 || C < 64 || C > 1024) return fail(WAN_ERR_UNSUPPORTED, "C=%d (multiple of 64, <= 1024)", C);
+  // pick the five tensors by suffix
+  std::vector<wan_tensor> t;
+  const char* suff[5] = {"norm.gamma", "to_qkv.weight", "to_qkv.bias", "proj.weight", "proj.bias"};
+  for (const char* sfx : suff) {
+    const wan_tensor* hit = nullptr;
+    for (int i = 0; i < n_weights; ++i) {
+      const char* nm = weights[i].name;
+      if (!nm) continue;
+      const size_t L = strlen(nm), Ls = strlen(sfx);
+      if (L >= Ls && strcmp(nm + L - Ls, sfx) == 0) hit = &weights[i];
+    }
+    if (!hit) return fail(WAN_ERR_MISSING_WEIGHT, "missing weight '*%s'", sfx);
+    wan_tensor c = *hit;
+    c.name = sfx;
+    t.push_back(c);
+  }
+  WeightTable wt{t.data(), (int)t.size()};
+  A->N = N;
+  A->H = H;
+  A->W = W;
+  A->C = C;
+  DevMem& mem = A->mem;
+  WAN_TRY(pack_gamma(wt, "norm.gamma", C, &A->g, mem, s));
+  WAN_TRY(pack_conv(wt, "to_qkv", 3 * C, C, 1, 1, 1, true, "", 0, A->qkv, mem, s));
+  WAN_TRY(pack_conv(wt, "proj", C, C, 1, 1, 1, true, "", 0, A->proj, mem, s));
+  AttnBufs& at = A->at;
+  at.HW = H * W;
+  at.HWs = (int)rup(at.HW, 16);
+  at.HWp = (int)rup(at.HW, 64);
+  at.Fmax = N;
+  at.B = 1;
+  at.C = C;
+  at.flash = attention_is_flash(false, C);
+  auto mk = [&](Act& a, int ch) -> wan_status {
+    a.B = 1;
+    a.F = N;
+    a.H = 1;
+    a.W = at.HW;
+    a.C = ch;
+    a.ldc = ch;
+    void* p;
+    WAN_TRY(mem.alloc(&p, a.bytes()));
+    a.p = (bf16*)p;
+    return WAN_OK;
+  };
+  WAN_TRY(mk(at.an, C));
+  WAN_TRY(mk(at.qkv, 3 * C));
+  WAN_TRY(mk(at.O, C));
+  void* p;
+  if (!at.flash) {
+    WAN_TRY(mem.alloc(&p, (size_t)at.s_bs() * sizeof(float)));
+    at.S = (float*)p;
+    WAN_TRY(mem.alloc(&p, (size_t)at.p_bs() * sizeof(bf16)));
+    at.P = (bf16*)p;
+    CUDA_TRY(cudaMemsetAsync(at.P, 0, (size_t)at.p_bs() * sizeof(bf16), s));
+  }
+  WAN_TRY(mem.alloc(&p, (size_t)at.vt_bs() * sizeof(bf16)));
+  at.Vt = (bf16*)p;
+  WAN_TRY(mem.alloc((void**)&A->err, 256));
+  CUDA_TRY(cudaMemsetAsync(at.Vt, 0, (size_t)at.vt_bs() * sizeof(bf16), s));
+  CUDA_TRY(cudaMemsetAsync(A->err, 0, 256, s));
+  return WAN_OK;
+}
+
+static wan_status attention_run(wan_attention* A, const void* x, void* out, cudaStream_t s) {
+  Act xa, ya;
+  xa.p = (bf16*)x;
+  ya.p = (bf16*)out;
+  for (Act* a : {&xa, &ya}) {
+    a->B = 1;
+    a->F = A->N;
+    a->H = 1;
+    a->W = A->at.HW;
+    a->C = A->C;
+    a->ldc = A->C;
+  }
+  return attention(A->g, A->qkv, A->proj, A->at, xa, ya, A->N, nullptr, A->err, s);
+}
+
+extern "C" {
+
 wan_status wan_attention_block(const void* x, int32_t N, int32_t H, int32_t W, int32_t C, const wan_tensor* weights,
                                int32_t n_weights, void* out, wan_cuda_stream stream) {
   API_GUARD({
     if (!x || !out || !weights) return fail(WAN_ERR_INVALID_ARG, "null argument");
-    if (N < 1 || H < 1 || W < 1) return fail(WAN_ERR_INVALID_ARG, "N=%d H=%d W=%d", N, H, W);
-    if (C % 64 || C < 64 || C > 1024) return fail(WAN_ERR_UNSUPPORTED, "C=%d (multiple of 64, <= 1024)", C);
     cudaStream_t s = (cudaStream_t)stream;
-    // pick the five tensors by suffix
-    std::vector<wan_tensor> t;
-    const char* suff[5] = {"norm.gamma", "to_qkv.weight", "to_qkv.bias", "proj.weight", "proj.bias"};
-    for (const char* sfx : suff) {
-      const wan_tensor* hit = nullptr;
-      for (int i = 0; i < n_weights; ++i) {
-        const char* nm = weights[i].name;
-        if (!nm) continue;
-        const size_t L = strlen(nm), Ls = strlen(sfx);
-        if (L >= Ls && strcmp(nm + L - Ls, sfx) == 0) hit = &weights[i];
-      }
-      if (!hit) return fail(WAN_ERR_MISSING_WEIGHT, "missing weight '*%s'", sfx);
-      wan_tensor c = *hit;
-      c.name = sfx;
-      t.push_back(c);
-    }
-    WeightTable wt{t.data(), (int)t.size()};
-    DevMem mem;
-    mem.use_async = true;
-    mem.async = s;
-    wan_status r = WAN_OK;
-    float* g = nullptr;
-    ConvW qkv, proj;
-    do {
-      if ((r = pack_gamma(wt, "norm.gamma", C, &g, mem, s)) != WAN_OK) break;
-      if ((r = pack_conv(wt, "to_qkv", 3 * C, C, 1, 1, 1, true, "", 0, qkv, mem, s)) != WAN_OK) break;
-      if ((r = pack_conv(wt, "proj", C, C, 1, 1, 1, true, "", 0, proj, mem, s)) != WAN_OK) break;
-      AttnBufs at;
-      at.HW = H * W;
-      at.HWs = (int)rup(at.HW, 16);
-      at.HWp = (int)rup(at.HW, 64);
-      at.Fmax = N;
-      at.B = 1;
-      at.C = C;
-      auto mk = [&](Act& a, int ch) -> wan_status {
-        a.B = 1;
-        a.F = N;
-        a.H = 1;
-        a.W = at.HW;
-        a.C = ch;
-        a.ldc = ch;
-        void* p;
-        WAN_TRY(mem.alloc(&p, a.bytes()));
-        a.p = (bf16*)p;
-        return WAN_OK;
-      };
-      if ((r = mk(at.an, C)) != WAN_OK || (r = mk(at.qkv, 3 * C)) != WAN_OK || (r = mk(at.O, C)) != WAN_OK) break;
-      void* p;
-      if ((r = mem.alloc(&p, (size_t)at.s_bs() * sizeof(float))) != WAN_OK) break;
-      at.S = (float*)p;
-      if ((r = mem.alloc(&p, (size_t)at.p_bs() * sizeof(bf16))) != WAN_OK) break;
-      at.P = (bf16*)p;
-      if ((r = mem.alloc(&p, (size_t)at.vt_bs() * sizeof(bf16))) != WAN_OK) break;
-      at.Vt = (bf16*)p;
-      int* err;
-      if ((r = mem.alloc((void**)&err, 256)) != WAN_OK) break;
-      if (cudaMemsetAsync(at.P, 0, (size_t)at.p_bs() * sizeof(bf16), s) != cudaSuccess ||
-          cudaMemsetAsync(at.Vt, 0, (size_t)at.vt_bs() * sizeof(bf16), s) != cudaSuccess ||
-          cudaMemsetAsync(err, 0, 256, s) != cudaSuccess) {
-        r = fail(WAN_ERR_CUDA, "memset failed");
-        break;
-      }
-      Act xa, ya;
-      xa.p = (bf16*)x;
-      ya.p = (bf16*)out;
-      for (Act* a : {&xa, &ya}) {
-        a->B = 1;
-        a->F = N;
-        a->H = 1;
-        a->W = at.HW;
-        a->C = C;
-        a->ldc = C;
-      }
-      r = attention(g, qkv, proj, at, xa, ya, N, nullptr, err, s);
-    } while (false);
-    mem.release();
+    wan_attention A;
+    A.mem.use_async = true;
+    A.mem.async = s;
+    wan_status r = attention_build(weights, n_weights, N, H, W, C, s, &A);
+    if (r == WAN_OK) r = attention_run(&A, x, out, s);
+    A.mem.release();
     return r;
   })
+}
+
+wan_status wan_attention_create(const wan_tensor* weights, int32_t n_weights, int32_t N, int32_t H, int32_t W,
+                                int32_t C, wan_cuda_stream stream, wan_attention** out) {
+  API_GUARD({
+    if (!out) return fail(WAN_ERR_INVALID_ARG, "null output handle");
+    *out = nullptr;
+    std::unique_ptr<wan_attention> A(new wan_attention());
+    WAN_TRY(attention_build(weights, n_weights, N, H, W, C, (cudaStream_t)stream, A.get()));
+    CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+    *out = A.release();
+    return WAN_OK;
+  })
+}
+
+wan_status wan_attention_run(wan_attention* A, const void* x, void* out, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!A || !x || !out) return fail(WAN_ERR_INVALID_ARG, "null argument");
+    return attention_run(A, x, out, (cudaStream_t)stream);
+  })
+}
+
+void wan_attention_destroy(wan_attention* A) {
+  if (!A) return;
+  cudaDeviceSynchronize();
+  A->mem.release();
+  delete A;
 }
 
 wan_status wan_causal_conv3d(const void* x, int32_t B, int32_t n_hist, int32_t F, int32_t H, int32_t W, int32_t Cin,
