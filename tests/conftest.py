@@ -22,9 +22,12 @@ def tiny_weights():
 def pytest_collection_finish(session):
     """Starts the background oracle runs of the full-size parity tests as soon
     as one of them is selected, so they overlap the other GPU tests."""
-    if any("test_gpu_fullsize.py" in item.nodeid for item in session.items):
-        from tests import oracle_jobs
-        oracle_jobs.start()
+    if session.config.option.collectonly:
+        return
+    from tests import oracle_jobs
+    jobs = oracle_jobs.jobs_for([item.nodeid for item in session.items])
+    if jobs:
+        oracle_jobs.start(jobs)
 
 
 def pytest_sessionfinish(session, exitstatus):

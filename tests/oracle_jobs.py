@@ -16,7 +16,6 @@ loop, on the first ``n_latent`` latent frames.
 
 from __future__ import annotations
 
-import concurrent.futures
 import multiprocessing
 import os
 
@@ -26,6 +25,16 @@ WORKERS = 3
 
 _pool = None
 _futures: dict = {}
+
+
+def jobs_for(nodeids) -> tuple:
+    """The jobs that the selected full-size tests need (by test id)."""
+    need = []
+    for job in JOBS:
+        tag = {"720p": "[720p]", "portrait": "[portrait]", "480p_b2": "480p", "wan21_720p": "wan21"}[job[0]]
+        if any("test_gpu_fullsize.py" in n and tag in n for n in nodeids):
+            need.append(job)
+    return tuple(need)
 
 
 def _init_worker(threads: int) -> None:
@@ -54,25 +63,26 @@ def start(jobs=JOBS) -> None:
     if _pool is not None:
         return
     cores = os.cpu_count() or 4
-    _pool = concurrent.futures.ProcessPoolExecutor(
-        max_workers=WORKERS, mp_context=multiprocessing.get_context("spawn"),
-        initializer=_init_worker, initargs=(max(1, cores // WORKERS),))
+    _pool = multiprocessing.get_context("spawn").Pool(
+        processes=WORKERS, initializer=_init_worker, initargs=(max(1, cores // WORKERS),))
     for name, n in jobs:
-        _futures[(name, n)] = _pool.submit(run_job, name, n)
+        _futures[(name, n)] = _pool.apply_async(run_job, (name, n))
 
 
 def result(name: str, n_latent: int):
     """The job's video (starting the pool if nobody has); blocks until done."""
+    if _pool is None:
+        start(((name, n_latent),))
     if (name, n_latent) not in _futures:
-        start()
-    if (name, n_latent) not in _futures:
-        _futures[(name, n_latent)] = _pool.submit(run_job, name, n_latent)
-    return _futures[(name, n_latent)].result()
+        _futures[(name, n_latent)] = _pool.apply_async(run_job, (name, n_latent))
+    return _futures[(name, n_latent)].get()
 
 
 def shutdown() -> None:
+    """Stops the workers, including any still computing."""
     global _pool
     if _pool is not None:
-        _pool.shutdown(wait=False, cancel_futures=True)
+        _pool.terminate()
+        _pool.join()
         _pool = None
         _futures.clear()
