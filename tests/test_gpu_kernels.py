@@ -69,7 +69,7 @@ def _attn_weights(C, seed, qkv_scale=1.0):
     }
 
 
-def _attention_check(wv, N, C, H, W, frames, seed, qkv_scale=1.0, rel_tol=1e-2):
+def _attention_check(wv, N, C, H, W, frames, seed, qkv_scale=1.0, rel_tol=1e-2, abs_tol=4e-2):
     w = _attn_weights(C, seed, qkv_scale)
     x = _bf(np.random.default_rng(seed + 1).standard_normal((N, H * W, C)))
     got = wv.attention_block(to_dev(x, torch.bfloat16), {k: to_dev(v) for k, v in w.items()}, H, W)
@@ -80,7 +80,7 @@ def _attention_check(wv, N, C, H, W, frames, seed, qkv_scale=1.0, rel_tol=1e-2):
         err = np.abs(got[f] - ref)
         rel = np.linalg.norm(got[f] - ref) / np.linalg.norm(ref)
         record(f"attention block C={C} {H}x{W} frame {f} (bf16)", float(err.max()), None, rel_l2=float(rel))
-        assert err.max() <= 4e-2 and rel <= rel_tol, (f, float(err.max()), float(rel))
+        assert err.max() <= abs_tol and rel <= rel_tol, (f, float(err.max()), float(rel))
 
 
 def test_attention_small(wv):
@@ -104,10 +104,12 @@ def test_attention_flash_large_logits(wv):
     """qkv weights 4x larger (logits 16x): over 4800 keys the row maxima of
     later key blocks exceed the first block's by more than the rescale
     threshold (8 in log2 units) for many rows, so the running max moves and
-    the output accumulator is rescaled.  The sharper softmax amplifies the
-    bf16 rounding of q and k (stored activations) by the logit scale, hence
-    the relative bound of 2e-2 instead of 1e-2."""
-    _attention_check(wv, N=1, C=384, H=60, W=80, frames=[0], seed=12, qkv_scale=4.0, rel_tol=2e-2)
+    the output accumulator is rescaled.  The GPU stores q and k in bf16 (the
+    oracle keeps them in fp32): a rounding of 2^-9 relative moves a logit of
+    30 by about 0.06, and the sharper softmax passes that on to the output,
+    so the bounds here are max |diff| <= 0.15 and relative L2 <= 2e-2 (a
+    wrong rescale factor would put whole rows off by O(1))."""
+    _attention_check(wv, N=1, C=384, H=60, W=80, frames=[0], seed=12, qkv_scale=4.0, rel_tol=2e-2, abs_tol=0.15)
 
 
 def test_attention_flash_wan21_720p_frame(wv):

@@ -12,8 +12,9 @@
 //   softmax      row max and exp2 of the scaled scores (online softmax: the
 //                running max m only moves when a block's max exceeds it by more
 //                than 8 in log2 units, so P <= 256 and O is rescaled rarely),
-//                P_j as bf16 into shared memory in the MMA's operand layout
-// and at the end O / l is written as bf16.  Keys past HW are masked to -inf;
+//                P_j rounded to bf16 into shared memory in the MMA's operand
+//                layout, and the row sum l of the rounded values
+// and at the end O / l is written as bf16 (the weights of V sum to one).  Keys past HW are masked to -inf;
 // queries past HW are computed on zero rows and not stored.
 //
 // Warp roles (256 threads): warp 0 lane 0 TMA producer (Q once; per key block
@@ -236,10 +237,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
         alpha = exp2f(m - mb);
         m = mb;
       }
+      // P in bf16, and the row sum of the rounded values: the weights that
+      // multiply V then sum to exactly 1 after the final division by l
       float rs = 0.f;
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
-        t[i] = exp2f(t[i] - m);
+        t[i] = __bfloat162float(__float2bfloat16_rn(exp2f(t[i] - m)));
         rs += t[i];
       }
       l = l * alpha + rs;

@@ -172,6 +172,26 @@ __host__ __device__ __forceinline__ long long conv_units(const ConvArgs& a, int 
   return (long long)a.tiles_n * (a.subpix ? 4 : 1) * sp * a.frames * a.batches;
 }
 
+// The k-th tile a cluster processes (-1 past the end).  With T > 1 (the
+// fused norm over T N tiles) it takes whole groups of T consecutive units --
+// the N tiles of one position tile, n fastest -- so one CTA sees every
+// channel of its positions; T = 1 is the plain stride over units.
+__device__ __forceinline__ int cluster_unit(int k, int unit0, int unit_step, int T, int num_units) {
+  const int g = unit0 + (k / T) * unit_step;
+  const int u = g * T + k % T;
+  return u < num_units ? u : -1;
+}
+
+// Output position of accumulator row m of a tile (sub-pixel tiles: of its
+// phase), and whether it lies inside the frame.
+__device__ __forceinline__ long long tile_pos(const ConvArgs& args, const TileCoord& tc, int m, bool* inside) {
+  const int yy = tc.ty * args.box_h + m / args.box_w;
+  const int xx = tc.tx * args.box_w + m % args.box_w;
+  *inside = yy < args.H && xx < args.W;
+  return args.subpix ? (long long)(2 * yy + (tc.phase >> 1)) * (2 * args.W) + (2 * xx + (tc.phase & 1))
+                     : (long long)yy * args.W + xx;
+}
+
 // Epilogue of a tile that holds all N output channels, with the RMS norm of
 // the output fused in.  Pass 1: y = acc + bias (+ residual), its sum of
 // squares, and the raw y to `out` if requested.  Pass 2: y again, scaled by
@@ -249,12 +269,105 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
   }
 }
 
+// Fused RMS norm over T > 1 N tiles (plain bf16 output; the cluster takes
+// the T tiles of a position tile one after the other, so the same thread
+// sees the same channels of each).  Pass 1, per tile: y = acc + bias (+
+// residual) is rounded to bf16 and stored raw -- to `out`, or, when the raw
+// output is not wanted, into out2 as a temporary -- and the sum of squares of
+// the stored values accumulates in ss_acc.  The TMEM buffer is free after it.
+template <int BN>
+__device__ __forceinline__ void norm_part_store(const ConvArgs& args, uint32_t tbase, int tn, int f, int b,
+                                                long long pos, bool valid, int c_begin, int c_end, float& ss_acc) {
+  const __nv_bfloat16* rp = nullptr;
+  if (args.res)
+    rp = static_cast<const __nv_bfloat16*>(args.res) + (long long)b * args.res_bs +
+         (long long)(args.res_f0 + f) * args.res_fs + pos * args.res_ldc;
+  __nv_bfloat16* raw =
+      args.out ? static_cast<__nv_bfloat16*>(args.out) + (long long)b * args.out_bs +
+                     (long long)(args.out_f0 + f * args.out_fmul) * args.out_fs + pos * args.out_ldc
+               : static_cast<__nv_bfloat16*>(args.out2) + (long long)b * args.out2_bs +
+                     (long long)ring_slot(args.out2_f0 + f, args.out2_fmod) * args.out2_fs + pos * args.out2_ldc;
+#pragma unroll 1
+  for (int c = c_begin; c < c_end; ++c) {
+    const int n0 = tn * BN + c * 16;
+    if (n0 >= args.N) break;  // warp-uniform
+    __syncwarp();
+    uint32_t r[16];
+    tmem_ld16(tbase + c * 16, r);
+    tmem_ld_wait();
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    if (args.bias) add_bias16(args.bias + n0, v);
+    if (!valid) continue;
+    if (rp) add16_bf16(rp + n0, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+      ss_acc = fmaf(v[i], v[i], ss_acc);
+    }
+    store16(raw + n0, 0, v);
+  }
+}
+
+// After the last of the T tiles: the two column halves' sums of squares are
+// combined through shared memory, and every channel of the position is read
+// back raw, scaled by 1 / max(||y||, 1e-12) and sqrt(C) * gamma, SiLU'd, and
+// written to out2.
+template <int BN>
+__device__ __forceinline__ void norm_finish(const ConvArgs& args, int T, int f, int b, long long pos, bool valid,
+                                            int c_begin, int c_end, float* red, int m, int h, uint32_t ssbar,
+                                            uint32_t ss_parity, float& ss_acc) {
+  const long long lim = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
+  red[h * 128 + m] = ss_acc;
+  mbar_arrive(ssbar);
+  mbar_wait_bounded(ssbar, ss_parity, args.err, kDevTimeoutAccum, lim);
+  const float rinv = 1.0f / fmaxf(sqrtf(ss_acc + red[(1 - h) * 128 + m]), 1e-12f);
+  ss_acc = 0.f;
+  if (!valid) return;
+  __nv_bfloat16* nrm = static_cast<__nv_bfloat16*>(args.out2) + (long long)b * args.out2_bs +
+                       (long long)ring_slot(args.out2_f0 + f, args.out2_fmod) * args.out2_fs + pos * args.out2_ldc;
+  const __nv_bfloat16* raw =
+      args.out ? static_cast<const __nv_bfloat16*>(args.out) + (long long)b * args.out_bs +
+                     (long long)(args.out_f0 + f * args.out_fmul) * args.out_fs + pos * args.out_ldc
+               : nrm;
+#pragma unroll 1
+  for (int t = 0; t < T; ++t) {
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; ++c) {
+      const int n0 = t * BN + c * 16;
+      if (n0 >= args.N) break;
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      add16_bf16(raw + n0, v);
+      float g[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 g4 = __ldg(reinterpret_cast<const float4*>(args.norm_gs + n0) + i);
+        g[4 * i] = g4.x;
+        g[4 * i + 1] = g4.y;
+        g[4 * i + 2] = g4.z;
+        g[4 * i + 3] = g4.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float y = v[i] * (rinv * g[i]);
+        if (args.norm_silu) y = __fdividef(y, 1.0f + __expf(-y));
+        v[i] = y;
+      }
+      store16(nrm + n0, 0, v);
+    }
+  }
+}
+
 // Epilogue of one tile: 4 warps, thread q*32 + lane owns accumulator row
 // (TMEM lane) q*32 + lane, i.e. one output position, and walks its BN columns
 // 16 at a time.
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tacc, const TileCoord& tc, int q, int h,
-                                              int lane, bool got, float* red, uint32_t ssbar, uint32_t ss_parity) {
+                                              int lane, bool got, float* red, uint32_t ssbar, uint32_t ss_parity,
+                                              float& ss_acc) {
   const int m = q * 32 + lane;
   const int pi = tc.phase >> 1, pj = tc.phase & 1;
   const int yy = tc.ty * args.box_h + m / args.box_w;
@@ -267,6 +380,10 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
   constexpr int NC = BN / 16;  // 16-column chunks; half h takes [h*NC/2, (h+1)*NC/2)
   const int c_begin = (h * NC) / 2, c_end = ((h + 1) * NC) / 2;
   if constexpr (EPI == kEpiStore) {
+    if (args.norm_gs && args.norm_tiles > 1) {
+      norm_part_store<BN>(args, tbase, tc.tn, f, b, pos, valid, c_begin, c_end, ss_acc);
+      return;
+    }
     if (args.norm_gs) {
       epilogue_norm_tile<BN>(args, tbase, f, b, pos, valid, c_begin, c_end, red, m, h, ssbar, ss_parity);
       return;
@@ -347,6 +464,15 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
         } else {
           add16(src + n0, 0, v, args.dup_lo);
         }
+        if (args.norm_tiles > 1) {
+          // fused norm over the N tiles (plain bf16): the sum of squares of
+          // the values as stored; the group's last tile normalises
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+            ss_acc = fmaf(v[i], v[i], ss_acc);
+          }
+        }
       }
       int fo = args.out_f0 + f * args.out_fmul;
       int no = n0;
@@ -401,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_units = (int)conv_units(args, CL);
   const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
   const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
+  const int T = args.norm_tiles > 1 ? args.norm_tiles : 1;  // N tiles per position group
   constexpr uint16_t kPairMask = (1u << CL) - 1;
 
   if (threadIdx.x == 0) {
@@ -438,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     int it = 0, ia = 0;  // B (or shared) stages and, in band mode, A boxes issued
     bool ok = true;
-    for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
+    for (int k = 0, unit; ok && (unit = cluster_unit(k, unit0, unit_step, T, num_units)) >= 0; ++k) {
       const TileCoord tc = tile_coord(args, unit, CL, rank);
       if constexpr (BAND) {
         // per tap (dt, dx) and 64-channel block: one 16 x 10 A box (rows from
@@ -572,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int last_kb = args.taps[0].nkb - 1;
     int ia_slot = 0, ia_phase = 0;  // band mode: A ring
     bool ok = true;
-    for (int unit = unit0; unit < num_units && ok; unit += unit_step, ++lt) {
+    for (int unit; ok && (unit = cluster_unit(lt, unit0, unit_step, T, num_units)) >= 0; ++lt) {
       const int buf = lt & 1, use = lt >> 1;
       if (use > 0 && !mbar_wait_bounded(smem_u32(&tempty[buf]), (use - 1) & 1, args.err, kDevTimeoutAccum, lim)) {
         *abort_flag = 1;
@@ -695,17 +822,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, h = (warp - 4) >> 2;
     int lt = 0;
-    for (int unit = unit0; unit < num_units; unit += unit_step, ++lt) {
+    float ss_acc = 0.f;  // fused norm over T tiles: this thread's partial sum of squares
+    for (int unit; (unit = cluster_unit(lt, unit0, unit_step, T, num_units)) >= 0; ++lt) {
       const int buf = lt & 1, use = lt >> 1;
       const bool got =
           !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum, lim);
       if (!got) *abort_flag = 1;
       tc_fence_after();
-      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tile_coord(args, unit, CL, rank), q, h, lane, got,
-                             red + buf * 256, smem_u32(&ssbar[buf]), use & 1);
+      const TileCoord tc = tile_coord(args, unit, CL, rank);
+      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tc, q, h, lane, got, red + buf * 256,
+                             smem_u32(&ssbar[buf]), use & 1, ss_acc);
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[buf]));
       if (!got) break;
+      if constexpr (EPI == kEpiStore || EPI == kEpiDup) {
+        if (T > 1 && lt % T == T - 1) {
+          // the group's last N tile: normalise all of its channels (groups
+          // alternate halves of the reduction buffer and use barrier 0)
+          const int grp = lt / T;
+          bool inside;
+          const long long pos = tile_pos(args, tc, q * 32 + lane, &inside);
+          constexpr int NC = BN / 16;
+          norm_finish<BN>(args, T, tc.f, tc.b, pos, inside, (h * NC) / 2, ((h + 1) * NC) / 2, red + (grp & 1) * 256,
+                          q * 32 + lane, h, smem_u32(&ssbar[0]), grp & 1, ss_acc);
+        }
+      }
     }
   }
   tc_fence_before();

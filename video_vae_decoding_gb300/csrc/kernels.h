@@ -104,6 +104,11 @@ struct ConvArgs {
   // (b, out2_f0 + f, position); `out` may be null (only the normalised y).
   const float* norm_gs;
   int norm_silu;
+  // > 1: the norm spans norm_tiles N tiles (== tiles_n; bf16 plain output);
+  // a CTA pair takes all N tiles of a position tile in a row, each tile
+  // stores y raw (to out, or into out2 when out is null) and the last one
+  // normalises all channels from the stored values.
+  int norm_tiles;
   void* out2;
   long long out2_bs, out2_fs;
   int out2_ldc, out2_f0, out2_lo;

@@ -908,8 +908,13 @@ struct NormOut {
   bool silu = true;
   const Act* ring = nullptr;
 };
-// One N tile holds every output channel: the epilogue can normalise.
-static bool single_tile(const ConvW& cw) { return cw.co_pad == cw.bn && !cw.subpix; }
+// The conv's epilogue can normalise its output: one N tile holds every
+// channel, or (plain bf16 format) up to four N tiles that one CTA pair takes
+// in a row (the last one normalises all channels from the stored raw values).
+static int norm_tiles(const ConvW& cw) { return cw.co_pad / cw.bn; }
+static bool norm_fusable(const ConvW& cw) {
+  return !cw.subpix && (norm_tiles(cw) == 1 || (!cw.split && norm_tiles(cw) <= 4));
+}
 
 // 3-frame causal conv over ring `in` (F current frames) into `out`.
 static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F, const OutSpec& o, const Act* res,
@@ -918,7 +923,11 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
   WAN_TRY(conv_setup(cw, in, 0, sc, 0, F, L));
   set_out(L.args, o);
   if (nrm) {
-    if (!single_tile(cw)) return fail(WAN_ERR_INTERNAL, "fused norm over several N tiles");
+    if (!norm_fusable(cw)) return fail(WAN_ERR_INTERNAL, "fused norm not available for this conv");
+    if (norm_tiles(cw) > 1) {
+      if (o.f32 || o.lo || (res && res->lo) || nrm->ring->lo) return fail(WAN_ERR_INTERNAL, "multi-tile norm format");
+      L.args.norm_tiles = norm_tiles(cw);
+    }
     L.args.norm_gs = nrm->gs;
     L.args.norm_silu = nrm->silu ? 1 : 0;
     L.args.out2 = nrm->ring->p;
@@ -953,7 +962,7 @@ static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act&
   if (!normed)
     ELT(&st->prof, kKindNorm, nb * r.ci,
         launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s, x.lo, ring1.lo));
-  if (single_tile(r.c1)) {  // conv1 writes SiLU(norm2(h)) straight into conv2's ring
+  if (norm_fusable(r.c1)) {  // conv1 writes SiLU(norm2(h)) straight into conv2's ring
     NormOut n2;
     n2.gs = r.g2;
     n2.ring = &ring2;
@@ -964,7 +973,7 @@ static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act&
     ELT(&st->prof, kKindNorm, nb * r.co,
         launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s, Ht.lo, ring2.lo));
   }
-  const bool fuse_next = next && single_tile(r.c2);
+  const bool fuse_next = next && norm_fusable(r.c2);
   if (next_done) *next_done = fuse_next;
   const NormOut* nx = fuse_next ? next : nullptr;
   if (r.ci != r.co)
@@ -1158,7 +1167,8 @@ static wan_status time_upsample(wan_vae_stream* st, const ConvW& tc, const Act& 
 // "The parts", fifth and sixth bullets); y is at twice x's resolution.  The
 // Wan2.1 decoder has no DupUp3D: the conv's result is stored as it is.
 static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, const Act& blk, int ft, bool first,
-                           Act& y, int F, cudaStream_t s) {
+                           Act& y, int F, cudaStream_t s, const NormOut* nrm = nullptr, bool* nrm_done = nullptr) {
+  if (nrm_done) *nrm_done = false;
   ConvLaunch L;
   if (!cw.subpix || y.H != 2 * x.H || y.W != 2 * x.W) return fail(WAN_ERR_INTERNAL, "resample shapes");
   WAN_TRY(conv_setup(cw, x, 0, nullptr, 0, F, L));
@@ -1186,6 +1196,19 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
     L.args.dup_pairs = 1;
   else
     return fail(WAN_ERR_UNSUPPORTED, "DupUp3D with %d -> %d channels, ft %d", blk.C, cw.Co, ft);
+  // the next block's first RMS norm + SiLU, fused over the N tiles (plain bf16)
+  if (nrm && !cw.split && norm_tiles(cw) > 1 && norm_tiles(cw) <= 4 && !y.lo && !nrm->ring->lo) {
+    L.args.norm_tiles = norm_tiles(cw);
+    L.args.norm_gs = nrm->gs;
+    L.args.norm_silu = nrm->silu ? 1 : 0;
+    L.args.out2 = nrm->ring->p;
+    L.args.out2_bs = nrm->ring->bs();
+    L.args.out2_fs = nrm->ring->fs();
+    L.args.out2_ldc = nrm->ring->ldc;
+    L.args.out2_f0 = nrm->ring->slot(2);
+    L.args.out2_fmod = nrm->ring->fmod;
+    if (nrm_done) *nrm_done = true;
+  }
   return run(L, &st->prof, kKindResample, nominal, st->err_dev, s, executed);
 }
 
@@ -1194,9 +1217,10 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
 // into the previous block's conv2 where possible.  `last` optionally names
 // the norm that consumes the final output.
 static wan_status resnet_chain(wan_vae_stream* st, const Resnet* r, Act* R, Act* rings, Act& Ht, int F,
-                               const NormOut* last, cudaStream_t s, bool* last_done = nullptr) {
+                               const NormOut* last, cudaStream_t s, bool* last_done = nullptr,
+                               bool first_normed = false) {
   const int io[3][2] = {{0, 1}, {1, 2}, {2, 1}};
-  bool normed = false;
+  bool normed = first_normed;  // rings[0] already holds SiLU(norm1(R[0])) from R[0]'s producer
   for (int j = 0; j < 3; ++j) {
     NormOut nx;
     const NormOut* next = nullptr;
@@ -1227,27 +1251,51 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
       launch_post_quant(z, z_f32, m->zdim, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b,
                         m->zstat_on ? m->zstat : nullptr, st->ringIn.view(2), m->split ? 0 : 1, s, st->ringIn.lo));
   // 2. conv_in, mid block
-  WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s));
-  WAN_TRY(resnet(st, m->mid[0], st->RA[0], st->ringA[0], st->ringA[1], st->HA, st->RA[1], FA, s));
+  // (conv_in also writes SiLU(norm1(.)) of its output into the first resnet's ring)
+  NormOut n_mid;
+  n_mid.gs = m->mid[0].g1;
+  n_mid.ring = &st->ringA[0];
+  const bool in_normed = norm_fusable(m->conv_in);
+  WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s, kKindConv333,
+                    in_normed ? &n_mid : nullptr));
+  WAN_TRY(resnet(st, m->mid[0], st->RA[0], st->ringA[0], st->ringA[1], st->HA, st->RA[1], FA, s, in_normed));
   WAN_TRY(attention(m->attn_g, m->qkv, m->proj, st->at, st->RA[1], st->RA[2], FA, &st->prof, st->err_dev, s));
-  WAN_TRY(resnet(st, m->mid[1], st->RA[2], st->ringA[2], st->ringA[3], st->HA, st->RA[0], FA, s));
+  // the second mid resnet's conv2 also normalises for up block 0's first resnet
+  NormOut n_up0;
+  n_up0.gs = m->ups[0][0].g1;
+  n_up0.ring = &st->ringA[4];
+  bool up0_normed = false;
+  WAN_TRY(resnet(st, m->mid[1], st->RA[2], st->ringA[2], st->ringA[3], st->HA, st->RA[0], FA, s, false, &n_up0,
+                 &up0_normed));
   // up block 0 (level A -> B); block input RA[0]
-  WAN_TRY(resnet_chain(st, m->ups[0], st->RA, st->ringA + 4, st->HA, FA, nullptr, s));
+  WAN_TRY(resnet_chain(st, m->ups[0], st->RA, st->ringA + 4, st->HA, FA, nullptr, s, nullptr, up0_normed));
   WAN_TRY(time_upsample(st, m->tconv[0], st->RA[1], st->tcA, st->tuA, FA, first, s));
-  WAN_TRY(resample(st, m->resample[0], st->tuA, st->RA[0], 2, first, st->RB[0], FB, s));
+  NormOut n_up1;
+  n_up1.gs = m->ups[1][0].g1;
+  n_up1.ring = &st->ringB[0];
+  bool up1_normed = false;
+  WAN_TRY(resample(st, m->resample[0], st->tuA, st->RA[0], 2, first, st->RB[0], FB, s, &n_up1, &up1_normed));
   // up block 1 (level B -> C); block input RB[0]
-  WAN_TRY(resnet_chain(st, m->ups[1], st->RB, st->ringB, st->HB, FB, nullptr, s));
+  WAN_TRY(resnet_chain(st, m->ups[1], st->RB, st->ringB, st->HB, FB, nullptr, s, nullptr, up1_normed));
   WAN_TRY(time_upsample(st, m->tconv[1], st->RB[1], st->tcB, st->tuB, FB, first, s));
-  WAN_TRY(resample(st, m->resample[1], st->tuB, st->RB[0], 2, first, st->RC[0], FC, s));
+  NormOut n_up2;
+  n_up2.gs = m->ups[2][0].g1;
+  n_up2.ring = &st->ringC[0];
+  bool up2_normed = false;
+  WAN_TRY(resample(st, m->resample[1], st->tuB, st->RB[0], 2, first, st->RC[0], FC, s, &n_up2, &up2_normed));
   // up block 2 (level C -> D); block input RC[0]
-  WAN_TRY(resnet_chain(st, m->ups[2], st->RC, st->ringC, st->HC, FC, nullptr, s));
-  WAN_TRY(resample(st, m->resample[2], st->RC[1], st->RC[0], 1, first, st->RD[0], FC, s));
+  WAN_TRY(resnet_chain(st, m->ups[2], st->RC, st->ringC, st->HC, FC, nullptr, s, nullptr, up2_normed));
+  NormOut n_up3;
+  n_up3.gs = m->ups[3][0].g1;
+  n_up3.ring = &st->ringD[0];
+  bool up3_normed = false;
+  WAN_TRY(resample(st, m->resample[2], st->RC[1], st->RC[0], 1, first, st->RD[0], FC, s, &n_up3, &up3_normed));
   // up block 3 (level D)
   NormOut nout;  // norm_out + SiLU, fused into the last conv2 when possible
   nout.gs = m->out_g;
   nout.ring = &st->ringOut;
   bool out_done = false;
-  WAN_TRY(resnet_chain(st, m->ups[3], st->RD, st->ringD, st->HD, FC, &nout, s, &out_done));
+  WAN_TRY(resnet_chain(st, m->ups[3], st->RD, st->ringD, st->HD, FC, &nout, s, &out_done, up3_normed));
   // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
   if (!out_done) {
     ELT(&st->prof, kKindNorm, 4.0 * st->B * FC * st->RD[1].H * st->RD[1].W * m->base * (m->split ? 2 : 1),
