@@ -172,16 +172,6 @@ __host__ __device__ __forceinline__ long long conv_units(const ConvArgs& a, int 
   return (long long)a.tiles_n * (a.subpix ? 4 : 1) * sp * a.frames * a.batches;
 }
 
-// The k-th tile a cluster processes (-1 past the end).  With T > 1 (the
-// fused norm over T N tiles) it takes whole groups of T consecutive units --
-// the N tiles of one position tile, n fastest -- so one CTA sees every
-// channel of its positions; T = 1 is the plain stride over units.
-__device__ __forceinline__ int cluster_unit(int k, int unit0, int unit_step, int T, int num_units) {
-  const int g = unit0 + (k / T) * unit_step;
-  const int u = g * T + k % T;
-  return u < num_units ? u : -1;
-}
-
 // Output position of accumulator row m of a tile (sub-pixel tiles: of its
 // phase), and whether it lies inside the frame.
 __device__ __forceinline__ long long tile_pos(const ConvArgs& args, const TileCoord& tc, int m, bool* inside) {
@@ -269,12 +259,11 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
   }
 }
 
-// Fused RMS norm over T > 1 N tiles (plain bf16 output; the cluster takes
-// the T tiles of a position tile one after the other, so the same thread
-// sees the same channels of each).  Pass 1, per tile: y = acc + bias (+
-// residual) is rounded to bf16 and stored raw -- to `out`, or, when the raw
-// output is not wanted, into out2 as a temporary -- and the sum of squares of
-// the stored values accumulates in ss_acc.  The TMEM buffer is free after it.
+// Fused RMS norm over T > 1 N tiles (plain bf16 output), first step, per
+// tile: y = acc + bias (+ residual) is rounded to bf16 and stored raw -- to
+// `out`, or, when the raw output is not wanted, into out2 as a temporary --
+// and the sum of squares of the stored values accumulates in ss_acc.  The
+// TMEM buffer is free after it.
 template <int BN>
 __device__ __forceinline__ void norm_part_store(const ConvArgs& args, uint32_t tbase, int tn, int f, int b,
                                                 long long pos, bool valid, int c_begin, int c_end, float& ss_acc) {
@@ -310,21 +299,16 @@ __device__ __forceinline__ void norm_part_store(const ConvArgs& args, uint32_t t
   }
 }
 
-// After the last of the T tiles: the two column halves' sums of squares are
-// combined through shared memory, and every channel of the position is read
-// back raw, scaled by 1 / max(||y||, 1e-12) and sqrt(C) * gamma, SiLU'd, and
-// written to out2.
+// The fused norm's last step, run by the CTA that completes a position
+// tile's group of T N tiles: every channel of the position (this thread's
+// column half of each of the T tiles) is read back raw -- bypassing L1, as
+// the other tiles were written by other SMs -- scaled by 1 / max(||y||,
+// 1e-12) and sqrt(C) * gamma, SiLU'd, and written to out2.
 template <int BN>
-__device__ __forceinline__ void norm_finish(const ConvArgs& args, int T, int f, int b, long long pos, bool valid,
-                                            int c_begin, int c_end, float* red, int m, int h, uint32_t ssbar,
-                                            uint32_t ss_parity, float& ss_acc) {
-  const long long lim = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
-  red[h * 128 + m] = ss_acc;
-  mbar_arrive(ssbar);
-  mbar_wait_bounded(ssbar, ss_parity, args.err, kDevTimeoutAccum, lim);
-  const float rinv = 1.0f / fmaxf(sqrtf(ss_acc + red[(1 - h) * 128 + m]), 1e-12f);
-  ss_acc = 0.f;
+__device__ __forceinline__ void norm_finish_global(const ConvArgs& args, int T, int f, int b, long long pos,
+                                                   bool valid, int c_begin, int c_end, float ss) {
   if (!valid) return;
+  const float rinv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
   __nv_bfloat16* nrm = static_cast<__nv_bfloat16*>(args.out2) + (long long)b * args.out2_bs +
                        (long long)ring_slot(args.out2_f0 + f, args.out2_fmod) * args.out2_fs + pos * args.out2_ldc;
   const __nv_bfloat16* raw =
@@ -338,9 +322,17 @@ __device__ __forceinline__ void norm_finish(const ConvArgs& args, int T, int f, 
       const int n0 = t * BN + c * 16;
       if (n0 >= args.N) break;
       float v[16];
+      const uint4* rs = reinterpret_cast<const uint4*>(raw + n0);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
-      add16_bf16(raw + n0, v);
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint4 a4 = __ldcg(rs + hh);
+        const uint32_t w[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * hh + 2 * i] = bf16_lo(w[i]);
+          v[8 * hh + 2 * i + 1] = bf16_hi(w[i]);
+        }
+      }
       float g[16];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -527,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_units = (int)conv_units(args, CL);
   const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
   const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
-  const int T = args.norm_tiles > 1 ? args.norm_tiles : 1;  // N tiles per position group
+  const int T = args.norm_tiles > 1 ? args.norm_tiles : 1;  // N tiles a fused norm spans
   constexpr uint16_t kPairMask = (1u << CL) - 1;
 
   if (threadIdx.x == 0) {
@@ -565,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     int it = 0, ia = 0;  // B (or shared) stages and, in band mode, A boxes issued
     bool ok = true;
-    for (int k = 0, unit; ok && (unit = cluster_unit(k, unit0, unit_step, T, num_units)) >= 0; ++k) {
+    for (int unit = unit0; unit < num_units && ok; unit += unit_step) {
       const TileCoord tc = tile_coord(args, unit, CL, rank);
       if constexpr (BAND) {
         // per tap (dt, dx) and 64-channel block: one 16 x 10 A box (rows from
@@ -699,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int last_kb = args.taps[0].nkb - 1;
     int ia_slot = 0, ia_phase = 0;  // band mode: A ring
     bool ok = true;
-    for (int unit; ok && (unit = cluster_unit(lt, unit0, unit_step, T, num_units)) >= 0; ++lt) {
+    for (int unit = unit0; unit < num_units && ok; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
       if (use > 0 && !mbar_wait_bounded(smem_u32(&tempty[buf]), (use - 1) & 1, args.err, kDevTimeoutAccum, lim)) {
         *abort_flag = 1;
@@ -823,10 +815,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, h = (warp - 4) >> 2;
     int lt = 0;
     float ss_acc = 0.f;  // fused norm over T tiles: this thread's partial sum of squares
-    for (int unit; (unit = cluster_unit(lt, unit0, unit_step, T, num_units)) >= 0; ++lt) {
+    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    for (int unit = unit0; unit < num_units; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
-      const bool got =
-          !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum, lim);
+      bool got = !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum, lim);
+      if (T > 1) got = epi_all(got);  // the epilogue warps meet at barriers below: agree first
       if (!got) *abort_flag = 1;
       tc_fence_after();
       const TileCoord tc = tile_coord(args, unit, CL, rank);
@@ -836,15 +829,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(smem_u32(&tempty[buf]));
       if (!got) break;
       if constexpr (EPI == kEpiStore || EPI == kEpiDup) {
-        if (T > 1 && lt % T == T - 1) {
-          // the group's last N tile: normalise all of its channels (groups
-          // alternate halves of the reduction buffer and use barrier 0)
-          const int grp = lt / T;
+        if (T > 1) {
+          // The N tiles of a position tile run on different CTAs: each adds
+          // its rows' partial sums of squares to the group's slots and counts
+          // itself in; the CTA that arrives last normalises every channel,
+          // reading the other tiles' raw values (fenced before their count).
+          const int grp = (unit / args.tiles_n) * CL + rank;  // the position tile (each CTA of a pair has its own)
+          const int m = q * 32 + lane;
           bool inside;
-          const long long pos = tile_pos(args, tc, q * 32 + lane, &inside);
-          constexpr int NC = BN / 16;
-          norm_finish<BN>(args, T, tc.f, tc.b, pos, inside, (h * NC) / 2, ((h + 1) * NC) / 2, red + (grp & 1) * 256,
-                          q * 32 + lane, h, smem_u32(&ssbar[0]), grp & 1, ss_acc);
+          const long long pos = tile_pos(args, tc, m, &inside);
+          atomicAdd(args.norm_ss + (long long)grp * 128 + m, ss_acc);
+          ss_acc = 0.f;
+          __threadfence();
+          epi_sync();
+          if (warp == 4 && lane == 0) *last_flag = atomicAdd(args.norm_cnt + grp, 1) == T - 1 ? 1 : 0;
+          epi_sync();
+          if (*last_flag) {
+            __threadfence();
+            constexpr int NC = BN / 16;
+            norm_finish_global<BN>(args, T, tc.f, tc.b, pos, inside, (h * NC) / 2, ((h + 1) * NC) / 2,
+                                   __ldcg(args.norm_ss + (long long)grp * 128 + m));
+            epi_sync();  // both column halves have read the group's sums
+            if (h == 0) args.norm_ss[(long long)grp * 128 + m] = 0.f;
+            if (warp == 4 && lane == 0) args.norm_cnt[grp] = 0;
+          }
         }
       }
     }
@@ -903,6 +911,18 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
 // otherwise set the pace; the B tensor map's box then holds BN / 2 rows.
 static bool conv_clustered(int bn) { return bn == 96 || bn == 192 || bn == 256; }
 int conv_b_box_rows(int bn) { return conv_clustered(bn) ? bn / 2 : bn; }
+
+// CTAs per cluster of the kernel launch_conv picks for L.
+static int conv_cluster_size(const ConvLaunch& L) {
+  if (L.args.band || L.args.row) return 2;
+  if (L.epi == kEpiVideo) return 1;
+  if (L.epi == kEpiDup) return L.bn == 256 ? 2 : 1;
+  return conv_clustered(L.bn) ? 2 : 1;
+}
+long long conv_norm_groups(const ConvLaunch& L) {
+  const int CL = conv_cluster_size(L);
+  return conv_units(L.args, CL) / (L.args.tiles_n > 0 ? L.args.tiles_n : 1) * CL;
+}
 
 cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
   if (L.args.band) {

@@ -55,21 +55,6 @@ struct VCfg {
                                   (size_t)kBox * kBox * kZS * 4 + 8 * (2 * kVStages + 5) + 16;
 };
 
-// All 256 epilogue threads (named barrier 1): true iff v is true in every one.
-__device__ __forceinline__ bool epi_all(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 256, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
 struct VTile {
   int f, tx, ty, b;
 };

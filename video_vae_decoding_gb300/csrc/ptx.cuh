@@ -106,6 +106,23 @@ __device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtens
       : "memory");
 }
 
+// ------------------------------------------------------- named barriers
+// Named barrier 1 over the 256 epilogue threads (warps 4-11) of a kernel.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The same barrier, returning true iff v is true in all 256 threads.
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
 // ------------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

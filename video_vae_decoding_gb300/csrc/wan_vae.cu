@@ -616,6 +616,11 @@ struct wan_vae_stream {
   Act RD[3], HD, ringD[6], ringOut;
   std::vector<Act*> rings;
   std::vector<std::pair<Act*, int>> advance;  // rings a chunk consumed, and its frames
+  // fused norms over several N tiles: per position tile a count of the tiles
+  // done and 128 partial sums of squares (zero between launches)
+  int* norm_cnt = nullptr;
+  float* norm_ss = nullptr;
+  long long norm_groups = 0;
   // decode_clip_host: double-buffered latent / video staging, a copy stream
   // and its events, created on first use and kept until destroy
   void* zb[2] = {nullptr, nullptr};
@@ -737,6 +742,16 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   WAN_TRY(ring(st->ringD[0], 4 * n, hD, wD, ciD));
   for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringD[i], 4 * n, hD, wD, coD));
   WAN_TRY(ring(st->ringOut, 4 * n, hD, wD, coD));
+  // fused-norm scratch: at most as many position tiles as a level-D launch
+  // of 4n frames has (16 x 8 tiles, or 128 x 1 row tiles), times the four
+  // sub-pixel phases
+  auto tiles = [](long long H, long long W) { return std::max(cdiv(H, 8) * cdiv(W, 16), H * cdiv(W, 128)); };
+  st->norm_groups = (long long)st->B * 4 * (4 * n) * tiles(hD, wD);
+  void* q;
+  WAN_TRY(make_raw(st, (size_t)st->norm_groups * sizeof(int), &q));
+  st->norm_cnt = (int*)q;
+  WAN_TRY(make_raw(st, (size_t)st->norm_groups * 128 * sizeof(float), &q));
+  st->norm_ss = (float*)q;
   return WAN_OK;
 }
 
@@ -927,6 +942,10 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
     if (norm_tiles(cw) > 1) {
       if (o.f32 || o.lo || (res && res->lo) || nrm->ring->lo) return fail(WAN_ERR_INTERNAL, "multi-tile norm format");
       L.args.norm_tiles = norm_tiles(cw);
+      L.args.norm_cnt = st->norm_cnt;
+      L.args.norm_ss = st->norm_ss;
+      if (conv_norm_groups(L) > st->norm_groups)
+        return fail(WAN_ERR_INTERNAL, "fused-norm scratch too small");
     }
     L.args.norm_gs = nrm->gs;
     L.args.norm_silu = nrm->silu ? 1 : 0;
@@ -1199,6 +1218,10 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
   // the next block's first RMS norm + SiLU, fused over the N tiles (plain bf16)
   if (nrm && !cw.split && norm_tiles(cw) > 1 && norm_tiles(cw) <= 4 && !y.lo && !nrm->ring->lo) {
     L.args.norm_tiles = norm_tiles(cw);
+    L.args.norm_cnt = st->norm_cnt;
+    L.args.norm_ss = st->norm_ss;
+    if (conv_norm_groups(L) > st->norm_groups)
+      return fail(WAN_ERR_INTERNAL, "fused-norm scratch too small");
     L.args.norm_gs = nrm->gs;
     L.args.norm_silu = nrm->silu ? 1 : 0;
     L.args.out2 = nrm->ring->p;
@@ -1432,6 +1455,10 @@ static wan_status decode_chunk_impl(wan_vae_stream* st, const void* z, int z_dty
 }
 
 static wan_status reset_impl(wan_vae_stream* st, cudaStream_t s) {
+  if (st->norm_cnt) {
+    CUDA_TRY(cudaMemsetAsync(st->norm_cnt, 0, (size_t)st->norm_groups * sizeof(int), s));
+    CUDA_TRY(cudaMemsetAsync(st->norm_ss, 0, (size_t)st->norm_groups * 128 * sizeof(float), s));
+  }
   for (Act* r : st->rings) {
     r->base = 0;
     for (int b = 0; b < r->B; ++b) CUDA_TRY(cudaMemsetAsync(r->p + b * r->bs(), 0, 2 * r->fs() * sizeof(bf16), s));
