@@ -172,16 +172,6 @@ __host__ __device__ __forceinline__ long long conv_units(const ConvArgs& a, int 
   return (long long)a.tiles_n * (a.subpix ? 4 : 1) * sp * a.frames * a.batches;
 }
 
-// Output position of accumulator row m of a tile (sub-pixel tiles: of its
-// phase), and whether it lies inside the frame.
-__device__ __forceinline__ long long tile_pos(const ConvArgs& args, const TileCoord& tc, int m, bool* inside) {
-  const int yy = tc.ty * args.box_h + m / args.box_w;
-  const int xx = tc.tx * args.box_w + m % args.box_w;
-  *inside = yy < args.H && xx < args.W;
-  return args.subpix ? (long long)(2 * yy + (tc.phase >> 1)) * (2 * args.W) + (2 * xx + (tc.phase & 1))
-                     : (long long)yy * args.W + xx;
-}
-
 // Epilogue of a tile that holds all N output channels, with the RMS norm of
 // the output fused in.  Pass 1: y = acc + bias (+ residual), its sum of
 // squares, and the raw y to `out` if requested.  Pass 2: y again, scaled by
@@ -259,107 +249,12 @@ __device__ __forceinline__ void epilogue_norm_tile(const ConvArgs& args, uint32_
   }
 }
 
-// Fused RMS norm over T > 1 N tiles (plain bf16 output), first step, per
-// tile: y = acc + bias (+ residual) is rounded to bf16 and stored raw -- to
-// `out`, or, when the raw output is not wanted, into out2 as a temporary --
-// and the sum of squares of the stored values accumulates in ss_acc.  The
-// TMEM buffer is free after it.
-template <int BN>
-__device__ __forceinline__ void norm_part_store(const ConvArgs& args, uint32_t tbase, int tn, int f, int b,
-                                                long long pos, bool valid, int c_begin, int c_end, float& ss_acc) {
-  const __nv_bfloat16* rp = nullptr;
-  if (args.res)
-    rp = static_cast<const __nv_bfloat16*>(args.res) + (long long)b * args.res_bs +
-         (long long)(args.res_f0 + f) * args.res_fs + pos * args.res_ldc;
-  __nv_bfloat16* raw =
-      args.out ? static_cast<__nv_bfloat16*>(args.out) + (long long)b * args.out_bs +
-                     (long long)(args.out_f0 + f * args.out_fmul) * args.out_fs + pos * args.out_ldc
-               : static_cast<__nv_bfloat16*>(args.out2) + (long long)b * args.out2_bs +
-                     (long long)ring_slot(args.out2_f0 + f, args.out2_fmod) * args.out2_fs + pos * args.out2_ldc;
-#pragma unroll 1
-  for (int c = c_begin; c < c_end; ++c) {
-    const int n0 = tn * BN + c * 16;
-    if (n0 >= args.N) break;  // warp-uniform
-    __syncwarp();
-    uint32_t r[16];
-    tmem_ld16(tbase + c * 16, r);
-    tmem_ld_wait();
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-    if (args.bias) add_bias16(args.bias + n0, v);
-    if (!valid) continue;
-    if (rp) add16_bf16(rp + n0, v);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
-      ss_acc = fmaf(v[i], v[i], ss_acc);
-    }
-    store16(raw + n0, 0, v);
-  }
-}
-
-// The fused norm's last step, run by the CTA that completes a position
-// tile's group of T N tiles: every channel of the position (this thread's
-// column half of each of the T tiles) is read back raw -- bypassing L1, as
-// the other tiles were written by other SMs -- scaled by 1 / max(||y||,
-// 1e-12) and sqrt(C) * gamma, SiLU'd, and written to out2.
-template <int BN>
-__device__ __forceinline__ void norm_finish_global(const ConvArgs& args, int T, int f, int b, long long pos,
-                                                   bool valid, int c_begin, int c_end, float ss) {
-  if (!valid) return;
-  const float rinv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
-  __nv_bfloat16* nrm = static_cast<__nv_bfloat16*>(args.out2) + (long long)b * args.out2_bs +
-                       (long long)ring_slot(args.out2_f0 + f, args.out2_fmod) * args.out2_fs + pos * args.out2_ldc;
-  const __nv_bfloat16* raw =
-      args.out ? static_cast<const __nv_bfloat16*>(args.out) + (long long)b * args.out_bs +
-                     (long long)(args.out_f0 + f * args.out_fmul) * args.out_fs + pos * args.out_ldc
-               : nrm;
-#pragma unroll 1
-  for (int t = 0; t < T; ++t) {
-#pragma unroll 1
-    for (int c = c_begin; c < c_end; ++c) {
-      const int n0 = t * BN + c * 16;
-      if (n0 >= args.N) break;
-      float v[16];
-      const uint4* rs = reinterpret_cast<const uint4*>(raw + n0);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint4 a4 = __ldcg(rs + hh);
-        const uint32_t w[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[8 * hh + 2 * i] = bf16_lo(w[i]);
-          v[8 * hh + 2 * i + 1] = bf16_hi(w[i]);
-        }
-      }
-      float g[16];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 g4 = __ldg(reinterpret_cast<const float4*>(args.norm_gs + n0) + i);
-        g[4 * i] = g4.x;
-        g[4 * i + 1] = g4.y;
-        g[4 * i + 2] = g4.z;
-        g[4 * i + 3] = g4.w;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float y = v[i] * (rinv * g[i]);
-        if (args.norm_silu) y = __fdividef(y, 1.0f + __expf(-y));
-        v[i] = y;
-      }
-      store16(nrm + n0, 0, v);
-    }
-  }
-}
-
 // Epilogue of one tile: 4 warps, thread q*32 + lane owns accumulator row
 // (TMEM lane) q*32 + lane, i.e. one output position, and walks its BN columns
 // 16 at a time.
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tacc, const TileCoord& tc, int q, int h,
-                                              int lane, bool got, float* red, uint32_t ssbar, uint32_t ss_parity,
-                                              float& ss_acc) {
+                                              int lane, bool got, float* red, uint32_t ssbar, uint32_t ss_parity) {
   const int m = q * 32 + lane;
   const int pi = tc.phase >> 1, pj = tc.phase & 1;
   const int yy = tc.ty * args.box_h + m / args.box_w;
@@ -372,10 +267,6 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
   constexpr int NC = BN / 16;  // 16-column chunks; half h takes [h*NC/2, (h+1)*NC/2)
   const int c_begin = (h * NC) / 2, c_end = ((h + 1) * NC) / 2;
   if constexpr (EPI == kEpiStore) {
-    if (args.norm_gs && args.norm_tiles > 1) {
-      norm_part_store<BN>(args, tbase, tc.tn, f, b, pos, valid, c_begin, c_end, ss_acc);
-      return;
-    }
     if (args.norm_gs) {
       epilogue_norm_tile<BN>(args, tbase, f, b, pos, valid, c_begin, c_end, red, m, h, ssbar, ss_parity);
       return;
@@ -456,15 +347,6 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
         } else {
           add16(src + n0, 0, v, args.dup_lo);
         }
-        if (args.norm_tiles > 1) {
-          // fused norm over the N tiles (plain bf16): the sum of squares of
-          // the values as stored; the group's last tile normalises
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
-            ss_acc = fmaf(v[i], v[i], ss_acc);
-          }
-        }
       }
       int fo = args.out_f0 + f * args.out_fmul;
       int no = n0;
@@ -519,7 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_units = (int)conv_units(args, CL);
   const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
   const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
-  const int T = args.norm_tiles > 1 ? args.norm_tiles : 1;  // N tiles a fused norm spans
   constexpr uint16_t kPairMask = (1u << CL) - 1;
 
   if (threadIdx.x == 0) {
@@ -814,47 +695,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, h = (warp - 4) >> 2;
     int lt = 0;
-    float ss_acc = 0.f;  // fused norm over T tiles: this thread's partial sum of squares
-    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
     for (int unit = unit0; unit < num_units; unit += unit_step, ++lt) {
       const int buf = lt & 1, use = lt >> 1;
-      bool got = !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum, lim);
-      if (T > 1) got = epi_all(got);  // the epilogue warps meet at barriers below: agree first
+      const bool got =
+          !*abort_flag && mbar_wait_bounded(smem_u32(&tfull[buf]), use & 1, args.err, kDevTimeoutAccum, lim);
       if (!got) *abort_flag = 1;
       tc_fence_after();
-      const TileCoord tc = tile_coord(args, unit, CL, rank);
-      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tc, q, h, lane, got, red + buf * 256,
-                             smem_u32(&ssbar[buf]), use & 1, ss_acc);
+      epilogue_tile<BN, EPI>(args, tmem + buf * kAccCols, tile_coord(args, unit, CL, rank), q, h, lane, got,
+                             red + buf * 256, smem_u32(&ssbar[buf]), use & 1);
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[buf]));
       if (!got) break;
-      if constexpr (EPI == kEpiStore || EPI == kEpiDup) {
-        if (T > 1) {
-          // The N tiles of a position tile run on different CTAs: each adds
-          // its rows' partial sums of squares to the group's slots and counts
-          // itself in; the CTA that arrives last normalises every channel,
-          // reading the other tiles' raw values (fenced before their count).
-          const int grp = (unit / args.tiles_n) * CL + rank;  // the position tile (each CTA of a pair has its own)
-          const int m = q * 32 + lane;
-          bool inside;
-          const long long pos = tile_pos(args, tc, m, &inside);
-          atomicAdd(args.norm_ss + (long long)grp * 128 + m, ss_acc);
-          ss_acc = 0.f;
-          __threadfence();
-          epi_sync();
-          if (warp == 4 && lane == 0) *last_flag = atomicAdd(args.norm_cnt + grp, 1) == T - 1 ? 1 : 0;
-          epi_sync();
-          if (*last_flag) {
-            __threadfence();
-            constexpr int NC = BN / 16;
-            norm_finish_global<BN>(args, T, tc.f, tc.b, pos, inside, (h * NC) / 2, ((h + 1) * NC) / 2,
-                                   __ldcg(args.norm_ss + (long long)grp * 128 + m));
-            epi_sync();  // both column halves have read the group's sums
-            if (h == 0) args.norm_ss[(long long)grp * 128 + m] = 0.f;
-            if (warp == 4 && lane == 0) args.norm_cnt[grp] = 0;
-          }
-        }
-      }
     }
   }
   tc_fence_before();
@@ -911,18 +762,6 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
 // otherwise set the pace; the B tensor map's box then holds BN / 2 rows.
 static bool conv_clustered(int bn) { return bn == 96 || bn == 192 || bn == 256; }
 int conv_b_box_rows(int bn) { return conv_clustered(bn) ? bn / 2 : bn; }
-
-// CTAs per cluster of the kernel launch_conv picks for L.
-static int conv_cluster_size(const ConvLaunch& L) {
-  if (L.args.band || L.args.row) return 2;
-  if (L.epi == kEpiVideo) return 1;
-  if (L.epi == kEpiDup) return L.bn == 256 ? 2 : 1;
-  return conv_clustered(L.bn) ? 2 : 1;
-}
-long long conv_norm_groups(const ConvLaunch& L) {
-  const int CL = conv_cluster_size(L);
-  return conv_units(L.args, CL) / (L.args.tiles_n > 0 ? L.args.tiles_n : 1) * CL;
-}
 
 cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
   if (L.args.band) {

@@ -174,7 +174,89 @@ __global__ void post_quant_kernel(const void* __restrict__ z, int z_f32, int Tz,
   }
 }
 
-// One 256-thread block per row.
+// Rows of up to 4096 scores: one 256-thread block per row, each thread
+// holding up to four float4 chunks of the row in registers, so the scores
+// are read once and exponentiated once.
+constexpr int kSoftmaxRegCols = 4096;
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, u) : v + u;
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float w = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : (is_max ? -INFINITY : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float u = __shfl_xor_sync(0xffffffffu, w, o);
+      w = is_max ? fmaxf(w, u) : w + u;
+    }
+    if (threadIdx.x == 0) red[0] = w;
+  }
+  __syncthreads();
+  const float r = red[0];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(256) softmax_rows_reg_kernel(const float* __restrict__ S, long long ld_s,
+                                                               __nv_bfloat16* __restrict__ Pm, long long ld_p, int n,
+                                                               float scale, int p_lo) {
+  const float4* s4 = reinterpret_cast<const float4*>(S + (long long)blockIdx.x * ld_s);
+  __nv_bfloat16* p = Pm + (long long)blockIdx.x * ld_p;
+  __shared__ float red[32];
+  float v[4][4];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int j = 4 * (threadIdx.x + 256 * k);
+    float4 a = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (j < n) a = __ldcs(s4 + threadIdx.x + 256 * k);
+    v[k][0] = j < n ? a.x : -INFINITY;
+    v[k][1] = j + 1 < n ? a.y : -INFINITY;
+    v[k][2] = j + 2 < n ? a.z : -INFINITY;
+    v[k][3] = j + 3 < n ? a.w : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx = fmaxf(mx, v[k][i]);
+  }
+  mx = block_reduce(mx, red, true);
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[k][i] = expf((v[k][i] - mx) * scale);  // exp(-inf) = 0 past the row
+      sum += v[k][i];
+    }
+  const float inv = 1.0f / block_reduce(sum, red, false);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int j = 4 * (threadIdx.x + 256 * k);
+    if (j >= n) continue;
+    float h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = v[k][i] * inv;
+    if (j + 3 < n) {
+      *reinterpret_cast<uint2*>(p + j) = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+      if (p_lo) {
+        float l[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) l[i] = h[i] - __bfloat162float(__float2bfloat16_rn(h[i]));
+        *reinterpret_cast<uint2*>(p + p_lo + j) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+      }
+    } else {
+      for (int i = 0; i < 4 && j + i < n; ++i) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(h[i]);
+        p[j + i] = b;
+        if (p_lo) p[p_lo + j + i] = __float2bfloat16_rn(h[i] - __bfloat162float(b));
+      }
+    }
+  }
+}
+
+// Longer rows: one 256-thread block per row, three passes over the scores.
 __global__ void softmax_rows_kernel(const float* __restrict__ S, long long ld_s, __nv_bfloat16* __restrict__ Pm,
                                     long long ld_p, int n, float scale, int p_lo) {
   const float* s = S + (long long)blockIdx.x * ld_s;
@@ -353,7 +435,13 @@ cudaError_t launch_softmax_rows(const float* S, long long ld_s, __nv_bfloat16* P
                                 float scale, cudaStream_t s, int p_lo) {
   if (R == 0) return cudaSuccess;
   if (R > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  softmax_rows_kernel<<<(unsigned)R, 256, 0, s>>>(S, ld_s, P, ld_p, n, scale, p_lo);
+  // the register version needs 16-byte aligned rows and even row starts in P
+  const bool reg = n <= kSoftmaxRegCols && ld_s % 4 == 0 && ld_p % 4 == 0 && p_lo % 4 == 0 &&
+                   reinterpret_cast<uintptr_t>(S) % 16 == 0 && reinterpret_cast<uintptr_t>(P) % 8 == 0;
+  if (reg)
+    softmax_rows_reg_kernel<<<(unsigned)R, 256, 0, s>>>(S, ld_s, P, ld_p, n, scale, p_lo);
+  else
+    softmax_rows_kernel<<<(unsigned)R, 256, 0, s>>>(S, ld_s, P, ld_p, n, scale, p_lo);
   return cudaGetLastError();
 }
 

@@ -104,14 +104,6 @@ struct ConvArgs {
   // (b, out2_f0 + f, position); `out` may be null (only the normalised y).
   const float* norm_gs;
   int norm_silu;
-  // > 1: the norm spans norm_tiles N tiles (== tiles_n; bf16 plain output).
-  // Each tile stores y raw (to out, or into out2 when out is null), adds its
-  // rows' sums of squares to norm_ss[group][128] and counts itself in
-  // norm_cnt[group] (group = unit / tiles_n); the tile that arrives last
-  // normalises all channels from the stored values and resets both slots.
-  int norm_tiles;
-  int* norm_cnt;
-  float* norm_ss;
   void* out2;
   long long out2_bs, out2_fs;
   int out2_ldc, out2_f0, out2_lo;
@@ -136,9 +128,6 @@ cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream);
 // Rows of the B tensor map's box for an N tile of bn (half of it when a
 // cluster of two CTAs shares the B block).
 int conv_b_box_rows(int bn);
-// Position tiles of a launch with a fused norm over several N tiles (the
-// slots of norm_cnt / norm_ss it uses).
-long long conv_norm_groups(const ConvLaunch& L);
 
 // ---------------------------------------------------------------------------
 // conv_out with the spatial taps folded into N (conv_out.cu): a causal

@@ -616,11 +616,6 @@ struct wan_vae_stream {
   Act RD[3], HD, ringD[6], ringOut;
   std::vector<Act*> rings;
   std::vector<std::pair<Act*, int>> advance;  // rings a chunk consumed, and its frames
-  // fused norms over several N tiles: per position tile a count of the tiles
-  // done and 128 partial sums of squares (zero between launches)
-  int* norm_cnt = nullptr;
-  float* norm_ss = nullptr;
-  long long norm_groups = 0;
   // decode_clip_host: double-buffered latent / video staging, a copy stream
   // and its events, created on first use and kept until destroy
   void* zb[2] = {nullptr, nullptr};
@@ -742,16 +737,6 @@ static wan_status plan_buffers(wan_vae_stream* st) {
   WAN_TRY(ring(st->ringD[0], 4 * n, hD, wD, ciD));
   for (int i = 1; i < 6; ++i) WAN_TRY(ring(st->ringD[i], 4 * n, hD, wD, coD));
   WAN_TRY(ring(st->ringOut, 4 * n, hD, wD, coD));
-  // fused-norm scratch: at most as many position tiles as a level-D launch
-  // of 4n frames has (16 x 8 tiles, or 128 x 1 row tiles), times the four
-  // sub-pixel phases
-  auto tiles = [](long long H, long long W) { return std::max(cdiv(H, 8) * cdiv(W, 16), H * cdiv(W, 128)); };
-  st->norm_groups = (long long)st->B * 4 * (4 * n) * tiles(hD, wD);
-  void* q;
-  WAN_TRY(make_raw(st, (size_t)st->norm_groups * sizeof(int), &q));
-  st->norm_cnt = (int*)q;
-  WAN_TRY(make_raw(st, (size_t)st->norm_groups * 128 * sizeof(float), &q));
-  st->norm_ss = (float*)q;
   return WAN_OK;
 }
 
@@ -923,13 +908,8 @@ struct NormOut {
   bool silu = true;
   const Act* ring = nullptr;
 };
-// The conv's epilogue can normalise its output: one N tile holds every
-// channel, or (plain bf16 format) up to four N tiles that one CTA pair takes
-// in a row (the last one normalises all channels from the stored raw values).
-static int norm_tiles(const ConvW& cw) { return cw.co_pad / cw.bn; }
-static bool norm_fusable(const ConvW& cw) {
-  return !cw.subpix && (norm_tiles(cw) == 1 || (!cw.split && norm_tiles(cw) <= 4));
-}
+// One N tile holds every output channel: the epilogue can normalise.
+static bool single_tile(const ConvW& cw) { return cw.co_pad == cw.bn && !cw.subpix; }
 
 // 3-frame causal conv over ring `in` (F current frames) into `out`.
 static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F, const OutSpec& o, const Act* res,
@@ -938,15 +918,7 @@ static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F,
   WAN_TRY(conv_setup(cw, in, 0, sc, 0, F, L));
   set_out(L.args, o);
   if (nrm) {
-    if (!norm_fusable(cw)) return fail(WAN_ERR_INTERNAL, "fused norm not available for this conv");
-    if (norm_tiles(cw) > 1) {
-      if (o.f32 || o.lo || (res && res->lo) || nrm->ring->lo) return fail(WAN_ERR_INTERNAL, "multi-tile norm format");
-      L.args.norm_tiles = norm_tiles(cw);
-      L.args.norm_cnt = st->norm_cnt;
-      L.args.norm_ss = st->norm_ss;
-      if (conv_norm_groups(L) > st->norm_groups)
-        return fail(WAN_ERR_INTERNAL, "fused-norm scratch too small");
-    }
+    if (!single_tile(cw)) return fail(WAN_ERR_INTERNAL, "fused norm over several N tiles");
     L.args.norm_gs = nrm->gs;
     L.args.norm_silu = nrm->silu ? 1 : 0;
     L.args.out2 = nrm->ring->p;
@@ -981,7 +953,7 @@ static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act&
   if (!normed)
     ELT(&st->prof, kKindNorm, nb * r.ci,
         launch_rms_norm(x.view(0), ring1.view(2), r.g1, r.ci, x.B, F, P, true, s, x.lo, ring1.lo));
-  if (norm_fusable(r.c1)) {  // conv1 writes SiLU(norm2(h)) straight into conv2's ring
+  if (single_tile(r.c1)) {  // conv1 writes SiLU(norm2(h)) straight into conv2's ring
     NormOut n2;
     n2.gs = r.g2;
     n2.ring = &ring2;
@@ -992,7 +964,7 @@ static wan_status resnet(wan_vae_stream* st, const Resnet& r, const Act& x, Act&
     ELT(&st->prof, kKindNorm, nb * r.co,
         launch_rms_norm(Ht.view(0), ring2.view(2), r.g2, r.co, x.B, F, P, true, s, Ht.lo, ring2.lo));
   }
-  const bool fuse_next = next && norm_fusable(r.c2);
+  const bool fuse_next = next && single_tile(r.c2);
   if (next_done) *next_done = fuse_next;
   const NormOut* nx = fuse_next ? next : nullptr;
   if (r.ci != r.co)
@@ -1186,8 +1158,7 @@ static wan_status time_upsample(wan_vae_stream* st, const ConvW& tc, const Act& 
 // "The parts", fifth and sixth bullets); y is at twice x's resolution.  The
 // Wan2.1 decoder has no DupUp3D: the conv's result is stored as it is.
 static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, const Act& blk, int ft, bool first,
-                           Act& y, int F, cudaStream_t s, const NormOut* nrm = nullptr, bool* nrm_done = nullptr) {
-  if (nrm_done) *nrm_done = false;
+                           Act& y, int F, cudaStream_t s) {
   ConvLaunch L;
   if (!cw.subpix || y.H != 2 * x.H || y.W != 2 * x.W) return fail(WAN_ERR_INTERNAL, "resample shapes");
   WAN_TRY(conv_setup(cw, x, 0, nullptr, 0, F, L));
@@ -1215,23 +1186,6 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
     L.args.dup_pairs = 1;
   else
     return fail(WAN_ERR_UNSUPPORTED, "DupUp3D with %d -> %d channels, ft %d", blk.C, cw.Co, ft);
-  // the next block's first RMS norm + SiLU, fused over the N tiles (plain bf16)
-  if (nrm && !cw.split && norm_tiles(cw) > 1 && norm_tiles(cw) <= 4 && !y.lo && !nrm->ring->lo) {
-    L.args.norm_tiles = norm_tiles(cw);
-    L.args.norm_cnt = st->norm_cnt;
-    L.args.norm_ss = st->norm_ss;
-    if (conv_norm_groups(L) > st->norm_groups)
-      return fail(WAN_ERR_INTERNAL, "fused-norm scratch too small");
-    L.args.norm_gs = nrm->gs;
-    L.args.norm_silu = nrm->silu ? 1 : 0;
-    L.args.out2 = nrm->ring->p;
-    L.args.out2_bs = nrm->ring->bs();
-    L.args.out2_fs = nrm->ring->fs();
-    L.args.out2_ldc = nrm->ring->ldc;
-    L.args.out2_f0 = nrm->ring->slot(2);
-    L.args.out2_fmod = nrm->ring->fmod;
-    if (nrm_done) *nrm_done = true;
-  }
   return run(L, &st->prof, kKindResample, nominal, st->err_dev, s, executed);
 }
 
@@ -1240,10 +1194,9 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
 // into the previous block's conv2 where possible.  `last` optionally names
 // the norm that consumes the final output.
 static wan_status resnet_chain(wan_vae_stream* st, const Resnet* r, Act* R, Act* rings, Act& Ht, int F,
-                               const NormOut* last, cudaStream_t s, bool* last_done = nullptr,
-                               bool first_normed = false) {
+                               const NormOut* last, cudaStream_t s, bool* last_done = nullptr) {
   const int io[3][2] = {{0, 1}, {1, 2}, {2, 1}};
-  bool normed = first_normed;  // rings[0] already holds SiLU(norm1(R[0])) from R[0]'s producer
+  bool normed = false;
   for (int j = 0; j < 3; ++j) {
     NormOut nx;
     const NormOut* next = nullptr;
@@ -1274,51 +1227,27 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
       launch_post_quant(z, z_f32, m->zdim, st->B, (int)Tz, (int)t0, FA, P, m->pq_w, m->pq_b,
                         m->zstat_on ? m->zstat : nullptr, st->ringIn.view(2), m->split ? 0 : 1, s, st->ringIn.lo));
   // 2. conv_in, mid block
-  // (conv_in also writes SiLU(norm1(.)) of its output into the first resnet's ring)
-  NormOut n_mid;
-  n_mid.gs = m->mid[0].g1;
-  n_mid.ring = &st->ringA[0];
-  const bool in_normed = norm_fusable(m->conv_in);
-  WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s, kKindConv333,
-                    in_normed ? &n_mid : nullptr));
-  WAN_TRY(resnet(st, m->mid[0], st->RA[0], st->ringA[0], st->ringA[1], st->HA, st->RA[1], FA, s, in_normed));
+  WAN_TRY(ring_conv(st, m->conv_in, st->ringIn, FA, out_of(st->RA[0]), nullptr, nullptr, s));
+  WAN_TRY(resnet(st, m->mid[0], st->RA[0], st->ringA[0], st->ringA[1], st->HA, st->RA[1], FA, s));
   WAN_TRY(attention(m->attn_g, m->qkv, m->proj, st->at, st->RA[1], st->RA[2], FA, &st->prof, st->err_dev, s));
-  // the second mid resnet's conv2 also normalises for up block 0's first resnet
-  NormOut n_up0;
-  n_up0.gs = m->ups[0][0].g1;
-  n_up0.ring = &st->ringA[4];
-  bool up0_normed = false;
-  WAN_TRY(resnet(st, m->mid[1], st->RA[2], st->ringA[2], st->ringA[3], st->HA, st->RA[0], FA, s, false, &n_up0,
-                 &up0_normed));
+  WAN_TRY(resnet(st, m->mid[1], st->RA[2], st->ringA[2], st->ringA[3], st->HA, st->RA[0], FA, s));
   // up block 0 (level A -> B); block input RA[0]
-  WAN_TRY(resnet_chain(st, m->ups[0], st->RA, st->ringA + 4, st->HA, FA, nullptr, s, nullptr, up0_normed));
+  WAN_TRY(resnet_chain(st, m->ups[0], st->RA, st->ringA + 4, st->HA, FA, nullptr, s));
   WAN_TRY(time_upsample(st, m->tconv[0], st->RA[1], st->tcA, st->tuA, FA, first, s));
-  NormOut n_up1;
-  n_up1.gs = m->ups[1][0].g1;
-  n_up1.ring = &st->ringB[0];
-  bool up1_normed = false;
-  WAN_TRY(resample(st, m->resample[0], st->tuA, st->RA[0], 2, first, st->RB[0], FB, s, &n_up1, &up1_normed));
+  WAN_TRY(resample(st, m->resample[0], st->tuA, st->RA[0], 2, first, st->RB[0], FB, s));
   // up block 1 (level B -> C); block input RB[0]
-  WAN_TRY(resnet_chain(st, m->ups[1], st->RB, st->ringB, st->HB, FB, nullptr, s, nullptr, up1_normed));
+  WAN_TRY(resnet_chain(st, m->ups[1], st->RB, st->ringB, st->HB, FB, nullptr, s));
   WAN_TRY(time_upsample(st, m->tconv[1], st->RB[1], st->tcB, st->tuB, FB, first, s));
-  NormOut n_up2;
-  n_up2.gs = m->ups[2][0].g1;
-  n_up2.ring = &st->ringC[0];
-  bool up2_normed = false;
-  WAN_TRY(resample(st, m->resample[1], st->tuB, st->RB[0], 2, first, st->RC[0], FC, s, &n_up2, &up2_normed));
+  WAN_TRY(resample(st, m->resample[1], st->tuB, st->RB[0], 2, first, st->RC[0], FC, s));
   // up block 2 (level C -> D); block input RC[0]
-  WAN_TRY(resnet_chain(st, m->ups[2], st->RC, st->ringC, st->HC, FC, nullptr, s, nullptr, up2_normed));
-  NormOut n_up3;
-  n_up3.gs = m->ups[3][0].g1;
-  n_up3.ring = &st->ringD[0];
-  bool up3_normed = false;
-  WAN_TRY(resample(st, m->resample[2], st->RC[1], st->RC[0], 1, first, st->RD[0], FC, s, &n_up3, &up3_normed));
+  WAN_TRY(resnet_chain(st, m->ups[2], st->RC, st->ringC, st->HC, FC, nullptr, s));
+  WAN_TRY(resample(st, m->resample[2], st->RC[1], st->RC[0], 1, first, st->RD[0], FC, s));
   // up block 3 (level D)
   NormOut nout;  // norm_out + SiLU, fused into the last conv2 when possible
   nout.gs = m->out_g;
   nout.ring = &st->ringOut;
   bool out_done = false;
-  WAN_TRY(resnet_chain(st, m->ups[3], st->RD, st->ringD, st->HD, FC, &nout, s, &out_done, up3_normed));
+  WAN_TRY(resnet_chain(st, m->ups[3], st->RD, st->ringD, st->HD, FC, &nout, s, &out_done));
   // norm_out, SiLU, conv_out with unpatchify + clamp in its epilogue
   if (!out_done) {
     ELT(&st->prof, kKindNorm, 4.0 * st->B * FC * st->RD[1].H * st->RD[1].W * m->base * (m->split ? 2 : 1),
@@ -1455,10 +1384,6 @@ static wan_status decode_chunk_impl(wan_vae_stream* st, const void* z, int z_dty
 }
 
 static wan_status reset_impl(wan_vae_stream* st, cudaStream_t s) {
-  if (st->norm_cnt) {
-    CUDA_TRY(cudaMemsetAsync(st->norm_cnt, 0, (size_t)st->norm_groups * sizeof(int), s));
-    CUDA_TRY(cudaMemsetAsync(st->norm_ss, 0, (size_t)st->norm_groups * 128 * sizeof(float), s));
-  }
   for (Act* r : st->rings) {
     r->base = 0;
     for (int b = 0; b < r->B; ++b) CUDA_TRY(cudaMemsetAsync(r->p + b * r->bs(), 0, 2 * r->fs() * sizeof(bf16), s));
