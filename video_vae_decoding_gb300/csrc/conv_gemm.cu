@@ -722,8 +722,19 @@ template <int BN, int EPI, int CL, bool ROW = false, bool BAND = false>
 static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
   using Cfg = ConvCfg<BN, ROW, BAND>;
   auto kern = conv_gemm_kernel<BN, EPI, CL, ROW, BAND>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+  // The shared-memory opt-in and the number of co-resident clusters depend
+  // only on the kernel and the device: set and queried once per device (the
+  // cluster occupancy query costs tens of microseconds of host time).
+  constexpr int kMaxDev = 64;
+  static int resident_cache[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDev && resident_cache[dev] > 0;
+  if (!cached) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+  }
   const ConvArgs& a = L.args;
   const long long units = conv_units(a, CL);
   if (units <= 0) return cudaSuccess;
@@ -733,7 +744,7 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
-  int resident = 0;  // CTAs (one per SM) or clusters that fit on the device at once
+  int resident = cached ? resident_cache[dev] : 0;  // CTAs (one per SM) or clusters that fit at once
   if (CL > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
@@ -742,14 +753,13 @@ static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(CL);
-    e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
-  } else {
-    int dev = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&resident, cudaDevAttrMultiProcessorCount, dev);
+    if (!cached) e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
+  } else if (!cached) {
+    e = cudaDeviceGetAttribute(&resident, cudaDevAttrMultiProcessorCount, dev);
   }
   if (e != cudaSuccess) return e;
   if (resident < 1) return cudaErrorInvalidConfiguration;
+  if (!cached && dev >= 0 && dev < kMaxDev) resident_cache[dev] = resident;
   const long long groups = units < resident ? units : resident;  // persistent: one wave of CTAs / clusters
   cfg.gridDim = dim3((unsigned)(groups * CL));
   e = cudaLaunchKernelEx(&cfg, kern, L.a0, L.a1, L.b, a);

@@ -21,30 +21,35 @@ __device__ __forceinline__ __nv_bfloat16* at_mut(const FrameView& v, int b, int 
 inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + per_block - 1) / per_block); }
 
 // RMS norm (+ SiLU) over channels.  Grid: (position blocks, frames,
-// batch).  A warp normalises R consecutive positions of one frame; lane l
-// holds channels l*8 + j*256 .. +7 (j < NCH) of each.  All R*NCH 16-byte loads
-// are issued before the first reduction, to keep enough bytes in flight.
+// batch).  A warp normalises R x (32 / G) consecutive positions of one
+// frame: G lanes per position (G = 16 for C <= 128, so that narrow widths do
+// not leave most lanes idle), lane l of a group holding channels l*8 + j*256
+// .. +7 (j < NCH).  All R*NCH 16-byte loads are issued before the first
+// reduction, to keep enough bytes in flight.
 constexpr int kNormMaxC = 1024;
-template <bool SILU, int R, int NCH, bool SPLIT>
+template <bool SILU, int R, int NCH, bool SPLIT, int G = 32>
 __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView out, const float* __restrict__ gs,
                                                        int C, int P, int in_lo, int out_lo) {
-  const int p0 = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * R;
-  const int lane = threadIdx.x & 31;
-  if (p0 >= P) return;  // warp-uniform
+  constexpr int PW = 32 / G;  // positions side by side in a warp
+  const int lane = threadIdx.x & (G - 1);
+  const int pw0 = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * R * PW;
+  if (pw0 >= P) return;  // warp-uniform
+  // position r of this lane group: p0 + r * PW
+  const int p0 = pw0 + (int)((threadIdx.x & 31) / G);
   const int f = blockIdx.y, b = blockIdx.z;
   const __nv_bfloat16* src = at(in, b, f, p0);
   __nv_bfloat16* dst0 = at_mut(out, b, f, p0);
   float x[R][NCH][8];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const bool ok = p0 + r < P;
+    const bool ok = p0 + r * PW < P;
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int c = lane * 8 + j * 256;
       uint4 a4 = make_uint4(0, 0, 0, 0), b4 = make_uint4(0, 0, 0, 0);
       if (ok && c < C) {
-        a4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * in.ldc + c));
-        if (SPLIT) b4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * in.ldc + in_lo + c));
+        a4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * PW * in.ldc + c));
+        if (SPLIT) b4 = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * PW * in.ldc + in_lo + c));
       }
       const uint32_t w[4] = {a4.x, a4.y, a4.z, a4.w}, u[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
@@ -65,7 +70,7 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView o
     rinv[r] = ss;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
+  for (int o = G / 2; o > 0; o >>= 1)  // within the lane group
 #pragma unroll
     for (int r = 0; r < R; ++r) rinv[r] += __shfl_xor_sync(0xffffffffu, rinv[r], o);
 #pragma unroll
@@ -79,8 +84,8 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView o
     const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      if (p0 + r >= P) continue;
-      __nv_bfloat16* dst = dst0 + (long long)r * out.ldc;
+      if (p0 + r * PW >= P) continue;
+      __nv_bfloat16* dst = dst0 + (long long)r * PW * out.ldc;
       float y[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -299,22 +304,58 @@ __global__ void softmax_rows_kernel(const float* __restrict__ S, long long ld_s,
   }
 }
 
-// 32 x 32 tiles through shared memory.
-__global__ void transpose_kernel(const __nv_bfloat16* __restrict__ src, long long src_gs, int ld_src,
-                                 __nv_bfloat16* __restrict__ dst, long long dst_gs, int ld_dst, int P, int C) {
-  __shared__ __nv_bfloat16 tile[32][34];
+// 64 x 64 tiles through shared memory, 16-byte global accesses: a thread
+// loads 8 channels of one position and stores 8 positions of one channel
+// (eight threads cover one 128-byte row of the output).  Shared memory holds
+// a row per position in 16-byte chunks, chunk q of row r at q ^ ((r / 8) % 8),
+// so the eight rows a warp reads together for one channel sit in distinct
+// banks.
+__global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16* __restrict__ src, long long src_gs,
+                                                        int ld_src, __nv_bfloat16* __restrict__ dst, long long dst_gs,
+                                                        int ld_dst, int P, int C) {
+  __shared__ __align__(16) __nv_bfloat16 tile[64][64];
   const int g = blockIdx.z;
-  const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
   const __nv_bfloat16* s = src + g * src_gs;
   __nv_bfloat16* d = dst + g * dst_gs;
-  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-    const int p = p0 + r, c = c0 + threadIdx.x;
-    if (p < P && c < C) tile[r][threadIdx.x] = s[(long long)p * ld_src + c];
+  const bool vec = (ld_src % 8 == 0) && (ld_dst % 8 == 0) && (c0 + 64 <= C) && (p0 + 64 <= P);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = threadIdx.x + 256 * k;  // 512 chunks: 64 positions x 8 channel chunks
+    const int r = i >> 3, q = i & 7;
+    __nv_bfloat16* t = &tile[r][8 * (q ^ ((r >> 3) & 7))];
+    const int p = p0 + r;
+    if (vec) {
+      *reinterpret_cast<uint4*>(t) = __ldg(reinterpret_cast<const uint4*>(s + (long long)p * ld_src + c0 + 8 * q));
+    } else {
+      for (int e = 0; e < 8; ++e) {
+        const int c = c0 + 8 * q + e;
+        t[e] = (p < P && c < C) ? s[(long long)p * ld_src + c] : __float2bfloat16_rn(0.f);
+      }
+    }
   }
   __syncthreads();
-  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-    const int c = c0 + r, p = p0 + threadIdx.x;
-    if (p < P && c < C) d[(long long)c * ld_dst + p] = tile[threadIdx.x][r];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = threadIdx.x + 256 * k;  // 512 chunks: 64 channels x 8 position chunks
+    const int c = i >> 3, pk = i & 7;     // channel, position chunk (rows 8 pk .. 8 pk + 7)
+    const int col = 8 * ((c >> 3) ^ pk) + (c & 7);
+    __nv_bfloat16 v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = tile[8 * pk + e][col];
+    __nv_bfloat16* o = d + (long long)(c0 + c) * ld_dst + p0 + 8 * pk;
+    if (vec) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        __nv_bfloat162 pr = __halves2bfloat162(v[2 * j], v[2 * j + 1]);
+        w[j] = *reinterpret_cast<uint32_t*>(&pr);
+      }
+      *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (c0 + c < C) {
+      for (int e = 0; e < 8; ++e)
+        if (p0 + 8 * pk + e < P) o[e] = v[e];
+    }
   }
 }
 
@@ -380,8 +421,11 @@ __global__ void to_f32_kernel(const void* __restrict__ src, int src_f32, const v
 template <bool SILU, bool SPLIT>
 static void norm_dispatch(FrameView in, FrameView out, const float* gs, int C, int B, int F, int P, int in_lo,
                           int out_lo, cudaStream_t s) {
-  // 8 warps per block, R positions per warp
-  if (C <= 256)
+  // 8 warps per block, R x 32 / G positions per warp
+  if (C <= 128)
+    rms_norm_kernel<SILU, 4, 1, SPLIT, 16><<<dim3(blocks_for(P, 64), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo,
+                                                                                         out_lo);
+  else if (C <= 256)
     rms_norm_kernel<SILU, 4, 1, SPLIT><<<dim3(blocks_for(P, 32), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
   else if (C <= 512)
     rms_norm_kernel<SILU, 2, 2, SPLIT><<<dim3(blocks_for(P, 16), F, B), 256, 0, s>>>(in, out, gs, C, P, in_lo, out_lo);
@@ -448,8 +492,10 @@ cudaError_t launch_softmax_rows(const float* S, long long ld_s, __nv_bfloat16* P
 cudaError_t launch_transpose(const __nv_bfloat16* src, long long src_gs, int ld_src, __nv_bfloat16* dst,
                              long long dst_gs, int ld_dst, int G, int P, int C, cudaStream_t s) {
   if (G == 0 || P == 0 || C == 0) return cudaSuccess;
-  dim3 grid((P + 31) / 32, (C + 31) / 32, G), block(32, 8);
-  transpose_kernel<<<grid, block, 0, s>>>(src, src_gs, ld_src, dst, dst_gs, ld_dst, P, C);
+  if (reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(dst) % 16 || src_gs % 8 || dst_gs % 8)
+    return cudaErrorInvalidValue;
+  dim3 grid((P + 63) / 64, (C + 63) / 64, G);
+  transpose_kernel<<<grid, 256, 0, s>>>(src, src_gs, ld_src, dst, dst_gs, ld_dst, P, C);
   return cudaGetLastError();
 }
 
