@@ -321,7 +321,8 @@ wan_status wan_conv_out_video(const void* x, int32_t B, int32_t n_hist, int32_t 
  * this library's own bounded waits).  Runs one small causal conv (64 -> cout
  * channels: cout 64 for the one-CTA kernel, 256 for the two-CTA cluster
  * kernel, 96 for the row-tile kernel whose CTA pairs on adjacent rows share
- * B) whose TMA producer withholds its first stage, with the wait limit
+ * B, 12 for conv_out's tap-folded kernel) whose TMA producer withholds its
+ * first stage, with the wait limit
  * shortened to about 10 ms: the MMA issuer's wait runs out, every role of the
  * kernel drains its copies and exits, and the kernel leaves an error code in
  * its device error word.  Blocks until done.  Returns WAN_ERR_INTERNAL and

@@ -1,7 +1,9 @@
 """Failure detection on the GPU without a fault: a conv kernel whose producer
 withholds one stage runs out its (shortened) bounded wait, drains and exits;
 the library reports WAN_ERR_INTERNAL with the device error code, and the
-context keeps working."""
+context keeps working (a normal conv afterwards is checked against the
+oracle).  Covered: the implicit-GEMM conv kernel in its one-CTA, cluster-pair
+and row-tile forms, and conv_out's tap-folded kernel."""
 
 import ctypes
 import math
@@ -16,7 +18,7 @@ from tests.gpu_util import lib_ready, to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cout", [64, 256, 96], ids=["one_cta", "cluster_of_two", "row_tiles_pair"])
+@pytest.mark.parametrize("cout", [64, 256, 96, 12], ids=["one_cta", "cluster_of_two", "row_tiles_pair", "conv_out"])
 def test_bounded_wait_expires_and_is_reported(cout):
     wv = lib_ready()
     lib = wv.load()
@@ -25,12 +27,18 @@ def test_bounded_wait_expires_and_is_reported(cout):
     assert status == 9, (status, lib.wan_vae_last_error())        # WAN_ERR_INTERNAL
     assert code.value in (1, 2, 3)
     assert b"bounded wait" in lib.wan_vae_last_error()
-    # the context is still usable: a normal conv right after is correct
+    # the context is still usable: the same kernel run normally right after is correct
     rng = np.random.default_rng(5)
     x = oracle.round_bf16(rng.standard_normal((1, 3, 8, 16, 64)))
     w = oracle.round_bf16(rng.uniform(-1, 1, (cout, 64, 3, 3, 3)) / math.sqrt(64 * 27))
     b = oracle.round_bf16(rng.uniform(-0.1, 0.1, cout))
-    got = wv.causal_conv3d(to_dev(x, torch.bfloat16), 2, to_dev(w), to_dev(b)).float().cpu().numpy()
     xn = x.transpose(0, 4, 1, 2, 3)
-    ref = oracle.causal_conv(xn[:, :, 2:], w, b, xn[:, :, :2]).transpose(0, 2, 3, 4, 1)
-    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max())
+    ref = oracle.causal_conv(xn[:, :, 2:], w, b, xn[:, :, :2])
+    if cout == 12:
+        _, got = wv.conv_out_video(to_dev(x, torch.bfloat16), 2, to_dev(w), to_dev(b), preclamp=True)
+        got, ref = got.cpu().numpy(), oracle.unpatchify(ref)
+        assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
+    else:
+        got = wv.causal_conv3d(to_dev(x, torch.bfloat16), 2, to_dev(w), to_dev(b)).float().cpu().numpy()
+        ref = ref.transpose(0, 2, 3, 4, 1)
+        assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max())

@@ -2176,15 +2176,61 @@ wan_status wan_conv_out_video(const void* x, int32_t B, int32_t n_hist, int32_t 
 extern "C" wan_status wan_selftest_wait_timeout(int32_t cout, int32_t* device_code, wan_cuda_stream stream) {
   API_GUARD({
     if (device_code) *device_code = 0;
-    if (cout != 64 && cout != 96 && cout != 256)
-      return fail(WAN_ERR_INVALID_ARG, "cout must be 64, 96 or 256, not %d", cout);
+    if (cout != 64 && cout != 96 && cout != 256 && cout != 12)
+      return fail(WAN_ERR_INVALID_ARG, "cout must be 64, 96, 256 or 12, not %d", cout);
     cudaStream_t s = (cudaStream_t)stream;
     DevMem mem;
     mem.use_async = true;
     mem.async = s;
     wan_status r = WAN_OK;
     int code = 0;
-    do {
+    if (cout == 12) do {
+      // conv_out's tap-folded kernel: 64 -> 12 channels over one 16 x 32
+      // frame (two history slots of zeros), the video 32 x 64
+      TapFoldW tf;
+      tf.Co = 12;
+      tf.Ci = 64;
+      tf.ci_pad = 64;
+      tf.n = video_conv_n(12);
+      Act x;
+      x.B = 1;
+      x.F = 3;
+      x.H = 16;
+      x.W = 32;
+      x.C = 64;
+      x.ldc = 64;
+      void *pw, *pb, *px, *po, *pe;
+      const size_t wb = (size_t)tf.n * 3 * tf.ci_pad * sizeof(bf16), bb = 16 * sizeof(float);
+      const size_t ob = (size_t)3 * 4 * x.H * x.W * sizeof(bf16);
+      if ((r = mem.alloc(&pw, wb)) || (r = mem.alloc(&pb, bb)) || (r = mem.alloc(&px, x.bytes())) ||
+          (r = mem.alloc(&po, ob)) || (r = mem.alloc(&pe, 256)))
+        break;
+      if (cudaMemsetAsync(pw, 0, wb, s) || cudaMemsetAsync(pb, 0, bb, s) || cudaMemsetAsync(px, 0, x.bytes(), s) ||
+          cudaMemsetAsync(pe, 0, 256, s)) {
+        r = fail(WAN_ERR_CUDA, "memset failed");
+        break;
+      }
+      tf.w = (bf16*)pw;
+      x.p = (bf16*)px;
+      VideoConvLaunch V;
+      if ((r = video_conv_setup(tf, (const float*)pb, x, 1, 2, V)) != WAN_OK) break;
+      V.args.out = po;
+      V.args.vid_cs = (long long)4 * x.H * x.W;
+      V.args.vid_bs = 3 * V.args.vid_cs;
+      V.args.err = (int*)pe;
+      V.args.wait_limit = 20000000;  // about 10 ms
+      V.args.stall_at1 = 1;          // the first K stage is never loaded
+      if (launch_video_conv(V, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "conv_out launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+        break;
+      }
+      if (cudaMemcpyAsync(&code, pe, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+          cudaStreamSynchronize(s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "reading the error word failed: %s", cudaGetErrorString(cudaGetLastError()));
+        break;
+      }
+    } while (false);
+    else do {
       // a causal 3x3x3 conv 64 -> cout over one 16 x 32 frame (two history slots of zeros)
       ConvW cw;
       cw.Co = cout;
