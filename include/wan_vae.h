@@ -261,7 +261,13 @@ wan_status wan_vae_decode(const void* z, int32_t z_dtype, int32_t B, int32_t T, 
                           const wan_tensor* weights, int32_t n_weights, void* out, int32_t dtype,
                           wan_cuda_stream stream);
 
-/* ---- layer entry points (the building blocks, exposed for testing) ---- */
+/* ---- layer entry points (the building blocks, exposed for testing) ----
+ * The one-shot layer calls below are stream-ordered and do not wait for the
+ * device: a bounded wait that runs out inside their kernels (about 2 s; it
+ * does not happen in normal operation) is recorded in a temporary error word
+ * that they do not read back.  The stream API reports such records
+ * (wan_vae_stream_sync_status, and the next chunk), as does
+ * wan_attention_status for a packed attention block. */
 
 /* The mid-block attention (page section "What is computed", "The parts",
  * fourth bullet, WanAttentionBlock), per frame: n = RMS norm of x; q, k, v =
@@ -287,6 +293,10 @@ typedef struct wan_attention wan_attention;
 wan_status wan_attention_create(const wan_tensor* weights, int32_t n_weights, int32_t N, int32_t H, int32_t W,
                                 int32_t C, wan_cuda_stream stream, wan_attention** out);
 wan_status wan_attention_run(wan_attention* block, const void* x, void* out, wan_cuda_stream stream);
+/* Waits for `stream`, then reports a bounded-wait timeout that any earlier
+ * run of this block recorded on the device (WAN_ERR_INTERNAL, and the record
+ * is cleared), or WAN_OK. */
+wan_status wan_attention_status(wan_attention* block, wan_cuda_stream stream);
 void wan_attention_destroy(wan_attention* block);
 
 /* One causal conv (page "The parts", first bullet, WanCausalConv3d): x

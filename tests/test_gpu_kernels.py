@@ -129,7 +129,7 @@ def test_attention_handle_matches_one_shot(wv):
         blk = wv.AttentionBlock(w, N, H, W, C)
         for _ in range(2):
             got = blk(x)
-            torch.cuda.synchronize()
+            blk.sync_status()
             assert torch.equal(got, ref), C
         blk.close()
 

@@ -276,6 +276,10 @@ class AttentionBlock:
         check(load().wan_attention_run(self._h, _dev(x, "x"), _dev(out, "out"), _stream(stream)))
         return out
 
+    def sync_status(self, stream=None):
+        """Waits for the stream; raises if a run recorded a bounded-wait timeout."""
+        check(load().wan_attention_status(self._h, _stream(stream)))
+
     def close(self):
         if getattr(self, "_h", None):
             load().wan_attention_destroy(self._h)

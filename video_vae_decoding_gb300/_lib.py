@@ -77,6 +77,7 @@ SIGNATURES = {
     "wan_attention_create": (_i32, [ctypes.POINTER(WanTensor), _i32, _i32, _i32, _i32, _i32, _vp,
                                     ctypes.POINTER(_vp)]),
     "wan_attention_run": (_i32, [_vp, _vp, _vp, _vp]),
+    "wan_attention_status": (_i32, [_vp, _vp]),
     "wan_attention_destroy": (None, [_vp]),
     "wan_causal_conv3d": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                  _vp, _vp]),

@@ -2029,6 +2029,20 @@ wan_status wan_attention_run(wan_attention* A, const void* x, void* out, wan_cud
   })
 }
 
+wan_status wan_attention_status(wan_attention* A, wan_cuda_stream stream) {
+  API_GUARD({
+    if (!A) return fail(WAN_ERR_INVALID_ARG, "null attention block");
+    int code = 0;
+    CUDA_TRY(cudaMemcpyAsync(&code, A->err, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream));
+    CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+    if (code) {
+      CUDA_TRY(cudaMemsetAsync(A->err, 0, sizeof(int), (cudaStream_t)stream));
+      return fail(WAN_ERR_INTERNAL, "an attention kernel reported error %d (a bounded wait expired)", code);
+    }
+    return WAN_OK;
+  })
+}
+
 void wan_attention_destroy(wan_attention* A) {
   if (!A) return;
   cudaDeviceSynchronize();
