@@ -17,11 +17,12 @@
 // and at the end O / l is written as bf16 (the weights of V sum to one).  Keys past HW are masked to -inf;
 // queries past HW are computed on zero rows and not stored.
 //
-// Warp roles (256 threads): warp 0 lane 0 TMA producer (Q once; per key block
+// Warp roles (384 threads): warp 0 lane 0 TMA producer (Q once; per key block
 // C/64 boxes of 128 keys x 64 channels of K and the V^T boxes of VR rows x 64
 // keys, through one 16 KB-slot ring in the order the MMA consumes them), warp
-// 1 lane 0 MMA issuer, warp 2 TMEM allocation, warps 4-7 softmax and output
-// (thread = query row = TMEM lane).  Every wait is bounded.
+// 1 lane 0 MMA issuer, warp 2 TMEM allocation, warps 4-11 softmax and output
+// (two threads per query row = TMEM lane, each taking half of the keys and
+// half of the output columns).  Every wait is bounded.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -29,7 +30,7 @@ namespace wan {
 
 namespace {
 
-constexpr int kFThreads = 256;
+constexpr int kFThreads = 384;
 constexpr int kFStages = 6;
 constexpr int kFUnit = 16384;  // one ring slot: 128 x 64 bf16
 
@@ -40,7 +41,8 @@ struct FCfg {
   static constexpr int NV = C / VR;                     // V^T row groups
   static constexpr int kVBytes = VR * 128;              // one V^T box: VR rows x 64 keys
   static constexpr int kTmemCols = (128 + C) <= 256 ? 256 : 512;
-  static constexpr size_t kSmem = 1024 + (size_t)NQ * kFUnit + 2 * kFUnit + (size_t)kFStages * kFUnit + 8 * 32;
+  static constexpr size_t kSmem =
+      1024 + (size_t)NQ * kFUnit + 2 * kFUnit + (size_t)kFStages * kFUnit + 8 * 32 + 2 * 128 * 4;
 };
 
 template <int NQ>
@@ -64,6 +66,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
   uint64_t* done = pv_done + 1;    // all MMAs of this CTA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // [2 halves][128 rows]: the row max exchange (reused from block to block:
+  // the barrier that opens each block orders a block's writes after the
+  // previous block's reads)
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qb = blockIdx.x, f = blockIdx.y, b = blockIdx.z;
@@ -77,8 +83,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     mbar_init(smem_u32(q_full), 1);
     mbar_init(smem_u32(s_full), 1);
-    mbar_init(smem_u32(s_free), 128);
-    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(s_free), 256);
+    mbar_init(smem_u32(p_full), 256);
     mbar_init(smem_u32(pv_done), 1);
     mbar_init(smem_u32(done), 1);
     *abort_flag = 0;
@@ -201,21 +207,26 @@ __global__ void __launch_bounds__(kFThreads, 1)
     mbar_wait_bounded(smem_u32(done), 0, args.err, kDevTimeoutAccum, lim);
   } else if (warp >= 4) {
     // ------------------------------------------------------ softmax, output
-    const int q = warp & 3;
+    // Eight warps: warp w reads TMEM lane quadrant w % 4, and half hk = (w - 4)
+    // / 4 of the row: keys 64 hk .. 64 hk + 63 of each block, output columns
+    // hk C/2 .. (hk + 1) C/2.  The two halves of a row exchange their maxima
+    // through shared memory, so both take the same reference max; all eight
+    // warps agree on every wait's outcome (named barrier 1) before going on.
+    const int q = warp & 3, hk = (warp - 4) >> 2;
     const int row = 32 * q + lane;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    constexpr int CH = Cfg::C / 2;  // output columns per half
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
-      ok = __all_sync(0xffffffffu, !*abort_flag &&
-                                       mbar_wait_bounded(smem_u32(s_full), j & 1, args.err, kDevTimeoutAccum, lim));
+      ok = epi_all(!*abort_flag && mbar_wait_bounded(smem_u32(s_full), j & 1, args.err, kDevTimeoutAccum, lim));
       if (!ok) break;
       tc_fence_after();
-      float t[128];
+      float t[64];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t r[16];
-        tmem_ld16(tS + lane_off + 16 * c, r);
+        tmem_ld16(tS + lane_off + 64 * hk + 16 * c, r);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) t[16 * c + i] = __uint_as_float(r[i]) * args.scale_log2;
@@ -223,15 +234,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(s_free));
       // keys past the frame's positions
-      const int kv = args.HW - 128 * j;
-      if (kv < 128) {
+      const int kv = args.HW - 128 * j - 64 * hk;
+      if (kv < 64) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i >= kv) t[i] = -INFINITY;
       }
       float mb = t[0];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mb = fmaxf(mb, t[i]);
+      for (int i = 1; i < 64; ++i) mb = fmaxf(mb, t[i]);
+      red[hk * 128 + row] = mb;
+      epi_sync();
+      mb = fmaxf(mb, red[(1 - hk) * 128 + row]);
       float alpha = 1.f;
       if (mb > m + 8.f) {  // move the reference max (and rescale O and l by alpha)
         alpha = exp2f(m - mb);
@@ -241,61 +255,60 @@ __global__ void __launch_bounds__(kFThreads, 1)
       // multiply V then sum to exactly 1 after the final division by l
       float rs = 0.f;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
+      for (int i = 0; i < 64; ++i) {
         t[i] = __bfloat162float(__float2bfloat16_rn(exp2f(t[i] - m)));
         rs += t[i];
       }
       l = l * alpha + rs;
       // P buffer free and O stable once O += P_{j-1} V_{j-1} has completed
       if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(pv_done), (j - 1) & 1, args.err, kDevTimeoutAccum, lim));
+        ok = epi_all(mbar_wait_bounded(smem_u32(pv_done), (j - 1) & 1, args.err, kDevTimeoutAccum, lim));
         if (!ok) break;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < Cfg::C / 16; ++c) {
+          for (int c = 0; c < CH / 16; ++c) {
             uint32_t r[16];
-            tmem_ld16(tO + lane_off + 16 * c, r);
+            tmem_ld16(tO + lane_off + CH * hk + 16 * c, r);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st16(tO + lane_off + 16 * c, r);
+            tmem_st16(tO + lane_off + CH * hk + 16 * c, r);
           }
           tmem_st_wait();
         }
       }
       // P_j (bf16) in the 128-byte-swizzled K-major layout: row `row`, key
       // chunk c of 8 keys at 16-byte slot c ^ (row & 7) of its 128-byte line
+      // (this half's 64 keys are one swizzled block)
+      uint8_t* line = sP + hk * kFUnit + row * 128;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint8_t* line = sP + h * kFUnit + row * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float* v = t + 64 * h + 8 * c;
-          const uint4 w = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                     pack_bf16x2(v[6], v[7]));
-          *reinterpret_cast<uint4*>(line + ((c ^ (row & 7)) << 4)) = w;
-        }
+      for (int c = 0; c < 8; ++c) {
+        const float* v = t + 8 * c;
+        const uint4 w = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                   pack_bf16x2(v[6], v[7]));
+        *reinterpret_cast<uint4*>(line + ((c ^ (row & 7)) << 4)) = w;
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(p_full));
     }
-    if (ok)
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait_bounded(smem_u32(pv_done), (nkb - 1) & 1, args.err, kDevTimeoutAccum, lim));
+    if (ok) ok = epi_all(mbar_wait_bounded(smem_u32(pv_done), (nkb - 1) & 1, args.err, kDevTimeoutAccum, lim));
     if (!ok) {
       *abort_flag = 1;
     } else {
       tc_fence_after();
+      // the row's weight sum: both halves' partial sums (taken against the same max)
+      red[hk * 128 + row] = l;
+      epi_sync();
+      const float rl = 1.f / (l + red[(1 - hk) * 128 + row]);
       const int qrow = 128 * qb + row;
-      const float rl = 1.f / l;
       __nv_bfloat16* dst = args.out + (long long)b * args.out_bs + (long long)f * args.out_fs +
-                           (long long)qrow * args.out_ldc;
+                           (long long)qrow * args.out_ldc + CH * hk;
 #pragma unroll 1
-      for (int c = 0; c < Cfg::C / 16; ++c) {
+      for (int c = 0; c < CH / 16; ++c) {
         uint32_t r[16];
-        tmem_ld16(tO + lane_off + 16 * c, r);
+        tmem_ld16(tO + lane_off + CH * hk + 16 * c, r);
         tmem_ld_wait();
         if (qrow < args.HW) {
           float v[16];
