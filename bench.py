@@ -186,8 +186,10 @@ def run_attention(args):
     """The isolated attention block: RMS norm, qkv 1x1 conv, softmax(q k^T / sqrt(C)) v over
     the frame's positions (one head, d = C), proj, + x; bf16.  Default: 8 frames of 44x80 at
     C = 1024 (the TI2V-5B mid block at 720p); --attn-shape N,C,H,W for others (e.g.
-    4,384,90,160: the Wan2.1 mid block at 720p, which runs the flash kernel).  Weights are
-    packed once, before the timed region (wan_attention_create)."""
+    4,384,90,160: the Wan2.1 mid block at 720p).  Head dims up to 384 run the one-CTA flash
+    kernel, 512 and 1024 the flash kernel with C / 256 CTAs per 128 queries (each computes the
+    scores: (C / 256 + 1) / 2 times the nominal attention-core FLOPs run on the tensor cores).
+    Weights are packed once, before the timed region (wan_attention_create)."""
     import torch
     from video_vae_decoding_gb300 import build as _build
     _build.build()
@@ -220,6 +222,8 @@ def run_attention(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     flops = 2.0 * N * HW * (3 * C * C + 2 * HW * C + C * C)
+    core = 4.0 * N * HW * HW * C
+    exec_flops = flops - core + core * ((C // 256 + 1) / 2.0 if C in (512, 1024) else 1.0)
     burst, sustained, _, src = _peaks()
     tf = flops / (ms / 1000.0) / 1e12
     print(json.dumps({
@@ -227,9 +231,12 @@ def run_attention(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "dtype": "bf16", "data": "synthetic", "config": {
             "workload": f"isolated mid-block attention, {N} frames of {H}x{W}, C {C}",
-            "kernel": "flash" if C <= 384 else "score GEMM + row softmax + P V GEMM",
+            "kernel": ("flash (one CTA per 128 queries)" if C <= 384 and C % 64 == 0 else
+                       "flash (C / 256 CTAs per 128 queries, scores computed by each)" if C in (512, 1024) else
+                       "score GEMM + row softmax + P V GEMM"),
             "weights": "packed before the timed region"},
-        "nominal_gflop_per_step": flops / 1e9, "frac_of_bf16_peak": {"burst": tf / burst, "sustained": tf / sustained,
+        "nominal_gflop_per_step": flops / 1e9, "executed_gflop_per_step": exec_flops / 1e9,
+        "tflops_executed": exec_flops / (ms / 1000.0) / 1e12, "frac_of_bf16_peak": {"burst": tf / burst, "sustained": tf / sustained,
                                                                     "source": src}}))
     block.close()
     return 0

@@ -178,10 +178,12 @@ wan_status wan_vae_stream_load(wan_vae_stream* st, const void* src, int64_t byte
  * kind index: 0 causal 3x3x3 convs (conv_in, residual blocks), 1 time convs,
  * 2 upsample2d convs (+DupUp3D), 3 attention GEMMs, 4 conv_out,
  * 5 RMS norm (+SiLU), 6 other memory-bound kernels (post_quant_conv, softmax,
- * transposes, frame copies, the cache ring shift).  Executed FLOPs count
- * the arithmetic the kernels run: equal to nominal except for the upsample2d
- * convs, which run in sub-pixel form (four 2x2 phase convs at the low
- * resolution: 4/9 of the nominal 3x3 conv at the high resolution). */
+ * transposes, frame copies).  Executed FLOPs count the arithmetic the
+ * kernels run: equal to nominal except for the upsample2d convs, which run in
+ * sub-pixel form (four 2x2 phase convs at the low resolution: 4/9 of the
+ * nominal 3x3 conv at the high resolution), and the attention core at head
+ * dims 512 and 1024, whose C / 256 CTAs per 128 queries each compute the
+ * scores ((C / 256 + 1) / 2 of the nominal q k^T and P V FLOPs). */
 typedef struct {
   int64_t launches;          /* all kernel launches enqueued */
   int64_t tc_launches;       /* tensor-core launches among them */
@@ -285,10 +287,11 @@ wan_status wan_attention_block(const void* x, int32_t N, int32_t H, int32_t W, i
  * for N frames of H x W positions at C channels (device memory owned by the
  * handle until destroy; blocks until the packing is done); run computes out =
  * block(x) for x, out [N][H*W][C] bf16 channels-last (device), stream-ordered,
- * no allocation; destroy waits for the device and frees.  Head dims up to 384
- * run the flash kernel (the HW x HW scores never leave the SM); wider heads
- * (1024) run a score GEMM, a row softmax and a P V GEMM over an fp32 score
- * workspace of N*HW*HW values.  Errors as wan_attention_block. */
+ * no allocation; destroy waits for the device and frees.  Head dims up to
+ * 384, 512 and 1024 run a flash kernel (online softmax; the HW x HW scores
+ * never leave the SM); other head dims run a score GEMM, a row softmax and a
+ * P V GEMM over an fp32 score workspace of N*HW*HW values.  Errors as
+ * wan_attention_block. */
 typedef struct wan_attention wan_attention;
 wan_status wan_attention_create(const wan_tensor* weights, int32_t n_weights, int32_t N, int32_t H, int32_t W,
                                 int32_t C, wan_cuda_stream stream, wan_attention** out);

@@ -112,6 +112,28 @@ def test_attention_flash_large_logits(wv):
     _attention_check(wv, N=1, C=384, H=60, W=80, frames=[0], seed=12, qkv_scale=4.0, rel_tol=2e-2, abs_tol=0.15)
 
 
+# Head dims 512 and 1024 run the cluster flash kernel (C / 256 CTAs per 128
+# queries, each with 256 output columns; key blocks of 256): ragged last key
+# and query blocks, exactly one key block, frames of fewer than 128 positions.
+@pytest.mark.parametrize("N,C,H,W", [(2, 1024, 13, 29), (1, 512, 10, 26), (3, 1024, 5, 7), (1, 512, 16, 16),
+                                     (1, 1024, 9, 57)], ids=lambda v: str(v))
+def test_attention_flash_split_widths(wv, N, C, H, W):
+    _attention_check(wv, N=N, C=C, H=H, W=W, frames=range(N), seed=16)
+
+
+def test_attention_flash_split_large_logits(wv):
+    """As the large-logit case above, at head dim 1024 (the cluster kernel):
+    1200 keys in 5 blocks of 256, qkv weights 4x larger, so the running max
+    moves and each CTA rescales its output columns; same bounds and reason."""
+    _attention_check(wv, N=1, C=1024, H=30, W=40, frames=[0], seed=17, qkv_scale=4.0, rel_tol=2e-2, abs_tol=0.15)
+
+
+def test_attention_gemm_path_width(wv):
+    """A head dim no flash kernel takes (768) runs the score GEMM, row
+    softmax and P V GEMM path."""
+    _attention_check(wv, N=2, C=768, H=11, W=27, frames=range(2), seed=18)
+
+
 def test_attention_flash_wan21_720p_frame(wv):
     """Wan2.1's mid block at 720p: 90 x 160 = 14,400 positions, C = 384, one
     frame against the oracle (113 key blocks)."""
@@ -120,9 +142,9 @@ def test_attention_flash_wan21_720p_frame(wv):
 
 def test_attention_handle_matches_one_shot(wv):
     """Weights packed once (wan_attention_create) and run twice give the
-    one-shot entry point's result bit for bit, for both kernels (flash at C =
-    384, score GEMMs at C = 1024)."""
-    for N, C, H, W in ((2, 384, 12, 20), (1, 1024, 8, 12)):
+    one-shot entry point's result bit for bit, for each path (flash at C =
+    384, the cluster flash kernel at C = 1024, score GEMMs at C = 768)."""
+    for N, C, H, W in ((2, 384, 12, 20), (1, 1024, 8, 12), (1, 768, 8, 12)):
         w = {k: to_dev(v) for k, v in _attn_weights(C, 14).items()}
         x = to_dev(_bf(np.random.default_rng(15).standard_normal((N, H * W, C))), torch.bfloat16)
         ref = wv.attention_block(x, w, H, W)

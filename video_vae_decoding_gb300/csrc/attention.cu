@@ -331,6 +331,385 @@ __global__ void __launch_bounds__(kFThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Head dims 512 and 1024 (TI2V-5B's mid block).  A 128-query fp32 output
+// accumulator is then C x 512 B, more than one SM's TMEM at C = 1024, and the
+// 128 x C block of q more than its shared memory.  So NSL = C / 256 CTAs (side
+// by side in the grid) take one block of 128 queries: CTA r accumulates
+// output columns [256 r, 256 r + 256) (256 TMEM columns) beside a score block
+// of 256 keys (the other 256).  Every CTA needs the full scores S_j = Q K_j^T
+// (the softmax weights of its output columns), so each computes them from q
+// and k chunks that are the same for all NSL CTAs (read from L2 by each), and
+// loads the v^T boxes of its own 256 output columns.  (Sharing the q and k
+// chunks by cluster multicast measured no faster: L2 was not the limit, and
+// clusters of four CTAs fit only four to a GPC.)
+// Per key block j (256 keys):
+//   MMA issuer   S_j = Q K_j^T over C / 64 stages of (q box 128 x 64, k box
+//                256 x 64), M = 128, N = 256; then O += P_{j-1} V_{j-1} over
+//                four stages of one v^T box (256 columns x 64 keys)
+//   softmax      the same online softmax as the kernel above (lazy reference
+//                max, P rounded to bf16, l summed over the rounded values),
+//                sixteen warps, four threads per query row with 64 keys and
+//                64 output columns each (the SFU's exp2; a mask-free path for
+//                all but the last key block).  P_j is formed in registers as
+//                soon as S_j is read, so S_{j+1} starts while P_{j-1} V_{j-1}
+//                is still running.
+// The stages run through a 4-slot ring of 48 KB (four stages in flight: three
+// did not cover the load latency).  A P V stage uses only the 32 KB B part
+// of its slot (the v^T box), and P_j's box kc lives in the A part of the slot
+// of stage kc of O += P_j V_j, so no separate P buffer is needed.  The
+// softmax threads write it once that slot's previous stage (four positions
+// earlier: one of the last four of S_{j+1}, or of the stages before O += P_j
+// V_j if no S follows) has been consumed: barrier pfree[kc], which the MMA
+// issuer commits after that stage, completes once per key block.  (The
+// slot's "empty" barrier cannot be used: it completes four times during
+// S_{j+1}, and a parity wait only tells neighbouring phases apart.)  Each box
+// has its own "written" barrier p_full[kc], so the P V stage of box 0 need
+// not wait for box 3.
+// ---------------------------------------------------------------------------
+constexpr int kSThreads = 640;  // warps 0-3 producer, MMA issuer, TMEM allocation, idle; 4-19 softmax
+constexpr int kSStages = 4;
+constexpr int kSStage = 49152;  // A part 16 KB (q box) + B part 32 KB (k box or v^T box)
+
+template <int NSL>
+struct SCfg {
+  static constexpr int C = 256 * NSL;
+  static constexpr int NC = C / 64;  // 64-channel chunks of the score contraction
+  static constexpr size_t kSmem = 1024 + (size_t)kSStages * kSStage + 256 + 4 * 128 * 4;
+};
+
+// The 512 softmax threads (warps 4-19) of the split kernel: named barrier 2.
+__device__ __forceinline__ void sm_sync() { asm volatile("bar.sync 2, 512;" ::: "memory"); }
+__device__ __forceinline__ bool sm_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 2, 512, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+// 2^x by the SFU's approximation (flushes subnormal results to zero); the
+// probabilities it feeds are rounded to bf16.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Position of stage kc of O += P_j V_j in the split kernel's stage sequence:
+// the NC chunks of S_0, then for j' = 1 .. nkb - 1 the NC chunks of S_j' and
+// the four stages of O += P_{j'-1} V_{j'-1}, then those of O += P_{nkb-1}
+// V_{nkb-1}.  (Putting the P V stages in the middle of S_j' measured 19%
+// slower: the softmax then has no P V MMAs to hide behind.)
+__device__ __forceinline__ int split_pv_pos(int j, int nkb, int NC, int kc) {
+  return NC * min(j + 2, nkb) + 4 * j + kc;
+}
+
+template <int NSL>
+__global__ void __launch_bounds__(kSThreads, 1)
+    flash_attn_split_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                            const __grid_constant__ CUtensorMap mapV, const __grid_constant__ FlashArgs args) {
+  using Cfg = SCfg<NSL>;
+  constexpr int S = kSStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sR = smem;  // ring
+  uint64_t* full = reinterpret_cast<uint64_t*>(sR + S * kSStage);
+  uint64_t* empty = full + S;
+  uint64_t* s_full = empty + S;    // S_j in TMEM
+  uint64_t* s_free = s_full + 1;   // S_j read by the softmax threads
+  uint64_t* p_full = s_free + 1;   // [4] P_j box kc written (and O rescaled)
+  uint64_t* pv_done = p_full + 4;  // O += P_j V_j complete
+  uint64_t* done = pv_done + 1;    // all MMAs of this CTA complete
+  uint64_t* pfree = done + 1;      // [4] the slot of P box kc is free
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pfree + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(sR + S * kSStage + 256);  // [4 quarters][128 rows]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = blockIdx.x % NSL;  // output column slice
+  const int qb = blockIdx.x / NSL, f = blockIdx.y, b = blockIdx.z;
+  const int nkb = args.nkb;
+  const long long lim = args.wait_limit > 0 ? args.wait_limit : kWaitLimitCycles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(s_full), 1);
+    mbar_init(smem_u32(s_free), 512);
+    for (int kc = 0; kc < 4; ++kc) mbar_init(smem_u32(&p_full[kc]), 512);
+    mbar_init(smem_u32(pv_done), 1);
+    mbar_init(smem_u32(done), 1);
+    for (int kc = 0; kc < 4; ++kc) mbar_init(smem_u32(&pfree[kc]), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&mapQ);
+    tma_prefetch_map(&mapK);
+    tma_prefetch_map(&mapV);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 256;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    // order of consumption: S stages of block 0, then for j = 1 .. nkb - 1
+    // the S stages of block j and the v^T stages of block j - 1, then the
+    // v^T stages of block nkb - 1
+    int it = 0;
+    bool ok = true;
+    for (int j = 0; j <= nkb && ok; ++j) {
+      const int nk = j < nkb ? Cfg::NC : 0, nv = j >= 1 ? 4 : 0;
+      for (int i = 0; i < nk + nv; ++i, ++it) {
+        const int s = it % S, r = it / S;
+        if (r > 0 && !mbar_wait_bounded(smem_u32(&empty[s]), (r - 1) & 1, args.err, kDevTimeoutEmpty, lim)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[s]);
+        const uint32_t slot = smem_u32(sR + s * kSStage);
+        if (i < nk) {
+          mbar_arrive_expect_tx(fb, kSStage);
+          tma_load_4d(slot, &mapQ, fb, args.q_c0 + 64 * i, 128 * qb, f, b);
+          tma_load_4d(slot + kFUnit, &mapK, fb, args.k_c0 + 64 * i, 256 * j, f, b);
+        } else {
+          mbar_arrive_expect_tx(fb, 2 * kFUnit);
+          tma_load_4d(slot + kFUnit, &mapV, fb, 256 * (j - 1) + 64 * (i - nk), 256 * rank, f, b);
+        }
+      }
+    }
+    // do not leave while copies into this CTA's shared memory are in flight
+    for (int jj = (it > S ? it - S : 0); jj < it; ++jj)
+      mbar_wait_bounded(smem_u32(&full[jj % S]), (jj / S) & 1, args.err, kDevTimeoutFull, lim);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idN256 = idesc_bf16_f32(128, 256);
+    bool ok = true;
+    int slot = 0, phase = 0;
+    for (int j = 0; j <= nkb && ok; ++j) {
+      if (j < nkb) {
+        // S_j = Q K_j^T, once the softmax has read S_{j-1}
+        if (j > 0 && !mbar_wait_bounded(smem_u32(s_free), (j - 1) & 1, args.err, kDevTimeoutAccum, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int c = 0; c < Cfg::NC && ok; ++c) {
+          if (!mbar_wait_bounded(smem_u32(&full[slot]), phase, args.err, kDevTimeoutFull, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k128(smem_u32(sR + slot * kSStage));
+          const uint64_t bd = sdesc_k128(smem_u32(sR + slot * kSStage + kFUnit));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) umma_bf16(tS, ad + 2 * k, bd + 2 * k, idN256, (c > 0 || k > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&empty[slot]));
+          // the slot's next stage is stage c + 4 - NC of O += P_{j-1} V_{j-1}
+          // (or, with a single key block, of O += P_0 V_0): its P box may go in
+          if (c >= Cfg::NC - 4 && (j >= 1 || nkb == 1)) umma_commit(smem_u32(&pfree[c + 4 - Cfg::NC]));
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(s_full));
+      }
+      if (j >= 1) {
+        // O += P_{j-1} V_{j-1}: stage kc once P_{j-1} box kc (in the A part
+        // of the stage's slot) is written and O rescaled
+        const int jv = j - 1;
+        for (int kc = 0; kc < 4 && ok; ++kc) {
+          if (!mbar_wait_bounded(smem_u32(&p_full[kc]), jv & 1, args.err, kDevTimeoutAccum, lim) ||
+              !mbar_wait_bounded(smem_u32(&full[slot]), phase, args.err, kDevTimeoutFull, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k128(smem_u32(sR + slot * kSStage));
+          const uint64_t bd = sdesc_k128(smem_u32(sR + slot * kSStage + kFUnit));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tO, ad + 2 * k, bd + 2 * k, idN256, (jv > 0 || kc > 0 || k > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&empty[slot]));
+          // with no S stages left, the slot's next stage is stage kc of O += P_{nkb-1} V_{nkb-1}
+          if (j == nkb - 1) umma_commit(smem_u32(&pfree[kc]));
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(pv_done));
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    // every MMA of this CTA completes before the TMEM is released
+    umma_commit(smem_u32(done));
+    mbar_wait_bounded(smem_u32(done), 0, args.err, kDevTimeoutAccum, lim);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ softmax, output
+    // warp w reads TMEM lane quadrant w % 4; quarter qt = (w - 4) / 4 of the
+    // row takes keys 64 qt .. 64 qt + 63 of each block (P box qt) and output
+    // columns 64 qt .. 64 qt + 63 of this CTA's 256.  The four quarters of a
+    // row exchange their maxima and, at the end, their sums through shared
+    // memory; all sixteen warps agree on every wait's outcome.
+    const int q = warp & 3, qt = (warp - 4) >> 2;
+    const int row = 32 * q + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const uint32_t tSq = tS + lane_off + 64 * qt, tOq = tO + lane_off + 64 * qt;
+    const float sc = args.scale_log2;
+    uint8_t* line_base = nullptr;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkb; ++j) {
+      ok = sm_all(!*abort_flag && mbar_wait_bounded(smem_u32(s_full), j & 1, args.err, kDevTimeoutAccum, lim));
+      if (!ok) break;
+      tc_fence_after();
+      const int kv = args.HW - 256 * j - 64 * qt;  // keys of this quarter inside the frame
+      // pass 1: the quarter-row max of the raw scores (the scale is positive)
+      float mb = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tSq + 16 * c, r);
+        tmem_ld_wait();
+        if (kv >= 64) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) mb = fmaxf(mb, __uint_as_float(r[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (16 * c + i < kv) mb = fmaxf(mb, __uint_as_float(r[i]));
+        }
+      }
+      mb *= sc;
+      red[qt * 128 + row] = mb;
+      sm_sync();
+      mb = fmaxf(fmaxf(red[row], red[128 + row]), fmaxf(red[256 + row], red[384 + row]));
+      float alpha = 1.f;
+      if (mb > m + 8.f) {  // move the reference max (and rescale O and l by alpha)
+        alpha = exp2f(m - mb);
+        m = mb;
+      }
+      // pass 2: P in bf16 (registers), and the row sum of the rounded values
+      uint32_t pk[32];
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tSq + 16 * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          float e0 = ex2_approx(fmaf(__uint_as_float(r[i]), sc, -m));
+          float e1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), sc, -m));
+          if (kv < 64) {
+            if (16 * c + i >= kv) e0 = 0.f;
+            if (16 * c + i + 1 >= kv) e1 = 0.f;
+          }
+          const uint32_t w = pack_bf16x2(e0, e1);
+          rs += bf16_lo(w) + bf16_hi(w);
+          pk[8 * c + i / 2] = w;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(s_free));
+      l = l * alpha + rs;
+      // O stable once O += P_{j-1} V_{j-1} has completed
+      if (j > 0) {
+        ok = sm_all(mbar_wait_bounded(smem_u32(pv_done), (j - 1) & 1, args.err, kDevTimeoutAccum, lim));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[16];
+            tmem_ld16(tOq + 16 * c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st16(tOq + 16 * c, r);
+          }
+          tmem_st_wait();
+        }
+      }
+      // O is rescaled: the P V stages of the other quarters' boxes may go
+      tc_fence_before();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k != qt) mbar_arrive(smem_u32(&p_full[k]));
+      // P_j box qt goes to the A part of the slot of stage qt of O += P_j V_j,
+      // free once pfree[qt] completes for the j-th time
+      ok = sm_all(mbar_wait_bounded(smem_u32(&pfree[qt]), j & 1, args.err, kDevTimeoutEmpty, lim));
+      if (!ok) break;
+      line_base = sR + (split_pv_pos(j, nkb, Cfg::NC, qt) % S) * kSStage;
+      // in the 128-byte-swizzled K-major layout: row `row`, chunk g of 8 keys
+      // at 16-byte slot g ^ (row & 7) of its 128-byte line
+      uint8_t* line = line_base + row * 128;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        *reinterpret_cast<uint4*>(line + ((g ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&p_full[qt]));
+    }
+    if (ok) ok = sm_all(mbar_wait_bounded(smem_u32(pv_done), (nkb - 1) & 1, args.err, kDevTimeoutAccum, lim));
+    if (!ok) {
+      *abort_flag = 1;
+    } else {
+      tc_fence_after();
+      // the row's weight sum: the four quarters' partial sums (taken against the same max)
+      red[qt * 128 + row] = l;
+      sm_sync();
+      const float rl = 1.f / ((red[row] + red[128 + row]) + (red[256 + row] + red[384 + row]));
+      const int qrow = 128 * qb + row;
+      __nv_bfloat16* dst = args.out + (long long)b * args.out_bs + (long long)f * args.out_fs +
+                           (long long)qrow * args.out_ldc + 256 * rank + 64 * qt;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tOq + 16 * c, r);
+        tmem_ld_wait();
+        if (qrow < args.HW) {
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) * rl;
+          uint4* d = reinterpret_cast<uint4*>(dst + 16 * c);
+          d[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                            pack_bf16x2(v[6], v[7]));
+          d[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                            pack_bf16x2(v[14], v[15]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 template <int NQ>
 cudaError_t launch_f(const FlashLaunch& L, cudaStream_t stream) {
   using Cfg = FCfg<NQ>;
@@ -340,17 +719,39 @@ cudaError_t launch_f(const FlashLaunch& L, cudaStream_t stream) {
   const FlashArgs& a = L.args;
   if (a.HW <= 0 || a.frames <= 0 || a.batches <= 0) return cudaSuccess;
   dim3 grid((unsigned)((a.HW + 127) / 128), (unsigned)a.frames, (unsigned)a.batches);
-  kern<<<grid, kFThreads, Cfg::kSmem, stream>>>(L.qk, L.v, a);
+  kern<<<grid, kFThreads, Cfg::kSmem, stream>>>(L.q, L.v, a);
+  return cudaGetLastError();
+}
+
+template <int NSL>
+cudaError_t launch_split(const FlashLaunch& L, cudaStream_t stream) {
+  using Cfg = SCfg<NSL>;
+  auto kern = flash_attn_split_kernel<NSL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  const FlashArgs& a = L.args;
+  if (a.HW <= 0 || a.frames <= 0 || a.batches <= 0) return cudaSuccess;
+  dim3 grid((unsigned)(NSL * ((a.HW + 127) / 128)), (unsigned)a.frames, (unsigned)a.batches);
+  kern<<<grid, kSThreads, Cfg::kSmem, stream>>>(L.q, L.k, L.v, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int flash_attn_max_c() { return 384; }
+bool flash_attn_supported(int C) { return C % 64 == 0 && C >= 64 && (C <= 384 || C == 512 || C == 1024); }
+
+FlashBoxes flash_attn_boxes(int C) {
+  if (C <= 384) return FlashBoxes{128, 128, C % 128 == 0 ? 128 : 64, 128};
+  return FlashBoxes{128, 256, 256, 256};
+}
+
+double flash_attn_exec_ratio(int C) { return C <= 384 ? 1.0 : (C / 256 + 1) / 2.0; }
 
 cudaError_t launch_flash_attn(const FlashLaunch& L, cudaStream_t stream) {
   const FlashArgs& a = L.args;
-  if (a.C % 64 || a.C < 64 || a.C > 384 || a.nkb != (a.HW + 127) / 128) return cudaErrorInvalidValue;
+  if (!flash_attn_supported(a.C) || a.HW < 0) return cudaErrorInvalidValue;
+  const int kb = flash_attn_boxes(a.C).key_block;
+  if (a.nkb != (a.HW + kb - 1) / kb) return cudaErrorInvalidValue;
   switch (a.C / 64) {
     case 1: return launch_f<1>(L, stream);
     case 2: return launch_f<2>(L, stream);
@@ -358,6 +759,8 @@ cudaError_t launch_flash_attn(const FlashLaunch& L, cudaStream_t stream) {
     case 4: return launch_f<4>(L, stream);
     case 5: return launch_f<5>(L, stream);
     case 6: return launch_f<6>(L, stream);
+    case 8: return launch_split<2>(L, stream);
+    case 16: return launch_split<4>(L, stream);
   }
   return cudaErrorInvalidValue;
 }

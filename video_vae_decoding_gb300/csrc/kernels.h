@@ -168,16 +168,18 @@ cudaError_t launch_pack_tapfold(const void* src, int src_f32, int Co, int Ci, in
 
 // ---------------------------------------------------------------------------
 // Flash-style attention core (attention.cu): per frame, O = softmax(q k^T *
-// scale) v over HW positions, head dim C (a multiple of 64, at most
-// flash_attn_max_c(): S and O share the 512 TMEM columns).  q and k are
-// channel ranges of one tensor [B][F][HW][ldc] (map qk: 4-D (channels, HW,
-// F, B), box 64 x 128); v comes transposed, [B][F][C][HWp] with zeros past
-// HW (map v: 4-D (HWp, C, F, B), box 64 x VR, VR = 128 if 128 divides C, else
-// 64).  O is written as bf16 [B][F][HW][out_ldc].
+// scale) v over HW positions, head dim C (a multiple of 64).  q and k are
+// channel ranges of one tensor [B][F][HW][ldc] (maps q and k: 4-D (channels,
+// HW, F, B)); v comes transposed, [B][F][C][HWp] with zeros past HW (map v:
+// 4-D (HWp, C, F, B)).  O is written as bf16 [B][F][HW][out_ldc].  Two
+// kernels: C <= 384 keeps S and all of O in one CTA's TMEM; C = 512 or 1024
+// runs C / 256 CTAs per 128 queries, CTA r accumulating output columns
+// [256 r, 256 r + 256) and each computing the full scores itself.
+// flash_attn_boxes gives the box of each map and the key block.
 // ---------------------------------------------------------------------------
 struct FlashArgs {
   int HW, frames, batches;
-  int nkb;             // key blocks: ceil(HW / 128)
+  int nkb;             // key blocks: ceil(HW / key_block)
   int C;               // head dim
   int q_c0, k_c0;      // first channel of q and of k in the qk tensor
   float scale_log2;    // log2(e) / sqrt(C)
@@ -188,10 +190,20 @@ struct FlashArgs {
   long long wait_limit;
 };
 struct FlashLaunch {
-  CUtensorMap qk, v;
+  CUtensorMap q, k, v;
   FlashArgs args;
 };
-int flash_attn_max_c();
+struct FlashBoxes {
+  int q_rows, k_rows;  // rows of the q and k boxes (64 channels wide)
+  int v_rows;          // rows (channels) of the v^T box (64 keys wide)
+  int key_block;       // keys per score block
+};
+// false if no flash kernel takes head dim C
+bool flash_attn_supported(int C);
+FlashBoxes flash_attn_boxes(int C);
+// tcgen05 work per nominal FLOP (the split kernel recomputes the scores in
+// each CTA of its cluster: (C / 256 + 1) / 2)
+double flash_attn_exec_ratio(int C);
 cudaError_t launch_flash_attn(const FlashLaunch& L, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------

@@ -587,11 +587,11 @@ struct AttnBufs {
   long long vt_bs() const { return (long long)Fmax * vt_fs(); }
 };
 
-// The flash kernel holds a 128-query block's scores and output (C columns)
-// in the 512 TMEM columns: head dims up to 384 (Wan2.1's 384, the narrow test
-// widths).  Wider heads (TI2V-5B's 1024) and the fp32 split format take the
-// score GEMM, row softmax and P V GEMM path.
-static bool attention_is_flash(bool split, int C) { return !split && C % 64 == 0 && C <= flash_attn_max_c(); }
+// The flash kernels: one CTA per 128 queries for head dims up to 384 (Wan2.1's
+// 384, the narrow test widths), a cluster of C / 256 CTAs for 512 and 1024
+// (TI2V-5B).  Other widths and the fp32 split format take the score GEMM, row
+// softmax and P V GEMM path.
+static bool attention_is_flash(bool split, int C) { return !split && flash_attn_supported(C); }
 
 struct wan_vae_stream {
   const wan_vae_model* m = nullptr;
@@ -1034,23 +1034,26 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
                            at.vt_fs(), (int)at.ldp(), F, HW, C, s));
     FlashLaunch FL;
     memset(&FL, 0, sizeof(FL));
+    const FlashBoxes fb = flash_attn_boxes(C);
     {
       const uint64_t dims[4] = {(uint64_t)at.qkv.chans(), (uint64_t)HW, (uint64_t)at.qkv.F, (uint64_t)B};
       const uint64_t strides[3] = {(uint64_t)at.qkv.ldc * 2, (uint64_t)at.qkv.fs() * 2, (uint64_t)at.qkv.bs() * 2};
-      const uint32_t box[4] = {64, 128, 1, 1};
-      WAN_TRY(encode(&FL.qk, 4, at.qkv.p, dims, strides, box));
+      const uint32_t qbox[4] = {64, (uint32_t)fb.q_rows, 1, 1};
+      WAN_TRY(encode(&FL.q, 4, at.qkv.p, dims, strides, qbox));
+      const uint32_t kbox[4] = {64, (uint32_t)fb.k_rows, 1, 1};
+      WAN_TRY(encode(&FL.k, 4, at.qkv.p, dims, strides, kbox));
     }
     {
       const uint64_t dims[4] = {(uint64_t)at.HWp, (uint64_t)C, (uint64_t)at.Fmax, (uint64_t)B};
       const uint64_t strides[3] = {(uint64_t)at.ldp() * 2, (uint64_t)at.vt_fs() * 2, (uint64_t)at.vt_bs() * 2};
-      const uint32_t box[4] = {64, (uint32_t)(C % 128 == 0 ? 128 : 64), 1, 1};
+      const uint32_t box[4] = {64, (uint32_t)fb.v_rows, 1, 1};
       WAN_TRY(encode(&FL.v, 4, at.Vt, dims, strides, box));
     }
     FlashArgs& a = FL.args;
     a.HW = HW;
     a.frames = F;
     a.batches = B;
-    a.nkb = (HW + 127) / 128;
+    a.nkb = (HW + fb.key_block - 1) / fb.key_block;
     a.C = C;
     a.q_c0 = 0;
     a.k_c0 = C;
@@ -1061,7 +1064,8 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
     a.out_ldc = at.O.ldc;
     a.err = err;
     cudaEvent_t e1 = nullptr;
-    if (prof) WAN_TRY(prof->begin(kKindAttention, 4.0 * M * HW * C, s, &e1));
+    const double nominal = 4.0 * M * HW * C;
+    if (prof) WAN_TRY(prof->begin(kKindAttention, nominal, s, &e1, nominal * flash_attn_exec_ratio(C)));
     CUDA_TRY(launch_flash_attn(FL, s));
     if (e1) CUDA_TRY(cudaEventRecord(e1, s));
     if (prof) prof->launches++;
