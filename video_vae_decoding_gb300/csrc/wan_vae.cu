@@ -96,6 +96,9 @@ struct Act {
   int B = 0, F = 0, H = 0, W = 0, C = 0, ldc = 0;
   int lo = 0;  // split format: low halves at channel offset lo (0: plain bf16)
   int fmod = 0, base = 0;  // circular ring: F slots, logical frame 0 at slot `base`
+  // ring: leading logical frames known to hold zeros (the history after a
+  // reset: 2); a causal conv skips the taps that would read them
+  int zhist = 0;
   int chans() const { return lo ? ldc : C; }  // channels a copy must move
   long long fs() const { return (long long)H * W * ldc; }
   long long bs() const { return (long long)F * fs(); }
@@ -672,6 +675,7 @@ static wan_status plan_buffers(wan_vae_stream* st) {
     WAN_TRY(make_act(st, a, 2 + F, H, W, C));
     a.fmod = a.F;
     a.base = 0;
+    a.zhist = 2;
     st->rings.push_back(&a);
     return WAN_OK;
   };
@@ -783,7 +787,10 @@ static wan_status add_tap(ConvArgs& A, int& nt, int src, int dt, int dy, int dx,
 
 // Fills the launch for conv `cw` reading A source 0 (`a0`, output frame 0 at
 // frame coordinate a0_f0 for dt = 0) and optionally the shortcut source a1.
-static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Act* a1, int a1_f0, int F, ConvLaunch& L) {
+// Taps of source 0 with dt < dt_min are left out (they would read frames of
+// zeros: the causal padding).
+static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Act* a1, int a1_f0, int F, ConvLaunch& L,
+                             int dt_min = 0) {
   memset(&L, 0, sizeof(L));
   ConvArgs& A = L.args;
   if (a0.ldc < cw.ci_pad || (a1 && a1->ldc < cw.sc_ci_pad))
@@ -826,7 +833,9 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
       for (int dx = 0; dx < cw.kw; ++dx) {
         // sub-pixel taps carry source offsets 0/1; the kernel adds the phase's (i - 1, j - 1)
         const int oy = cw.subpix ? dy : dy - cw.kh / 2, ox = cw.subpix ? dx : dx - cw.kw / 2;
-        if (band) {
+        if (dt < dt_min) {
+          // the tap reads only causal zero padding
+        } else if (band) {
           // taps (dt, dx) in that order, each standing for its three dy taps
           if (dy == 0) {
             const int kd = ((dt * cw.kh + 0) * cw.kw + dx) * cw.ci_pad;
@@ -911,32 +920,50 @@ struct NormOut {
 // One N tile holds every output channel: the epilogue can normalise.
 static bool single_tile(const ConvW& cw) { return cw.co_pad == cw.bn && !cw.subpix; }
 
-// 3-frame causal conv over ring `in` (F current frames) into `out`.
+// 3-frame causal conv over ring `in` (F current frames) into `out`.  While
+// the ring's history holds the zero padding of a stream's start (in.zhist
+// leading zero frames), output frame f < zhist reads zeros through its taps
+// dt < zhist - f: those frames run as launches of their own without those
+// taps (the zero padding is applied by leaving the taps out, not computed).
 static wan_status ring_conv(wan_vae_stream* st, const ConvW& cw, Act& in, int F, const OutSpec& o, const Act* res,
                             const Act* sc, cudaStream_t s, int kind = kKindConv333, const NormOut* nrm = nullptr) {
-  ConvLaunch L;
-  WAN_TRY(conv_setup(cw, in, 0, sc, 0, F, L));
-  set_out(L.args, o);
-  if (nrm) {
-    if (!single_tile(cw)) return fail(WAN_ERR_INTERNAL, "fused norm over several N tiles");
-    L.args.norm_gs = nrm->gs;
-    L.args.norm_silu = nrm->silu ? 1 : 0;
-    L.args.out2 = nrm->ring->p;
-    L.args.out2_bs = nrm->ring->bs();
-    L.args.out2_fs = nrm->ring->fs();
-    L.args.out2_ldc = nrm->ring->ldc;
-    L.args.out2_f0 = nrm->ring->slot(2);
-    L.args.out2_fmod = nrm->ring->fmod;
-    L.args.out2_lo = nrm->ring->lo;
+  if (nrm && !single_tile(cw)) return fail(WAN_ERR_INTERNAL, "fused norm over several N tiles");
+  const int z = cw.kt == 3 ? std::min(in.zhist, 2) : 0;
+  const double kfull = (double)cw.kt * cw.kh * cw.kw * cw.Ci + cw.sc_Ci;
+  for (int f0 = 0; f0 < F;) {
+    // frames [f0, f1) share dt_min: one frame at a time while f0 < z
+    const int dt_min = f0 < z ? z - f0 : 0;
+    const int f1 = f0 < z ? f0 + 1 : F;
+    const int nf = f1 - f0;
+    ConvLaunch L;
+    WAN_TRY(conv_setup(cw, in, f0, sc, f0, nf, L, dt_min));
+    OutSpec of = o;
+    of.f0 = o.f0 + f0 * o.fmul;
+    set_out(L.args, of);
+    if (nrm) {
+      L.args.norm_gs = nrm->gs;
+      L.args.norm_silu = nrm->silu ? 1 : 0;
+      L.args.out2 = nrm->ring->p;
+      L.args.out2_bs = nrm->ring->bs();
+      L.args.out2_fs = nrm->ring->fs();
+      L.args.out2_ldc = nrm->ring->ldc;
+      L.args.out2_f0 = nrm->ring->slot(2 + f0);
+      L.args.out2_fmod = nrm->ring->fmod;
+      L.args.out2_lo = nrm->ring->lo;
+    }
+    if (res) {
+      L.args.res = res->p;
+      L.args.res_bs = res->bs();
+      L.args.res_fs = res->fs();
+      L.args.res_ldc = res->ldc;
+      L.args.res_lo = res->lo;
+      L.args.res_f0 = f0;
+    }
+    const double nominal = conv_flops(cw, in, nf);
+    const double kept = (double)(cw.kt - dt_min) * cw.kh * cw.kw * cw.Ci + cw.sc_Ci;
+    WAN_TRY(run(L, &st->prof, kind, nominal, st->err_dev, s, nominal * kept / kfull));
+    f0 = f1;
   }
-  if (res) {
-    L.args.res = res->p;
-    L.args.res_bs = res->bs();
-    L.args.res_fs = res->fs();
-    L.args.res_ldc = res->ldc;
-    L.args.res_lo = res->lo;
-  }
-  WAN_TRY(run(L, &st->prof, kind, conv_flops(cw, in, F), st->err_dev, s));
   st->advance.push_back({&in, F});
   return WAN_OK;
 }
@@ -1291,7 +1318,10 @@ static wan_status run_chunk(wan_vae_stream* st, const void* z, int z_f32, long l
     st->advance.push_back({&st->ringOut, FC});
   }
   // 3. the causal caches: each ring's last two frames become its history
-  for (auto& r : st->advance) r.first->base = r.first->slot(r.second);
+  for (auto& r : st->advance) {
+    r.first->base = r.first->slot(r.second);
+    r.first->zhist = std::max(0, r.first->zhist - r.second);
+  }
   st->first = false;
   if (st->err_host) {
     CUDA_TRY(cudaMemcpyAsync(st->err_host, st->err_dev, sizeof(int), cudaMemcpyDeviceToHost, s));
@@ -1390,6 +1420,7 @@ static wan_status decode_chunk_impl(wan_vae_stream* st, const void* z, int z_dty
 static wan_status reset_impl(wan_vae_stream* st, cudaStream_t s) {
   for (Act* r : st->rings) {
     r->base = 0;
+    r->zhist = 2;
     for (int b = 0; b < r->B; ++b) CUDA_TRY(cudaMemsetAsync(r->p + b * r->bs(), 0, 2 * r->fs() * sizeof(bf16), s));
   }
   st->first = true;
@@ -1705,6 +1736,7 @@ wan_status wan_vae_stream_load(wan_vae_stream* st, const void* src, int64_t byte
     const char* o = static_cast<const char*>(src) + rup(sizeof(StateHeader), 256);
     for (Act* r : st->rings) {
       r->base = 0;  // the history goes to slots 0 and 1
+      r->zhist = hd.first ? 2 : 0;  // a state saved before the first chunk holds the zero history
       for (int b = 0; b < r->B; ++b) {
         const size_t n = 2 * r->fs() * sizeof(bf16);
         CUDA_TRY(cudaMemcpyAsync(r->p + b * r->bs(), o, n, cudaMemcpyDefault, s));
