@@ -343,6 +343,15 @@ wan_status wan_conv_out_video(const void* x, int32_t B, int32_t n_hist, int32_t 
  * WAN_OK if it was not; the CUDA context stays usable either way. */
 wan_status wan_selftest_wait_timeout(int32_t cout, int32_t* device_code, wan_cuda_stream stream);
 
+/* The same self test for the flash attention kernels: one frame of 200
+ * positions at head dim C (up to 384: the one-CTA kernel; 512 or 1024: the
+ * kernel with C / 256 CTAs per 128 queries), zeros in, the TMA producer
+ * withholding its first ring stage, the wait limit about 10 ms.  Blocks until
+ * done.  Returns WAN_ERR_INVALID_ARG if no flash kernel takes C,
+ * WAN_ERR_INTERNAL and the code (1..3) in *device_code when the timeout was
+ * detected and reported, WAN_OK if it was not; the context stays usable. */
+wan_status wan_selftest_attention_timeout(int32_t C, int32_t* device_code, wan_cuda_stream stream);
+
 /* wan_causal_conv3d without any device allocation.  The pages have no
  * counterpart: this is for callers that must not allocate device memory --
  * code that runs while a host framework owns all GPU memory through its own

@@ -3,7 +3,8 @@ withholds one stage runs out its (shortened) bounded wait, drains and exits;
 the library reports WAN_ERR_INTERNAL with the device error code, and the
 context keeps working (a normal conv afterwards is checked against the
 oracle).  Covered: the implicit-GEMM conv kernel in its one-CTA, cluster-pair
-and row-tile forms, and conv_out's tap-folded kernel."""
+and row-tile forms, conv_out's tap-folded kernel, and both flash attention
+kernels (one CTA per 128 queries; C / 256 CTAs per 128 queries)."""
 
 import ctypes
 import math
@@ -42,3 +43,17 @@ def test_bounded_wait_expires_and_is_reported(cout):
         got = wv.causal_conv3d(to_dev(x, torch.bfloat16), 2, to_dev(w), to_dev(b)).float().cpu().numpy()
         ref = ref.transpose(0, 2, 3, 4, 1)
         assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("C", [384, 1024], ids=["flash_one_cta", "flash_four_ctas"])
+def test_flash_attention_bounded_wait_expires_and_is_reported(C):
+    wv = lib_ready()
+    lib = wv.load()
+    code = ctypes.c_int32(0)
+    status = lib.wan_selftest_attention_timeout(C, ctypes.byref(code), None)
+    assert status == 9, (status, lib.wan_vae_last_error())        # WAN_ERR_INTERNAL
+    assert code.value in (1, 2, 3)
+    assert b"bounded wait" in lib.wan_vae_last_error()
+    # the context is still usable: the attention block at the same width is right
+    from tests.test_gpu_kernels import _attention_check
+    _attention_check(wv, N=1, C=C, H=9, W=23, frames=[0], seed=19)

@@ -84,6 +84,7 @@ SIGNATURES = {
     "wan_conv_out_video": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _i32, _vp,
                                   _vp]),
     "wan_selftest_wait_timeout": (_i32, [_i32, ctypes.POINTER(_i32), _vp]),
+    "wan_selftest_attention_timeout": (_i32, [_i32, ctypes.POINTER(_i32), _vp]),
     "wan_causal_conv3d_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                          _i32, _vp, _vp]),
 }

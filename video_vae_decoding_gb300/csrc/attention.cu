@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           ok = false;
           break;
         }
+        if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
         const uint32_t fb = smem_u32(&full[s]);
         if (i < nk) {
           mbar_arrive_expect_tx(fb, kFUnit);
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           ok = false;
           break;
         }
+        if (it + 1 == args.stall_at1) continue;  // injected failure: this stage never fills
         const uint32_t fb = smem_u32(&full[s]);
         const uint32_t slot = smem_u32(sR + s * kSStage);
         if (i < nk) {

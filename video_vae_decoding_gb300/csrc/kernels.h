@@ -188,6 +188,7 @@ struct FlashArgs {
   int out_ldc;
   int* err;
   long long wait_limit;
+  int stall_at1;       // failure self test: 1-based ring stage the producer never loads (0: none)
 };
 struct FlashLaunch {
   CUtensorMap q, k, v;

@@ -1036,6 +1036,43 @@ static wan_status gemm_setup(ConvLaunch& L, const bf16* a_base, int a_ldc, int a
   return WAN_OK;
 }
 
+// The flash kernel's launch for F frames of the buffers `at` (q, k in
+// at.qkv channels [0, C) and [C, 2C), V^T in at.Vt, O into at.O).
+static wan_status flash_setup(const AttnBufs& at, int F, int* err, FlashLaunch& FL) {
+  const int C = at.C, HW = at.HW, B = at.B;
+  memset(&FL, 0, sizeof(FL));
+  const FlashBoxes fb = flash_attn_boxes(C);
+  {
+    const uint64_t dims[4] = {(uint64_t)at.qkv.chans(), (uint64_t)HW, (uint64_t)at.qkv.F, (uint64_t)B};
+    const uint64_t strides[3] = {(uint64_t)at.qkv.ldc * 2, (uint64_t)at.qkv.fs() * 2, (uint64_t)at.qkv.bs() * 2};
+    const uint32_t qbox[4] = {64, (uint32_t)fb.q_rows, 1, 1};
+    WAN_TRY(encode(&FL.q, 4, at.qkv.p, dims, strides, qbox));
+    const uint32_t kbox[4] = {64, (uint32_t)fb.k_rows, 1, 1};
+    WAN_TRY(encode(&FL.k, 4, at.qkv.p, dims, strides, kbox));
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)at.HWp, (uint64_t)C, (uint64_t)at.Fmax, (uint64_t)B};
+    const uint64_t strides[3] = {(uint64_t)at.ldp() * 2, (uint64_t)at.vt_fs() * 2, (uint64_t)at.vt_bs() * 2};
+    const uint32_t box[4] = {64, (uint32_t)fb.v_rows, 1, 1};
+    WAN_TRY(encode(&FL.v, 4, at.Vt, dims, strides, box));
+  }
+  FlashArgs& a = FL.args;
+  a.HW = HW;
+  a.frames = F;
+  a.batches = B;
+  a.nkb = (HW + fb.key_block - 1) / fb.key_block;
+  a.C = C;
+  a.q_c0 = 0;
+  a.k_c0 = C;
+  a.scale_log2 = 1.4426950408889634f / std::sqrt((float)C);
+  a.out = at.O.p;
+  a.out_bs = at.O.bs();
+  a.out_fs = at.O.fs();
+  a.out_ldc = at.O.ldc;
+  a.err = err;
+  return WAN_OK;
+}
+
 // Mid-block attention over F frames of x (level A) into y = attn(x) + x
 // (page "The parts", fourth bullet): RMS norm; qkv = 1x1 conv C -> 3C;
 // S = q k^T per frame (fp32); P = softmax(S / sqrt(C)); O = P v; y = proj(O) + x.
@@ -1060,36 +1097,7 @@ static wan_status attention(const float* g, const ConvW& qkv, const ConvW& proj,
           launch_transpose(at.qkv.p + b * at.qkv.bs() + 2 * C, at.qkv.fs(), at.qkv.ldc, at.Vt + b * at.vt_bs(),
                            at.vt_fs(), (int)at.ldp(), F, HW, C, s));
     FlashLaunch FL;
-    memset(&FL, 0, sizeof(FL));
-    const FlashBoxes fb = flash_attn_boxes(C);
-    {
-      const uint64_t dims[4] = {(uint64_t)at.qkv.chans(), (uint64_t)HW, (uint64_t)at.qkv.F, (uint64_t)B};
-      const uint64_t strides[3] = {(uint64_t)at.qkv.ldc * 2, (uint64_t)at.qkv.fs() * 2, (uint64_t)at.qkv.bs() * 2};
-      const uint32_t qbox[4] = {64, (uint32_t)fb.q_rows, 1, 1};
-      WAN_TRY(encode(&FL.q, 4, at.qkv.p, dims, strides, qbox));
-      const uint32_t kbox[4] = {64, (uint32_t)fb.k_rows, 1, 1};
-      WAN_TRY(encode(&FL.k, 4, at.qkv.p, dims, strides, kbox));
-    }
-    {
-      const uint64_t dims[4] = {(uint64_t)at.HWp, (uint64_t)C, (uint64_t)at.Fmax, (uint64_t)B};
-      const uint64_t strides[3] = {(uint64_t)at.ldp() * 2, (uint64_t)at.vt_fs() * 2, (uint64_t)at.vt_bs() * 2};
-      const uint32_t box[4] = {64, (uint32_t)fb.v_rows, 1, 1};
-      WAN_TRY(encode(&FL.v, 4, at.Vt, dims, strides, box));
-    }
-    FlashArgs& a = FL.args;
-    a.HW = HW;
-    a.frames = F;
-    a.batches = B;
-    a.nkb = (HW + fb.key_block - 1) / fb.key_block;
-    a.C = C;
-    a.q_c0 = 0;
-    a.k_c0 = C;
-    a.scale_log2 = 1.4426950408889634f / std::sqrt((float)C);
-    a.out = at.O.p;
-    a.out_bs = at.O.bs();
-    a.out_fs = at.O.fs();
-    a.out_ldc = at.O.ldc;
-    a.err = err;
+    WAN_TRY(flash_setup(at, F, err, FL));
     cudaEvent_t e1 = nullptr;
     const double nominal = 4.0 * M * HW * C;
     if (prof) WAN_TRY(prof->begin(kKindAttention, nominal, s, &e1, nominal * flash_attn_exec_ratio(C)));
@@ -2333,6 +2341,70 @@ extern "C" wan_status wan_selftest_wait_timeout(int32_t cout, int32_t* device_co
     CUDA_TRY(cudaStreamSynchronize(s));
     if (device_code) *device_code = code;
     if (code) return fail(WAN_ERR_INTERNAL, "a conv kernel reported error %d (a bounded wait expired)", code);
+    return WAN_OK;
+  })
+}
+
+extern "C" wan_status wan_selftest_attention_timeout(int32_t C, int32_t* device_code, wan_cuda_stream stream) {
+  API_GUARD({
+    if (device_code) *device_code = 0;
+    if (!flash_attn_supported(C)) return fail(WAN_ERR_INVALID_ARG, "no flash kernel takes head dim %d", C);
+    cudaStream_t s = (cudaStream_t)stream;
+    DevMem mem;
+    mem.use_async = true;
+    mem.async = s;
+    wan_status r = WAN_OK;
+    int code = 0;
+    do {
+      // one frame of 200 positions (two query blocks) of zeros
+      AttnBufs at;
+      at.HW = 200;
+      at.HWs = (int)rup(at.HW, 16);
+      at.HWp = (int)rup(at.HW, 64);
+      at.Fmax = 1;
+      at.B = 1;
+      at.C = C;
+      at.flash = true;
+      auto mk = [&](Act& a, int ch) -> wan_status {
+        a.B = 1;
+        a.F = 1;
+        a.H = 1;
+        a.W = at.HW;
+        a.C = ch;
+        a.ldc = ch;
+        void* p;
+        WAN_TRY(mem.alloc(&p, a.bytes()));
+        a.p = (bf16*)p;
+        return cudaMemsetAsync(p, 0, a.bytes(), s) == cudaSuccess ? WAN_OK : fail(WAN_ERR_CUDA, "memset failed");
+      };
+      void *pv, *pe;
+      if ((r = mk(at.qkv, 3 * C)) || (r = mk(at.O, C)) ||
+          (r = mem.alloc(&pv, (size_t)at.vt_bs() * sizeof(bf16))) || (r = mem.alloc(&pe, 256)))
+        break;
+      at.Vt = (bf16*)pv;
+      if (cudaMemsetAsync(pv, 0, (size_t)at.vt_bs() * sizeof(bf16), s) || cudaMemsetAsync(pe, 0, 256, s)) {
+        r = fail(WAN_ERR_CUDA, "memset failed");
+        break;
+      }
+      FlashLaunch FL;
+      if ((r = flash_setup(at, 1, (int*)pe, FL)) != WAN_OK) break;
+      FL.args.wait_limit = 20000000;  // about 10 ms
+      FL.args.stall_at1 = 1;          // the first ring stage is never loaded
+      if (launch_flash_attn(FL, s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "flash attention launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+        break;
+      }
+      if (cudaMemcpyAsync(&code, pe, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+          cudaStreamSynchronize(s) != cudaSuccess) {
+        r = fail(WAN_ERR_CUDA, "reading the error word failed: %s", cudaGetErrorString(cudaGetLastError()));
+        break;
+      }
+    } while (false);
+    mem.release();
+    if (r != WAN_OK) return r;
+    CUDA_TRY(cudaStreamSynchronize(s));
+    if (device_code) *device_code = code;
+    if (code) return fail(WAN_ERR_INTERNAL, "the flash attention kernel reported error %d (a bounded wait expired)", code);
     return WAN_OK;
   })
 }
