@@ -45,6 +45,14 @@ struct FCfg {
       1024 + (size_t)NQ * kFUnit + 2 * kFUnit + (size_t)kFStages * kFUnit + 8 * 32 + 2 * 128 * 4;
 };
 
+// 2^x by the SFU's approximation (flushes subnormal results to zero); the
+// probabilities it feeds are rounded to bf16.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int NQ>
 __global__ void __launch_bounds__(kFThreads, 1)
     flash_attn_kernel(const __grid_constant__ CUtensorMap mapQK, const __grid_constant__ CUtensorMap mapV,
@@ -223,6 +231,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       ok = epi_all(!*abort_flag && mbar_wait_bounded(smem_u32(s_full), j & 1, args.err, kDevTimeoutAccum, lim));
       if (!ok) break;
       tc_fence_after();
+      // the raw scores (the scale is applied in the exponent below)
       float t[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         tmem_ld16(tS + lane_off + 64 * hk + 16 * c, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) t[16 * c + i] = __uint_as_float(r[i]) * args.scale_log2;
+        for (int i = 0; i < 16; ++i) t[16 * c + i] = __uint_as_float(r[i]);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(s_free));
@@ -244,6 +253,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       float mb = t[0];
 #pragma unroll
       for (int i = 1; i < 64; ++i) mb = fmaxf(mb, t[i]);
+      mb *= args.scale_log2;  // the scale is positive: the max of the scaled scores
       red[hk * 128 + row] = mb;
       epi_sync();
       mb = fmaxf(mb, red[(1 - hk) * 128 + row]);
@@ -255,9 +265,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
       // P in bf16, and the row sum of the rounded values: the weights that
       // multiply V then sum to exactly 1 after the final division by l
       float rs = 0.f;
+      const float sc = args.scale_log2;
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        t[i] = __bfloat162float(__float2bfloat16_rn(exp2f(t[i] - m)));
+        t[i] = __bfloat162float(__float2bfloat16_rn(ex2_approx(fmaf(t[i], sc, -m))));
         rs += t[i];
       }
       l = l * alpha + rs;
@@ -392,13 +403,6 @@ __device__ __forceinline__ bool sm_all(bool v) {
       : "r"((uint32_t)v)
       : "memory");
   return r != 0;
-}
-// 2^x by the SFU's approximation (flushes subnormal results to zero); the
-// probabilities it feeds are rounded to bf16.
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // Position of stage kc of O += P_j V_j in the split kernel's stage sequence:
