@@ -27,6 +27,16 @@ inline unsigned blocks_for(long long n, int per_block) { return (unsigned)((n + 
 // .. +7 (j < NCH).  All R*NCH 16-byte loads are issued before the first
 // reduction, to keep enough bytes in flight.
 constexpr int kNormMaxC = 1024;
+// SiLU y * sigmoid(y) with sigmoid(y) = (1 + tanh(y / 2)) / 2: one SFU
+// operation (tanh.approx, relative error near 2^-11) instead of an exponential
+// and a reciprocal, for outputs rounded to bf16 (relative step 2^-8).
+__device__ __forceinline__ float silu_tanh(float y) {
+  const float h = 0.5f * y;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
+
 template <bool SILU, int R, int NCH, bool SPLIT, int G = 32>
 __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView out, const float* __restrict__ gs,
                                                        int C, int P, int in_lo, int out_lo) {
@@ -90,9 +100,10 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(FrameView in, FrameView o
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         y[i] = x[r][j][i] * (rinv[r] * g[i]);
-        // SiLU: y * sigmoid(y); for y << 0 the exponential overflows to +inf
-        // and the approximate division returns -0
-        if (SILU) y[i] = __fdividef(y[i], 1.0f + __expf(-y[i]));
+        // SiLU: y * sigmoid(y).  The split (fp32) format keeps the exponential
+        // form (for y << 0 the exponential overflows to +inf and the
+        // approximate division returns -0); bf16 outputs take the tanh form.
+        if (SILU) y[i] = SPLIT ? __fdividef(y[i], 1.0f + __expf(-y[i])) : silu_tanh(y[i]);
       }
       if (SPLIT) {
         float h[8], l[8];
