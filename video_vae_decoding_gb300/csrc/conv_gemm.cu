@@ -31,17 +31,18 @@ constexpr int kBandABox = 16 * kBandBoxRows * 128;
 // Row mode: 130 pixels x 128 B, rounded up to whole 1 KB swizzle atoms.
 constexpr int kRowABox = 17 * 1024;
 
-template <int BN, bool ROW = false, bool BAND = false>
+template <int BN, bool ROW = false, bool BAND = false, int NDX = 3>
 struct ConvCfg {
   // as many stages as fit in 227 KB: 16 KB of A plus BN x 128 B of B each;
   // row mode: a 130-row A box (17 KB) and three taps of B; band mode: A
   // boxes (16 x 10 pixels, 20 KB) and one-tap B blocks in separate rings
   static constexpr int kStages = BAND ? (BN >= 256 ? 5 : 6)
-                                      : ROW ? (BN <= 96 ? 4 : (BN <= 128 ? 3 : 2))
+                                      : ROW ? (NDX == 2 ? (BN <= 96 ? 5 : (BN <= 128 ? 4 : 3))
+                                                          : (BN <= 96 ? 4 : (BN <= 128 ? 3 : 2)))
                                             : (BN >= 256 ? 4 : (BN > 128 ? 5 : (BN == 128 ? 6 : (BN > 64 ? 7 : 8))));
   static constexpr int kAStages = BAND ? 3 : kStages;  // A slots (the B ring has kStages)
   static constexpr int kABytes = ROW ? kRowABox : BAND ? kBandABox : kTileM * kBlockK * 2;  // 17 / 20 / 16 KB
-  static constexpr int kBBytes = (ROW ? 3 : 1) * BN * kBlockK * 2;
+  static constexpr int kBBytes = (ROW ? NDX : 1) * BN * kBlockK * 2;
   // one accumulator buffer of BN columns; two are allocated, kAccCols apart
   // (a power of two, so the allocation is one too)
   static constexpr int kAccCols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
@@ -370,11 +371,11 @@ __device__ __forceinline__ void epilogue_tile(const ConvArgs& args, uint32_t tac
 // the B block and multicasts it to both, and each MMA issuer frees a B slot
 // in both CTAs (the slot's "empty" barrier counts both), so L2 delivers B
 // once per pair.
-template <int BN, int EPI, int CL, bool ROW, bool BAND>
+template <int BN, int EPI, int CL, bool ROW, bool BAND, int NDX = 3>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                      const __grid_constant__ CUtensorMap mapB, const __grid_constant__ ConvArgs args) {
-  using Cfg = ConvCfg<BN, ROW, BAND>;
+  using Cfg = ConvCfg<BN, ROW, BAND, NDX>;
   static_assert(!BAND || CL == 2, "band mode shares B across a pair of CTAs");
   constexpr int S = Cfg::kStages;
   constexpr int SA = Cfg::kAStages;
@@ -488,11 +489,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       } else if constexpr (ROW) {
         // per tap (dt, dy) and 64-channel block: one 130-pixel A box (x from
-        // tile start - 1) and the B blocks of its three dx taps
+        // tile start - 1) and the B blocks of its NDX dx taps.  In the
+        // sub-pixel form (NDX = 2) the box starts at the phase's first column
+        // offset (j - 1) and the row offset (i - 1) is added; B's third
+        // coordinate is the phase
+        const int sx = args.subpix ? (tc.phase & 1) : 0, sy = args.subpix ? (tc.phase >> 1) - 1 : 0;
+        const int gR = args.subpix ? tc.phase : 0;
         for (int ti = 0; ti < args.n_taps && ok; ++ti) {
           const ConvTap tp = args.taps[ti];
           const int fr = ring_slot(args.src_f0[0] + tc.f + tp.dt, args.src_fmod);
-          const int x0 = tc.tx * kTileM - 1, y0 = tc.ty + tp.dy;
+          const int x0 = tc.tx * kTileM - 1 + sx, y0 = tc.ty + tp.dy + sy;
           for (int kb = 0; kb < tp.nkb; ++kb, ++it) {
             const int s = it % S;
             const int r = it / S;
@@ -509,14 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = smem_u32(&full[s]);
             mbar_arrive_expect_tx(fb, (kTileM + 2) * kBlockK * 2 + Cfg::kBBytes);
             tma_load_5d(smem_u32(sA + s * Cfg::kABytes), &mapA0, fb, tp.a_c0 + kb * kBlockK, x0, y0, fr, tc.b);
-            for (int j = 0; j < 3; ++j) {
+            for (int j = 0; j < NDX; ++j) {
               const uint32_t dst = smem_u32(sB + s * Cfg::kBBytes + j * (BN * kBlockK * 2) +
                                             rank * (BN / CL) * kBlockK * 2);
               const int k = tp.b_k0 + j * args.row_bdk + kb * kBlockK;
               if constexpr (CL > 1)
-                tma_load_3d_multicast(dst, &mapB, fb, k, tc.tn * BN + rank * (BN / CL), 0, kPairMask);
+                tma_load_3d_multicast(dst, &mapB, fb, k, tc.tn * BN + rank * (BN / CL), gR, kPairMask);
               else
-                tma_load_3d(dst, &mapB, fb, k, tc.tn * BN, 0);
+                tma_load_3d(dst, &mapB, fb, k, tc.tn * BN, gR);
             }
           }
         }
@@ -657,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++kbc > last_kb) kbc = 0;
           if (tail && args.tail_k16 == 2) {
 #pragma unroll
-            for (int j = 0; j < 3; ++j) {
+            for (int j = 0; j < NDX; ++j) {
               const uint64_t ad = a0 + (uint64_t)((j * 128) >> 4);
               const uint64_t bd = b0 + (uint64_t)((j * BN * kBlockK * 2) >> 4);
 #pragma unroll
@@ -666,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 3; ++j) {
+            for (int j = 0; j < NDX; ++j) {
               const uint64_t ad = a0 + (uint64_t)((j * 128) >> 4);
               const uint64_t bd = b0 + (uint64_t)((j * BN * kBlockK * 2) >> 4);
 #pragma unroll
@@ -718,10 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int EPI, int CL, bool ROW = false, bool BAND = false>
+template <int BN, int EPI, int CL, bool ROW = false, bool BAND = false, int NDX = 3>
 static cudaError_t launch_t(const ConvLaunch& L, cudaStream_t stream) {
-  using Cfg = ConvCfg<BN, ROW, BAND>;
-  auto kern = conv_gemm_kernel<BN, EPI, CL, ROW, BAND>;
+  using Cfg = ConvCfg<BN, ROW, BAND, NDX>;
+  auto kern = conv_gemm_kernel<BN, EPI, CL, ROW, BAND, NDX>;
   // The shared-memory opt-in and the number of co-resident clusters depend
   // only on the kernel and the device: set and queried once per device (the
   // cluster occupancy query costs tens of microseconds of host time).
@@ -781,7 +787,13 @@ cudaError_t launch_conv(const ConvLaunch& L, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   }
   if (L.args.row) {
-    if (L.epi != kEpiStore || L.args.subpix) return cudaErrorInvalidValue;
+    if (L.epi != kEpiStore) return cudaErrorInvalidValue;
+    if (L.args.subpix) {  // 2 x 2 taps per phase: two dx taps per A box
+      if (L.bn == 96) return launch_t<96, kEpiStore, 2, true, false, 2>(L, stream);
+      if (L.bn == 128) return launch_t<128, kEpiStore, 2, true, false, 2>(L, stream);
+      if (L.bn == 192) return launch_t<192, kEpiStore, 2, true, false, 2>(L, stream);
+      return cudaErrorInvalidValue;
+    }
     if (L.bn == 96) return launch_t<96, kEpiStore, 2, true>(L, stream);
     if (L.bn == 128) return launch_t<128, kEpiStore, 2, true>(L, stream);
     if (L.bn == 192) return launch_t<192, kEpiStore, 2, true>(L, stream);

@@ -788,17 +788,22 @@ static wan_status add_tap(ConvArgs& A, int& nt, int src, int dt, int dy, int dx,
 // Fills the launch for conv `cw` reading A source 0 (`a0`, output frame 0 at
 // frame coordinate a0_f0 for dt = 0) and optionally the shortcut source a1.
 // Taps of source 0 with dt < dt_min are left out (they would read frames of
-// zeros: the causal padding).
+// zeros: the causal padding).  subpix_row: a sub-pixel conv with a plain
+// store epilogue may take row mode.
 static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Act* a1, int a1_f0, int F, ConvLaunch& L,
-                             int dt_min = 0) {
+                             int dt_min = 0, bool subpix_row = false) {
   memset(&L, 0, sizeof(L));
   ConvArgs& A = L.args;
   if (a0.ldc < cw.ci_pad || (a1 && a1->ldc < cw.sc_ci_pad))
     return fail(WAN_ERR_INTERNAL, "conv source narrower than its packed channels");
   // row mode (narrow N, 3x3 spatial taps, one source): 128-pixel row tiles,
   // one 130-pixel A box per (dt, dy) serving its three dx taps
-  const bool row = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
-                   (cw.bn == 96 || cw.bn == 128);
+  // (sub-pixel convs too, N tile 96, 128 or 192: each phase's two dx taps
+  // read one 130-pixel box)
+  const bool row = (!cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
+                    (cw.bn == 96 || cw.bn == 128)) ||
+                   (subpix_row && !cw.split && cw.subpix && cw.kh == 2 && cw.kw == 2 && !cw.sc_ci_pad && !a1 &&
+                    (cw.bn == 96 || cw.bn == 128 || cw.bn == 192));
   // band mode (256-wide 3x3 convs, one source): a 16 x 10 A box per (dt, dx)
   // serving its three dy taps
   const bool band = !cw.split && !cw.subpix && cw.kh == 3 && cw.kw == 3 && !cw.sc_ci_pad && !a1 &&
@@ -813,7 +818,7 @@ static wan_status conv_setup(const ConvW& cw, const Act& a0, int a0_f0, const Ac
   } else if (row) {
     WAN_TRY(act_map(&L.a0, a0, 130, 1));
     L.a1 = L.a0;
-    const uint64_t dims[3] = {(uint64_t)cw.ktot, (uint64_t)cw.co_pad, 1};
+    const uint64_t dims[3] = {(uint64_t)cw.ktot, (uint64_t)cw.co_pad, (uint64_t)(cw.subpix ? 4 : 1)};
     const uint64_t strides[2] = {(uint64_t)cw.ktot * 2, (uint64_t)cw.ktot * cw.co_pad * 2};
     const uint32_t box[3] = {64, (uint32_t)(cw.bn / 2), 1};  // each CTA of a pair loads half
     WAN_TRY(encode(&L.b, 3, cw.w, dims, strides, box));
@@ -1200,7 +1205,8 @@ static wan_status resample(wan_vae_stream* st, const ConvW& cw, const Act& x, co
                            Act& y, int F, cudaStream_t s) {
   ConvLaunch L;
   if (!cw.subpix || y.H != 2 * x.H || y.W != 2 * x.W) return fail(WAN_ERR_INTERNAL, "resample shapes");
-  WAN_TRY(conv_setup(cw, x, 0, nullptr, 0, F, L));
+  // Wan2.1's resamplers (plain store epilogue) may run in row mode
+  WAN_TRY(conv_setup(cw, x, 0, nullptr, 0, F, L, 0, st->m->wan21));
   set_out(L.args, out_of(y));
   // nominal FLOPs: the 3x3 conv at the upsampled resolution; executed: the
   // four phases' 2x2 convs at the low resolution (4/9 of nominal)
