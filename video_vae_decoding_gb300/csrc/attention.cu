@@ -4,10 +4,12 @@
 // the frame's HW positions, without the HW x HW score matrix ever leaving the
 // SM.
 //
-// One CTA takes 128 queries of one frame.  The score block S = Q K_j^T of 128
-// keys and the output accumulator O (128 x C fp32) both live in tensor memory
-// (128 + C <= 512 columns, so C <= 384); Q stays in shared memory for the
-// whole key loop.  Per key block j:
+// Two kernels.  flash_attn_kernel (head dims up to 384): one CTA takes 128
+// queries of one frame; the score block S = Q K_j^T of 128 keys and the output
+// accumulator O (128 x C fp32) both live in tensor memory (128 + C <= 512
+// columns); Q stays in shared memory for the whole key loop.
+// flash_attn_split_kernel (head dims 512 and 1024) is described further down.
+// Per key block j of the first:
 //   MMA issuer   S_j = Q K_j^T (M=128, N=128, K=C), then O += P_{j-1} V_{j-1}
 //   softmax      row max and exp2 of the scaled scores (online softmax: the
 //                running max m only moves when a block's max exceeds it by more
