@@ -369,17 +369,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
 //                soon as S_j is read, so S_{j+1} starts while P_{j-1} V_{j-1}
 //                is still running.
 // The stages run through a 4-slot ring of 48 KB (four stages in flight: three
-// did not cover the load latency).  A P V stage uses only the 32 KB B part
-// of its slot (the v^T box), and P_j's box kc lives in the A part of the slot
-// of stage kc of O += P_j V_j, so no separate P buffer is needed.  The
-// softmax threads write it once that slot's previous stage (four positions
-// earlier: one of the last four of S_{j+1}, or of the stages before O += P_j
-// V_j if no S follows) has been consumed: barrier pfree[kc], which the MMA
-// issuer commits after that stage, completes once per key block.  (The
-// slot's "empty" barrier cannot be used: it completes four times during
-// S_{j+1}, and a parity wait only tells neighbouring phases apart.)  Each box
-// has its own "written" barrier p_full[kc], so the P V stage of box 0 need
-// not wait for box 3.
+// did not cover the load latency).  P_j's boxes 0 and 1 have a 32 KB buffer
+// of their own, written as soon as the softmax is done; a P V stage uses only
+// the 32 KB B part of its slot (the v^T box), and boxes 2 and 3 live in the A
+// part of the slot of their own P V stage (no room for a 64 KB P buffer
+// beside four stages).  The softmax threads write box 2 or 3 once that slot's
+// previous stage (four positions earlier: one of the last two of S_{j+1}, or
+// of the stages before O += P_j V_j if no S follows) has been consumed:
+// barrier pfree[kc], which the MMA issuer commits after that stage, completes
+// once per key block.  (The slot's "empty" barrier cannot be used: it
+// completes four times during S_{j+1}, and a parity wait only tells
+// neighbouring phases apart.)  Each box has its own "written" barrier
+// p_full[kc], so the P V stage of box 0 need not wait for box 3.
 // ---------------------------------------------------------------------------
 constexpr int kSThreads = 640;  // warps 0-3 producer, MMA issuer, TMEM allocation, idle; 4-19 softmax
 constexpr int kSStages = 4;
@@ -389,7 +390,7 @@ template <int NSL>
 struct SCfg {
   static constexpr int C = 256 * NSL;
   static constexpr int NC = C / 64;  // 64-channel chunks of the score contraction
-  static constexpr size_t kSmem = 1024 + (size_t)kSStages * kSStage + 256 + 4 * 128 * 4;
+  static constexpr size_t kSmem = 1024 + (size_t)kSStages * kSStage + 2 * kFUnit + 192 + 2 * 128 * 4;
 };
 
 // The 512 softmax threads (warps 4-19) of the split kernel: named barrier 2.
@@ -424,8 +425,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   constexpr int S = kSStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sR = smem;  // ring
-  uint64_t* full = reinterpret_cast<uint64_t*>(sR + S * kSStage);
+  uint8_t* sR = smem;                // ring
+  uint8_t* sP = sR + S * kSStage;    // P boxes 0 and 1 (boxes 2 and 3 live in ring slots)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sP + 2 * kFUnit);
   uint64_t* empty = full + S;
   uint64_t* s_full = empty + S;    // S_j in TMEM
   uint64_t* s_free = s_full + 1;   // S_j read by the softmax threads
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   uint64_t* pfree = done + 1;      // [4] the slot of P box kc is free
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pfree + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(sR + S * kSStage + 256);  // [4 quarters][128 rows]
+  float* red = reinterpret_cast<float*>(sP + 2 * kFUnit + 192);  // [2][128 rows]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = blockIdx.x % NSL;  // output column slice
@@ -531,8 +533,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
           for (int k = 0; k < 4; ++k) umma_bf16(tS, ad + 2 * k, bd + 2 * k, idN256, (c > 0 || k > 0) ? 1u : 0u);
           umma_commit(smem_u32(&empty[slot]));
           // the slot's next stage is stage c + 4 - NC of O += P_{j-1} V_{j-1}
-          // (or, with a single key block, of O += P_0 V_0): its P box may go in
-          if (c >= Cfg::NC - 4 && (j >= 1 || nkb == 1)) umma_commit(smem_u32(&pfree[c + 4 - Cfg::NC]));
+          // (or, with a single key block, of O += P_0 V_0): P box 2 or 3 may go in
+          if (c >= Cfg::NC - 2 && (j >= 1 || nkb == 1)) umma_commit(smem_u32(&pfree[c + 4 - Cfg::NC]));
           if (++slot == S) {
             slot = 0;
             phase ^= 1;
@@ -542,8 +544,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
         umma_commit(smem_u32(s_full));
       }
       if (j >= 1) {
-        // O += P_{j-1} V_{j-1}: stage kc once P_{j-1} box kc (in the A part
-        // of the stage's slot) is written and O rescaled
+        // O += P_{j-1} V_{j-1}: stage kc once P_{j-1} box kc (boxes 0 and 1
+        // in the P buffer, 2 and 3 in the A part of the stage's slot) is
+        // written and O rescaled
         const int jv = j - 1;
         for (int kc = 0; kc < 4 && ok; ++kc) {
           if (!mbar_wait_bounded(smem_u32(&p_full[kc]), jv & 1, args.err, kDevTimeoutAccum, lim) ||
@@ -552,14 +555,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_k128(smem_u32(sR + slot * kSStage));
+          const uint64_t ad = sdesc_k128(smem_u32(kc < 2 ? sP + kc * kFUnit : sR + slot * kSStage));
           const uint64_t bd = sdesc_k128(smem_u32(sR + slot * kSStage + kFUnit));
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             umma_bf16(tO, ad + 2 * k, bd + 2 * k, idN256, (jv > 0 || kc > 0 || k > 0) ? 1u : 0u);
           umma_commit(smem_u32(&empty[slot]));
           // with no S stages left, the slot's next stage is stage kc of O += P_{nkb-1} V_{nkb-1}
-          if (j == nkb - 1) umma_commit(smem_u32(&pfree[kc]));
+          if (j == nkb - 1 && kc >= 2) umma_commit(smem_u32(&pfree[kc]));
           if (++slot == S) {
             slot = 0;
             phase ^= 1;
@@ -610,9 +613,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
       }
       mb *= sc;
-      red[qt * 128 + row] = mb;
+      // the row max over the four quarters: quarters 2 and 3 hand theirs to 0
+      // and 1, which leave max(0, 2) and max(1, 3) for all to read
+      if (qt >= 2) red[(qt - 2) * 128 + row] = mb;
       sm_sync();
-      mb = fmaxf(fmaxf(red[row], red[128 + row]), fmaxf(red[256 + row], red[384 + row]));
+      if (qt < 2) red[qt * 128 + row] = mb = fmaxf(mb, red[qt * 128 + row]);
+      sm_sync();
+      mb = fmaxf(red[row], red[128 + row]);
       float alpha = 1.f;
       if (mb > m + 8.f) {  // move the reference max (and rescale O and l by alpha)
         alpha = exp2f(m - mb);
@@ -665,11 +672,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         if (k != qt) mbar_arrive(smem_u32(&p_full[k]));
-      // P_j box qt goes to the A part of the slot of stage qt of O += P_j V_j,
-      // free once pfree[qt] completes for the j-th time
-      ok = sm_all(mbar_wait_bounded(smem_u32(&pfree[qt]), j & 1, args.err, kDevTimeoutEmpty, lim));
-      if (!ok) break;
-      line_base = sR + (split_pv_pos(j, nkb, Cfg::NC, qt) % S) * kSStage;
+      // P_j box qt: boxes 0 and 1 go to the P buffer (free: O += P_{j-1}
+      // V_{j-1} has completed), boxes 2 and 3 to the A part of the slot of
+      // their P V stage, free once pfree[qt] completes for the j-th time.
+      // This wait is per thread, so that boxes 0 and 1 are not held up: a
+      // thread whose wait runs out raises the abort flag and skips its box,
+      // and all threads leave together at the next agreement.
+      line_base = sP + qt * kFUnit;
+      if (qt >= 2) {
+        if (!mbar_wait_bounded(smem_u32(&pfree[qt]), j & 1, args.err, kDevTimeoutEmpty, lim)) {
+          ok = false;
+          *abort_flag = 1;
+          continue;
+        }
+        line_base = sR + (split_pv_pos(j, nkb, Cfg::NC, qt) % S) * kSStage;
+      }
       // in the 128-byte-swizzled K-major layout: row `row`, chunk g of 8 keys
       // at 16-byte slot g ^ (row & 7) of its 128-byte line
       uint8_t* line = line_base + row * 128;
@@ -680,15 +697,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&p_full[qt]));
     }
-    if (ok) ok = sm_all(mbar_wait_bounded(smem_u32(pv_done), (nkb - 1) & 1, args.err, kDevTimeoutAccum, lim));
+    // every thread takes part (a thread that left the loop early has ok false)
+    ok = sm_all(ok && !*abort_flag &&
+                mbar_wait_bounded(smem_u32(pv_done), (nkb - 1) & 1, args.err, kDevTimeoutAccum, lim));
     if (!ok) {
       *abort_flag = 1;
     } else {
       tc_fence_after();
-      // the row's weight sum: the four quarters' partial sums (taken against the same max)
-      red[qt * 128 + row] = l;
+      // the row's weight sum: the four quarters' partial sums (taken against
+      // the same max), combined as the maxima were
+      if (qt >= 2) red[(qt - 2) * 128 + row] = l;
       sm_sync();
-      const float rl = 1.f / ((red[row] + red[128 + row]) + (red[256 + row] + red[384 + row]));
+      if (qt < 2) red[qt * 128 + row] += l;
+      sm_sync();
+      const float rl = 1.f / (red[row] + red[128 + row]);
       const int qrow = 128 * qb + row;
       __nv_bfloat16* dst = args.out + (long long)b * args.out_bs + (long long)f * args.out_fs +
                            (long long)qrow * args.out_ldc + 256 * rank + 64 * qt;
