@@ -382,8 +382,11 @@ def main():
     w = wan_synth.make_weights(base=WORKLOAD["base"], seed=WORKLOAD["weight_seed"],
                                variant=WORKLOAD.get("variant", "ti2v"))
     wdev = {k: torch.from_numpy(np.array(v)).to(dev) for k, v in w.items()}
-    model = wv.Model(wdev, dtype=torch.bfloat16)
     torch.cuda.synchronize()
+    t_pack = time.perf_counter()
+    model = wv.Model(wdev, dtype=torch.bfloat16)  # weight packing: outside the timed region
+    torch.cuda.synchronize()
+    pack_ms = (time.perf_counter() - t_pack) * 1000.0
     del wdev
     z_np = wan_synth.make_latents((B, Z, T, H_LAT, W_LAT), WORKLOAD["latent_seed"])
     z = torch.from_numpy(z_np).to(dev)
@@ -393,6 +396,8 @@ def main():
     for _ in range(args.warmup):
         st.decode_clip(z, out)
     st.sync_status()
+    free_b, total_b = torch.cuda.mem_get_info()
+    mem_used_gb = (total_b - free_b) / 1e9  # all of the device in use: packed weights, workspace, I/O, context
     gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
     sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
 
@@ -487,6 +492,8 @@ def main():
         "by_kind": kinds,
         "gpu_launches": prof["launches"],
         "workspace_gb": st.workspace_bytes / 1e9,
+        "weight_pack_ms": pack_ms,
+        "device_memory_used_gb": mem_used_gb,
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
