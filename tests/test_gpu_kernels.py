@@ -112,11 +112,12 @@ def test_attention_flash_large_logits(wv):
     _attention_check(wv, N=1, C=384, H=60, W=80, frames=[0], seed=12, qkv_scale=4.0, rel_tol=2e-2, abs_tol=0.15)
 
 
-# Head dims 512 and 1024 run the cluster flash kernel (C / 256 CTAs per 128
+# Head dims 512 and 1024 run the four-CTA flash kernel (C / 256 CTAs per 128
 # queries, each with 256 output columns; key blocks of 256): ragged last key
-# and query blocks, exactly one key block, frames of fewer than 128 positions.
+# and query blocks, exactly one key block, frames of fewer than 128 positions,
+# and frames of one position (one key: the output is proj(v) + x).
 @pytest.mark.parametrize("N,C,H,W", [(2, 1024, 13, 29), (1, 512, 10, 26), (3, 1024, 5, 7), (1, 512, 16, 16),
-                                     (1, 1024, 9, 57)], ids=lambda v: str(v))
+                                     (1, 1024, 9, 57), (2, 1024, 1, 1), (1, 512, 1, 1)], ids=lambda v: str(v))
 def test_attention_flash_split_widths(wv, N, C, H, W):
     _attention_check(wv, N=N, C=C, H=H, W=W, frames=range(N), seed=16)
 
